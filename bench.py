@@ -1,0 +1,482 @@
+"""Benchmark of the virtual-rank AllReduce on one GB300 (replicas on N GPUs).
+
+A step is one sum AllReduce over N=8 virtual ranks of 134,217,728 bf16
+elements (256 MiB) per rank, N(0,1)*(1+r) values, fp32 accumulation -- the
+large-message workload -- through the C ABI with inputs resident in HBM.
+Printed metric: algbw = per-rank bytes / step time (GB/s), plus the HBM
+roofline fraction of the kernel (algorithmic traffic 2*N*S per launch).
+Extra keys carry the decode-size sweep (16 KiB..4 MiB per rank, p50 us), the
+ReduceScatter / AllGather and ring-barrier figures, the end-to-end number
+through the host-buffer entry point, the oracle's CPU baseline and the SM
+clocks sampled during the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+("replicas only": the virtual-rank path has no exchange between GPUs).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from driven_collective_communication_gb300 import workloads as W  # noqa: E402
+
+GB = 1e9
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "allreduce_twoshot_bf16_n8.txt")
+KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "coll_bf16.cu"]
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Dist:
+    def __init__(self):
+        self.ws, self.rank, self.local = dist_env()
+        self.pg = None
+        if self.ws > 1:
+            import torch.distributed as td
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            td.init_process_group("gloo", rank=self.rank, world_size=self.ws)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x):
+        if not self.pg:
+            return x
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x):
+        if not self.pg:
+            return x
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "driven_collective_communication_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary,
+    or None if the kernel sources changed since the counters were taken."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    m = re.search(r"^traffic_bytes_per_full_launch:\s*(\d+)", text, re.M)
+    h = re.search(r"^kernel_source_hash:\s*(\w+)", text, re.M)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d_%d.csv" % (os.getpid(), self.gpu))
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [float(r[3]) for r in rows if re.match(r"^[\d.]+$", r[3])]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def time_launches(fn, steps, stream):
+    """Per-launch CUDA-event durations (ms) on `stream` and the whole span."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    t1.record(stream)
+    t1.synchronize()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, t0.elapsed_time(t1)
+
+
+# ------------------------------------------------------------------ oracle CPU leg
+def oracle_sample_run(seconds, elems):
+    """Time the oracle (all host cores) on a prefix of `elems` elements per rank
+    of the large-message workload.  Returns (GB/s algbw, threads, sample text, calls)."""
+    import oracle
+    w = W.C4
+    xs = [W.to_storage(t) for t in W.rank_inputs(w, device="cpu", count=elems)]
+    threads = os.cpu_count() or 1
+    oracle.allreduce(xs, "bf16", nthreads=threads)  # warm
+    n_calls, t_total = 0, 0.0
+    while t_total < seconds:
+        t = time.perf_counter()
+        oracle.allreduce(xs, "bf16", nthreads=threads)
+        t_total += time.perf_counter() - t
+        n_calls += 1
+    per_call = t_total / n_calls
+    sample = ("oracle AllReduce, N=8 bf16, first %d elements (%d MiB) of each rank's 256 MiB "
+              "buffer, %d calls, %.1f s" % (elems, elems * 2 >> 20, n_calls, t_total))
+    return elems * 2 / per_call / GB, threads, sample, per_call
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, dist):
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    stream = torch.cuda.Stream(device=dev)
+    w = W.C4
+    n = w.n_ranks
+    S = w.bytes_per_rank
+
+    with torch.cuda.stream(stream):
+        xs = W.rank_inputs(w, device=dev)
+        ys = [torch.empty_like(x) for x in xs]
+    torch.cuda.synchronize()
+    comm = dcc.Comm(n)
+    comm.register_all("input", xs)
+    comm.register_all("output", ys)
+    h = comm.handle
+    algo = "auto"
+    blocks, threads = dcc.dcc_launch_shape(h, w.count, "bf16", algo)
+    chosen = dcc.dcc_select_algo(h, w.count, "bf16")
+
+    def step():
+        dcc.dcc_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    if comm.check(stream) != dcc.DCC_OK:
+        raise RuntimeError("device failure during warm-up")
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    per, span_ms = time_launches(step, args.steps, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    rc = comm.check(stream)
+    if rc != dcc.DCC_OK:
+        raise RuntimeError("device failure in the timed region: " + dcc.dcc_error_string(rc))
+
+    ms_per_step = dist.max(span_ms / args.steps)
+    kernel_ms = sum(per) / len(per)
+    # whole job: every replica processes one S-byte-per-rank AllReduce per step
+    value = dist.ws * S / (ms_per_step / 1e3) / GB
+    peak, peak_src = measured_peaks()
+    algo_bytes = 2 * n * S
+    achieved = algo_bytes / (kernel_ms / 1e3) / GB
+
+    out = {
+        "metric": "AllReduce algbw GB/s & % HBM roofline vs msg size at N=8 virtual ranks; p50 us @16KB",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_ranks": n, "elem": "bf16", "accumulate": "f32",
+                   "count_per_rank": w.count, "bytes_per_rank": S, "algo": chosen,
+                   "blocks_per_rank": blocks, "threads": threads,
+                   "values": "N(0,1)*(1+r), seed 3+r", "l2": "inputs larger than L2 (2 GiB read per step)",
+                   "parallelism": "replicas" if dist.ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "algorithmic_bytes": algo_bytes, "peak_source": peak_src,
+                     "kernel_ms": round(kernel_ms, 5)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+    if dist.rank == 0 and not args.quick:
+        out["e2e"] = e2e_host(dcc, comm, xs, ys, w, args, stream)
+        out["sweep_c3"] = sweep_c3(dcc, dev, stream)
+        out["other"] = other_workloads(dcc, dev, stream)
+        gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
+        out["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
+                               "kind": "oracle", "sample": sample}
+    comm.close()
+    return out
+
+
+def e2e_host(dcc, comm, xs, ys, w, args, stream):
+    """The same AllReduce through dcc_allreduce_from_host: pinned host inputs
+    copied in, the collective, outputs copied back -- all inside the timing."""
+    hin = [x.cpu().pin_memory() for x in xs]
+    hout = [torch.empty_like(t).pin_memory() for t in hin]
+    h = comm.handle
+
+    def step():
+        dcc.dcc_allreduce_from_host(h, hin, hout, xs, ys, w.count, "bf16", "auto", stream)
+
+    for _ in range(2):
+        step()
+    stream.synchronize()
+    steps = max(3, min(10, args.steps // 100))
+    t0 = time.perf_counter()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    ev1.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    wall = (time.perf_counter() - t0) / steps
+    nbytes = w.n_ranks * w.bytes_per_rank
+    return {"value": round(w.bytes_per_rank / (ms / 1e3) / GB, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+            "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3), "steps": steps}
+
+
+def sweep_c3(dcc, dev, stream):
+    """Decode-shaped sizes: per-launch p50 (events) and CUDA-graph-amortised us
+    per algorithm.  Steady state: the 8 x 16 KiB..4 MiB inputs stay in L2."""
+    res = []
+    for tokens in W.C3_TOKENS:
+        w = W.c3(tokens)
+        with torch.cuda.stream(stream):
+            xs = W.rank_inputs(w, device=dev)
+            ys = [torch.empty_like(x) for x in xs]
+        torch.cuda.synchronize()
+        comm = dcc.Comm(8)
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        h = comm.handle
+        row = {"tokens": tokens, "bytes_per_rank": w.bytes_per_rank}
+        for algo in ("one_shot", "two_shot"):
+            def step():
+                dcc.dcc_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
+            for _ in range(50):
+                step()
+            per, _ = time_launches(step, 500, stream)
+            p50 = statistics.median(per) * 1e3
+            g = torch.cuda.CUDAGraph()
+            reps = 100
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    step()
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            graph_us = e0.elapsed_time(e1) * 1e3 / (5 * reps)
+            row[algo] = {"p50_us": round(p50, 2), "graph_us": round(graph_us, 2),
+                         "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
+        assert comm.check(stream) == dcc.DCC_OK
+        comm.close()
+        res.append(row)
+    return res
+
+
+def other_workloads(dcc, dev, stream):
+    """C2 (int32 in-place, both algorithms), C5 (ReduceScatter, AllGather,
+    ring barrier): device-event timings."""
+    out = {}
+    w = W.C2
+    with torch.cuda.stream(stream):
+        xs = W.rank_inputs(w, device=dev)
+    torch.cuda.synchronize()
+    comm = dcc.Comm(8)
+    comm.register_all("input", xs)
+    for algo in ("one_shot", "two_shot"):
+        def step():
+            dcc.dcc_allreduce(comm.handle, xs, xs, w.count, "int32", algo, stream)
+        for _ in range(3):
+            step()
+        per, _ = time_launches(step, 20, stream)
+        ms = statistics.median(per)
+        out["c2_int32_inplace_" + algo] = {"ms": round(ms, 4),
+                                           "algbw_gbs": round(w.bytes_per_rank / ms / 1e6, 2),
+                                           "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+    assert comm.check(stream) == dcc.DCC_OK
+    comm.close()
+    del xs
+    w = W.C5
+    m = w.count // 8
+    with torch.cuda.stream(stream):
+        xs = W.rank_inputs(w, device=dev)
+        rs = [torch.empty(m, dtype=torch.float16, device=dev) for _ in range(8)]
+        ag = [torch.empty(w.count, dtype=torch.float16, device=dev) for _ in range(8)]
+    torch.cuda.synchronize()
+    comm = dcc.Comm(8)
+    comm.register_all("input", xs)
+    comm.register_all("output", rs)
+    comm.register_all("output", ag)
+    for name, fn, nbytes in (
+            ("c5_reduce_scatter", lambda: dcc.dcc_reduce_scatter(comm.handle, xs, rs, m, "fp16", stream),
+             8 * w.bytes_per_rank + w.bytes_per_rank),
+            ("c5_allgather", lambda: dcc.dcc_allgather(comm.handle, rs, ag, m, "fp16", stream),
+             w.bytes_per_rank + 8 * w.bytes_per_rank)):
+        for _ in range(3):
+            fn()
+        per, _ = time_launches(fn, 20, stream)
+        ms = statistics.median(per)
+        out[name] = {"ms": round(ms, 4), "hbm_gbs": round(nbytes / ms / 1e6, 1),
+                     "algorithmic_bytes": nbytes}
+    assert comm.check(stream) == dcc.DCC_OK
+    comm.close()
+    with dcc.Comm(8, connect="ring") as ring:
+        ring.ring_barrier(100, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ring.ring_barrier(W.BARRIER_ITERS, stream)
+        e1.record(stream)
+        e1.synchronize()
+        assert ring.check(stream) == dcc.DCC_OK
+        us = e0.elapsed_time(e1) * 1e3 / W.BARRIER_ITERS
+        out["c5_ring_barrier"] = {"iters": W.BARRIER_ITERS, "round_trip_us": round(us, 3),
+                                  "per_hop_us": round(us / 8, 3)}
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, dist):
+    """The oracle timed as the reference arm on the host cores (rank 0 only)."""
+    if dist.rank != 0:
+        return None
+    per_step_s = []
+    threads = os.cpu_count() or 1
+    import oracle
+    w = W.C4
+    elems = args.ref_elems
+    xs = [W.to_storage(t) for t in W.rank_inputs(w, device="cpu", count=elems)]
+    for _ in range(args.warmup):
+        oracle.allreduce(xs, "bf16", nthreads=threads)
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.allreduce(xs, "bf16", nthreads=threads)
+        per_step_s.append(time.perf_counter() - t)
+    t_step = sum(per_step_s) / len(per_step_s)
+    value = elems * 2 / t_step / GB
+    sample = ("oracle AllReduce, N=8 bf16, first %d elements (%d MiB) of each rank's 256 MiB "
+              "buffer per step" % (elems, elems * 2 >> 20))
+    return {
+        "impl": "reference",
+        "metric": "AllReduce algbw GB/s & % HBM roofline vs msg size at N=8 virtual ranks; p50 us @16KB",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": dist.ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_ranks": 8, "elem": "bf16", "accumulate": "f32",
+                   "count_per_rank": w.count, "sample_elems_per_rank": elems},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only (no sweep, e2e, CPU leg)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-elems", type=int, default=1 << 24)
+    ap.add_argument("--ref-elems", type=int, default=1 << 22)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    try:
+        out = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
+        if out is not None and dist.rank == 0:
+            print(json.dumps(out), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,382 @@
+// collectives.cuh -- sum AllReduce (one-shot, two-shot push, two-shot via
+// scratch), ReduceScatter and AllGather kernels for N virtual ranks.
+//
+// The collectives are the standard ones of the MSCCL++ abstract, point (3);
+// the AllReduce is the tensor-parallel serving case of the project summary's
+// "Highlighted Details".  Every data access goes through a MemoryChannel
+// (get = read of a peer's 16-byte vector, put = write into a peer's buffer);
+// signal/wait order the phases that need it.
+//
+// Arithmetic (identical in every kernel, so every algorithm and launch shape
+// returns the same bits): per element, acc = x_0; acc += x_p for p = 1..N-1 in
+// rank order; fp16/bf16 are widened exactly to fp32, adds are fp32
+// round-to-nearest-even (__fadd_rn, no contraction, subnormals kept: the build
+// uses no fast-math and no flush-to-zero); one RNE rounding to the output type
+// at the end (cvt.rn); int32 adds wrap.
+//
+// Layout: rank r's buffers are separate allocations; a rank is the group of
+// `blocks` consecutive CTAs starting at r * blocks.  Each thread works on
+// whole 16-byte vectors; the < 16-byte remainder of a buffer (the "tail") is
+// done element by element by one CTA.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "memory_channel.cuh"
+
+namespace dcc {
+
+constexpr int kThreads = 512;       // threads per CTA of the data kernels
+constexpr int kInplaceUnroll = 4;   // vectors per thread per chunk, in-place one-shot
+
+// ------------------------------------------------------------- element lanes
+template <typename T>
+struct Lanes;
+
+template <>
+struct Lanes<int32_t> {
+  static constexpr int VW = 4;  // elements per 16-byte vector
+  struct Acc { uint32_t v[4]; };
+  using S = int32_t;            // scalar storage
+  using SAcc = uint32_t;
+  __device__ static void init(Acc& a, uint4 x) { a.v[0] = x.x; a.v[1] = x.y; a.v[2] = x.z; a.v[3] = x.w; }
+  __device__ static void add(Acc& a, uint4 x) { a.v[0] += x.x; a.v[1] += x.y; a.v[2] += x.z; a.v[3] += x.w; }
+  __device__ static uint4 pack(const Acc& a) { return make_uint4(a.v[0], a.v[1], a.v[2], a.v[3]); }
+  __device__ static SAcc sinit(S x) { return (uint32_t)x; }
+  __device__ static SAcc sadd(SAcc a, S x) { return a + (uint32_t)x; }
+  __device__ static S spack(SAcc a) { return (int32_t)a; }
+};
+
+template <>
+struct Lanes<float> {
+  static constexpr int VW = 4;
+  struct Acc { float v[4]; };
+  using S = float;
+  using SAcc = float;
+  __device__ static void init(Acc& a, uint4 x) {
+    a.v[0] = __uint_as_float(x.x); a.v[1] = __uint_as_float(x.y);
+    a.v[2] = __uint_as_float(x.z); a.v[3] = __uint_as_float(x.w);
+  }
+  __device__ static void add(Acc& a, uint4 x) {
+    a.v[0] = __fadd_rn(a.v[0], __uint_as_float(x.x)); a.v[1] = __fadd_rn(a.v[1], __uint_as_float(x.y));
+    a.v[2] = __fadd_rn(a.v[2], __uint_as_float(x.z)); a.v[3] = __fadd_rn(a.v[3], __uint_as_float(x.w));
+  }
+  __device__ static uint4 pack(const Acc& a) {
+    return make_uint4(__float_as_uint(a.v[0]), __float_as_uint(a.v[1]), __float_as_uint(a.v[2]),
+                      __float_as_uint(a.v[3]));
+  }
+  __device__ static SAcc sinit(S x) { return x; }
+  __device__ static SAcc sadd(SAcc a, S x) { return __fadd_rn(a, x); }
+  __device__ static S spack(SAcc a) { return a; }
+};
+
+// 16-bit floats: 8 per vector, widened pairwise (exact), narrowed pairwise RNE.
+template <typename H2, typename Ops>
+struct HalfLanes {
+  static constexpr int VW = 8;
+  struct Acc { float v[8]; };
+  using S = uint16_t;  // raw storage bits
+  using SAcc = float;
+  __device__ static float2 widen2(uint32_t w) {
+    H2 h;
+    memcpy(&h, &w, 4);
+    return Ops::to_float2(h);
+  }
+  __device__ static uint32_t narrow2(float lo, float hi) {
+    H2 h = Ops::from_floats(lo, hi);
+    uint32_t w;
+    memcpy(&w, &h, 4);
+    return w;
+  }
+  __device__ static void init(Acc& a, uint4 x) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 f = widen2(w[k]);
+      a.v[2 * k] = f.x;
+      a.v[2 * k + 1] = f.y;
+    }
+  }
+  __device__ static void add(Acc& a, uint4 x) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 f = widen2(w[k]);
+      a.v[2 * k] = __fadd_rn(a.v[2 * k], f.x);
+      a.v[2 * k + 1] = __fadd_rn(a.v[2 * k + 1], f.y);
+    }
+  }
+  __device__ static uint4 pack(const Acc& a) {
+    return make_uint4(narrow2(a.v[0], a.v[1]), narrow2(a.v[2], a.v[3]), narrow2(a.v[4], a.v[5]),
+                      narrow2(a.v[6], a.v[7]));
+  }
+  __device__ static SAcc sinit(S x) { return widen2((uint32_t)x).x; }
+  __device__ static SAcc sadd(SAcc a, S x) { return __fadd_rn(a, widen2((uint32_t)x).x); }
+  __device__ static S spack(SAcc a) { return (uint16_t)(narrow2(a, 0.0f) & 0xFFFFu); }
+};
+
+struct Bf16Ops {
+  __device__ static float2 to_float2(__nv_bfloat162 h) { return __bfloat1622float2(h); }
+  __device__ static __nv_bfloat162 from_floats(float lo, float hi) { return __floats2bfloat162_rn(lo, hi); }
+};
+struct F16Ops {
+  __device__ static float2 to_float2(__half2 h) { return __half22float2(h); }
+  __device__ static __half2 from_floats(float lo, float hi) { return __floats2half2_rn(lo, hi); }
+};
+
+template <>
+struct Lanes<__nv_bfloat16> : HalfLanes<__nv_bfloat162, Bf16Ops> {};
+template <>
+struct Lanes<__half> : HalfLanes<__half2, F16Ops> {};
+
+// ------------------------------------------------------------- reductions
+// Sum of vector v over the N ranks' buffers src[0..N-1], rank order.  With a
+// compile-time N all N gets are issued before the first add.
+template <typename T, int NT>
+__device__ __forceinline__ uint4 reduce_vec(void* const* src, int n, size_t v) {
+  using L = Lanes<T>;
+  typename L::Acc acc;
+  if constexpr (NT > 0) {
+    uint4 x[NT];
+#pragma unroll
+    for (int p = 0; p < NT; ++p) x[p] = ld_vec(static_cast<const uint4*>(src[p]) + v);
+    L::init(acc, x[0]);
+#pragma unroll
+    for (int p = 1; p < NT; ++p) L::add(acc, x[p]);
+  } else {
+    L::init(acc, ld_vec(static_cast<const uint4*>(src[0]) + v));
+    for (int p = 1; p < n; ++p) L::add(acc, ld_vec(static_cast<const uint4*>(src[p]) + v));
+  }
+  return L::pack(acc);
+}
+
+template <typename T>
+__device__ __forceinline__ typename Lanes<T>::S reduce_scalar(void* const* src, int n, size_t i) {
+  using L = Lanes<T>;
+  using S = typename L::S;
+  typename L::SAcc acc = L::sinit(static_cast<const S*>(src[0])[i]);
+  for (int p = 1; p < n; ++p) acc = L::sadd(acc, static_cast<const S*>(src[p])[i]);
+  return L::spack(acc);
+}
+
+// Two-shot shard of rank r, in vectors: whole vectors, the last rank also
+// takes the remainder (and the element tail).
+__device__ __forceinline__ void shard_vecs(size_t nvec, int n, int r, size_t& s0, size_t& s1) {
+  const size_t per = nvec / (size_t)n;
+  s0 = per * (size_t)r;
+  s1 = (r == n - 1) ? nvec : s0 + per;
+}
+
+// ------------------------------------------------------------- one-shot
+// Every rank gets all N inputs and reduces its whole output.  Out of place no
+// rank writes what another reads, so there is no synchronisation.  In place,
+// rank r's output is an input of every peer: the N CTAs of a block slot
+// process the same chunk together -- get and reduce into registers, then a
+// signal/wait barrier ("everyone has read this chunk"), then store.
+template <typename T, int NT>
+__global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
+  using L = Lanes<T>;
+  const int n = NT > 0 ? NT : dc.n;
+  const int B = a.blocks;
+  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  const size_t nvec = a.count / L::VW;
+  const size_t tail0 = nvec * L::VW;
+  uint4* out = static_cast<uint4*>(a.recv[rank]);
+  using S = typename L::S;
+
+  if (!a.inplace) {
+    const size_t stride = (size_t)B * blockDim.x;
+    for (size_t v = (size_t)blk * blockDim.x + threadIdx.x; v < nvec; v += stride)
+      st_vec(out + v, reduce_vec<T, NT>(a.send, n, v));
+    if (blk == 0 && tail0 + threadIdx.x < a.count)
+      static_cast<S*>(a.recv[rank])[tail0 + threadIdx.x] = reduce_scalar<T>(a.send, n, tail0 + threadIdx.x);
+    return;
+  }
+
+  unsigned long long expected = 0;
+  const bool waiter = (int)threadIdx.x < n && (int)threadIdx.x != rank;
+  if (waiter) expected = dc.expect[sem_slot(rank, threadIdx.x, blk)];
+  const size_t chunk = (size_t)kInplaceUnroll * blockDim.x;
+  const size_t nchunks = (nvec + chunk - 1) / chunk;
+  bool ok = true;
+  for (size_t c = blk; c < nchunks; c += B) {
+    uint4 res[kInplaceUnroll];
+#pragma unroll
+    for (int u = 0; u < kInplaceUnroll; ++u) {
+      const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
+      if (v < nvec) res[u] = reduce_vec<T, NT>(a.send, n, v);
+    }
+    ok = group_barrier(dc, rank, n, blk, expected);
+    if (!ok) break;
+#pragma unroll
+    for (int u = 0; u < kInplaceUnroll; ++u) {
+      const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
+      if (v < nvec) st_vec(out + v, res[u]);
+    }
+  }
+  if (ok && blk == 0 && tail0 < a.count) {  // same on every rank: all slot-0 CTAs take part
+    const size_t i = tail0 + threadIdx.x;
+    S r{};
+    if (i < a.count) r = reduce_scalar<T>(a.send, n, i);
+    ok = group_barrier(dc, rank, n, blk, expected);
+    if (ok && i < a.count) static_cast<S*>(a.recv[rank])[i] = r;
+  }
+  if (waiter) dc.expect[sem_slot(rank, threadIdx.x, blk)] = expected;
+}
+
+// ------------------------------------------------------------- two-shot, push
+// Rank r gets shard r of all N inputs, reduces it, and puts the result into
+// shard r of all N outputs (ReduceScatter fused with a push AllGather).  Only
+// rank r's CTAs touch shard r of any buffer and every thread reads all N
+// values of a vector before writing it anywhere, so in place is safe without
+// synchronisation.  Traffic: N*S read + N*S written in total, the minimum.
+template <typename T, int NT>
+__global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, CollArgs a) {
+  using L = Lanes<T>;
+  using S = typename L::S;
+  const int n = NT > 0 ? NT : dc.n;
+  const int B = a.blocks;
+  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  const size_t nvec = a.count / L::VW;
+  size_t s0, s1;
+  shard_vecs(nvec, n, rank, s0, s1);
+  const size_t stride = (size_t)B * blockDim.x;
+  for (size_t v = s0 + (size_t)blk * blockDim.x + threadIdx.x; v < s1; v += stride) {
+    const uint4 r = reduce_vec<T, NT>(a.send, n, v);
+    if constexpr (NT > 0) {
+#pragma unroll
+      for (int p = 0; p < NT; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + v, r);
+    } else {
+      for (int p = 0; p < n; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + v, r);
+    }
+  }
+  const size_t i = nvec * L::VW + threadIdx.x;
+  if (rank == n - 1 && blk == 0 && i < a.count) {
+    const S r = reduce_scalar<T>(a.send, n, i);
+    for (int p = 0; p < n; ++p) static_cast<S*>(a.recv[p])[i] = r;
+  }
+}
+
+// ------------------------------------------------------------- two-shot, scratch
+// Phase 1: rank r reduces shard r into its own scratch.  Barrier: each CTA
+// signals its N-1 peers of the same block slot and waits for theirs.  Phase 2:
+// rank r gets every shard q from rank q's scratch into its output.  CTA
+// (r, blk) reads exactly the scratch vectors CTA (q, blk) wrote, so the
+// per-slot barrier is enough.  In place is safe: rank r overwrites shard q of
+// its buffer only after CTA (q, blk) has read it.
+template <typename T, int NT>
+__global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm dc, CollArgs a) {
+  using L = Lanes<T>;
+  using S = typename L::S;
+  const int n = NT > 0 ? NT : dc.n;
+  const int B = a.blocks;
+  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  const size_t nvec = a.count / L::VW;
+  const size_t stride = (size_t)B * blockDim.x;
+  const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
+  const size_t tail_i = nvec * L::VW + threadIdx.x;
+  const bool tail_thread = blk == 0 && tail_i < a.count;
+
+  size_t s0, s1;
+  shard_vecs(nvec, n, rank, s0, s1);
+  uint4* mine = static_cast<uint4*>(a.scratch[rank]);
+  for (size_t v = s0 + first; v < s1; v += stride) st_vec(mine + (v - s0), reduce_vec<T, NT>(a.send, n, v));
+  if (rank == n - 1 && tail_thread)
+    reinterpret_cast<S*>(mine + (s1 - s0))[threadIdx.x] = reduce_scalar<T>(a.send, n, tail_i);
+
+  unsigned long long expected = 0;
+  const bool waiter = (int)threadIdx.x < n && (int)threadIdx.x != rank;
+  if (waiter) expected = dc.expect[sem_slot(rank, threadIdx.x, blk)];
+  const bool ok = group_barrier(dc, rank, n, blk, expected);
+  if (waiter) dc.expect[sem_slot(rank, threadIdx.x, blk)] = expected;
+  if (!ok) return;
+
+  uint4* out = static_cast<uint4*>(a.recv[rank]);
+  for (int q = 0; q < n; ++q) {
+    size_t q0, q1;
+    shard_vecs(nvec, n, q, q0, q1);
+    MemoryChannel ch = MemoryChannel::make(dc, rank, q, blk, a.scratch[q], nullptr);
+    for (size_t v = q0 + first; v < q1; v += stride) st_vec(out + v, ld_vec_l2(reinterpret_cast<const uint4*>(ch.remote_src) + (v - q0)));
+    if (q == n - 1 && tail_thread)
+      static_cast<S*>(a.recv[rank])[tail_i] = __ldcg(reinterpret_cast<const S*>(
+          reinterpret_cast<const uint4*>(ch.remote_src) + (q1 - q0)) + threadIdx.x);
+  }
+}
+
+// ------------------------------------------------------------- ReduceScatter
+// recv[r][j] = sum_p send[p][r*m + j].  Rank r's CTAs get shard r of every
+// input.  Vector path when a shard starts on a 16-byte boundary, else scalar.
+template <typename T, int NT>
+__global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArgs a) {
+  using L = Lanes<T>;
+  using S = typename L::S;
+  const int n = NT > 0 ? NT : dc.n;
+  const int B = a.blocks;
+  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  const size_t m = a.count;
+  const size_t stride = (size_t)B * blockDim.x;
+  const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
+  if ((m * sizeof(S)) % 16 == 0) {
+    const size_t nv = m / L::VW, base = (size_t)rank * nv;
+    uint4* out = static_cast<uint4*>(a.recv[rank]);
+    for (size_t v = first; v < nv; v += stride) st_vec(out + v, reduce_vec<T, NT>(a.send, n, base + v));
+  } else {
+    S* out = static_cast<S*>(a.recv[rank]);
+    const size_t base = (size_t)rank * m;
+    for (size_t j = first; j < m; j += stride) out[j] = reduce_scalar<T>(a.send, n, base + j);
+  }
+}
+
+// ------------------------------------------------------------- AllGather
+// recv[p][q*m + j] = send[q][j]: rank q's CTAs put their input into slot q of
+// every rank's output.  A bit copy of elem_bytes-sized elements.
+template <int NT>
+__global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, int elem_bytes) {
+  const int n = NT > 0 ? NT : dc.n;
+  const int B = a.blocks;
+  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  const size_t bytes = a.count * (size_t)elem_bytes;
+  const size_t stride = (size_t)B * blockDim.x;
+  const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
+  if (bytes % 16 == 0) {
+    const size_t nv = bytes / 16;
+    const uint4* src = static_cast<const uint4*>(a.send[rank]);
+    for (size_t v = first; v < nv; v += stride) {
+      const uint4 x = ld_vec(src + v);
+      if constexpr (NT > 0) {
+#pragma unroll
+        for (int p = 0; p < NT; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + (size_t)rank * nv + v, x);
+      } else {
+        for (int p = 0; p < n; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + (size_t)rank * nv + v, x);
+      }
+    }
+  } else if (elem_bytes == 4) {
+    const uint32_t* src = static_cast<const uint32_t*>(a.send[rank]);
+    for (size_t j = first; j < a.count; j += stride) {
+      const uint32_t x = src[j];
+      for (int p = 0; p < n; ++p) static_cast<uint32_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
+    }
+  } else {
+    const uint16_t* src = static_cast<const uint16_t*>(a.send[rank]);
+    for (size_t j = first; j < a.count; j += stride) {
+      const uint16_t x = src[j];
+      for (int p = 0; p < n; ++p) static_cast<uint16_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
+    }
+  }
+}
+
+// ------------------------------------------------------------- kernel tables
+enum KernelKind { kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3 };
+
+// Kernel of `kind` for element type T and n ranks (compile-time N for
+// 1..8 and 16, a runtime-N instance otherwise).
+template <typename T>
+const void* reduce_kernel(int kind, int n);
+
+const void* allgather_kernel(int n);
+
+}  // namespace dcc

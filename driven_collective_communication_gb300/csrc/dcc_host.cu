@@ -1,0 +1,704 @@
+// dcc_host.cu -- host side of libdcc: communicator, buffer registration,
+// channel table, argument checks, algorithm choice and kernel launches.
+//
+// The MSCCL++ README ("Host-Side Communication Proxy") sets up a bootstrap, a
+// Communicator and the connections on the host, then launches kernels; the
+// "Channels" section builds channels on the host and copies them to the GPU.
+// Here one process owns all N virtual ranks of one GPU, so the bootstrap
+// collapses into dcc_comm_create and a "connection" is a channel-table entry.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "collectives.cuh"
+#include "dcc.h"
+#include "dcc_internal.h"
+#include "sync_kernels.cuh"
+
+namespace {
+
+struct Window {
+  char* ptr;
+  size_t bytes;
+};
+
+size_t elem_bytes(dcc_dtype_t t) {
+  switch (t) {
+    case DCC_INT32: case DCC_FP32: return 4;
+    case DCC_FP16: case DCC_BF16: return 2;
+    default: return 0;
+  }
+}
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v && *v && std::strcmp(v, "0") != 0;
+}
+
+// Messages at or below this many bytes per rank run one-shot under AUTO.
+// Measured crossover on GB300 (see the tuning notes of this repository).
+constexpr size_t kDefaultOneShotMaxBytes = 0;
+
+}  // namespace
+
+struct dcc_comm {
+  int n = 0;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<Window> win[DCC_MAX_RANKS][3];
+  bool chan[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
+  bool table_dirty = true;
+  dcc::DevChannel h_table[DCC_MAX_RANKS * DCC_MAX_RANKS] = {};
+  dcc::DevChannel* d_table = nullptr;
+  unsigned long long* d_block = nullptr;  // sem | expect | status
+  dcc::DevComm dev{};
+  int blocks_override = 0;
+  size_t one_shot_max[4] = {kDefaultOneShotMaxBytes, kDefaultOneShotMaxBytes,
+                            kDefaultOneShotMaxBytes, kDefaultOneShotMaxBytes};
+  int forced_algo = -1;  // DCC_ALGO environment override of AUTO
+  int sticky = DCC_OK;
+  int err_rank = -1, err_peer = -1, err_block = -1;
+  bool log = false;
+};
+
+namespace {
+
+// Makes the communicator's device current for the scope of a call.
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceScope() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+};
+
+int max_active_per_sm(const void* fn, int threads) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(fn);
+  if (it != cache.end()) return it->second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cache[fn] = nb;
+  return nb;
+}
+
+bool in_window(const dcc_comm* c, int rank, int kind, const void* p, size_t bytes) {
+  const char* q = static_cast<const char*>(p);
+  for (const Window& w : c->win[rank][kind])
+    if (q >= w.ptr && bytes <= w.bytes && (size_t)(q - w.ptr) <= w.bytes - bytes) return true;
+  return false;
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return an && bn && x < y + bn && y < x + an;
+}
+
+// Checks the send/recv arrays of a collective.  inplace_ok: send[r] == recv[r]
+// (same byte count) is allowed.  Reports whether any rank is in place.
+int check_buffers(const dcc_comm* c, void* const* send, size_t send_bytes, void* const* recv,
+                  size_t recv_bytes, bool inplace_ok, bool* any_inplace) {
+  if (!send || !recv) return DCC_ERR_INVALID_ARG;
+  *any_inplace = false;
+  for (int r = 0; r < c->n; ++r) {
+    if (!send[r] || !recv[r]) return DCC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(send[r]) | reinterpret_cast<uintptr_t>(recv[r])) & 15u)
+      return DCC_ERR_MISALIGNED;
+    if (!in_window(c, r, DCC_BUF_INPUT, send[r], send_bytes) &&
+        !in_window(c, r, DCC_BUF_OUTPUT, send[r], send_bytes))
+      return DCC_ERR_NOT_REGISTERED;
+    if (!in_window(c, r, DCC_BUF_INPUT, recv[r], recv_bytes) &&
+        !in_window(c, r, DCC_BUF_OUTPUT, recv[r], recv_bytes))
+      return DCC_ERR_NOT_REGISTERED;
+  }
+  for (int r = 0; r < c->n; ++r) {
+    for (int p = 0; p < c->n; ++p) {
+      if (overlaps(recv[r], recv_bytes, send[p], send_bytes)) {
+        const bool same = r == p && recv[r] == send[r] && send_bytes == recv_bytes;
+        if (!(inplace_ok && same)) return DCC_ERR_INVALID_ARG;
+        *any_inplace = true;
+      }
+      if (p != r && overlaps(recv[r], recv_bytes, recv[p], recv_bytes)) return DCC_ERR_INVALID_ARG;
+    }
+  }
+  return DCC_OK;
+}
+
+int check_channels_all_pairs(const dcc_comm* c) {
+  for (int r = 0; r < c->n; ++r)
+    for (int p = 0; p < c->n; ++p)
+      if (r != p && !c->chan[r][p]) return DCC_ERR_NO_CHANNEL;
+  return DCC_OK;
+}
+
+void shard_of(size_t count, int n, int rank, size_t eb, size_t* b, size_t* e) {
+  const size_t vw = 16 / eb;
+  const size_t nvec = count / vw;
+  const size_t per = nvec / (size_t)n;
+  *b = per * (size_t)rank * vw;
+  *e = (rank == n - 1) ? count : per * (size_t)(rank + 1) * vw;
+}
+
+int upload_table(dcc_comm* c, cudaStream_t s) {
+  if (!c->table_dirty) return DCC_OK;
+  for (int a = 0; a < c->n; ++a) {
+    for (int b = 0; b < c->n; ++b) {
+      dcc::DevChannel& d = c->h_table[a * DCC_MAX_RANKS + b];
+      std::memset(&d, 0, sizeof d);
+      if (!c->chan[a][b]) continue;
+      d.connected = 1;
+      auto first = [&](int rank, int kind, char** p, size_t* bytes) {
+        if (!c->win[rank][kind].empty()) {
+          *p = c->win[rank][kind][0].ptr;
+          *bytes = c->win[rank][kind][0].bytes;
+        }
+      };
+      first(a, DCC_BUF_INPUT, &d.local_in, &d.local_in_bytes);
+      first(a, DCC_BUF_OUTPUT, &d.local_out, &d.local_out_bytes);
+      first(b, DCC_BUF_INPUT, &d.remote_in, &d.remote_in_bytes);
+      first(b, DCC_BUF_OUTPUT, &d.remote_out, &d.remote_out_bytes);
+    }
+  }
+  if (cudaMemcpyAsync(c->d_table, c->h_table, sizeof(c->h_table), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return DCC_ERR_CUDA;
+  // the host copy must not change before the transfer has read it
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DCC_ERR_CUDA;
+  c->table_dirty = false;
+  return DCC_OK;
+}
+
+int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  return DCC_OK;
+}
+
+const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
+  switch (t) {
+    case DCC_INT32: return dcc::reduce_kernel<int32_t>(kind, n);
+    case DCC_FP32: return dcc::reduce_kernel<float>(kind, n);
+    case DCC_FP16: return dcc::reduce_kernel<__half>(kind, n);
+    case DCC_BF16: return dcc::reduce_kernel<__nv_bfloat16>(kind, n);
+    default: return nullptr;
+  }
+}
+
+// CTAs per rank: enough for one vector per thread, at most one full wave of
+// the GPU (co-residency is required when the kernel waits), at most
+// DCC_MAX_BLOCKS_PER_RANK (the semaphore slots).
+int pick_blocks(const dcc_comm* c, const void* fn, int threads, size_t work_vecs_per_rank,
+                int* blocks) {
+  const int per_sm = max_active_per_sm(fn, threads);
+  if (per_sm < 1) return DCC_ERR_LAUNCH;
+  int bmax = per_sm * c->num_sms / c->n;
+  if (bmax < 1) return DCC_ERR_LAUNCH;
+  if (bmax > DCC_MAX_BLOCKS_PER_RANK) bmax = DCC_MAX_BLOCKS_PER_RANK;
+  size_t want = c->blocks_override > 0 ? (size_t)c->blocks_override
+                                       : (work_vecs_per_rank + threads - 1) / threads;
+  if (want < 1) want = 1;
+  *blocks = want > (size_t)bmax ? bmax : (int)want;
+  return DCC_OK;
+}
+
+dcc_algo_t resolve_algo(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a) {
+  if (a != DCC_ALGO_AUTO) return a;
+  if (c->forced_algo > 0) return (dcc_algo_t)c->forced_algo;
+  return count * elem_bytes(t) <= c->one_shot_max[t] ? DCC_ALGO_ONE_SHOT : DCC_ALGO_TWO_SHOT;
+}
+
+dcc::DevComm dev_view(const dcc_comm* c) { return c->dev; }
+
+struct Shape {
+  const void* fn;
+  int blocks;
+  int threads;
+  bool cooperative;
+};
+
+int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t algo, bool inplace,
+                    Shape* sh) {
+  const size_t vw = 16 / elem_bytes(t);
+  const size_t nvec = count / vw;
+  int kind;
+  size_t work;
+  switch (algo) {
+    case DCC_ALGO_ONE_SHOT: kind = dcc::kOneShot; work = nvec; break;
+    case DCC_ALGO_TWO_SHOT: kind = dcc::kTwoShot; work = nvec / c->n + 1; break;
+    case DCC_ALGO_TWO_SHOT_SCRATCH: kind = dcc::kTwoShotScratch; work = nvec / c->n + 1; break;
+    default: return DCC_ERR_INVALID_ARG;
+  }
+  sh->fn = reduce_kernel_for(t, kind, c->n);
+  if (!sh->fn) return DCC_ERR_INVALID_ARG;
+  sh->threads = dcc::kThreads;
+  sh->cooperative = (algo == DCC_ALGO_ONE_SHOT && inplace && c->n > 1) ||
+                    (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1);
+  if (algo == DCC_ALGO_ONE_SHOT && inplace) work = (nvec + dcc::kInplaceUnroll - 1) / dcc::kInplaceUnroll;
+  return pick_blocks(c, sh->fn, sh->threads, work, &sh->blocks);
+}
+
+int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t count,
+                     dcc_dtype_t t, dcc_algo_t a, cudaStream_t s) {
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (a < DCC_ALGO_AUTO || a > DCC_ALGO_TWO_SHOT_SCRATCH) return DCC_ERR_INVALID_ARG;
+  if (count == 0) return DCC_OK;
+  const size_t bytes = count * elem_bytes(t);
+  if (bytes / elem_bytes(t) != count) return DCC_ERR_INVALID_ARG;
+  bool inplace = false;
+  int rc = check_buffers(c, send, bytes, recv, bytes, true, &inplace);
+  if (rc != DCC_OK) return rc;
+  rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  const dcc_algo_t algo = resolve_algo(c, count, t, a);
+
+  dcc::CollArgs args{};
+  for (int r = 0; r < c->n; ++r) {
+    args.send[r] = send[r];
+    args.recv[r] = recv[r];
+  }
+  args.count = count;
+  args.inplace = inplace ? 1 : 0;
+  if (algo == DCC_ALGO_TWO_SHOT_SCRATCH) {
+    for (int r = 0; r < c->n; ++r) {
+      size_t b, e;
+      shard_of(count, c->n, r, elem_bytes(t), &b, &e);
+      const size_t need = (e - b) * elem_bytes(t);
+      if (c->win[r][DCC_BUF_SCRATCH].empty()) return DCC_ERR_NOT_REGISTERED;
+      const Window& w = c->win[r][DCC_BUF_SCRATCH][0];
+      if (w.bytes < need) return DCC_ERR_NOT_REGISTERED;
+      for (int p = 0; p < c->n; ++p)
+        if (overlaps(w.ptr, need, send[p], bytes) || overlaps(w.ptr, need, recv[p], bytes))
+          return DCC_ERR_INVALID_ARG;
+      args.scratch[r] = w.ptr;
+    }
+  }
+  Shape sh;
+  rc = allreduce_shape(c, count, t, algo, inplace, &sh);
+  if (rc != DCC_OK) return rc;
+  args.blocks = sh.blocks;
+  if (c->log)
+    std::fprintf(stderr, "dcc_allreduce: n=%d count=%zu dtype=%d algo=%d inplace=%d blocks/rank=%d\n",
+                 c->n, count, (int)t, (int)algo, (int)inplace, sh.blocks);
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &args};
+  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative, kargs, s);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* dcc_error_string(int code) {
+  switch (code) {
+    case DCC_OK: return "DCC_OK";
+    case DCC_ERR_INVALID_ARG: return "DCC_ERR_INVALID_ARG";
+    case DCC_ERR_NOT_REGISTERED: return "DCC_ERR_NOT_REGISTERED";
+    case DCC_ERR_MISALIGNED: return "DCC_ERR_MISALIGNED";
+    case DCC_ERR_NO_CHANNEL: return "DCC_ERR_NO_CHANNEL";
+    case DCC_ERR_CUDA: return "DCC_ERR_CUDA";
+    case DCC_ERR_LAUNCH: return "DCC_ERR_LAUNCH";
+    case DCC_ERR_TIMEOUT: return "DCC_ERR_TIMEOUT";
+    case DCC_ERR_UNSUPPORTED: return "DCC_ERR_UNSUPPORTED";
+    default: return "DCC_ERR_UNKNOWN";
+  }
+}
+
+const char* dcc_version(void) { return "dcc 0.1 (sm_103a)"; }
+
+int dcc_shard_range(size_t count, int n_ranks, int rank, size_t eb, size_t* begin, size_t* end) {
+  if (n_ranks < 1 || n_ranks > DCC_MAX_RANKS || rank < 0 || rank >= n_ranks || !begin || !end)
+    return DCC_ERR_INVALID_ARG;
+  if (eb != 2 && eb != 4) return DCC_ERR_INVALID_ARG;
+  shard_of(count, n_ranks, rank, eb, begin, end);
+  return DCC_OK;
+}
+
+int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
+  if (!out || n_ranks < 1 || n_ranks > DCC_MAX_RANKS) return DCC_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  dcc_comm* c = new dcc_comm();
+  c->n = n_ranks;
+  c->device = dev;
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return DCC_ERR_CUDA;
+  }
+  const size_t sem_words = dcc::kSemSlots * dcc::kSemWords;
+  const size_t words = sem_words + dcc::kSemSlots + 32;  // sem | expect | status (padded)
+  if (cudaMalloc(&c->d_block, words * sizeof(unsigned long long)) != cudaSuccess ||
+      cudaMalloc(&c->d_table, sizeof(c->h_table)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(c->d_block);
+    delete c;
+    return DCC_ERR_CUDA;
+  }
+  if (cudaMemset(c->d_block, 0, words * sizeof(unsigned long long)) != cudaSuccess ||
+      cudaMemset(c->d_table, 0, sizeof(c->h_table)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(c->d_block);
+    cudaFree(c->d_table);
+    delete c;
+    return DCC_ERR_CUDA;
+  }
+  c->dev.n = n_ranks;
+  c->dev.skip_signal_rank = -1;
+  c->dev.timeout_ns = 2000000ull * 1000ull;
+  if (const char* v = std::getenv("DCC_WAIT_TIMEOUT_US")) {
+    const unsigned long long us = std::strtoull(v, nullptr, 10);
+    if (us > 0) c->dev.timeout_ns = us * 1000ull;
+  }
+  if (const char* v = std::getenv("DCC_BLOCKS_PER_RANK")) c->blocks_override = std::atoi(v);
+  if (const char* v = std::getenv("DCC_ALGO")) {
+    if (!std::strcmp(v, "one_shot")) c->forced_algo = DCC_ALGO_ONE_SHOT;
+    else if (!std::strcmp(v, "two_shot")) c->forced_algo = DCC_ALGO_TWO_SHOT;
+    else if (!std::strcmp(v, "two_shot_scratch")) c->forced_algo = DCC_ALGO_TWO_SHOT_SCRATCH;
+  }
+  c->log = env_flag("DCC_LOG");
+  c->dev.sem = c->d_block;
+  c->dev.expect = c->d_block + sem_words;
+  c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
+  *out = c;
+  return DCC_OK;
+}
+
+int dcc_comm_destroy(dcc_comm_t c) {
+  if (!c) return DCC_OK;
+  int rc = DCC_OK;
+  {
+    DeviceScope ds(c->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) rc = DCC_ERR_CUDA;
+    if (cudaFree(c->d_block) != cudaSuccess) rc = DCC_ERR_CUDA;
+    if (cudaFree(c->d_table) != cudaSuccess) rc = DCC_ERR_CUDA;
+    cudaGetLastError();
+  }
+  delete c;
+  return rc;
+}
+
+int dcc_register_buffer(dcc_comm_t c, int rank, dcc_buf_kind_t kind, void* dev_ptr, size_t bytes) {
+  if (!c || rank < 0 || rank >= c->n || kind < DCC_BUF_INPUT || kind > DCC_BUF_SCRATCH ||
+      !dev_ptr || bytes == 0)
+    return DCC_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(dev_ptr) & 15u) return DCC_ERR_MISALIGNED;
+  auto& v = c->win[rank][kind];
+  for (const Window& w : v)
+    if (w.ptr == dev_ptr && w.bytes == bytes) return DCC_OK;
+  if (v.size() >= DCC_MAX_WINDOWS) return DCC_ERR_INVALID_ARG;
+  v.push_back(Window{static_cast<char*>(dev_ptr), bytes});
+  c->table_dirty = true;
+  return DCC_OK;
+}
+
+int dcc_memory_channel_make(dcc_comm_t c, int src, int dst) {
+  if (!c || src < 0 || dst < 0 || src >= c->n || dst >= c->n || src == dst)
+    return DCC_ERR_INVALID_ARG;
+  c->chan[src][dst] = true;
+  c->table_dirty = true;
+  return DCC_OK;
+}
+
+int dcc_allreduce(dcc_comm_t c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
+                  dcc_algo_t a, dcc_stream_t s) {
+  if (!c) return DCC_ERR_INVALID_ARG;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  return allreduce_launch(c, send, recv, count, t, a, static_cast<cudaStream_t>(s));
+}
+
+int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* const* host_recv,
+                            void* const* dev_send, void* const* dev_recv, size_t count,
+                            dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s) {
+  if (!c || !host_send || !host_recv) return DCC_ERR_INVALID_ARG;
+  if (elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (count == 0) return DCC_OK;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  const size_t bytes = count * elem_bytes(t);
+  bool inplace = false;
+  int rc = check_buffers(c, dev_send, bytes, dev_recv, bytes, true, &inplace);
+  if (rc != DCC_OK) return rc;
+  for (int r = 0; r < c->n; ++r)
+    if (!host_send[r] || !host_recv[r]) return DCC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  for (int r = 0; r < c->n; ++r)
+    if (cudaMemcpyAsync(dev_send[r], host_send[r], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return DCC_ERR_CUDA;
+  rc = allreduce_launch(c, dev_send, dev_recv, count, t, a, st);
+  if (rc != DCC_OK) return rc;
+  for (int r = 0; r < c->n; ++r)
+    if (cudaMemcpyAsync(host_recv[r], dev_recv[r], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return DCC_ERR_CUDA;
+  return DCC_OK;
+}
+
+int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
+                       dcc_dtype_t t, dcc_stream_t s) {
+  if (!c || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (recv_count == 0) return DCC_OK;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  const size_t rb = recv_count * elem_bytes(t);
+  const size_t sb = rb * (size_t)c->n;
+  if (rb / elem_bytes(t) != recv_count || sb / (size_t)c->n != rb) return DCC_ERR_INVALID_ARG;
+  bool inplace = false;
+  int rc = check_buffers(c, send, sb, recv, rb, false, &inplace);
+  if (rc != DCC_OK) return rc;
+  rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  dcc::CollArgs args{};
+  for (int r = 0; r < c->n; ++r) {
+    args.send[r] = send[r];
+    args.recv[r] = recv[r];
+  }
+  args.count = recv_count;
+  const void* fn = reduce_kernel_for(t, dcc::kReduceScatter, c->n);
+  const size_t vw = 16 / elem_bytes(t);
+  rc = pick_blocks(c, fn, dcc::kThreads, (recv_count + vw - 1) / vw, &args.blocks);
+  if (rc != DCC_OK) return rc;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &args};
+  return launch(fn, args.blocks * c->n, dcc::kThreads, false, kargs, static_cast<cudaStream_t>(s));
+}
+
+int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
+                  dcc_dtype_t t, dcc_stream_t s) {
+  if (!c || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (send_count == 0) return DCC_OK;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  const size_t sb = send_count * elem_bytes(t);
+  const size_t rb = sb * (size_t)c->n;
+  if (sb / elem_bytes(t) != send_count || rb / (size_t)c->n != sb) return DCC_ERR_INVALID_ARG;
+  bool inplace = false;
+  int rc = check_buffers(c, send, sb, recv, rb, false, &inplace);
+  if (rc != DCC_OK) return rc;
+  rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  dcc::CollArgs args{};
+  for (int r = 0; r < c->n; ++r) {
+    args.send[r] = send[r];
+    args.recv[r] = recv[r];
+  }
+  args.count = send_count;
+  int eb = (int)elem_bytes(t);
+  const void* fn = dcc::allgather_kernel(c->n);
+  rc = pick_blocks(c, fn, dcc::kThreads, (sb + 15) / 16, &args.blocks);
+  if (rc != DCC_OK) return rc;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &args, &eb};
+  return launch(fn, args.blocks * c->n, dcc::kThreads, false, kargs, static_cast<cudaStream_t>(s));
+}
+
+int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {
+  if (!c || iters < 0) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  for (int r = 0; r < c->n && c->n > 1; ++r)
+    if (!c->chan[r][(r + 1) % c->n]) return DCC_ERR_NO_CHANNEL;
+  if (iters == 0) return DCC_OK;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &iters};
+  return launch(dcc::ring_barrier_kernel(), c->n, 32, true, kargs, static_cast<cudaStream_t>(s));
+}
+
+int dcc_comm_check(dcc_comm_t c, dcc_stream_t s) {
+  if (!c) return DCC_ERR_INVALID_ARG;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(s)) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  unsigned long long st = 0;
+  if (cudaMemcpy(&st, c->dev.status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  if (st != 0 && c->sticky == DCC_OK) {
+    c->sticky = DCC_ERR_TIMEOUT;
+    c->err_rank = (int)((st >> 8) & 0xFF);
+    c->err_peer = (int)((st >> 16) & 0xFF);
+    c->err_block = (int)((st >> 24) & 0xFFFF);
+  }
+  return c->sticky;
+}
+
+int dcc_comm_error_detail(dcc_comm_t c, int* rank, int* peer, int* block) {
+  if (!c || c->sticky == DCC_OK) return DCC_ERR_INVALID_ARG;
+  if (rank) *rank = c->err_rank;
+  if (peer) *peer = c->err_peer;
+  if (block) *block = c->err_block;
+  return DCC_OK;
+}
+
+int dcc_channel_put(dcc_comm_t c, int src, int dst, size_t remote_off, size_t local_off,
+                    size_t bytes, int signal, dcc_stream_t s) {
+  if (!c || src < 0 || dst < 0 || src >= c->n || dst >= c->n || src == dst)
+    return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (!c->chan[src][dst] || (signal && !c->chan[dst][src])) return DCC_ERR_NO_CHANNEL;
+  if ((remote_off | local_off | bytes) & 15u) return DCC_ERR_MISALIGNED;
+  if (c->win[src][DCC_BUF_INPUT].empty() || c->win[dst][DCC_BUF_OUTPUT].empty())
+    return DCC_ERR_NOT_REGISTERED;
+  const Window& li = c->win[src][DCC_BUF_INPUT][0];
+  const Window& ro = c->win[dst][DCC_BUF_OUTPUT][0];
+  if (local_off > li.bytes || bytes > li.bytes - local_off || remote_off > ro.bytes ||
+      bytes > ro.bytes - remote_off)
+    return DCC_ERR_NOT_REGISTERED;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  int rc = upload_table(c, st);
+  if (rc != DCC_OK) return rc;
+  dcc::PrimArgs pa{src, dst, remote_off, local_off, bytes, signal ? 1 : 0, c->d_table};
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &pa};
+  return launch(dcc::channel_put_kernel(), 2, 256, true, kargs, st);
+}
+
+int dcc_channel_get(dcc_comm_t c, int src, int dst, size_t remote_off, size_t local_off,
+                    size_t bytes, dcc_stream_t s) {
+  if (!c || src < 0 || dst < 0 || src >= c->n || dst >= c->n || src == dst)
+    return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (!c->chan[src][dst]) return DCC_ERR_NO_CHANNEL;
+  if ((remote_off | local_off | bytes) & 15u) return DCC_ERR_MISALIGNED;
+  if (c->win[src][DCC_BUF_OUTPUT].empty() || c->win[dst][DCC_BUF_INPUT].empty())
+    return DCC_ERR_NOT_REGISTERED;
+  const Window& lo = c->win[src][DCC_BUF_OUTPUT][0];
+  const Window& ri = c->win[dst][DCC_BUF_INPUT][0];
+  if (local_off > lo.bytes || bytes > lo.bytes - local_off || remote_off > ri.bytes ||
+      bytes > ri.bytes - remote_off)
+    return DCC_ERR_NOT_REGISTERED;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  int rc = upload_table(c, st);
+  if (rc != DCC_OK) return rc;
+  dcc::PrimArgs pa{src, dst, remote_off, local_off, bytes, 0, c->d_table};
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &pa};
+  return launch(dcc::channel_get_kernel(), 1, 256, false, kargs, st);
+}
+
+int dcc_comm_read_semaphores(dcc_comm_t c, int block, uint64_t* inbound, uint64_t* expected,
+                             dcc_stream_t s) {
+  if (!c || block < 0 || block >= DCC_MAX_BLOCKS_PER_RANK) return DCC_ERR_INVALID_ARG;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(s)) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  for (int d = 0; d < c->n; ++d) {
+    for (int q = 0; q < c->n; ++q) {
+      const size_t slot = dcc::sem_slot(d, q, block);
+      if (inbound && cudaMemcpy(&inbound[d * c->n + q], c->dev.sem + slot * dcc::kSemWords,
+                                sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DCC_ERR_CUDA;
+      if (expected && cudaMemcpy(&expected[d * c->n + q], c->dev.expect + slot, sizeof(uint64_t),
+                                 cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DCC_ERR_CUDA;
+    }
+  }
+  return DCC_OK;
+}
+
+int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us) {
+  if (!c || us == 0 || us > 3600ull * 1000000ull) return DCC_ERR_INVALID_ARG;
+  c->dev.timeout_ns = us * 1000ull;
+  return DCC_OK;
+}
+
+int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks) {
+  if (!c || blocks < 0 || blocks > DCC_MAX_BLOCKS_PER_RANK) return DCC_ERR_INVALID_ARG;
+  c->blocks_override = blocks;
+  return DCC_OK;
+}
+
+int dcc_set_algo_threshold(dcc_comm_t c, dcc_dtype_t t, size_t bytes) {
+  if (!c || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  c->one_shot_max[t] = bytes;
+  return DCC_OK;
+}
+
+int dcc_select_algo(dcc_comm_t c, size_t count, dcc_dtype_t t, dcc_algo_t* out) {
+  if (!c || !out || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  *out = resolve_algo(c, count, t, DCC_ALGO_AUTO);
+  return DCC_OK;
+}
+
+int dcc_debug_skip_signal(dcc_comm_t c, int rank) {
+  if (!c || rank < -1 || rank >= c->n) return DCC_ERR_INVALID_ARG;
+  c->dev.skip_signal_rank = rank;
+  return DCC_OK;
+}
+
+int dcc_launch_shape(dcc_comm_t c, size_t count, dcc_dtype_t t, dcc_algo_t a, int* blocks,
+                     int* threads) {
+  if (!c || !blocks || !threads || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  *blocks = 0;
+  *threads = 0;
+  if (count == 0) return DCC_OK;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  Shape sh;
+  const int rc = allreduce_shape(c, count, t, resolve_algo(c, count, t, a), false, &sh);
+  if (rc != DCC_OK) return rc;
+  *blocks = sh.blocks;
+  *threads = sh.threads;
+  return DCC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// dcc_internal.h -- structures passed from the host library to the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "dcc.h"
+
+namespace dcc {
+
+// One inbound semaphore per (dst rank, src rank, block slot), each in its own
+// 32-byte sector so that no two counters (and no data) share a sector.
+constexpr int kSemWords = 4;
+
+__host__ __device__ inline size_t sem_slot(int dst, int src, int blk) {
+  return ((size_t)dst * DCC_MAX_RANKS + (size_t)src) * DCC_MAX_BLOCKS_PER_RANK + (size_t)blk;
+}
+constexpr size_t kSemSlots = (size_t)DCC_MAX_RANKS * DCC_MAX_RANKS * DCC_MAX_BLOCKS_PER_RANK;
+
+// Packed first-failure record written by a device wait that gave up.
+//   bits 0..7 code (1 = timeout), 8..15 rank, 16..23 peer, 24..39 block.
+constexpr unsigned long long kStatusTimeout = 1ull;
+__host__ __device__ inline unsigned long long pack_status(unsigned long long code, int rank,
+                                                          int peer, int blk) {
+  return code | ((unsigned long long)(rank & 0xFF) << 8) |
+         ((unsigned long long)(peer & 0xFF) << 16) | ((unsigned long long)(blk & 0xFFFF) << 24);
+}
+
+// Device view of a communicator, passed by value to every kernel.
+struct DevComm {
+  int n;                        // virtual ranks
+  int skip_signal_rank;         // test knob: this rank sends no signals (-1 = none)
+  unsigned long long timeout_ns;
+  unsigned long long* sem;      // kSemSlots counters, kSemWords apart
+  unsigned long long* expect;   // kSemSlots waiter-side completed-wait counts
+  unsigned long long* status;   // first failure, 0 = none
+};
+
+// A channel as the host builds it (one per ordered pair src -> dst) and copies
+// to the device: the local and remote windows it binds.
+struct DevChannel {
+  char* local_in;
+  char* local_out;
+  char* remote_in;
+  char* remote_out;
+  size_t local_in_bytes, local_out_bytes, remote_in_bytes, remote_out_bytes;
+  int connected;
+  int pad;
+};
+
+// Per-call arguments of a collective kernel.
+struct CollArgs {
+  void* send[DCC_MAX_RANKS];
+  void* recv[DCC_MAX_RANKS];
+  void* scratch[DCC_MAX_RANKS];
+  size_t count;   // elements: per-rank buffer (AllReduce), recv_count (RS), send_count (AG)
+  int blocks;     // CTAs per rank
+  int inplace;    // some rank has send == recv
+};
+
+// Arguments of the primitive (put/get) kernels.
+struct PrimArgs {
+  int src, dst;
+  size_t remote_off, local_off, bytes;
+  int signal;
+  const DevChannel* table;  // device channel table, [src * DCC_MAX_RANKS + dst]
+};
+
+}  // namespace dcc

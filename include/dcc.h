@@ -1,0 +1,234 @@
+/*
+ * dcc.h -- C ABI of libdcc, GB300-native virtual-rank collectives.
+ *
+ * N "virtual ranks" live on one GPU: rank r owns its own input, output and
+ * scratch allocations in HBM, and in every collective kernel rank r is a group
+ * of CTAs.  Ranks talk through MemoryChannels -- the memory-mapped channel of
+ * the MSCCL++ README ("PortChannel and MemoryChannel"): GPU threads read and
+ * write the peer's memory directly, and synchronise with signal/flush/wait
+ * ("On-GPU Communication Interfaces: Channels").  Channels are built on the
+ * host and copied to the device before the first launch, as that section
+ * describes.  The collectives are the standard sum collectives of the MSCCL++
+ * abstract, point (3) ("a library of efficient algorithms implementing the
+ * standard collective API"); AllReduce is the one the project summary singles
+ * out ("Highlighted Details": tensor-parallel LLM serving).
+ *
+ * Conventions for every function below:
+ *  - Return value: DCC_OK (0) or a negative dcc_result_t.  dcc_error_string()
+ *    names it.  A host-side error returns before anything is launched.
+ *  - Pointers named dev_* / send / recv are DEVICE addresses on the GPU the
+ *    communicator was created on; the arrays that hold them (send[], recv[])
+ *    are HOST arrays of n_ranks entries.  Pointers named host_* are host
+ *    addresses (pinned memory recommended).
+ *  - Ownership: the caller owns every data buffer and every stream.  The
+ *    library owns only what dcc_comm_create allocates (semaphores, waiter
+ *    counters, the channel table, the status word) and frees it in
+ *    dcc_comm_destroy.  No data-path call allocates memory.
+ *  - Streams: dcc_stream_t is a cudaStream_t passed as an opaque pointer;
+ *    NULL is the legacy default stream.  Collectives are asynchronous on it.
+ *  - Device failures (a wait that gave up) do not abort the process: the
+ *    kernel records them in a status word and returns; dcc_comm_check reads it.
+ *  - Layout: every buffer is a dense 1-D array of `count` elements of the
+ *    given type, native (little-endian) storage; bf16 and fp16 are raw 16-bit
+ *    IEEE patterns.  Data pointers must be 16-byte aligned.
+ *  - Threading: a communicator is not thread-safe; serialise calls on it.
+ */
+#ifndef DCC_H
+#define DCC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DCC_MAX_RANKS 16            /* virtual ranks per communicator */
+#define DCC_MAX_BLOCKS_PER_RANK 128 /* CTAs per rank in one collective kernel */
+#define DCC_MAX_WINDOWS 8           /* registered windows per (rank, kind) */
+
+typedef struct dcc_comm* dcc_comm_t;
+typedef void* dcc_stream_t; /* cudaStream_t */
+
+typedef enum {
+  DCC_OK = 0,
+  DCC_ERR_INVALID_ARG = -1,    /* bad rank, count, enum value, NULL, overlap */
+  DCC_ERR_NOT_REGISTERED = -2, /* a data range lies outside the rank's windows */
+  DCC_ERR_MISALIGNED = -3,     /* a data pointer is not 16-byte aligned */
+  DCC_ERR_NO_CHANNEL = -4,     /* a (src, dst) channel the call needs was never made */
+  DCC_ERR_CUDA = -5,           /* a CUDA runtime call failed */
+  DCC_ERR_LAUNCH = -6,         /* the grid cannot be co-resident on this GPU */
+  DCC_ERR_TIMEOUT = -7,        /* a device wait gave up (sticky for the communicator) */
+  DCC_ERR_UNSUPPORTED = -8     /* valid request this build does not implement */
+} dcc_result_t;
+
+typedef enum { DCC_INT32 = 0, DCC_FP32 = 1, DCC_FP16 = 2, DCC_BF16 = 3 } dcc_dtype_t;
+
+typedef enum {
+  DCC_ALGO_AUTO = 0,   /* pick by message size from the measured crossover table */
+  DCC_ALGO_ONE_SHOT = 1, /* every rank gets all N inputs and reduces its whole output */
+  DCC_ALGO_TWO_SHOT = 2, /* rank r reduces shard r, then puts it into all N outputs */
+  DCC_ALGO_TWO_SHOT_SCRATCH = 3 /* rank r reduces shard r into its scratch, signal/wait,
+                                   then every rank gets all shards from the scratches */
+} dcc_algo_t;
+
+typedef enum { DCC_BUF_INPUT = 0, DCC_BUF_OUTPUT = 1, DCC_BUF_SCRATCH = 2 } dcc_buf_kind_t;
+
+/* ------------------------------------------------------------------------ */
+/* Set-up: the host-side objects of the README's "Host-Side Communication   */
+/* Proxy" example (bootstrap + Communicator + connection set-up), collapsed */
+/* into one process that owns all N virtual ranks.                          */
+/* ------------------------------------------------------------------------ */
+
+/* Create a communicator of n_ranks (1..DCC_MAX_RANKS) virtual ranks on the
+ * CUDA device that is current on the calling thread.  Allocates and zeroes the
+ * semaphore block, waiter counters, channel table and status word (the only
+ * device memory the library owns).  *out receives the handle.  Errors:
+ * INVALID_ARG (n_ranks out of range, out NULL; checked before any CUDA call),
+ * CUDA (no device / allocation failed). */
+int dcc_comm_create(int n_ranks, dcc_comm_t* out);
+
+/* Synchronise the device, free everything dcc_comm_create allocated, and free
+ * the handle.  NULL is a no-op. */
+int dcc_comm_destroy(dcc_comm_t c);
+
+/* Register [dev_ptr, dev_ptr + bytes) as a window of `kind` for `rank`.  Every
+ * data range a collective touches must lie inside one window of that rank
+ * (INPUT or OUTPUT kind for send/recv buffers; SCRATCH for the two-shot
+ * scratch algorithm).  Up to DCC_MAX_WINDOWS per (rank, kind).  The first
+ * INPUT and OUTPUT windows of a rank are the local/remote memory its channels
+ * bind (see dcc_channel_put/get).  Errors: INVALID_ARG (rank, kind, NULL,
+ * bytes == 0, table full), MISALIGNED (dev_ptr not 16-byte aligned). */
+int dcc_register_buffer(dcc_comm_t c, int rank, dcc_buf_kind_t kind, void* dev_ptr,
+                        size_t bytes);
+
+/* Make the MemoryChannel from src_rank to dst_rank (idempotent): src may then
+ * put into / get from dst's memory and signal dst's inbound semaphore for
+ * src; dst waits on it through its own channel to src.  A collective over N
+ * ranks needs the channel for every ordered pair r != p; the ring barrier
+ * needs r -> (r+1) mod N.  Channels are uploaded to the device lazily before
+ * the next launch.  Errors: INVALID_ARG (rank out of range, src == dst). */
+int dcc_memory_channel_make(dcc_comm_t c, int src_rank, int dst_rank);
+
+/* ------------------------------------------------------------------------ */
+/* Collectives (sum).  Per element, ranks are added in order 0..N-1 starting */
+/* from rank 0's value; fp32/fp16/bf16 accumulate in fp32 and round once    */
+/* (round-to-nearest-even) to the output type; int32 wraps.  Results are    */
+/* therefore the same bits for every algorithm and every launch shape.      */
+/* ------------------------------------------------------------------------ */
+
+/* AllReduce: recv[r][i] = sum_p send[p][i] for every rank r, i < count.
+ * send[r] == recv[r] is in-place for rank r; any other overlap between the
+ * ranges is rejected.  algo selects the schedule (AUTO uses the crossover
+ * table, see dcc_select_algo).  count == 0 is a no-op.  Errors: INVALID_ARG,
+ * NOT_REGISTERED, MISALIGNED, NO_CHANNEL, LAUNCH, CUDA, TIMEOUT (a previous
+ * device failure on this communicator). */
+int dcc_allreduce(dcc_comm_t c, void* const* send, void* const* recv, size_t count,
+                  dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);
+
+/* ReduceScatter: recv[r][j] = sum_p send[p][r*recv_count + j], j < recv_count.
+ * send[p] holds N*recv_count elements.  Ranges must not overlap. */
+int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
+                       dcc_dtype_t t, dcc_stream_t s);
+
+/* AllGather: recv[p][q*send_count + j] = send[q][j] for all p, q, j < send_count.
+ * recv[p] holds N*send_count elements.  Ranges must not overlap.  A bit copy:
+ * t only fixes the element size. */
+int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
+                  dcc_dtype_t t, dcc_stream_t s);
+
+/* Host-buffer AllReduce: copies host_send[r] -> dev_send[r] (one
+ * cudaMemcpyAsync per rank), runs dcc_allreduce(dev_send, dev_recv), and
+ * copies dev_recv[r] -> host_recv[r], all asynchronously on s.  The device
+ * buffers follow dcc_allreduce's rules; the host buffers must stay valid until
+ * s has drained. */
+int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* const* host_recv,
+                            void* const* dev_send, void* const* dev_recv, size_t count,
+                            dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);
+
+/* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
+ * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
+ * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One
+ * kernel runs all `iters` (>= 0) iterations. */
+int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s);
+
+/* Synchronise s, read the device status word and return DCC_OK or the first
+ * device failure (DCC_ERR_TIMEOUT).  A failure is sticky: the semaphores are
+ * unbalanced afterwards, so the communicator must be destroyed. */
+int dcc_comm_check(dcc_comm_t c, dcc_stream_t s);
+
+/* After dcc_comm_check returned a failure: the rank, peer and block of the
+ * wait that gave up (any pointer may be NULL).  INVALID_ARG if none. */
+int dcc_comm_error_detail(dcc_comm_t c, int* rank, int* peer, int* block);
+
+/* Name of a dcc_result_t (static storage). */
+const char* dcc_error_string(int code);
+
+/* ------------------------------------------------------------------------ */
+/* MemoryChannel primitives on their own (README, "On-GPU Communication     */
+/* Interfaces: Channels": put copies from local to remote memory; signal,   */
+/* flush, wait synchronise a pair of ranks).  The channel src -> dst binds  */
+/* src's first INPUT window as local source, src's first OUTPUT window as   */
+/* local destination, dst's first INPUT window as remote source and dst's  */
+/* first OUTPUT window as remote destination.                              */
+/* ------------------------------------------------------------------------ */
+
+/* put: dst.OUTPUT[remote_off, +bytes) <- src.INPUT[local_off, +bytes), by one
+ * CTA of warp-cooperative 16-byte vector stores; then, if signal != 0, flush
+ * and signal dst, and dst's CTA waits for that signal before the kernel ends.
+ * Offsets and bytes must be multiples of 16 and inside the windows. */
+int dcc_channel_put(dcc_comm_t c, int src_rank, int dst_rank, size_t remote_off,
+                    size_t local_off, size_t bytes, int signal, dcc_stream_t s);
+
+/* get: src.OUTPUT[local_off, +bytes) <- dst.INPUT[remote_off, +bytes). */
+int dcc_channel_get(dcc_comm_t c, int src_rank, int dst_rank, size_t remote_off,
+                    size_t local_off, size_t bytes, dcc_stream_t s);
+
+/* Copy the semaphore state of block slot `block` to the host: inbound[d*N+s]
+ * = signals rank d has received from rank s; expected[d*N+s] = waits rank d
+ * has completed on rank s.  Each array holds N*N uint64 (NULL to skip).
+ * Synchronises s. */
+int dcc_comm_read_semaphores(dcc_comm_t c, int block, uint64_t* inbound, uint64_t* expected,
+                             dcc_stream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Tuning and test knobs.                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Wait limit of every device-side wait, microseconds (default 2,000,000, or
+ * DCC_WAIT_TIMEOUT_US from the environment at create time). */
+int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us);
+
+/* CTAs per rank for the collectives; 0 = choose by size (default, or
+ * DCC_BLOCKS_PER_RANK from the environment).  Clamped to what fits. */
+int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks);
+
+/* AUTO picks ONE_SHOT for messages of at most `bytes` per rank and TWO_SHOT
+ * above, for this dtype.  Defaults come from the measured crossover. */
+int dcc_set_algo_threshold(dcc_comm_t c, dcc_dtype_t t, size_t bytes);
+
+/* The algorithm AUTO would run for this request (pure host logic). */
+int dcc_select_algo(dcc_comm_t c, size_t count, dcc_dtype_t t, dcc_algo_t* out);
+
+/* Test knob: rank `rank` skips every signal it would send (-1 = off), so its
+ * peers' waits run out and report DCC_ERR_TIMEOUT.  Nothing faults. */
+int dcc_debug_skip_signal(dcc_comm_t c, int rank);
+
+/* Launch shape a collective would use: CTAs per rank and threads per CTA
+ * (0 when no launch is needed).  Pure host logic except the occupancy query. */
+int dcc_launch_shape(dcc_comm_t c, size_t count, dcc_dtype_t t, dcc_algo_t a, int* blocks_per_rank,
+                     int* threads);
+
+/* Two-shot shard of `rank` for `count` elements of `elem_bytes` each over
+ * n_ranks ranks, in elements: [*begin, *end).  Shards are whole 16-byte
+ * vectors; the last rank also takes the remainder.  Pure host logic, no GPU. */
+int dcc_shard_range(size_t count, int n_ranks, int rank, size_t elem_bytes, size_t* begin,
+                    size_t* end);
+
+/* Library version string (static storage). */
+const char* dcc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DCC_H */

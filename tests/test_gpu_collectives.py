@@ -1,0 +1,519 @@
+"""GPU parity of the collectives against the CPU oracle, through the C ABI.
+
+Every floating-point result is compared bit for bit: the kernels keep the
+oracle's rank order and fp32 accumulation, so any correct schedule returns
+the same bits (the tolerance of the method -- 1e-6*N*max|x| for fp32, 1 ulp of
+the output type for fp16/bf16 -- is only needed for other orders and is never
+used here).  int32 is exact by definition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from driven_collective_communication_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+RECIPES = {"fp32": W.C1, "int32": W.C2, "bf16": W.C4, "fp16": W.C5}
+ALGOS = ("one_shot", "two_shot", "two_shot_scratch")
+
+
+@pytest.fixture(scope="module")
+def dcc():
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc as mod
+    torch.cuda.set_device(0)
+    return mod
+
+
+def same(got, expect, dtype):
+    """Bit equality; NaN payloads may differ (only NaN-ness is compared)."""
+    got = np.asarray(got)
+    expect = np.asarray(expect)
+    if dtype == "int32":
+        return np.array_equal(got, expect)
+    wide_g = oracle.to_f32(got, dtype) if dtype != "fp32" else got
+    wide_e = oracle.to_f32(expect, dtype) if dtype != "fp32" else expect
+    ng, ne = np.isnan(wide_g), np.isnan(wide_e)
+    if not np.array_equal(ng, ne):
+        return False
+    return np.array_equal(got[~ng].view(np.uint32 if dtype == "fp32" else np.uint16),
+                          expect[~ne].view(np.uint32 if dtype == "fp32" else np.uint16))
+
+
+class Arena:
+    """Per-rank input/output/scratch buffers registered once; cases use slices."""
+
+    def __init__(self, dcc, n, elems_per_rank, elem_bytes=4):
+        self.dcc = dcc
+        self.n = n
+        self.comm = dcc.Comm(n)
+        nbytes = elems_per_rank * elem_bytes + 4096
+        self.inp = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(n)]
+        self.out = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(n)]
+        self.scr = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(n)]
+        for r in range(n):
+            self.comm.register(r, "input", self.inp[r])
+            self.comm.register(r, "output", self.out[r])
+            self.comm.register(r, "scratch", self.scr[r])
+
+    def view(self, bufs, dtype, count, offset=0):
+        tdt = W.TORCH_DTYPES[dtype]
+        eb = W.ELEM_BYTES[dtype]
+        return [b[offset: offset + count * eb].view(tdt) for b in bufs]
+
+    def close(self):
+        self.comm.close()
+
+
+def run_allreduce(dcc, arena, xs_host, dtype, algo, inplace, offset=0):
+    count = xs_host[0].numel()
+    send = arena.view(arena.inp, dtype, count, offset)
+    for r in range(arena.n):
+        send[r].copy_(xs_host[r])
+    recv = send if inplace else arena.view(arena.out, dtype, count, offset)
+    if not inplace:
+        for r in range(arena.n):
+            recv[r].fill_(0)
+    dcc.dcc_allreduce(arena.comm.handle, send, recv, count, dtype, algo)
+    rc = arena.comm.check()
+    assert rc == dcc.DCC_OK, dcc.dcc_error_string(rc)
+    return [W.to_storage(t) for t in recv]
+
+
+# ---------------------------------------------------------------- small parity sweep
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16])
+def test_allreduce_parity_sweep(dcc, n):
+    """All dtypes x algorithms x in/out-of-place x counts (empty, 1 element,
+    below one vector, ragged, several CTAs' worth + tail) against the oracle."""
+    counts = [1, 5, 8, 16 * n + 3, 3 * 512 * 8 + 5, 70001]
+    arena = Arena(dcc, n, max(counts))
+    try:
+        for dtype, recipe in RECIPES.items():
+            for count in counts:
+                w = W.with_count(recipe, count, n_ranks=n)
+                xs = W.rank_inputs(w)
+                expect = oracle.allreduce([W.to_storage(x) for x in xs], dtype)
+                for algo in ALGOS:
+                    for inplace in (False, True):
+                        outs = run_allreduce(dcc, arena, xs, dtype, algo, inplace)
+                        for r in range(n):
+                            assert same(outs[r], expect, dtype), (dtype, count, algo, inplace, r)
+    finally:
+        arena.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_allreduce_special_values(dcc, dtype):
+    """Raw random bit patterns: subnormals (no flush to zero), signed zeros,
+    infinities, NaNs, overflow of the fp32 sum."""
+    n, count = 8, 4099
+    rng = np.random.default_rng(17)
+    if dtype == "fp32":
+        xs = [torch.from_numpy(rng.integers(0, 2 ** 32, size=count, dtype=np.uint64)
+                               .astype(np.uint32).view(np.float32)) for _ in range(n)]
+    else:
+        xs = [W.from_storage(rng.integers(0, 2 ** 16, size=count, dtype=np.uint64).astype(np.uint16),
+                             dtype) for _ in range(n)]
+    # add a block of pure subnormals and -0.0 columns
+    for r in range(n):
+        if dtype == "fp32":
+            xs[r][:64] = torch.tensor(np.full(64, 1e-45 * (r + 1), np.float32))
+            xs[r][64:128] = -0.0
+        else:
+            sub = np.arange(1, 65, dtype=np.uint16) + r
+            xs[r][:64] = W.from_storage(sub, dtype)
+            xs[r][64:128] = W.from_storage(np.full(64, 0x8000, np.uint16), dtype)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], dtype)
+    arena = Arena(dcc, n, count)
+    try:
+        for algo in ALGOS:
+            for inplace in (False, True):
+                outs = run_allreduce(dcc, arena, xs, dtype, algo, inplace)
+                for r in range(n):
+                    assert same(outs[r], expect, dtype), (algo, inplace, r)
+    finally:
+        arena.close()
+
+
+def test_launch_shape_does_not_change_bits(dcc):
+    """Any number of CTAs per rank returns the same bits (fixed per-element order)."""
+    n, count = 8, 123457
+    w = W.with_count(W.C4, count)
+    xs = W.rank_inputs(w)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
+    arena = Arena(dcc, n, count)
+    try:
+        for blocks in (1, 2, 7, 19, 128):
+            dcc.dcc_set_blocks_per_rank(arena.comm.handle, blocks)
+            for algo in ALGOS:
+                for inplace in (False, True):
+                    outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace)
+                    assert all(same(o, expect, "bf16") for o in outs), (blocks, algo, inplace)
+    finally:
+        arena.close()
+
+
+# ---------------------------------------------------------------- the five workloads
+def test_c1_fp32_n2_one_shot_full(dcc):
+    w = W.C1
+    xs = W.rank_inputs(w)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "fp32")
+    exact = sum(W.to_storage(x).astype(np.int64) for x in xs)
+    assert np.array_equal(expect.astype(np.int64), exact)
+    arena = Arena(dcc, 2, w.count)
+    try:
+        outs = run_allreduce(dcc, arena, xs, "fp32", "one_shot", inplace=False)
+        for o in outs:
+            assert same(o, expect, "fp32")
+    finally:
+        arena.close()
+
+
+def test_c2_int32_n8_inplace_both_algorithms_full(dcc):
+    w = W.C2
+    xs = [x for x in W.rank_inputs(w, device="cuda")]
+    host = [W.to_storage(x) for x in xs]
+    expect = oracle.allreduce(host, "int32", nthreads=16)
+    comm = dcc.Comm(8)
+    try:
+        for algo in ("one_shot", "two_shot"):
+            bufs = [x.clone() for x in xs]
+            comm.register_all("input", bufs)
+            comm.allreduce(bufs, bufs, algo=algo)
+            assert comm.check() == dcc.DCC_OK
+            for b in bufs:
+                assert np.array_equal(W.to_storage(b), expect), algo
+            del bufs
+    finally:
+        comm.close()
+
+
+@pytest.mark.parametrize("tokens", W.C3_TOKENS)
+def test_c3_bf16_decode_sizes(dcc, tokens):
+    w = W.c3(tokens)
+    xs = W.rank_inputs(w)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
+    arena = Arena(dcc, 8, w.count, elem_bytes=2)
+    try:
+        for algo in ALGOS:
+            outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace=False)
+            for o in outs:
+                assert same(o, expect, "bf16"), algo
+    finally:
+        arena.close()
+
+
+def sampled_indices(count, n, k=200000, seed=0):
+    """Random indices plus every shard boundary neighbourhood and the tail."""
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, count, size=k)]
+    for r in range(n + 1):
+        b = (count // n) * r
+        idx.append(np.arange(max(0, b - 9), min(count, b + 9)))
+    idx.append(np.arange(max(0, count - 17), count))
+    return np.unique(np.concatenate(idx))
+
+
+def test_c4_bf16_n8_256MiB_sampled(dcc):
+    """Full size, the launch configuration the benchmark times (AUTO -> two-shot
+    push), checked on sampled elements one by one and by the identical-ranks
+    invariant over every element."""
+    w = W.C4
+    xs = W.rank_inputs(w, device="cuda")
+    recv = [torch.empty_like(x) for x in xs]
+    comm = dcc.Comm(8)
+    try:
+        comm.register_all("input", xs)
+        comm.register_all("output", recv)
+        comm.allreduce(xs, recv, algo="auto")
+        assert comm.check() == dcc.DCC_OK
+        for r in range(1, 8):
+            assert torch.equal(recv[r].view(torch.int16), recv[0].view(torch.int16))
+        idx = sampled_indices(w.count, 8)
+        idx_t = torch.from_numpy(idx).cuda()
+        host = [W.to_storage(x[idx_t]) for x in xs]
+        expect = oracle.allreduce(host, "bf16")  # elementwise: sampled columns
+        assert same(W.to_storage(recv[3][idx_t]), expect, "bf16")
+    finally:
+        comm.close()
+
+
+def test_c5_fp16_reduce_scatter_and_allgather_full(dcc):
+    w = W.C5
+    n = 8
+    xs = W.rank_inputs(w, device="cuda")
+    m = w.count // n
+    rs_out = [torch.empty(m, dtype=torch.float16, device="cuda") for _ in range(n)]
+    ag_out = [torch.empty(w.count, dtype=torch.float16, device="cuda") for _ in range(n)]
+    comm = dcc.Comm(n)
+    try:
+        comm.register_all("input", xs)
+        comm.register_all("output", rs_out)
+        comm.register_all("output", ag_out)
+        comm.reduce_scatter(xs, rs_out)
+        assert comm.check() == dcc.DCC_OK
+        host = [W.to_storage(x) for x in xs]
+        for r in range(n):
+            assert same(W.to_storage(rs_out[r]), oracle.reduce_scatter(host, "fp16", r, m), "fp16"), r
+        comm.allgather(rs_out, ag_out)
+        assert comm.check() == dcc.DCC_OK
+        ag_expect = oracle.allgather([W.to_storage(t) for t in rs_out], "fp16")
+        for r in range(n):
+            assert np.array_equal(W.to_storage(ag_out[r]), ag_expect), r
+        # AG(RS(x)) is the AllReduce
+        ar = oracle.allreduce(host, "fp16", nthreads=16)
+        assert np.array_equal(ag_expect, ar)
+    finally:
+        comm.close()
+
+
+@pytest.mark.parametrize("n,count", [(2, 1), (3, 5), (8, 1000), (8, 1001), (5, 77777), (16, 4096)])
+@pytest.mark.parametrize("dtype", ["int32", "fp32", "fp16", "bf16"])
+def test_reduce_scatter_allgather_ragged(dcc, n, count, dtype):
+    """Shards that do not start on 16-byte boundaries take the element path."""
+    w = W.with_count(RECIPES[dtype], count * n, n_ranks=n)
+    xs = [x.cuda() for x in W.rank_inputs(w)]
+    rs_out = [torch.empty(count, dtype=xs[0].dtype, device="cuda") for _ in range(n)]
+    ag_out = [torch.empty(count * n, dtype=xs[0].dtype, device="cuda") for _ in range(n)]
+    comm = dcc.Comm(n)
+    try:
+        comm.register_all("input", xs)
+        comm.register_all("output", rs_out)
+        comm.register_all("output", ag_out)
+        comm.reduce_scatter(xs, rs_out)
+        comm.allgather(rs_out, ag_out)
+        assert comm.check() == dcc.DCC_OK
+        host = [W.to_storage(x) for x in xs]
+        full = oracle.allreduce(host, dtype)
+        for r in range(n):
+            assert same(W.to_storage(rs_out[r]), full[r * count:(r + 1) * count], dtype)
+            assert same(W.to_storage(ag_out[r]), full, dtype)
+    finally:
+        comm.close()
+
+
+# ---------------------------------------------------------------- synchronisation
+@pytest.mark.parametrize("n", [1, 2, 8, 16])
+def test_ring_barrier_counts(dcc, n):
+    iters = W.BARRIER_ITERS
+    comm = dcc.Comm(n, connect="ring")
+    try:
+        comm.ring_barrier(iters)
+        assert comm.check() == dcc.DCC_OK
+        inbound, expected = dcc.dcc_comm_read_semaphores(comm.handle, n)
+        ref = oracle.ring_barrier_counts(n, iters)
+        assert np.array_equal(inbound, ref)
+        assert np.array_equal(expected, ref)
+        comm.ring_barrier(3)
+        assert comm.check() == dcc.DCC_OK
+        inbound, _ = dcc.dcc_comm_read_semaphores(comm.handle, n)
+        assert np.array_equal(inbound, oracle.ring_barrier_counts(n, iters + 3))
+    finally:
+        comm.close()
+
+
+def test_put_get_and_signal(dcc):
+    n = 4
+    comm = dcc.Comm(n)
+    try:
+        ins = [torch.arange(4096, dtype=torch.int32, device="cuda") + 10000 * r for r in range(n)]
+        outs = [torch.full((4096,), -1, dtype=torch.int32, device="cuda") for _ in range(n)]
+        comm.register_all("input", ins)
+        comm.register_all("output", outs)
+        # put 1 KiB from rank 1's input (offset 256 B) into rank 3's output (offset 512 B), signalled
+        dcc.dcc_channel_put(comm.handle, 1, 3, 512, 256, 1024, signal=True)
+        assert comm.check() == dcc.DCC_OK
+        got = outs[3].cpu().numpy()
+        assert np.array_equal(got[128:384], ins[1].cpu().numpy()[64:320])
+        assert np.all(got[:128] == -1) and np.all(got[384:] == -1)
+        inbound, expected = dcc.dcc_comm_read_semaphores(comm.handle, n)
+        assert inbound[3, 1] == 1 and expected[3, 1] == 1 and inbound.sum() == 1
+        # get: rank 0's output [0, 4 KiB) <- rank 2's input [8 KiB, 12 KiB)
+        dcc.dcc_channel_get(comm.handle, 0, 2, 8192, 0, 4096)
+        assert comm.check() == dcc.DCC_OK
+        assert np.array_equal(outs[0].cpu().numpy()[:1024], ins[2].cpu().numpy()[2048:3072])
+    finally:
+        comm.close()
+
+
+def test_repeated_calls_never_need_a_reset(dcc):
+    """10^4 back-to-back collectives that synchronise through semaphores
+    (in-place one-shot, two-shot via scratch) plus barriers, no reset."""
+    n, count = 8, 4096 + 3
+    w = W.with_count(W.C2, count)
+    xs = W.rank_inputs(w)
+    arena = Arena(dcc, n, count)
+    try:
+        send = arena.view(arena.inp, "int32", count)
+        recv = arena.view(arena.out, "int32", count)
+        for r in range(n):
+            send[r].copy_(xs[r])
+        h = arena.comm.handle
+        for i in range(5000):
+            dcc.dcc_allreduce(h, send, recv, count, "int32", "two_shot_scratch")
+            dcc.dcc_allreduce(h, recv, recv, count, "int32", "one_shot")
+        dcc.dcc_ring_barrier(h, 100)
+        assert arena.comm.check() == dcc.DCC_OK
+        # recv = 8 * sum(x) after each pair; it is recomputed from send every time
+        expect = oracle.allreduce([W.to_storage(x) for x in xs], "int32").astype(np.int64) * n
+        expect = ((expect + 2 ** 31) % 2 ** 32 - 2 ** 31).astype(np.int32)
+        for r in range(n):
+            assert np.array_equal(W.to_storage(recv[r]), expect)
+        inbound, expected = dcc.dcc_comm_read_semaphores(h, n, block=0)
+        assert np.array_equal(inbound, expected)
+    finally:
+        arena.close()
+
+
+def test_graph_replay_keeps_epochs(dcc):
+    """Collectives captured once into a CUDA graph and replayed: the waits
+    count in device memory, so every replay synchronises correctly."""
+    n, count = 8, 20000 + 1
+    w = W.with_count(W.C4, count)
+    xs = W.rank_inputs(w)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
+    arena = Arena(dcc, n, count)
+    try:
+        send = arena.view(arena.inp, "bf16", count)
+        recv = arena.view(arena.out, "bf16", count)
+        for r in range(n):
+            send[r].copy_(xs[r])
+        h = arena.comm.handle
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dcc.dcc_allreduce(h, send, recv, count, "bf16", "two_shot_scratch", stream=s)
+            dcc.dcc_allreduce(h, send, recv, count, "bf16", "one_shot", stream=s)
+            dcc.dcc_allreduce(h, send, recv, count, "bf16", "two_shot", stream=s)
+        for _ in range(200):
+            g.replay()
+        torch.cuda.synchronize()
+        assert arena.comm.check() == dcc.DCC_OK
+        for r in range(n):
+            assert same(W.to_storage(recv[r]), expect, "bf16")
+    finally:
+        arena.close()
+
+
+def test_lost_signal_times_out_cleanly(dcc):
+    """A rank that never signals makes its peers' waits run out: the kernel
+    records DCC_ERR_TIMEOUT and returns; the GPU stays usable."""
+    n = 4
+    comm = dcc.Comm(n, connect="all")
+    try:
+        dcc.dcc_set_wait_timeout_us(comm.handle, 50000)
+        dcc.dcc_debug_skip_signal(comm.handle, 1)
+        comm.ring_barrier(10)
+        assert comm.check() == dcc.DCC_ERR_TIMEOUT
+        # ranks 2, 3 and 0 all wait from the start; whichever gives up first
+        # records itself, always as a wait on its ring predecessor
+        rank, peer, block = dcc.dcc_comm_error_detail(comm.handle)
+        assert rank in (2, 3, 0) and (rank - peer) % n == 1 and block == 0
+        with pytest.raises(dcc.DccError) as e:
+            comm.ring_barrier(1)
+        assert e.value.code == dcc.DCC_ERR_TIMEOUT
+    finally:
+        comm.close()
+    # the same for a collective that synchronises through every channel
+    comm = dcc.Comm(n)
+    try:
+        count = 100000
+        bufs = [torch.ones(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+        scr = [torch.empty(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+        comm.register_all("input", bufs)
+        comm.register_all("scratch", scr)
+        dcc.dcc_set_wait_timeout_us(comm.handle, 50000)
+        dcc.dcc_debug_skip_signal(comm.handle, 3)
+        comm.allreduce(bufs, bufs, algo="two_shot_scratch")
+        assert comm.check() == dcc.DCC_ERR_TIMEOUT
+        assert dcc.dcc_comm_error_detail(comm.handle)[1] == 3
+    finally:
+        comm.close()
+    # a fresh communicator works
+    with dcc.Comm(2) as c2:
+        a = [torch.ones(1000, device="cuda") for _ in range(2)]
+        c2.register_all("input", a)
+        c2.allreduce(a, a, algo="one_shot")
+        assert c2.check() == dcc.DCC_OK
+        assert torch.all(a[0] == 2)
+
+
+# ---------------------------------------------------------------- host-side errors on a device
+def test_argument_errors(dcc):
+    n = 2
+    comm = dcc.Comm(n, connect="none")
+    try:
+        h = comm.handle
+        a = [torch.zeros(1024, device="cuda") for _ in range(n)]
+        b = [torch.zeros(1024, device="cuda") for _ in range(n)]
+        E = dcc.DccError
+
+        def code(f, *args, **kw):
+            with pytest.raises(E) as e:
+                f(*args, **kw)
+            return e.value.code
+
+        assert code(dcc.dcc_allreduce, h, a, b, 1024, "fp32") == dcc.DCC_ERR_NOT_REGISTERED
+        comm.register_all("input", a)
+        comm.register_all("output", b)
+        assert code(dcc.dcc_allreduce, h, a, b, 1024, "fp32") == dcc.DCC_ERR_NO_CHANNEL
+        dcc.dcc_memory_channel_make(h, 0, 1)
+        dcc.dcc_memory_channel_make(h, 1, 0)
+        dcc.dcc_memory_channel_make(h, 1, 0)  # idempotent
+        dcc.dcc_allreduce(h, a, b, 1024, "fp32")
+        assert code(dcc.dcc_allreduce, h, a, b, 1025, "fp32") == dcc.DCC_ERR_NOT_REGISTERED
+        mis = [x[1:] for x in a]
+        assert code(dcc.dcc_allreduce, h, mis, b, 100, "fp32") == dcc.DCC_ERR_MISALIGNED
+        over = [b[0][4:], b[1]]
+        assert code(dcc.dcc_allreduce, h, [b[0], b[1]], [b[0][4:], a[1]], 100, "fp32") == \
+            dcc.DCC_ERR_INVALID_ARG
+        del over
+        assert code(dcc.dcc_allreduce, h, a, b, 16, 7) == dcc.DCC_ERR_INVALID_ARG
+        assert code(dcc.dcc_allreduce, h, a, b, 16, "fp32", 9) == dcc.DCC_ERR_INVALID_ARG
+        assert code(dcc.dcc_allreduce, h, a, b, 16, "fp32", "two_shot_scratch") == \
+            dcc.DCC_ERR_NOT_REGISTERED  # no scratch window
+        assert code(dcc.dcc_memory_channel_make, h, 0, 0) == dcc.DCC_ERR_INVALID_ARG
+        assert code(dcc.dcc_memory_channel_make, h, 0, 2) == dcc.DCC_ERR_INVALID_ARG
+        assert code(dcc.dcc_register_buffer, h, 0, "input", a[0][1:], 16) == dcc.DCC_ERR_MISALIGNED
+        assert code(dcc.dcc_register_buffer, h, 2, "input", a[0]) == dcc.DCC_ERR_INVALID_ARG
+        assert code(dcc.dcc_ring_barrier, h, -1) == dcc.DCC_ERR_INVALID_ARG
+        dcc.dcc_allreduce(h, a, b, 0, "fp32")  # empty: no-op
+        # RS/AG with overlapping ranges are rejected
+        assert code(dcc.dcc_reduce_scatter, h, a, [a[0][:256], a[1][:256]], 256, "fp32") == \
+            dcc.DCC_ERR_INVALID_ARG
+        assert comm.check() == dcc.DCC_OK
+    finally:
+        comm.close()
+
+
+def test_allreduce_from_host(dcc):
+    n, count = 8, 300001
+    w = W.with_count(W.C4, count)
+    xs = [x.pin_memory() for x in W.rank_inputs(w)]
+    outs = [torch.empty_like(x).pin_memory() for x in xs]
+    dev_in = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    dev_out = [torch.empty_like(d) for d in dev_in]
+    comm = dcc.Comm(n)
+    try:
+        comm.register_all("input", dev_in)
+        comm.register_all("output", dev_out)
+        dcc.dcc_allreduce_from_host(comm.handle, xs, outs, dev_in, dev_out, count, "bf16")
+        assert comm.check() == dcc.DCC_OK
+        expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
+        for o in outs:
+            assert same(W.to_storage(o), expect, "bf16")
+    finally:
+        comm.close()
+
+
+def test_auto_selection(dcc):
+    with dcc.Comm(8) as c:
+        dcc.dcc_set_algo_threshold(c.handle, "bf16", 65536)
+        assert dcc.dcc_select_algo(c.handle, 32768, "bf16") == "one_shot"
+        assert dcc.dcc_select_algo(c.handle, 32769, "bf16") == "two_shot"
+        b, t = dcc.dcc_launch_shape(c.handle, W.C4.count, "bf16", "two_shot")
+        assert 1 <= b <= dcc.DCC_MAX_BLOCKS_PER_RANK and t > 0
