@@ -75,6 +75,7 @@ _SIGS = {
     "dcc_debug_skip_signal": [_vp, _i],
     "dcc_launch_shape": [_vp, _sz, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "dcc_shard_range": [_sz, _i, _i, _sz, ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
+    "dcc_allreduce_noalloc": [_i, _PP, _PP, _sz, _i, _vp],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -256,6 +257,16 @@ def dcc_shard_range(count, n_ranks, rank, elem_bytes):
     _check(_lib.dcc_shard_range(count, n_ranks, rank, elem_bytes, ctypes.byref(b), ctypes.byref(e)),
            "dcc_shard_range")
     return b.value, e.value
+
+
+def dcc_allreduce_noalloc(n_ranks, send, recv, count, dtype, stream=None):
+    """AllReduce with no communicator and no allocation (see dcc.h)."""
+    return _check(_lib.dcc_allreduce_noalloc(n_ranks, _ptrs(send), _ptrs(recv), count,
+                                             _dtype(dtype), _stream(stream)),
+                  "dcc_allreduce_noalloc")
+
+
+DCC_NOALLOC_MAX_BYTES = 4 << 20
 
 
 def raw_call(name, *args):

@@ -165,6 +165,40 @@ int dcc_comm_error_detail(dcc_comm_t c, int* rank, int* peer, int* block);
 const char* dcc_error_string(int code);
 
 /* ------------------------------------------------------------------------ */
+/* AllReduce without any allocation.  The MSCCL++ pages have no counterpart */
+/* to this entry point; it exists for callers that cannot call cudaMalloc   */
+/* when they need the collective -- a framework whose caching allocator     */
+/* owns all device memory, a serving loop that cannot afford cudaMalloc's   */
+/* implicit device synchronisation, a deployment with a fixed audited       */
+/* memory budget -- and so cannot create a communicator.                    */
+/* ------------------------------------------------------------------------ */
+
+#define DCC_NOALLOC_MAX_BYTES (4u << 20) /* largest message per rank: 4 MiB */
+
+/* Two-shot AllReduce through scratch (DCC_ALGO_TWO_SHOT_SCRATCH semantics and
+ * bits) over n_ranks (1..DCC_MAX_RANKS) virtual ranks on the current device,
+ * with no communicator, no registration and no channel set-up.  The caller
+ * passes inputs and outputs only (send[r] == recv[r] is in place; other
+ * overlaps are rejected; 16-byte alignment as for dcc_allreduce).  All
+ * working memory -- reduced shards, semaphores, waiter counts, status word --
+ * lives in one fixed device array of DCC_NOALLOC_MAX_BYTES plus 1.25 MiB that
+ * every GPU that loads the library holds until the process exits.
+ *  - Never allocates: no cudaMalloc/cudaFree or other allocating call.
+ *  - The first call on a device resolves that array's device address for the
+ *    device (once); make that first call before any stream capture.
+ *  - Every call clears the array's synchronisation part on s before its
+ *    kernel; calls share the array, so calls that overlap on the GPU (on
+ *    different streams, or on several host threads) race and must not be
+ *    issued.
+ *  - A device wait that runs out (the same bounded waits as the communicator
+ *    path) leaves that call's outputs incomplete; there is no communicator to
+ *    report it through.
+ * Errors: INVALID_ARG (n_ranks, NULL, dtype, overlap), MISALIGNED,
+ * UNSUPPORTED (count * element size > DCC_NOALLOC_MAX_BYTES), LAUNCH, CUDA. */
+int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const* recv, size_t count,
+                          dcc_dtype_t t, dcc_stream_t s);
+
+/* ------------------------------------------------------------------------ */
 /* MemoryChannel primitives on their own (README, "On-GPU Communication     */
 /* Interfaces: Channels": put copies from local to remote memory; signal,   */
 /* flush, wait synchronise a pair of ranks).  The channel src -> dst binds  */
