@@ -456,8 +456,66 @@ def run_reference(args, dist):
     }
 
 
+# ------------------------------------------------------------------ profiling cases
+PROFILE_CASES = ("allreduce_two_shot", "allreduce_one_shot", "allreduce_one_shot_inplace",
+                 "allreduce_two_shot_scratch", "reduce_scatter", "allgather", "ring_barrier")
+
+
+def run_profile_case(args):
+    """One operation, `warmup` + `steps` launches, on a reduced size: the
+    command that Nsight Compute captures (a few hundred MB on the device)."""
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    recipe = {"bf16": W.C4, "fp16": W.C5, "int32": W.C2, "fp32": W.C1}[args.dtype]
+    n = 8
+    w = W.with_count(recipe, args.count, n_ranks=n)
+    case = args.profile_case
+    xs = W.rank_inputs(w, device=dev)
+    comm = dcc.Comm(n, connect="ring" if case == "ring_barrier" else "all")
+    if case == "reduce_scatter":
+        m = w.count // n
+        ys = [torch.empty(m, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+        fn = lambda: dcc.dcc_reduce_scatter(comm.handle, xs, ys, m, args.dtype)  # noqa: E731
+    elif case == "allgather":
+        m = w.count // n
+        xs = [x[:m].clone() for x in xs]
+        ys = [torch.empty(w.count, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+        fn = lambda: dcc.dcc_allgather(comm.handle, xs, ys, m, args.dtype)  # noqa: E731
+    elif case == "ring_barrier":
+        ys = []
+        fn = lambda: dcc.dcc_ring_barrier(comm.handle, W.BARRIER_ITERS)  # noqa: E731
+    else:
+        algo = case[len("allreduce_"):]
+        inplace = algo.endswith("_inplace")
+        algo = algo.replace("_inplace", "")
+        ys = xs if inplace else [torch.empty_like(x) for x in xs]
+        if algo == "two_shot_scratch":
+            comm.register_all("scratch", [torch.empty_like(x) for x in xs])
+        fn = lambda: dcc.dcc_allreduce(comm.handle, xs, ys, w.count, args.dtype, algo)  # noqa: E731
+    if case != "ring_barrier":
+        comm.register_all("input", xs)
+        if ys is not xs:
+            comm.register_all("output", ys)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    rc = comm.check()
+    comm.close()
+    if rc != dcc.DCC_OK:
+        raise RuntimeError(dcc.dcc_error_string(rc))
+    print(json.dumps({"profile_case": case, "dtype": args.dtype, "count_per_rank": w.count,
+                      "launches": args.warmup + args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
+                    help="run one operation for an Nsight Compute capture (no timing)")
+    ap.add_argument("--count", type=int, default=1 << 24, help="elements per rank (profile case)")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "int32", "fp32"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
@@ -469,6 +527,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_case:
+        run_profile_case(args)
+        return
     dist = Dist()
     try:
         out = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
