@@ -25,7 +25,11 @@ import sys
 import time
 
 import numpy as np
-import torch
+
+# the PortChannel measurement waits on the proxy's stream: one hardware queue
+# per stream (set before the CUDA context exists)
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+import torch  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -329,29 +333,56 @@ def sweep_c3(dcc, dev, stream):
         h = comm.handle
         row = {"tokens": tokens, "bytes_per_rank": w.bytes_per_rank}
         for algo in ("one_shot", "two_shot"):
-            def step():
-                dcc.dcc_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
+            step = dcc.prepare_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
             for _ in range(50):
                 step()
-            per, _ = time_launches(step, 500, stream)
+            per, _ = time_launches(step, 1000, stream)
             p50 = statistics.median(per) * 1e3
+            # host cost of one call (launch included), no device wait in between
+            stream.synchronize()
+            t = time.perf_counter()
+            for _ in range(1000):
+                step()
+            host_us = (time.perf_counter() - t) * 1e3
+            stream.synchronize()
             g = torch.cuda.CUDAGraph()
             reps = 100
             with torch.cuda.graph(g, stream=stream):
                 for _ in range(reps):
                     step()
-            g.replay()
-            stream.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(5):
+            with torch.cuda.stream(stream):  # replay() launches on the current stream
                 g.replay()
-            e1.record(stream)
+                stream.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(10):
+                    g.replay()
+                e1.record(stream)
             e1.synchronize()
-            graph_us = e0.elapsed_time(e1) * 1e3 / (5 * reps)
-            row[algo] = {"p50_us": round(p50, 2), "graph_us": round(graph_us, 2),
+            graph_us = e0.elapsed_time(e1) * 1e3 / (10 * reps)
+            row[algo] = {"p50_us": round(p50, 2), "host_us_per_call": round(host_us, 2),
+                         "graph_us": round(graph_us, 2),
                          "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
+        if w.bytes_per_rank <= dcc.DCC_LL_MAX_BYTES:  # in place: barrier one-shot vs LL
+            for algo in ("one_shot", "one_shot_ll"):
+                step = dcc.prepare_allreduce(h, xs, xs, w.count, "bf16", algo, stream)
+                for _ in range(20):
+                    step()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(100):
+                        step()
+                with torch.cuda.stream(stream):
+                    g.replay()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(10):
+                        g.replay()
+                    e1.record(stream)
+                e1.synchronize()
+                row[algo + "_inplace"] = {"graph_us": round(e0.elapsed_time(e1) * 1e3 / 1000, 2)}
         assert comm.check(stream) == dcc.DCC_OK
         comm.close()
         res.append(row)
@@ -362,6 +393,28 @@ def other_workloads(dcc, dev, stream):
     """C2 (int32 in-place, both algorithms), C5 (ReduceScatter, AllGather,
     ring barrier): device-event timings."""
     out = {}
+    # every AllReduce schedule on the headline size
+    w = W.C4
+    with torch.cuda.stream(stream):
+        xs = W.rank_inputs(w, device=dev)
+        ys = [torch.empty_like(x) for x in xs]
+        scr = [torch.empty_like(x) for x in xs]
+    torch.cuda.synchronize()
+    comm = dcc.Comm(8)
+    comm.register_all("input", xs)
+    comm.register_all("output", ys)
+    comm.register_all("scratch", scr)
+    for algo in ("two_shot", "two_shot_bulk", "two_shot_scratch", "one_shot"):
+        step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", algo, stream)
+        for _ in range(3):
+            step()
+        per, _ = time_launches(step, 30, stream)
+        ms = statistics.median(per)
+        out["c4_bf16_" + algo] = {"ms": round(ms, 4),
+                                  "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+    assert comm.check(stream) == dcc.DCC_OK
+    comm.close()
+    del xs, ys, scr
     w = W.C2
     with torch.cuda.stream(stream):
         xs = W.rank_inputs(w, device=dev)
@@ -405,6 +458,20 @@ def other_workloads(dcc, dev, stream):
                      "algorithmic_bytes": nbytes}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
+    # the same AllGather through PortChannels: the host proxy drives copy engines
+    with dcc.Comm(8) as pc:
+        pc.register_all("input", rs)
+        pc.register_all("output", ag)
+        dcc.dcc_proxy_start(pc.handle)
+        fn = lambda: dcc.dcc_port_allgather(pc.handle, rs, ag, m, "fp16", stream)  # noqa: E731
+        for _ in range(3):
+            fn()
+        per, _ = time_launches(fn, 10, stream)
+        assert pc.check(stream) == dcc.DCC_OK
+        assert dcc.dcc_proxy_stop(pc.handle) == dcc.DCC_OK
+        ms = statistics.median(per)
+        out["c5_allgather_port_channel"] = {"ms": round(ms, 4), "hbm_gbs": round(
+            (w.bytes_per_rank + 8 * w.bytes_per_rank) / ms / 1e6, 1)}
     with dcc.Comm(8, connect="ring") as ring:
         ring.ring_barrier(100, stream)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -457,8 +524,9 @@ def run_reference(args, dist):
 
 
 # ------------------------------------------------------------------ profiling cases
-PROFILE_CASES = ("allreduce_two_shot", "allreduce_one_shot", "allreduce_one_shot_inplace",
-                 "allreduce_two_shot_scratch", "reduce_scatter", "allgather", "ring_barrier")
+PROFILE_CASES = ("allreduce_two_shot", "allreduce_two_shot_bulk", "allreduce_one_shot",
+                 "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "reduce_scatter",
+                 "allgather", "ring_barrier")
 
 
 def run_profile_case(args):

@@ -23,7 +23,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=fal
               "-I" + INCLUDE, "-I" + CSRC]
 
 SOURCES = ["dcc_host.cu", "sync_kernels.cu", "coll_allgather.cu",
-           "coll_int32.cu", "coll_fp32.cu", "coll_fp16.cu", "coll_bf16.cu", "noalloc.cu"]
+           "coll_int32.cu", "coll_fp32.cu", "coll_fp16.cu", "coll_bf16.cu", "noalloc.cu",
+           "proxy.cu"]
 
 
 def nvcc():

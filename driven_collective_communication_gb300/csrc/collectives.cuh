@@ -176,7 +176,9 @@ __device__ __forceinline__ void shard_vecs(size_t nvec, int n, int r, size_t& s0
 // rank writes what another reads, so there is no synchronisation.  In place,
 // rank r's output is an input of every peer: the N CTAs of a block slot
 // process the same chunk together -- get and reduce into registers, then a
-// signal/wait barrier ("everyone has read this chunk"), then store.
+// signal/wait barrier ("everyone has read this chunk"), then store.  (Getting
+// the next chunk while the signals travel measured slower on GB300: 0.53 vs
+// 0.43 ms for 8 x 64 MiB int32.)
 template <typename T, int NT>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
@@ -370,7 +372,9 @@ __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, 
 }
 
 // ------------------------------------------------------------- kernel tables
-enum KernelKind { kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3 };
+enum KernelKind {
+  kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3, kTwoShotBulk = 4, kOneShotLL = 5
+};
 
 // Kernel of `kind` for element type T and n ranks (compile-time N for
 // 1..8 and 16, a runtime-N instance otherwise).
@@ -378,5 +382,6 @@ template <typename T>
 const void* reduce_kernel(int kind, int n);
 
 const void* allgather_kernel(int n);
+const void* allgather_bulk_kernel(int n);
 
 }  // namespace dcc

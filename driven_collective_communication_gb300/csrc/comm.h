@@ -1,0 +1,211 @@
+// comm.h -- the communicator object and host helpers shared by the host
+// translation units of libdcc (dcc_host.cu, proxy.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "dcc.h"
+#include "dcc_internal.h"
+
+struct ProxyState;  // proxy.cu
+struct dcc_comm;
+void dcc_proxy_release(dcc_comm* c);  // proxy.cu: stops the proxy thread and frees its state
+int dcc_preload_kernels();            // dcc_host.cu: loads every collective kernel now
+
+namespace dcc_host {
+struct Window {
+  char* ptr;
+  size_t bytes;
+};
+
+inline size_t elem_bytes(dcc_dtype_t t) {
+  switch (t) {
+    case DCC_INT32: case DCC_FP32: return 4;
+    case DCC_FP16: case DCC_BF16: return 2;
+    default: return 0;
+  }
+}
+
+inline bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v && *v && std::strcmp(v, "0") != 0;
+}
+
+// Messages at or below this many bytes per rank run one-shot under AUTO.
+// Measured on GB300, 8 ranks bf16, CUDA-graph-amortised: one-shot 1.34 us vs
+// two-shot 1.46 us at 16 KiB, 1.60 vs 1.66 us at 32 KiB, even at 64 KiB, and
+// two-shot ahead from 128 KiB (1.79 vs 2.05 us) upwards.
+constexpr size_t kDefaultOneShotMaxBytes = 32 * 1024;
+
+// Threads per CTA of the thread-copy kernels, by work (16-byte vectors per
+// rank): small messages want many small CTAs spread over many SMs (latency),
+// large ones one full wave of 512-thread CTAs (bandwidth).  Measured on GB300
+// over 16 KiB .. 4 MiB per rank.
+inline int threads_for(dcc_algo_t algo, size_t work_vecs_per_rank) {
+  if (algo == DCC_ALGO_ONE_SHOT) return work_vecs_per_rank <= 65536 ? 128 : 512;
+  if (work_vecs_per_rank <= 8192) return 64;
+  if (work_vecs_per_rank <= 65536) return 128;
+  return 512;
+}
+
+// Host-buffer AllReduce: elements per rank per pipeline chunk (8 MiB of bf16).
+constexpr size_t kPipeChunkBytes = 8u << 20;
+
+// AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
+constexpr size_t kAgBulkMinBytes = 64 * 1024;
+
+}  // namespace dcc_host
+
+struct dcc_comm {
+  int n = 0;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<dcc_host::Window> win[DCC_MAX_RANKS][3];
+  bool chan[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
+  bool table_dirty = true;
+  dcc::DevChannel h_table[DCC_MAX_RANKS * DCC_MAX_RANKS] = {};
+  dcc::DevChannel* d_table = nullptr;
+  unsigned long long* d_block = nullptr;  // sem | expect | status | LL epochs
+  char* d_ll = nullptr;                   // LL packet buffers
+  dcc::DevComm dev{};
+  int blocks_override = 0;
+  int threads_override = 0;  // threads per CTA of the thread-copy kernels (0 = by size)
+  bool cooperative = true;   // DCC_COOPERATIVE=0: plain launches (diagnostic only)
+  size_t one_shot_max[4] = {dcc_host::kDefaultOneShotMaxBytes, dcc_host::kDefaultOneShotMaxBytes,
+                            dcc_host::kDefaultOneShotMaxBytes, dcc_host::kDefaultOneShotMaxBytes};
+  int forced_algo = -1;  // DCC_ALGO environment override of AUTO
+  // AUTO: messages of at least bulk_min_bytes per rank run large_algo
+  size_t bulk_min_bytes = (size_t)1 << 62;
+  dcc_algo_t large_algo = DCC_ALGO_TWO_SHOT;
+  bool ag_bulk = true;  // AllGather through the bulk-copy pipeline when aligned and large
+  int sticky = DCC_OK;
+  int err_rank = -1, err_peer = -1, err_block = -1;
+  bool log = false;
+  // host-buffer pipeline (created on first use): copy-in and copy-out streams
+  // and the events that chain them to the caller's stream
+  bool pipe_ready = false;
+  cudaStream_t pipe_in = nullptr, pipe_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_kernel = nullptr, ev_done = nullptr;
+  ProxyState* proxy = nullptr;  // PortChannel proxy (created by dcc_proxy_start)
+};
+
+namespace dcc_host {
+
+// Makes the communicator's device current for the scope of a call.
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceScope() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+};
+
+// Resident CTAs per SM of `fn` with `threads` threads and `smem` bytes of
+// dynamic shared memory (raising the kernel's dynamic shared-memory limit the
+// first time).  Cached per (kernel, smem, threads).
+inline int max_active_per_sm(const void* fn, int threads, size_t smem = 0) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, std::unordered_map<size_t, int>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto& per_fn = cache[fn];
+  const size_t key = smem * 2048 + (size_t)threads;
+  auto it = per_fn.find(key);
+  if (it != per_fn.end()) return it->second;
+  int nb = 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  per_fn[key] = nb;
+  return nb;
+}
+
+inline bool in_window(const dcc_comm* c, int rank, int kind, const void* p, size_t bytes) {
+  const char* q = static_cast<const char*>(p);
+  for (const Window& w : c->win[rank][kind])
+    if (q >= w.ptr && bytes <= w.bytes && (size_t)(q - w.ptr) <= w.bytes - bytes) return true;
+  return false;
+}
+
+inline bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return an && bn && x < y + bn && y < x + an;
+}
+
+// Checks the send/recv arrays of a collective.  inplace_ok: send[r] == recv[r]
+// (same byte count) is allowed.  Reports whether any rank is in place.
+inline int check_buffers(const dcc_comm* c, void* const* send, size_t send_bytes, void* const* recv,
+                  size_t recv_bytes, bool inplace_ok, bool* any_inplace) {
+  if (!send || !recv) return DCC_ERR_INVALID_ARG;
+  *any_inplace = false;
+  for (int r = 0; r < c->n; ++r) {
+    if (!send[r] || !recv[r]) return DCC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(send[r]) | reinterpret_cast<uintptr_t>(recv[r])) & 15u)
+      return DCC_ERR_MISALIGNED;
+    if (!in_window(c, r, DCC_BUF_INPUT, send[r], send_bytes) &&
+        !in_window(c, r, DCC_BUF_OUTPUT, send[r], send_bytes))
+      return DCC_ERR_NOT_REGISTERED;
+    if (!in_window(c, r, DCC_BUF_INPUT, recv[r], recv_bytes) &&
+        !in_window(c, r, DCC_BUF_OUTPUT, recv[r], recv_bytes))
+      return DCC_ERR_NOT_REGISTERED;
+  }
+  for (int r = 0; r < c->n; ++r) {
+    for (int p = 0; p < c->n; ++p) {
+      if (overlaps(recv[r], recv_bytes, send[p], send_bytes)) {
+        const bool same = r == p && recv[r] == send[r] && send_bytes == recv_bytes;
+        if (!(inplace_ok && same)) return DCC_ERR_INVALID_ARG;
+        *any_inplace = true;
+      }
+      if (p != r && overlaps(recv[r], recv_bytes, recv[p], recv_bytes)) return DCC_ERR_INVALID_ARG;
+    }
+  }
+  return DCC_OK;
+}
+
+inline int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s,
+           size_t smem = 0) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  return DCC_OK;
+}
+
+}  // namespace dcc_host

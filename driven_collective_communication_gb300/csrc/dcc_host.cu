@@ -15,133 +15,15 @@
 #include <unordered_map>
 #include <vector>
 
+#include "bulk.cuh"
+#include "ll.cuh"
 #include "collectives.cuh"
-#include "dcc.h"
-#include "dcc_internal.h"
+#include "comm.h"
 #include "sync_kernels.cuh"
 
 namespace {
 
-struct Window {
-  char* ptr;
-  size_t bytes;
-};
-
-size_t elem_bytes(dcc_dtype_t t) {
-  switch (t) {
-    case DCC_INT32: case DCC_FP32: return 4;
-    case DCC_FP16: case DCC_BF16: return 2;
-    default: return 0;
-  }
-}
-
-bool env_flag(const char* name) {
-  const char* v = std::getenv(name);
-  return v && *v && std::strcmp(v, "0") != 0;
-}
-
-// Messages at or below this many bytes per rank run one-shot under AUTO.
-// Measured crossover on GB300 (see the tuning notes of this repository).
-constexpr size_t kDefaultOneShotMaxBytes = 0;
-
-}  // namespace
-
-struct dcc_comm {
-  int n = 0;
-  int device = 0;
-  int num_sms = 0;
-  std::vector<Window> win[DCC_MAX_RANKS][3];
-  bool chan[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
-  bool table_dirty = true;
-  dcc::DevChannel h_table[DCC_MAX_RANKS * DCC_MAX_RANKS] = {};
-  dcc::DevChannel* d_table = nullptr;
-  unsigned long long* d_block = nullptr;  // sem | expect | status
-  dcc::DevComm dev{};
-  int blocks_override = 0;
-  size_t one_shot_max[4] = {kDefaultOneShotMaxBytes, kDefaultOneShotMaxBytes,
-                            kDefaultOneShotMaxBytes, kDefaultOneShotMaxBytes};
-  int forced_algo = -1;  // DCC_ALGO environment override of AUTO
-  int sticky = DCC_OK;
-  int err_rank = -1, err_peer = -1, err_block = -1;
-  bool log = false;
-};
-
-namespace {
-
-// Makes the communicator's device current for the scope of a call.
-class DeviceScope {
- public:
-  explicit DeviceScope(int dev) {
-    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
-    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
-  }
-  ~DeviceScope() {
-    if (prev_ >= 0) cudaSetDevice(prev_);
-  }
-  bool ok() const { return ok_; }
-
- private:
-  int prev_ = -1;
-  bool ok_ = true;
-};
-
-int max_active_per_sm(const void* fn, int threads) {
-  static std::mutex mu;
-  static std::unordered_map<const void*, int> cache;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(fn);
-  if (it != cache.end()) return it->second;
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, 0) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cache[fn] = nb;
-  return nb;
-}
-
-bool in_window(const dcc_comm* c, int rank, int kind, const void* p, size_t bytes) {
-  const char* q = static_cast<const char*>(p);
-  for (const Window& w : c->win[rank][kind])
-    if (q >= w.ptr && bytes <= w.bytes && (size_t)(q - w.ptr) <= w.bytes - bytes) return true;
-  return false;
-}
-
-bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
-  const char* x = static_cast<const char*>(a);
-  const char* y = static_cast<const char*>(b);
-  return an && bn && x < y + bn && y < x + an;
-}
-
-// Checks the send/recv arrays of a collective.  inplace_ok: send[r] == recv[r]
-// (same byte count) is allowed.  Reports whether any rank is in place.
-int check_buffers(const dcc_comm* c, void* const* send, size_t send_bytes, void* const* recv,
-                  size_t recv_bytes, bool inplace_ok, bool* any_inplace) {
-  if (!send || !recv) return DCC_ERR_INVALID_ARG;
-  *any_inplace = false;
-  for (int r = 0; r < c->n; ++r) {
-    if (!send[r] || !recv[r]) return DCC_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(send[r]) | reinterpret_cast<uintptr_t>(recv[r])) & 15u)
-      return DCC_ERR_MISALIGNED;
-    if (!in_window(c, r, DCC_BUF_INPUT, send[r], send_bytes) &&
-        !in_window(c, r, DCC_BUF_OUTPUT, send[r], send_bytes))
-      return DCC_ERR_NOT_REGISTERED;
-    if (!in_window(c, r, DCC_BUF_INPUT, recv[r], recv_bytes) &&
-        !in_window(c, r, DCC_BUF_OUTPUT, recv[r], recv_bytes))
-      return DCC_ERR_NOT_REGISTERED;
-  }
-  for (int r = 0; r < c->n; ++r) {
-    for (int p = 0; p < c->n; ++p) {
-      if (overlaps(recv[r], recv_bytes, send[p], send_bytes)) {
-        const bool same = r == p && recv[r] == send[r] && send_bytes == recv_bytes;
-        if (!(inplace_ok && same)) return DCC_ERR_INVALID_ARG;
-        *any_inplace = true;
-      }
-      if (p != r && overlaps(recv[r], recv_bytes, recv[p], recv_bytes)) return DCC_ERR_INVALID_ARG;
-    }
-  }
-  return DCC_OK;
-}
+using namespace dcc_host;
 
 int check_channels_all_pairs(const dcc_comm* c) {
   for (int r = 0; r < c->n; ++r)
@@ -187,31 +69,6 @@ int upload_table(dcc_comm* c, cudaStream_t s) {
   return DCC_OK;
 }
 
-int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  if (cooperative) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    cudaGetLastError();
-    return DCC_ERR_LAUNCH;
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return DCC_ERR_CUDA;
-  }
-  return DCC_OK;
-}
-
 const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
   switch (t) {
     case DCC_INT32: return dcc::reduce_kernel<int32_t>(kind, n);
@@ -226,22 +83,30 @@ const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
 // the GPU (co-residency is required when the kernel waits), at most
 // DCC_MAX_BLOCKS_PER_RANK (the semaphore slots).
 int pick_blocks(const dcc_comm* c, const void* fn, int threads, size_t work_vecs_per_rank,
-                int* blocks) {
-  const int per_sm = max_active_per_sm(fn, threads);
+                int* blocks, size_t smem = 0, size_t work_per_block = 0) {
+  const int per_sm = max_active_per_sm(fn, threads, smem);
   if (per_sm < 1) return DCC_ERR_LAUNCH;
   int bmax = per_sm * c->num_sms / c->n;
   if (bmax < 1) return DCC_ERR_LAUNCH;
   if (bmax > DCC_MAX_BLOCKS_PER_RANK) bmax = DCC_MAX_BLOCKS_PER_RANK;
+  const size_t unit = work_per_block ? work_per_block : (size_t)threads;
   size_t want = c->blocks_override > 0 ? (size_t)c->blocks_override
-                                       : (work_vecs_per_rank + threads - 1) / threads;
+                                       : (work_vecs_per_rank + unit - 1) / unit;
   if (want < 1) want = 1;
   *blocks = want > (size_t)bmax ? bmax : (int)want;
   return DCC_OK;
 }
 
-dcc_algo_t resolve_algo(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a) {
+// AUTO: in place, the two-shot push needs no synchronisation while one-shot
+// must wait for every peer to read a chunk before overwriting it (measured on
+// GB300 at 16 KiB x 8 ranks: 1.5 us vs 4.8 us), so in-place requests always go
+// two-shot; out of place, one-shot up to the per-dtype threshold.
+dcc_algo_t resolve_algo(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a,
+                        bool inplace = false) {
   if (a != DCC_ALGO_AUTO) return a;
   if (c->forced_algo > 0) return (dcc_algo_t)c->forced_algo;
+  if (count * elem_bytes(t) >= c->bulk_min_bytes) return c->large_algo;
+  if (inplace) return DCC_ALGO_TWO_SHOT;
   return count * elem_bytes(t) <= c->one_shot_max[t] ? DCC_ALGO_ONE_SHOT : DCC_ALGO_TWO_SHOT;
 }
 
@@ -252,7 +117,11 @@ struct Shape {
   int blocks;
   int threads;
   bool cooperative;
+  size_t smem;
 };
+
+// The compile-time rank count a kernel table holds for n (0 = runtime-N instance).
+int compiled_n(int n) { return (n >= 1 && n <= 8) || n == 16 ? n : 0; }
 
 int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t algo, bool inplace,
                     Shape* sh) {
@@ -264,11 +133,29 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
     case DCC_ALGO_ONE_SHOT: kind = dcc::kOneShot; work = nvec; break;
     case DCC_ALGO_TWO_SHOT: kind = dcc::kTwoShot; work = nvec / c->n + 1; break;
     case DCC_ALGO_TWO_SHOT_SCRATCH: kind = dcc::kTwoShotScratch; work = nvec / c->n + 1; break;
+    case DCC_ALGO_TWO_SHOT_BULK: kind = dcc::kTwoShotBulk; work = nvec / c->n + 1; break;
+    case DCC_ALGO_ONE_SHOT_LL: kind = dcc::kOneShotLL; work = nvec; break;
     default: return DCC_ERR_INVALID_ARG;
   }
   sh->fn = reduce_kernel_for(t, kind, c->n);
   if (!sh->fn) return DCC_ERR_INVALID_ARG;
-  sh->threads = dcc::kThreads;
+  sh->smem = 0;
+  if (algo == DCC_ALGO_ONE_SHOT_LL) {  // fixed launch shape (see ll.cuh)
+    if (count * elem_bytes(t) > dcc::kLLMaxBytes) return DCC_ERR_UNSUPPORTED;
+    sh->threads = dcc::kLLThreads;
+    sh->blocks = dcc::kLLBlocks;
+    sh->cooperative = c->n > 1;
+    const int per_sm = max_active_per_sm(sh->fn, sh->threads);
+    if (per_sm < 1 || per_sm * c->num_sms < dcc::kLLBlocks * c->n) return DCC_ERR_LAUNCH;
+    return DCC_OK;
+  }
+  if (algo == DCC_ALGO_TWO_SHOT_BULK) {
+    sh->threads = dcc::kBulkThreads;
+    sh->cooperative = false;
+    sh->smem = dcc::bulk_smem_bytes(compiled_n(c->n), c->n);
+    return pick_blocks(c, sh->fn, sh->threads, work, &sh->blocks, sh->smem, dcc::kBulkTileVecs);
+  }
+  sh->threads = c->threads_override > 0 ? c->threads_override : threads_for(algo, work);
   sh->cooperative = (algo == DCC_ALGO_ONE_SHOT && inplace && c->n > 1) ||
                     (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1);
   if (algo == DCC_ALGO_ONE_SHOT && inplace) work = (nvec + dcc::kInplaceUnroll - 1) / dcc::kInplaceUnroll;
@@ -279,7 +166,7 @@ int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t c
                      dcc_dtype_t t, dcc_algo_t a, cudaStream_t s) {
   if (c->sticky != DCC_OK) return c->sticky;
   if (elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
-  if (a < DCC_ALGO_AUTO || a > DCC_ALGO_TWO_SHOT_SCRATCH) return DCC_ERR_INVALID_ARG;
+  if (a < DCC_ALGO_AUTO || a > DCC_ALGO_ONE_SHOT_LL) return DCC_ERR_INVALID_ARG;
   if (count == 0) return DCC_OK;
   const size_t bytes = count * elem_bytes(t);
   if (bytes / elem_bytes(t) != count) return DCC_ERR_INVALID_ARG;
@@ -288,7 +175,7 @@ int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t c
   if (rc != DCC_OK) return rc;
   rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
-  const dcc_algo_t algo = resolve_algo(c, count, t, a);
+  const dcc_algo_t algo = resolve_algo(c, count, t, a, inplace);
 
   dcc::CollArgs args{};
   for (int r = 0; r < c->n; ++r) {
@@ -320,10 +207,38 @@ int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t c
                  c->n, count, (int)t, (int)algo, (int)inplace, sh.blocks);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative, kargs, s);
+  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative && c->cooperative, kargs, s, sh.smem);
 }
 
 }  // namespace
+
+// Loads every collective kernel of the library into the current context now
+// rather than at its first launch.  With lazy module loading, loading a kernel
+// waits for the kernels already running; if one of those waits on the host
+// proxy, the proxy's CUDA calls stall behind the load until that kernel's wait
+// limit runs out.  Preloading before the proxy starts removes the hazard for
+// this library's own kernels.
+int dcc_preload_kernels() {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const dcc_dtype_t types[] = {DCC_INT32, DCC_FP32, DCC_FP16, DCC_BF16};
+  const int ns[] = {1, 2, 3, 4, 5, 6, 7, 8, 16, 9};  // 9: the runtime-N instances
+  cudaFuncAttributes attr;
+  auto load = [&](const void* fn) {
+    if (fn && cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    return true;
+  };
+  bool ok = true;
+  for (dcc_dtype_t t : types)
+    for (int n : ns)
+      for (int kind = dcc::kOneShot; kind <= dcc::kOneShotLL; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
+  for (int n : ns) ok &= load(dcc::allgather_kernel(n)) && load(dcc::allgather_bulk_kernel(n));
+  ok &= load(dcc::ring_barrier_kernel()) && load(dcc::channel_put_kernel()) && load(dcc::channel_get_kernel());
+  return ok ? DCC_OK : DCC_ERR_CUDA;
+}
 
 // ====================================================================== C ABI
 extern "C" {
@@ -370,20 +285,27 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
     return DCC_ERR_CUDA;
   }
   const size_t sem_words = dcc::kSemSlots * dcc::kSemWords;
-  const size_t words = sem_words + dcc::kSemSlots + 32;  // sem | expect | status (padded)
+  const size_t ll_epochs = (size_t)DCC_MAX_RANKS * DCC_MAX_BLOCKS_PER_RANK;
+  // sem | expect | status (own 256-byte line) | LL epochs
+  const size_t words = sem_words + dcc::kSemSlots + 32 + ll_epochs;
+  const size_t ll_bytes = (size_t)n_ranks * dcc::kLLBufBytes;
   if (cudaMalloc(&c->d_block, words * sizeof(unsigned long long)) != cudaSuccess ||
-      cudaMalloc(&c->d_table, sizeof(c->h_table)) != cudaSuccess) {
+      cudaMalloc(&c->d_table, sizeof(c->h_table)) != cudaSuccess ||
+      cudaMalloc(&c->d_ll, ll_bytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(c->d_block);
+    cudaFree(c->d_table);
+    cudaFree(c->d_ll);
     delete c;
     return DCC_ERR_CUDA;
   }
   if (cudaMemset(c->d_block, 0, words * sizeof(unsigned long long)) != cudaSuccess ||
       cudaMemset(c->d_table, 0, sizeof(c->h_table)) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
+      cudaMemset(c->d_ll, 0, ll_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(c->d_block);
     cudaFree(c->d_table);
+    cudaFree(c->d_ll);
     delete c;
     return DCC_ERR_CUDA;
   }
@@ -395,15 +317,24 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
     if (us > 0) c->dev.timeout_ns = us * 1000ull;
   }
   if (const char* v = std::getenv("DCC_BLOCKS_PER_RANK")) c->blocks_override = std::atoi(v);
+  if (const char* v = std::getenv("DCC_COOPERATIVE")) c->cooperative = std::strcmp(v, "0") != 0;
+  if (const char* v = std::getenv("DCC_THREADS")) {
+    const int t = std::atoi(v);
+    if (t >= 32 && t <= dcc::kThreads && t % 32 == 0) c->threads_override = t;
+  }
   if (const char* v = std::getenv("DCC_ALGO")) {
     if (!std::strcmp(v, "one_shot")) c->forced_algo = DCC_ALGO_ONE_SHOT;
     else if (!std::strcmp(v, "two_shot")) c->forced_algo = DCC_ALGO_TWO_SHOT;
     else if (!std::strcmp(v, "two_shot_scratch")) c->forced_algo = DCC_ALGO_TWO_SHOT_SCRATCH;
+    else if (!std::strcmp(v, "two_shot_bulk")) c->forced_algo = DCC_ALGO_TWO_SHOT_BULK;
   }
   c->log = env_flag("DCC_LOG");
+  if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
+  c->dev.ll_epoch = c->d_block + sem_words + dcc::kSemSlots + 32;
+  c->dev.ll_buf = c->d_ll;
   *out = c;
   return DCC_OK;
 }
@@ -413,9 +344,19 @@ int dcc_comm_destroy(dcc_comm_t c) {
   int rc = DCC_OK;
   {
     DeviceScope ds(c->device);
+    dcc_proxy_release(c);
     if (cudaDeviceSynchronize() != cudaSuccess) rc = DCC_ERR_CUDA;
+    if (c->pipe_ready) {
+      cudaStreamDestroy(c->pipe_in);
+      cudaStreamDestroy(c->pipe_out);
+      cudaEventDestroy(c->ev_start);
+      cudaEventDestroy(c->ev_in);
+      cudaEventDestroy(c->ev_kernel);
+      cudaEventDestroy(c->ev_done);
+    }
     if (cudaFree(c->d_block) != cudaSuccess) rc = DCC_ERR_CUDA;
     if (cudaFree(c->d_table) != cudaSuccess) rc = DCC_ERR_CUDA;
+    if (cudaFree(c->d_ll) != cudaSuccess) rc = DCC_ERR_CUDA;
     cudaGetLastError();
   }
   delete c;
@@ -452,6 +393,12 @@ int dcc_allreduce(dcc_comm_t c, void* const* send, void* const* recv, size_t cou
   return allreduce_launch(c, send, recv, count, t, a, static_cast<cudaStream_t>(s));
 }
 
+// The message is cut into chunks of whole vectors.  Chunk i's inputs are
+// copied in on the copy-in stream, reduced on the caller's stream once they
+// have landed, and copied out on the copy-out stream once reduced, so the two
+// copy directions and the kernels of different chunks overlap.  The caller's
+// stream first hands its prior work to both copy streams and finally waits
+// for the last copy out, so the call is one stream-ordered operation on s.
 int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* const* host_recv,
                             void* const* dev_send, void* const* dev_recv, size_t count,
                             dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s) {
@@ -461,21 +408,60 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
   if (count == 0) return DCC_OK;
   DeviceScope ds(c->device);
   if (!ds.ok()) return DCC_ERR_CUDA;
-  const size_t bytes = count * elem_bytes(t);
+  const size_t eb = elem_bytes(t);
+  const size_t bytes = count * eb;
   bool inplace = false;
   int rc = check_buffers(c, dev_send, bytes, dev_recv, bytes, true, &inplace);
   if (rc != DCC_OK) return rc;
-  for (int r = 0; r < c->n; ++r)
-    if (!host_send[r] || !host_recv[r]) return DCC_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(s);
-  for (int r = 0; r < c->n; ++r)
-    if (cudaMemcpyAsync(dev_send[r], host_send[r], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return DCC_ERR_CUDA;
-  rc = allreduce_launch(c, dev_send, dev_recv, count, t, a, st);
+  rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
   for (int r = 0; r < c->n; ++r)
-    if (cudaMemcpyAsync(host_recv[r], dev_recv[r], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!host_send[r] || !host_recv[r]) return DCC_ERR_INVALID_ARG;
+  if (!c->pipe_ready) {
+    if (cudaStreamCreateWithFlags(&c->pipe_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c->pipe_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_kernel, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
       return DCC_ERR_CUDA;
+    }
+    c->pipe_ready = true;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  const size_t vw = 16 / eb;
+  size_t chunk = kPipeChunkBytes / eb / vw * vw;
+  if (chunk < vw) chunk = vw;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(c->ev_start, st)) || !ok(cudaStreamWaitEvent(c->pipe_in, c->ev_start, 0)) ||
+      !ok(cudaStreamWaitEvent(c->pipe_out, c->ev_start, 0)))
+    return DCC_ERR_CUDA;
+  void* send_i[DCC_MAX_RANKS];
+  void* recv_i[DCC_MAX_RANKS];
+  for (size_t c0 = 0; c0 < count; c0 += chunk) {
+    const size_t n_el = count - c0 < chunk ? count - c0 : chunk;
+    const size_t off = c0 * eb, nb = n_el * eb;
+    for (int r = 0; r < c->n; ++r) {
+      send_i[r] = static_cast<char*>(dev_send[r]) + off;
+      recv_i[r] = static_cast<char*>(dev_recv[r]) + off;
+      if (!ok(cudaMemcpyAsync(send_i[r], static_cast<const char*>(host_send[r]) + off, nb,
+                              cudaMemcpyHostToDevice, c->pipe_in)))
+        return DCC_ERR_CUDA;
+    }
+    if (!ok(cudaEventRecord(c->ev_in, c->pipe_in)) || !ok(cudaStreamWaitEvent(st, c->ev_in, 0)))
+      return DCC_ERR_CUDA;
+    rc = allreduce_launch(c, send_i, recv_i, n_el, t, a, st);
+    if (rc != DCC_OK) return rc;
+    if (!ok(cudaEventRecord(c->ev_kernel, st)) || !ok(cudaStreamWaitEvent(c->pipe_out, c->ev_kernel, 0)))
+      return DCC_ERR_CUDA;
+    for (int r = 0; r < c->n; ++r)
+      if (!ok(cudaMemcpyAsync(static_cast<char*>(host_recv[r]) + off, recv_i[r], nb,
+                              cudaMemcpyDeviceToHost, c->pipe_out)))
+        return DCC_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(c->ev_done, c->pipe_out)) || !ok(cudaStreamWaitEvent(st, c->ev_done, 0)))
+    return DCC_ERR_CUDA;
   return DCC_OK;
 }
 
@@ -502,11 +488,13 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
   args.count = recv_count;
   const void* fn = reduce_kernel_for(t, dcc::kReduceScatter, c->n);
   const size_t vw = 16 / elem_bytes(t);
-  rc = pick_blocks(c, fn, dcc::kThreads, (recv_count + vw - 1) / vw, &args.blocks);
+  const size_t work = (recv_count + vw - 1) / vw;
+  const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);
+  rc = pick_blocks(c, fn, threads, work, &args.blocks);
   if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(fn, args.blocks * c->n, dcc::kThreads, false, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
 }
 
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
@@ -531,12 +519,21 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   }
   args.count = send_count;
   int eb = (int)elem_bytes(t);
-  const void* fn = dcc::allgather_kernel(c->n);
-  rc = pick_blocks(c, fn, dcc::kThreads, (sb + 15) / 16, &args.blocks);
-  if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args, &eb};
-  return launch(fn, args.blocks * c->n, dcc::kThreads, false, kargs, static_cast<cudaStream_t>(s));
+  if (c->ag_bulk && sb % 16 == 0 && sb >= kAgBulkMinBytes) {
+    const void* fn = dcc::allgather_bulk_kernel(c->n);
+    const size_t smem = dcc::ag_smem_bytes();
+    rc = pick_blocks(c, fn, 32, (sb + dcc::kAgTile - 1) / dcc::kAgTile, &args.blocks, smem, 1);
+    if (rc != DCC_OK) return rc;
+    return launch(fn, args.blocks * c->n, 32, false, kargs, static_cast<cudaStream_t>(s), smem);
+  }
+  const void* fn = dcc::allgather_kernel(c->n);
+  const size_t work = (sb + 15) / 16;
+  const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);
+  rc = pick_blocks(c, fn, threads, work, &args.blocks);
+  if (rc != DCC_OK) return rc;
+  return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {

@@ -33,6 +33,8 @@ struct DevComm {
   unsigned long long* sem;      // kSemSlots counters, kSemWords apart
   unsigned long long* expect;   // kSemSlots waiter-side completed-wait counts
   unsigned long long* status;   // first failure, 0 = none
+  unsigned long long* ll_epoch; // LL protocol epochs, [rank][slot] (DCC_MAX_BLOCKS_PER_RANK slots)
+  char* ll_buf;                 // LL packet buffers, one per rank (library-owned, zeroed at create)
 };
 
 // A channel as the host builds it (one per ordered pair src -> dst) and copies

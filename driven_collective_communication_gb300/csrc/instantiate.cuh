@@ -1,7 +1,8 @@
 // instantiate.cuh -- kernel table of one element type (included by one .cu per type,
 // so the four types compile in parallel).
 #pragma once
-#include "collectives.cuh"
+#include "bulk.cuh"
+#include "ll.cuh"
 
 namespace dcc {
 
@@ -12,6 +13,8 @@ const void* pick_kernel(int kind) {
     case kTwoShot: return reinterpret_cast<const void*>(&k_allreduce_twoshot<T, NT>);
     case kTwoShotScratch: return reinterpret_cast<const void*>(&k_allreduce_twoshot_scratch<T, NT>);
     case kReduceScatter: return reinterpret_cast<const void*>(&k_reduce_scatter<T, NT>);
+    case kTwoShotBulk: return reinterpret_cast<const void*>(&k_allreduce_twoshot_bulk<T, NT>);
+    case kOneShotLL: return reinterpret_cast<const void*>(&k_allreduce_oneshot_ll<T, NT>);
     default: return nullptr;
   }
 }

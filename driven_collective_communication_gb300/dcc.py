@@ -35,6 +35,9 @@ DCC_ERR_UNSUPPORTED = -8
 
 DCC_INT32, DCC_FP32, DCC_FP16, DCC_BF16 = 0, 1, 2, 3
 DCC_ALGO_AUTO, DCC_ALGO_ONE_SHOT, DCC_ALGO_TWO_SHOT, DCC_ALGO_TWO_SHOT_SCRATCH = 0, 1, 2, 3
+DCC_ALGO_TWO_SHOT_BULK = 4
+DCC_ALGO_ONE_SHOT_LL = 5
+DCC_LL_MAX_BYTES = 256 << 10
 DCC_BUF_INPUT, DCC_BUF_OUTPUT, DCC_BUF_SCRATCH = 0, 1, 2
 DCC_MAX_RANKS = 16
 DCC_MAX_BLOCKS_PER_RANK = 128
@@ -43,7 +46,8 @@ DTYPE_CODES = {"int32": DCC_INT32, "fp32": DCC_FP32, "fp16": DCC_FP16, "bf16": D
 TORCH_CODES = {torch.int32: DCC_INT32, torch.float32: DCC_FP32, torch.float16: DCC_FP16,
                torch.bfloat16: DCC_BF16}
 ALGO_CODES = {"auto": DCC_ALGO_AUTO, "one_shot": DCC_ALGO_ONE_SHOT, "two_shot": DCC_ALGO_TWO_SHOT,
-              "two_shot_scratch": DCC_ALGO_TWO_SHOT_SCRATCH}
+              "two_shot_scratch": DCC_ALGO_TWO_SHOT_SCRATCH, "two_shot_bulk": DCC_ALGO_TWO_SHOT_BULK,
+              "one_shot_ll": DCC_ALGO_ONE_SHOT_LL}
 KIND_CODES = {"input": DCC_BUF_INPUT, "output": DCC_BUF_OUTPUT, "scratch": DCC_BUF_SCRATCH}
 
 # ------------------------------------------------------------------ signatures
@@ -76,6 +80,14 @@ _SIGS = {
     "dcc_launch_shape": [_vp, _sz, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "dcc_shard_range": [_sz, _i, _i, _sz, ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
     "dcc_allreduce_noalloc": [_i, _PP, _PP, _sz, _i, _vp],
+    "dcc_proxy_start": [_vp],
+    "dcc_proxy_stop": [_vp],
+    "dcc_proxy_set_handler": [_vp, _vp, _vp],
+    "dcc_proxy_stats": [_vp, _vp, _vp],
+    "dcc_port_put": [_vp, _i, _i, _sz, _sz, _sz, _i, _i, _vp],
+    "dcc_port_allgather": [_vp, _PP, _PP, _sz, _i, _vp],
+    "dcc_fifo_push": [_vp, _vp, _vp, _i, _vp],
+    "dcc_proxy_state": [_vp, _vp, _i],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -267,6 +279,77 @@ def dcc_allreduce_noalloc(n_ranks, send, recv, count, dtype, stream=None):
 
 
 DCC_NOALLOC_MAX_BYTES = 4 << 20
+
+TRIGGER_HANDLER = ctypes.CFUNCTYPE(None, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p)
+_handlers = {}  # keeps the ctypes callbacks alive per communicator
+
+
+def dcc_proxy_start(comm):
+    return _check(_lib.dcc_proxy_start(comm), "dcc_proxy_start")
+
+
+def dcc_proxy_stop(comm):
+    """Stops the proxy; returns its first error code (0 if none), does not raise."""
+    return _lib.dcc_proxy_stop(comm)
+
+
+def dcc_proxy_set_handler(comm, fn):
+    """fn(fst, snd) runs on the proxy thread for every custom trigger (None removes it)."""
+    key = comm.value if isinstance(comm, ctypes.c_void_p) else int(comm)
+    cb = TRIGGER_HANDLER(lambda fst, snd, user: fn(fst, snd)) if fn is not None else None
+    _handlers[key] = cb
+    return _check(_lib.dcc_proxy_set_handler(comm, ctypes.cast(cb, ctypes.c_void_p) if cb else None,
+                                             None), "dcc_proxy_set_handler")
+
+
+def dcc_proxy_stats(comm):
+    p, cu = ctypes.c_uint64(), ctypes.c_uint64()
+    rc = _lib.dcc_proxy_stats(comm, ctypes.byref(p), ctypes.byref(cu))
+    return rc, p.value, cu.value
+
+
+def dcc_proxy_state(comm, n_ranks):
+    """Diagnostic snapshot: dict with FIFO head/tail, flush word, counts and the
+    port signal / wait matrices [dst][src]."""
+    import numpy as np
+    nw = 6 + 2 * n_ranks * n_ranks
+    w = np.zeros(nw, dtype=np.uint64)
+    _check(_lib.dcc_proxy_state(comm, w.ctypes.data, nw), "dcc_proxy_state")
+    nn = n_ranks * n_ranks
+    return {"head": int(w[0]), "tail": int(w[1]), "done": int(w[2]), "processed": int(w[3]),
+            "custom": int(w[4]), "error": int(w[5].astype(np.int64)),
+            "signals": w[6:6 + nn].reshape(n_ranks, n_ranks), "waits": w[6 + nn:].reshape(n_ranks, n_ranks)}
+
+
+def dcc_port_put(comm, src, dst, remote_off, local_off, nbytes, signal=False, flush=False, stream=None):
+    return _check(_lib.dcc_port_put(comm, src, dst, remote_off, local_off, nbytes, 1 if signal else 0,
+                                    1 if flush else 0, _stream(stream)), "dcc_port_put")
+
+
+def dcc_port_allgather(comm, send, recv, send_count, dtype, stream=None):
+    return _check(_lib.dcc_port_allgather(comm, _ptrs(send), _ptrs(recv), send_count, _dtype(dtype),
+                                          _stream(stream)), "dcc_port_allgather")
+
+
+def dcc_fifo_push(comm, fst, snd=None, stream=None):
+    n = len(fst)
+    f = (ctypes.c_uint64 * n)(*fst)
+    s = (ctypes.c_uint64 * n)(*snd) if snd is not None else None
+    return _check(_lib.dcc_fifo_push(comm, f, s, n, _stream(stream)), "dcc_fifo_push")
+
+
+def prepare_allreduce(comm, send, recv, count, dtype, algo="auto", stream=None):
+    """Marshal the arguments of one dcc_allreduce once and return a callable that
+    repeats exactly that call (for launch loops where Python overhead matters)."""
+    args = (comm, _ptrs(send), _ptrs(recv), count, _dtype(dtype), _code(ALGO_CODES, algo, "algo"),
+            _stream(stream))
+    f = _lib.dcc_allreduce
+
+    def call():
+        rc = f(*args)
+        if rc != DCC_OK:
+            raise DccError(rc, "dcc_allreduce")
+    return call
 
 
 def raw_call(name, *args):

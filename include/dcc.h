@@ -68,9 +68,16 @@ typedef enum {
   DCC_ALGO_AUTO = 0,   /* pick by message size from the measured crossover table */
   DCC_ALGO_ONE_SHOT = 1, /* every rank gets all N inputs and reduces its whole output */
   DCC_ALGO_TWO_SHOT = 2, /* rank r reduces shard r, then puts it into all N outputs */
-  DCC_ALGO_TWO_SHOT_SCRATCH = 3 /* rank r reduces shard r into its scratch, signal/wait,
-                                   then every rank gets all shards from the scratches */
+  DCC_ALGO_TWO_SHOT_SCRATCH = 3, /* rank r reduces shard r into its scratch, signal/wait,
+                                    then every rank gets all shards from the scratches */
+  DCC_ALGO_TWO_SHOT_BULK = 4, /* TWO_SHOT through shared-memory tiles moved by the bulk
+                                 asynchronous copy engine (TMA): bulk gets, bulk puts */
+  DCC_ALGO_ONE_SHOT_LL = 5 /* ONE_SHOT with a low-latency packet protocol: data and flag travel
+                              in the same 16-byte store, no signal/wait round trip; messages of
+                              at most DCC_LL_MAX_BYTES per rank */
 } dcc_algo_t;
+
+#define DCC_LL_MAX_BYTES (256u << 10) /* largest message per rank of DCC_ALGO_ONE_SHOT_LL */
 
 typedef enum { DCC_BUF_INPUT = 0, DCC_BUF_OUTPUT = 1, DCC_BUF_SCRATCH = 2 } dcc_buf_kind_t;
 
@@ -137,11 +144,14 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
                   dcc_dtype_t t, dcc_stream_t s);
 
-/* Host-buffer AllReduce: copies host_send[r] -> dev_send[r] (one
- * cudaMemcpyAsync per rank), runs dcc_allreduce(dev_send, dev_recv), and
- * copies dev_recv[r] -> host_recv[r], all asynchronously on s.  The device
- * buffers follow dcc_allreduce's rules; the host buffers must stay valid until
- * s has drained. */
+/* Host-buffer AllReduce: host_send[r] -> dev_send[r], dcc_allreduce(dev_send,
+ * dev_recv), dev_recv[r] -> host_recv[r], as one stream-ordered operation on s.
+ * The message is pipelined in 8 MiB-per-rank chunks: chunk i is copied in on
+ * the communicator's copy-in stream (one cudaMemcpyAsync per rank), reduced on
+ * s, and copied out on its copy-out stream, so both copy directions and the
+ * kernels overlap.  The device buffers follow dcc_allreduce's rules; the host
+ * buffers (pinned memory for asynchronous copies) must stay valid until s has
+ * drained.  Results are the same bits as dcc_allreduce on the whole message. */
 int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* const* host_recv,
                             void* const* dev_send, void* const* dev_recv, size_t count,
                             dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);
@@ -224,6 +234,70 @@ int dcc_channel_get(dcc_comm_t c, int src_rank, int dst_rank, size_t remote_off,
  * Synchronises s. */
 int dcc_comm_read_semaphores(dcc_comm_t c, int block, uint64_t* inbound, uint64_t* expected,
                              dcc_stream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* PortChannels and the host-side proxy (README, "PortChannel and           */
+/* MemoryChannel", "Host-Side Communication Proxy").  One GPU thread pushes */
+/* 16-byte triggers {fst, snd} into a FIFO in pinned host memory; a proxy   */
+/* thread of the communicator pops them and carries them out: PUT = a      */
+/* cudaMemcpyAsync device-to-device on a copy engine from the source rank's */
+/* first INPUT window to the destination rank's first OUTPUT window; SIGNAL */
+/* and FLUSH = value writes the GPU polls (bounded), all on one proxy       */
+/* stream in FIFO order.  A trigger whose fst is non-zero with bit 63 clear */
+/* is a custom trigger for the installed handler.  Windows must not change  */
+/* while the proxy runs.  The GPU must not multiplex the proxy's stream     */
+/* onto the hardware queue of a kernel that waits for it: with many streams */
+/* set CUDA_DEVICE_MAX_CONNECTIONS=32 before the CUDA context exists.       */
+/* ------------------------------------------------------------------------ */
+
+typedef void (*dcc_trigger_handler_t)(uint64_t fst, uint64_t snd, void* user);
+
+/* Start / stop the proxy thread (ProxyService startProxy/stopProxy).  The first
+ * start allocates the FIFO (pinned host memory), the completion words and the
+ * proxy's streams; every start loads all of libdcc's kernels into the context.
+ * PortChannel kernels wait on the proxy's CUDA calls: a host call that waits
+ * for the running kernels (the first launch of a kernel under lazy module
+ * loading, a device-wide synchronisation) stalls the proxy until the waiting
+ * kernel's limit runs out.  Load the application's own kernels before running
+ * PortChannel kernels (e.g. CUDA_MODULE_LOADING=EAGER).  Stop reads how many triggers GPU threads have claimed
+ * (call it after the pushing kernels have finished), lets the thread carry
+ * those out (at most 5 s), joins it, waits for the proxy's copies, and returns
+ * DCC_OK or the first error a trigger hit (NOT_REGISTERED, CUDA). */
+int dcc_proxy_start(dcc_comm_t c);
+int dcc_proxy_stop(dcc_comm_t c);
+
+/* Install the handler for custom triggers (custom proxy); proxy stopped.
+ * fn runs on the proxy thread, in FIFO order.  NULL removes it. */
+int dcc_proxy_set_handler(dcc_comm_t c, dcc_trigger_handler_t fn, void* user);
+
+/* Triggers the proxy has taken so far, and how many were custom.  Returns the
+ * proxy's first error (or DCC_OK).  INVALID_ARG before the first start. */
+int dcc_proxy_stats(dcc_comm_t c, uint64_t* processed, uint64_t* custom);
+
+/* Diagnostic snapshot (synchronous): words[0..5] = FIFO head (claimed by GPU
+ * threads), tail (taken by the proxy), flush word, triggers processed, custom
+ * triggers, first error; then N*N port signal counts [dst][src] and N*N
+ * completed port waits [dst][src].  nwords >= 6 + 2*N*N. */
+int dcc_proxy_state(dcc_comm_t c, uint64_t* words, int nwords);
+
+/* PortChannel put: one GPU thread of src pushes PUT (+SIGNAL if signal != 0)
+ * for dst.OUTPUT[remote_off, +bytes) <- src.INPUT[local_off, +bytes); with
+ * flush != 0 it then waits until the proxy has carried the copy out; with
+ * signal != 0 a thread of dst waits for the signal.  Offsets and bytes are
+ * multiples of 16.  Needs a running proxy (INVALID_ARG otherwise). */
+int dcc_port_put(dcc_comm_t c, int src_rank, int dst_rank, size_t remote_off, size_t local_off,
+                 size_t bytes, int signal, int flush, dcc_stream_t s);
+
+/* AllGather through PortChannels (copy engines driven by the proxy):
+ * recv[p][q*send_count + j] = send[q][j].  send[q] must lie in rank q's first
+ * INPUT window and recv[p] in rank p's first OUTPUT window; send_count *
+ * element size must be a multiple of 16.  Same result as dcc_allgather. */
+int dcc_port_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
+                       dcc_dtype_t t, dcc_stream_t s);
+
+/* Push `count` (<= 32) custom triggers {fst[i], snd[i]} from one GPU thread
+ * (snd may be NULL: zeros).  fst[i] must be non-zero with bit 63 clear. */
+int dcc_fifo_push(dcc_comm_t c, const uint64_t* fst, const uint64_t* snd, int count, dcc_stream_t s);
 
 /* ------------------------------------------------------------------------ */
 /* Tuning and test knobs.                                                   */

@@ -3,6 +3,11 @@ import sys
 
 import pytest
 
+# PortChannel kernels wait on the host proxy's stream: give every stream its
+# own hardware queue so that stream cannot queue behind the waiting kernel
+# (must be set before the CUDA context exists).
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

@@ -102,6 +102,13 @@ def test_null_communicator_is_rejected(dcc):
         ("dcc_select_algo", None, 4, 1, ctypes.byref(i)),
         ("dcc_debug_skip_signal", None, 0),
         ("dcc_launch_shape", None, 4, 1, 0, ctypes.byref(i), ctypes.byref(i)),
+        ("dcc_proxy_start", None),
+        ("dcc_proxy_stop", None),
+        ("dcc_proxy_set_handler", None, None, None),
+        ("dcc_proxy_stats", None, None, None),
+        ("dcc_port_put", None, 0, 1, 0, 0, 16, 0, 0, None),
+        ("dcc_port_allgather", None, arr, arr, 4, 1, None),
+        ("dcc_fifo_push", None, None, None, 1, None),
     ]
     for name, *args in calls:
         assert dcc.raw_call(name, *args) == dcc.DCC_ERR_INVALID_ARG, name

@@ -16,7 +16,7 @@ from driven_collective_communication_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 RECIPES = {"fp32": W.C1, "int32": W.C2, "bf16": W.C4, "fp16": W.C5}
-ALGOS = ("one_shot", "two_shot", "two_shot_scratch")
+ALGOS = ("one_shot", "two_shot", "two_shot_scratch", "two_shot_bulk", "one_shot_ll")
 
 
 @pytest.fixture(scope="module")
@@ -69,7 +69,15 @@ class Arena:
 
 
 def run_allreduce(dcc, arena, xs_host, dtype, algo, inplace, offset=0):
+    """One AllReduce through the C ABI; None when the algorithm rejects the size
+    (LL beyond its maximum, checked to be DCC_ERR_UNSUPPORTED)."""
     count = xs_host[0].numel()
+    if algo == "one_shot_ll" and count * W.ELEM_BYTES[dtype] > dcc.DCC_LL_MAX_BYTES:
+        send = arena.view(arena.inp, dtype, count, offset)
+        with pytest.raises(dcc.DccError) as e:
+            dcc.dcc_allreduce(arena.comm.handle, send, send, count, dtype, algo)
+        assert e.value.code == dcc.DCC_ERR_UNSUPPORTED
+        return None
     send = arena.view(arena.inp, dtype, count, offset)
     for r in range(arena.n):
         send[r].copy_(xs_host[r])
@@ -99,7 +107,7 @@ def test_allreduce_parity_sweep(dcc, n):
                 for algo in ALGOS:
                     for inplace in (False, True):
                         outs = run_allreduce(dcc, arena, xs, dtype, algo, inplace)
-                        for r in range(n):
+                        for r in range(n if outs is not None else 0):
                             assert same(outs[r], expect, dtype), (dtype, count, algo, inplace, r)
     finally:
         arena.close()
@@ -132,10 +140,31 @@ def test_allreduce_special_values(dcc, dtype):
         for algo in ALGOS:
             for inplace in (False, True):
                 outs = run_allreduce(dcc, arena, xs, dtype, algo, inplace)
-                for r in range(n):
+                for r in range(n if outs is not None else 0):
                     assert same(outs[r], expect, dtype), (algo, inplace, r)
     finally:
         arena.close()
+
+
+def test_allgather_bulk_and_thread_paths_agree(dcc, monkeypatch):
+    """The bulk-copy AllGather and the thread-copy AllGather produce the same bytes."""
+    n, m = 8, 3 * 16384 // 2 + 8  # fp16: 48 KiB + 16 B per rank, several 16 KiB tiles + a partial one
+    m = 2 * m  # > 64 KiB per rank: the bulk path
+    xs = [torch.randn(m, device="cuda").half() for _ in range(n)]
+    outs = {}
+    for flag in ("1", "0"):
+        monkeypatch.setenv("DCC_AG_BULK", flag)
+        ys = [torch.full((n * m,), float("nan"), device="cuda").half() for _ in range(n)]
+        with dcc.Comm(n) as comm:
+            comm.register_all("input", xs)
+            comm.register_all("output", ys)
+            comm.allgather(xs, ys)
+            assert comm.check() == dcc.DCC_OK
+        outs[flag] = ys
+    ref = torch.cat(xs).view(torch.int16)
+    for r in range(n):
+        assert torch.equal(outs["1"][r].view(torch.int16), ref)
+        assert torch.equal(outs["0"][r].view(torch.int16), ref)
 
 
 def test_launch_shape_does_not_change_bits(dcc):
@@ -151,7 +180,8 @@ def test_launch_shape_does_not_change_bits(dcc):
             for algo in ALGOS:
                 for inplace in (False, True):
                     outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace)
-                    assert all(same(o, expect, "bf16") for o in outs), (blocks, algo, inplace)
+                    assert outs is None or all(same(o, expect, "bf16") for o in outs), \
+                        (blocks, algo, inplace)
     finally:
         arena.close()
 
@@ -199,9 +229,10 @@ def test_c3_bf16_decode_sizes(dcc, tokens):
     arena = Arena(dcc, 8, w.count, elem_bytes=2)
     try:
         for algo in ALGOS:
-            outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace=False)
-            for o in outs:
-                assert same(o, expect, "bf16"), algo
+            for inplace in (False, True):
+                outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace=inplace)
+                for o in outs or []:
+                    assert same(o, expect, "bf16"), (algo, inplace)
     finally:
         arena.close()
 
@@ -218,25 +249,29 @@ def sampled_indices(count, n, k=200000, seed=0):
 
 
 def test_c4_bf16_n8_256MiB_sampled(dcc):
-    """Full size, the launch configuration the benchmark times (AUTO -> two-shot
-    push), checked on sampled elements one by one and by the identical-ranks
-    invariant over every element."""
+    """Full size, the launch configuration the benchmark times (AUTO) and every
+    other large-message schedule, checked on sampled elements one by one and by
+    the identical-ranks invariant over every element."""
     w = W.C4
     xs = W.rank_inputs(w, device="cuda")
     recv = [torch.empty_like(x) for x in xs]
     comm = dcc.Comm(8)
+    idx = sampled_indices(w.count, 8)
+    idx_t = torch.from_numpy(idx).cuda()
+    host = [W.to_storage(x[idx_t]) for x in xs]
+    expect = oracle.allreduce(host, "bf16")  # elementwise: sampled columns
     try:
         comm.register_all("input", xs)
         comm.register_all("output", recv)
-        comm.allreduce(xs, recv, algo="auto")
-        assert comm.check() == dcc.DCC_OK
-        for r in range(1, 8):
-            assert torch.equal(recv[r].view(torch.int16), recv[0].view(torch.int16))
-        idx = sampled_indices(w.count, 8)
-        idx_t = torch.from_numpy(idx).cuda()
-        host = [W.to_storage(x[idx_t]) for x in xs]
-        expect = oracle.allreduce(host, "bf16")  # elementwise: sampled columns
-        assert same(W.to_storage(recv[3][idx_t]), expect, "bf16")
+        for algo in ("auto", "two_shot", "two_shot_bulk"):
+            for r in range(8):
+                recv[r].fill_(0)
+            comm.allreduce(xs, recv, algo=algo)
+            assert comm.check() == dcc.DCC_OK
+            for r in range(1, 8):
+                assert torch.equal(recv[r].view(torch.int16), recv[0].view(torch.int16)), algo
+            for r in (0, 3, 7):
+                assert same(W.to_storage(recv[r][idx_t]), expect, "bf16"), (algo, r)
     finally:
         comm.close()
 
@@ -270,7 +305,8 @@ def test_c5_fp16_reduce_scatter_and_allgather_full(dcc):
         comm.close()
 
 
-@pytest.mark.parametrize("n,count", [(2, 1), (3, 5), (8, 1000), (8, 1001), (5, 77777), (16, 4096)])
+@pytest.mark.parametrize("n,count", [(2, 1), (3, 5), (8, 1000), (8, 1001), (5, 77777), (16, 4096),
+                                     (8, 40960), (3, 50000), (2, 262144 + 8)])
 @pytest.mark.parametrize("dtype", ["int32", "fp32", "fp16", "bf16"])
 def test_reduce_scatter_allgather_ragged(dcc, n, count, dtype):
     """Shards that do not start on 16-byte boundaries take the element path."""
@@ -355,9 +391,11 @@ def test_repeated_calls_never_need_a_reset(dcc):
         for i in range(5000):
             dcc.dcc_allreduce(h, send, recv, count, "int32", "two_shot_scratch")
             dcc.dcc_allreduce(h, recv, recv, count, "int32", "one_shot")
+            dcc.dcc_allreduce(h, send, recv, count, "int32", "one_shot_ll")
+            dcc.dcc_allreduce(h, recv, recv, count, "int32", "one_shot_ll")
         dcc.dcc_ring_barrier(h, 100)
         assert arena.comm.check() == dcc.DCC_OK
-        # recv = 8 * sum(x) after each pair; it is recomputed from send every time
+        # recv = 8 * sum(x) after each group; it is recomputed from send every time
         expect = oracle.allreduce([W.to_storage(x) for x in xs], "int32").astype(np.int64) * n
         expect = ((expect + 2 ** 31) % 2 ** 32 - 2 ** 31).astype(np.int32)
         for r in range(n):
@@ -389,6 +427,8 @@ def test_graph_replay_keeps_epochs(dcc):
             dcc.dcc_allreduce(h, send, recv, count, "bf16", "two_shot_scratch", stream=s)
             dcc.dcc_allreduce(h, send, recv, count, "bf16", "one_shot", stream=s)
             dcc.dcc_allreduce(h, send, recv, count, "bf16", "two_shot", stream=s)
+            dcc.dcc_allreduce(h, send, recv, count, "bf16", "two_shot_bulk", stream=s)
+            dcc.dcc_allreduce(h, send, recv, count, "bf16", "one_shot_ll", stream=s)
         for _ in range(200):
             g.replay()
         torch.cuda.synchronize()
@@ -490,22 +530,32 @@ def test_argument_errors(dcc):
         comm.close()
 
 
-def test_allreduce_from_host(dcc):
-    n, count = 8, 300001
+@pytest.mark.parametrize("count,inplace", [(300001, False), (3 * 4194304 + 13, False),
+                                           (2 * 4194304 + 8, True)])
+def test_allreduce_from_host(dcc, count, inplace):
+    """Host buffers in, host buffers out, pipelined in 8 MiB-per-rank chunks
+    (one chunk; three chunks with a ragged last one; in place)."""
+    n = 8
     w = W.with_count(W.C4, count)
     xs = [x.pin_memory() for x in W.rank_inputs(w)]
     outs = [torch.empty_like(x).pin_memory() for x in xs]
     dev_in = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
-    dev_out = [torch.empty_like(d) for d in dev_in]
+    dev_out = dev_in if inplace else [torch.empty_like(d) for d in dev_in]
     comm = dcc.Comm(n)
     try:
         comm.register_all("input", dev_in)
-        comm.register_all("output", dev_out)
-        dcc.dcc_allreduce_from_host(comm.handle, xs, outs, dev_in, dev_out, count, "bf16")
-        assert comm.check() == dcc.DCC_OK
-        expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
-        for o in outs:
-            assert same(W.to_storage(o), expect, "bf16")
+        if not inplace:
+            comm.register_all("output", dev_out)
+        s = torch.cuda.Stream()
+        for _ in range(2):  # twice: the second call reuses the pipeline's streams and events
+            for o in outs:
+                o.zero_()
+            dcc.dcc_allreduce_from_host(comm.handle, xs, outs, dev_in, dev_out, count, "bf16",
+                                        stream=s)
+            assert comm.check(s) == dcc.DCC_OK
+            expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16", nthreads=8)
+            for o in outs:
+                assert same(W.to_storage(o), expect, "bf16")
     finally:
         comm.close()
 
