@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from driven_collective_communication_gb300 import workloads as W  # noqa: E402
+from driven_collective_communication_gb300.replicas import Dist  # noqa: E402
 
 GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
@@ -43,46 +44,6 @@ KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "c
 
 
 # ------------------------------------------------------------------ helpers
-def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
-
-
-class Dist:
-    def __init__(self):
-        self.ws, self.rank, self.local = dist_env()
-        self.pg = None
-        if self.ws > 1:
-            import torch.distributed as td
-            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-            td.init_process_group("gloo", rank=self.rank, world_size=self.ws)
-            self.pg = td
-
-    def barrier(self):
-        if self.pg:
-            self.pg.barrier()
-
-    def max(self, x):
-        if not self.pg:
-            return x
-        t = torch.tensor([float(x)], dtype=torch.float64)
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum(self, x):
-        if not self.pg:
-            return x
-        t = torch.tensor([float(x)], dtype=torch.float64)
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
-        return float(t.item())
-
-    def close(self):
-        if self.pg:
-            self.pg.destroy_process_group()
-
-
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -415,6 +376,28 @@ def other_workloads(dcc, dev, stream):
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
     del xs, ys, scr
+    # more ranks and another dtype at the large size (two-shot push, 256 MiB per rank)
+    for n_ranks, dtype in ((2, "bf16"), (4, "bf16"), (16, "bf16"), (8, "fp32")):
+        recipe = W.C4 if dtype == "bf16" else W.C1
+        count = (256 << 20) // W.ELEM_BYTES[dtype]
+        wk = W.with_count(recipe, count, n_ranks=n_ranks)
+        with torch.cuda.stream(stream):
+            xs = W.rank_inputs(wk, device=dev)
+            ys = [torch.empty_like(x) for x in xs]
+        torch.cuda.synchronize()
+        with dcc.Comm(n_ranks) as cn:
+            cn.register_all("input", xs)
+            cn.register_all("output", ys)
+            step = dcc.prepare_allreduce(cn.handle, xs, ys, count, dtype, "auto", stream)
+            for _ in range(3):
+                step()
+            per, _ = time_launches(step, 20, stream)
+            assert cn.check(stream) == dcc.DCC_OK
+        ms = statistics.median(per)
+        out["allreduce_%s_n%d_256MiB" % (dtype, n_ranks)] = {
+            "ms": round(ms, 4), "algbw_gbs": round((256 << 20) / ms / 1e6, 1),
+            "hbm_gbs_2NS": round(2 * n_ranks * (256 << 20) / ms / 1e6, 1)}
+        del xs, ys
     w = W.C2
     with torch.cuda.stream(stream):
         xs = W.rank_inputs(w, device=dev)

@@ -40,9 +40,10 @@ def _load():
         lib.orc_ring_barrier_counts.argtypes = [i32, ctypes.c_uint64, vp]
         lib.orc_convert_to_f32.argtypes = [vp, vp, sz, i32]
         lib.orc_convert_from_f32.argtypes = [vp, vp, sz, i32]
+        lib.orc_linear_allreduce.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, sz, i32, vp]
         for name in ("orc_allreduce", "orc_allreduce_at", "orc_allreduce_mt",
                      "orc_reduce_scatter", "orc_allgather", "orc_ring_barrier_counts",
-                     "orc_convert_to_f32", "orc_convert_from_f32"):
+                     "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -136,6 +137,24 @@ def from_f32(vals, dtype):
     out = np.empty(len(vals), dtype=np.uint16)
     _ok(lib.orc_convert_from_f32(vals.ctypes.data, out.ctypes.data, len(vals), DTYPES[dtype]),
         "from_f32")
+    return out
+
+
+def linear_allreduce(ws, xs, dtype, rows, kp):
+    """y[i] = R(sum_p sum_k W_p[i, k] x_p[k]) for rank weights ws[p] (rows*kp,
+    row-major) and inputs xs[p] (kp): the row-parallel linear layer + AllReduce."""
+    lib = _load()
+    if dtype not in ("fp16", "bf16"):
+        raise ValueError("fp16 or bf16 only")
+    warrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in ws]
+    xarrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in xs]
+    if len(warrs) != len(xarrs) or any(len(a) != rows * kp for a in warrs) or any(len(a) != kp for a in xarrs):
+        raise ValueError("shapes")
+    wp = (ctypes.c_void_p * len(warrs))(*[a.ctypes.data for a in warrs])
+    xp = (ctypes.c_void_p * len(xarrs))(*[a.ctypes.data for a in xarrs])
+    out = np.empty(rows, dtype=np.uint16)
+    _ok(lib.orc_linear_allreduce(len(warrs), wp, xp, rows, kp, DTYPES[dtype], out.ctypes.data),
+        "linear_allreduce")
     return out
 
 

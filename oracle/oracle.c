@@ -277,6 +277,30 @@ int orc_ring_barrier_counts(int n, uint64_t iters, uint64_t* counts)
     return 0;
 }
 
+/* ---------------------------------------------------------------------- */
+/* Row-parallel linear layer followed by the sum AllReduce (tensor-parallel */
+/* decode: every rank holds a slice of the contraction dimension).          */
+/*   y[i] = R( sum_p sum_k W_p[i][k] * x_p[k] ),  i < rows, k < kp          */
+/* W_p is rows x kp row-major, x_p has kp elements (fp16 or bf16).  The     */
+/* products of two 16-bit floats are exact in binary64 and the sum is taken */
+/* in binary64 (for the small-integer inputs the tests pin it with, exactly */
+/* the real sum), then rounded once to the output type.                     */
+/* ---------------------------------------------------------------------- */
+int orc_linear_allreduce(int n, const void* const* w, const void* const* x, size_t rows, size_t kp,
+                         int dtype, void* out)
+{
+    if (n < 1 || !w || !x || (rows && !out) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    for (int p = 0; p < n; ++p) if (!w[p] || !x[p]) return -1;
+    for (size_t i = 0; i < rows; ++i) {
+        double acc = 0.0;
+        for (int p = 0; p < n; ++p)
+            for (size_t k = 0; k < kp; ++k)
+                acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);
+        narrow_store(out, i, (float)acc, dtype);
+    }
+    return 0;
+}
+
 /* exported conversions over arrays (used by the tests' pins) */
 int orc_convert_to_f32(const uint16_t* src, float* dst, size_t count, int dtype)
 {

@@ -352,3 +352,46 @@ def test_rejects_bad_arguments():
         oracle.allreduce([np.zeros(3, np.float32)], "fp64")
     with pytest.raises(ValueError):
         oracle.reduce_scatter([np.zeros(3, np.float32)] * 2, "fp32", 1, 2)
+
+
+# --------------------------------------------------------------------- fused linear + AllReduce
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_allreduce_closed_forms(dtype):
+    """All-ones weights and inputs give N*kp in every row; a one-hot input
+    picks one weight column per rank; a rank's zero input drops that rank."""
+    n, rows, kp = 4, 16, 32
+    one = value_to_storage(1, dtype)
+    ws = [np.full(rows * kp, one, np.uint16) for _ in range(n)]
+    xs = [np.full(kp, one, np.uint16) for _ in range(n)]
+    got = storage_to_float(oracle.linear_allreduce(ws, xs, dtype, rows, kp), dtype)
+    assert np.all(got == n * kp)
+    rng = np.random.default_rng(1)
+    ws = [np.array([value_to_storage(v, dtype) for v in rng.integers(-3, 4, size=rows * kp)],
+                   np.uint16) for _ in range(n)]
+    xs = []
+    for p in range(n):
+        x = np.full(kp, value_to_storage(0, dtype), np.uint16)
+        x[p] = one  # rank p selects its column p
+        xs.append(x)
+    expect = sum(storage_to_float(ws[p], dtype).reshape(rows, kp)[:, p] for p in range(n))
+    got = storage_to_float(oracle.linear_allreduce(ws, xs, dtype, rows, kp), dtype)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_allreduce_matches_float64_matmul(dtype):
+    """Against numpy's float64 matrix product of the concatenated shards,
+    rounded once to the output type (a library routine, not the oracle's loop)."""
+    n, rows, kp = 3, 24, 40
+    rng = np.random.default_rng(2)
+    ws = [W.to_storage(torch.randn(rows * kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    xs = [W.to_storage(torch.randn(kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    a = np.concatenate([storage_to_float(w, dtype).reshape(rows, kp) for w in ws], axis=1)
+    x = np.concatenate([storage_to_float(v, dtype) for v in xs])
+    ref = W.to_storage(torch.from_numpy(a @ x).float().to(W.TORCH_DTYPES[dtype]))
+    got = oracle.linear_allreduce(ws, xs, dtype, rows, kp)
+    # the fp64 sums of a float64 matmul may differ from the oracle's loop in the
+    # last bits of binary64; after rounding to 16 bits they agree except at
+    # ties, which random normal data does not produce
+    assert np.array_equal(got, ref)
+    del rng

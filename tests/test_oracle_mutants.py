@@ -39,6 +39,8 @@ MUTANTS = {
         "orc_f32_to_f16(t) : orc_f32_to_bf16(t); acc = dtype == ORC_FP32 ? t : (dtype == ORC_FP16 ? "
         "orc_f16_to_f32(h) : orc_bf16_to_f32(h)); }"),
     "ring_wrong_neighbour": ("(s == (d + n - 1) % n)", "(s == (d + 1) % n)"),
+    "linear_drops_rank_weight": ("acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);",
+                                 "acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p ? p - 1 : 0], k, dtype);"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
