@@ -455,6 +455,54 @@ def other_workloads(dcc, dev, stream):
         ms = statistics.median(per)
         out["c5_allgather_port_channel"] = {"ms": round(ms, 4), "hbm_gbs": round(
             (w.bytes_per_rank + 8 * w.bytes_per_rank) / ms / 1e6, 1)}
+    # fused row-parallel linear + AllReduce vs per-rank GEMV (cuBLAS) then AllReduce,
+    # tensor-parallel decode shapes: hidden 8192 rows, 8 ranks, kp = 1024 and 3584
+    for kp in (1024, 3584):
+        rows = 8192
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+        xin = [torch.randn(kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
+        yf = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        part = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        ysep = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        with dcc.Comm(8) as lc:
+            lc.register_all("input", wts)
+            lc.register_all("input", xin)
+            lc.register_all("output", yf)
+            lc.register_all("input", part)
+            lc.register_all("output", ysep)
+            fused = lambda: dcc.dcc_linear_allreduce(lc.handle, wts, xin, yf, rows, kp, "bf16", stream)  # noqa
+            ar = dcc.prepare_allreduce(lc.handle, part, ysep, rows, "bf16", "auto", stream)
+
+            def unfused():
+                with torch.cuda.stream(stream):
+                    for r in range(8):
+                        torch.matmul(wts[r], xin[r], out=part[r])
+                ar()
+            res = {}
+            for name, fn in (("fused", fused), ("gemv_then_allreduce", unfused)):
+                for _ in range(5):
+                    fn()
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g2, stream=stream):
+                    for _ in range(20):
+                        fn()
+                with torch.cuda.stream(stream):
+                    g2.replay()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(5):
+                        g2.replay()
+                    e1.record(stream)
+                e1.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / 100
+                res[name + "_us"] = round(us, 2)
+                res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
+            assert lc.check(stream) == dcc.DCC_OK
+        out["linear_allreduce_bf16_n8_rows8192_kp%d" % kp] = res
+        del wts, xin, yf, part, ysep
     with dcc.Comm(8, connect="ring") as ring:
         ring.ring_barrier(100, stream)
         e0 = torch.cuda.Event(enable_timing=True)

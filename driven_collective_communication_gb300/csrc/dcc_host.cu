@@ -19,6 +19,7 @@
 #include "ll.cuh"
 #include "collectives.cuh"
 #include "comm.h"
+#include "fused.cuh"
 #include "sync_kernels.cuh"
 
 namespace {
@@ -236,6 +237,8 @@ int dcc_preload_kernels() {
     for (int n : ns)
       for (int kind = dcc::kOneShot; kind <= dcc::kOneShotLL; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
   for (int n : ns) ok &= load(dcc::allgather_kernel(n)) && load(dcc::allgather_bulk_kernel(n));
+  for (int n : ns)
+    ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n));
   ok &= load(dcc::ring_barrier_kernel()) && load(dcc::channel_put_kernel()) && load(dcc::channel_get_kernel());
   return ok ? DCC_OK : DCC_ERR_CUDA;
 }
@@ -534,6 +537,54 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   rc = pick_blocks(c, fn, threads, work, &args.blocks);
   if (rc != DCC_OK) return rc;
   return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
+}
+
+int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
+                         size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+  if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
+  if (rows % dcc::kFusedRows || kp % 8) return DCC_ERR_UNSUPPORTED;
+  if (rows == 0 || kp == 0) return DCC_OK;
+  const size_t eb = 2;
+  if (rows > ((size_t)1 << 40) / kp) return DCC_ERR_INVALID_ARG;
+  const size_t wb = rows * kp * eb, xb = kp * eb, yb = rows * eb;
+  for (int r = 0; r < c->n; ++r) {
+    if (!weight[r] || !x[r] || !y[r]) return DCC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(weight[r]) | reinterpret_cast<uintptr_t>(x[r]) |
+         reinterpret_cast<uintptr_t>(y[r])) & 15u)
+      return DCC_ERR_MISALIGNED;
+    const void* ptrs[3] = {weight[r], x[r], y[r]};
+    const size_t lens[3] = {wb, xb, yb};
+    for (int j = 0; j < 3; ++j)
+      if (!in_window(c, r, DCC_BUF_INPUT, ptrs[j], lens[j]) && !in_window(c, r, DCC_BUF_OUTPUT, ptrs[j], lens[j]))
+        return DCC_ERR_NOT_REGISTERED;
+  }
+  for (int r = 0; r < c->n; ++r)
+    for (int p = 0; p < c->n; ++p) {
+      if (overlaps(y[r], yb, weight[p], wb) || overlaps(y[r], yb, x[p], xb)) return DCC_ERR_INVALID_ARG;
+      if (p != r && overlaps(y[r], yb, y[p], yb)) return DCC_ERR_INVALID_ARG;
+    }
+  int rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  dcc::LinearArgs a{};
+  for (int r = 0; r < c->n; ++r) {
+    a.weight[r] = weight[r];
+    a.x[r] = x[r];
+    a.y[r] = y[r];
+  }
+  a.rows = rows;
+  a.kp = kp;
+  const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
+                                 : dcc::linear_allreduce_kernel<__half>(c->n);
+  const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // 8-row items per rank
+  rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, dcc::kFusedThreads / 32);
+  if (rc != DCC_OK) return rc;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &a};
+  return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s));
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {

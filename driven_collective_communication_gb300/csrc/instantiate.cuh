@@ -2,6 +2,7 @@
 // so the four types compile in parallel).
 #pragma once
 #include "bulk.cuh"
+#include "fused.cuh"
 #include "ll.cuh"
 
 namespace dcc {
@@ -32,6 +33,18 @@ const void* reduce_kernel_impl(int kind, int n) {
     case 8: return pick_kernel<T, 8>(kind);
     case 16: return pick_kernel<T, 16>(kind);
     default: return pick_kernel<T, 0>(kind);
+  }
+}
+
+template <typename T>
+const void* linear_kernel_impl(int n) {
+  switch (n) {
+    case 1: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 1>);
+    case 2: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 2>);
+    case 4: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 4>);
+    case 8: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 8>);
+    case 16: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 16>);
+    default: return reinterpret_cast<const void*>(&k_linear_allreduce<T, 0>);
   }
 }
 

@@ -88,6 +88,7 @@ _SIGS = {
     "dcc_port_allgather": [_vp, _PP, _PP, _sz, _i, _vp],
     "dcc_fifo_push": [_vp, _vp, _vp, _i, _vp],
     "dcc_proxy_state": [_vp, _vp, _i],
+    "dcc_linear_allreduce": [_vp, _PP, _PP, _PP, _sz, _sz, _i, _vp],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -197,6 +198,11 @@ def dcc_allreduce_from_host(comm, host_send, host_recv, dev_send, dev_recv, coun
                                                _ptrs(dev_send), _ptrs(dev_recv), count,
                                                _dtype(dtype), _code(ALGO_CODES, algo, "algo"),
                                                _stream(stream)), "dcc_allreduce_from_host")
+
+
+def dcc_linear_allreduce(comm, weight, x, y, rows, kp, dtype, stream=None):
+    return _check(_lib.dcc_linear_allreduce(comm, _ptrs(weight), _ptrs(x), _ptrs(y), rows, kp,
+                                            _dtype(dtype), _stream(stream)), "dcc_linear_allreduce")
 
 
 def dcc_ring_barrier(comm, iters, stream=None):

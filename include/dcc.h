@@ -156,6 +156,20 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
                             void* const* dev_send, void* const* dev_recv, size_t count,
                             dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);
 
+/* Row-parallel linear layer fused with the AllReduce (tensor-parallel decode;
+ * the project summary's communication-to-computation overlap): rank p holds
+ * weight[p] (rows x kp, row-major) and x[p] (kp elements), and every rank
+ * receives y[r][i] = R(sum_p sum_k weight[p][i*kp + k] * x[p][k]), i < rows.
+ * One kernel: rank r's CTAs compute shard r of the rows, getting every rank's
+ * weight rows and input slice, accumulate fp32 dot products, add the ranks'
+ * partials in rank order, and put the result into all N outputs.  fp16/bf16;
+ * rows and kp multiples of 8 (UNSUPPORTED otherwise); 16-byte aligned,
+ * registered, outputs disjoint from every input.  The dot products use a
+ * fixed lane/shuffle order: exact when every fp32 partial sum is exact, else
+ * within the fp32 dot-product error bound before the final rounding. */
+int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
+                         size_t kp, dcc_dtype_t t, dcc_stream_t s);
+
 /* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
  * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
  * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One

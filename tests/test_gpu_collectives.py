@@ -449,10 +449,10 @@ def test_lost_signal_times_out_cleanly(dcc):
         dcc.dcc_debug_skip_signal(comm.handle, 1)
         comm.ring_barrier(10)
         assert comm.check() == dcc.DCC_ERR_TIMEOUT
-        # ranks 2, 3 and 0 all wait from the start; whichever gives up first
-        # records itself, always as a wait on its ring predecessor
+        # once rank 1's signal is lost every rank ends up waiting on its ring
+        # predecessor; whichever wait gives up first records itself
         rank, peer, block = dcc.dcc_comm_error_detail(comm.handle)
-        assert rank in (2, 3, 0) and (rank - peer) % n == 1 and block == 0
+        assert 0 <= rank < n and (rank - peer) % n == 1 and block == 0
         with pytest.raises(dcc.DccError) as e:
             comm.ring_barrier(1)
         assert e.value.code == dcc.DCC_ERR_TIMEOUT

@@ -1,0 +1,101 @@
+"""Row-parallel linear layer fused with the AllReduce, against the oracle.
+
+Small-integer data make every fp32 partial sum exact, so the kernel must match
+the oracle bit for bit whatever its internal order.  Random data are held to
+the fp32 dot-product bound: |acc - exact| <= (kp + N) * 2^-24 * sum|w x| before
+one rounding to the output type, i.e. |y - y_oracle| <= 2 (kp + N) 2^-24 S + ulp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from driven_collective_communication_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TD = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def dcc():
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc as mod
+    torch.cuda.set_device(0)
+    return mod
+
+
+def run(dcc, ws, xs, rows, kp, dtype):
+    n = len(ws)
+    dw = [w.cuda() for w in ws]
+    dx = [x.cuda() for x in xs]
+    dy = [torch.full((rows,), float("nan"), dtype=TD[dtype], device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", dw)
+        for r in range(n):
+            comm.register(r, "input", dx[r])
+        comm.register_all("output", dy)
+        dcc.dcc_linear_allreduce(comm.handle, dw, dx, dy, rows, kp, dtype)
+        assert comm.check() == dcc.DCC_OK
+    for r in range(1, n):
+        assert torch.equal(dy[r].view(torch.int16), dy[0].view(torch.int16))
+    return W.to_storage(dy[0])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,rows,kp", [(1, 8, 8), (2, 64, 40), (8, 1032, 1032), (16, 256, 1024),
+                                        (5, 136, 2056), (8, 8192, 64)])
+def test_integer_data_bit_exact(dcc, dtype, n, rows, kp):
+    g = torch.Generator().manual_seed(n * 1000 + kp)
+    ws = [torch.randint(-3, 4, (rows * kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randint(-3, 4, (kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+    got = run(dcc, ws, xs, rows, kp, dtype)
+    expect = oracle.linear_allreduce([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                     dtype, rows, kp)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,rows,kp", [(8, 8192, 1024), (8, 512, 3584), (3, 64, 4104)])
+def test_random_data_within_bound(dcc, dtype, n, rows, kp):
+    g = torch.Generator().manual_seed(7 + n + kp)
+    ws = [(torch.randn(rows * kp, generator=g) * 0.05).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randn(kp, generator=g).to(TD[dtype]) for _ in range(n)]
+    got = run(dcc, ws, xs, rows, kp, dtype)
+    expect = oracle.linear_allreduce([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                     dtype, rows, kp)
+    gf = W.from_storage(got, dtype).double().numpy()
+    ef = W.from_storage(expect, dtype).double().numpy()
+    s = sum(np.abs(w.double().numpy().reshape(rows, kp)) @ np.abs(x.double().numpy())
+            for w, x in zip(ws, xs))
+    big = np.maximum(np.abs(gf), np.abs(ef))
+    ulp = np.abs(np.spacing(big.astype(np.float16 if dtype == "fp16" else np.float32)).astype(np.float64))
+    if dtype == "bf16":
+        ulp = np.exp2(np.floor(np.log2(np.maximum(big, 2.0 ** -126))) - 7)
+    bound = 2 * (kp + n) * 2.0 ** -24 * s + ulp
+    assert np.all(np.abs(gf - ef) <= bound)
+    # and nearly always the same bits
+    assert np.mean(got == expect) > 0.98
+
+
+def test_argument_errors(dcc):
+    n, rows, kp = 2, 16, 16
+    ws = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    xs = [torch.zeros(kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ys = [torch.zeros(rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", ws)
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        h = comm.handle
+        for args, code in [((rows - 1, kp, "bf16"), dcc.DCC_ERR_UNSUPPORTED),
+                           ((rows, kp - 4, "bf16"), dcc.DCC_ERR_UNSUPPORTED),
+                           ((rows, kp, "fp32"), dcc.DCC_ERR_UNSUPPORTED),
+                           ((rows * 2, kp, "bf16"), dcc.DCC_ERR_NOT_REGISTERED)]:
+            with pytest.raises(dcc.DccError) as e:
+                dcc.dcc_linear_allreduce(h, ws, xs, ys, *args)
+            assert e.value.code == code, args
+        with pytest.raises(dcc.DccError) as e:  # output overlapping a weight
+            dcc.dcc_linear_allreduce(h, ws, xs, [ws[0][:rows], ys[1]], rows, kp, "bf16")
+        assert e.value.code == dcc.DCC_ERR_INVALID_ARG
+        assert comm.check() == dcc.DCC_OK
