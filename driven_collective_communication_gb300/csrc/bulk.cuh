@@ -2,8 +2,8 @@
 // engine (TMA, non-tensor cp.async.bulk) for the large-message kernels.
 //
 // The MemoryChannel of the MSCCL++ README ("PortChannel and MemoryChannel")
-// moves data with GPU threads and "may need many GPU threads ... to achieve
-// high copying bandwidth".  On sm_103a one thread can hand whole tiles to the
+// moves data with GPU threads, and the README notes that bandwidth then takes
+// a large number of them.  On sm_103a one thread can hand whole tiles to the
 // copy engine instead: a get becomes a cp.async.bulk global->shared load that
 // completes on an mbarrier, a put becomes a cp.async.bulk shared->global store.
 // Threads only reduce shared-memory tiles; the tile a rank reduced is stored

@@ -1,9 +1,8 @@
 // ll.cuh -- one-shot AllReduce with a low-latency (LL) packet protocol.
 //
-// The MemoryChannel of the MSCCL++ README ("PortChannel and MemoryChannel") is
-// "especially performant for low-latency scenarios"; the project summary
-// ("How It Works") promises synchronisation "without deadlocks" and custom
-// collectives.  LL takes the synchronisation out of a separate signal/wait
+// The MSCCL++ README ("PortChannel and MemoryChannel") presents the
+// MemoryChannel as the channel for latency-sensitive transfers; the project
+// summary ("How It Works") adds custom collectives that cannot deadlock.  LL takes the synchronisation out of a separate signal/wait
 // round trip and puts it into the data: every 8-byte half of a 16-byte packet
 // holds 4 bytes of payload and a 4-byte flag, written with one 16-byte store,
 // and a reader accepts a packet only when both flags carry the current epoch.

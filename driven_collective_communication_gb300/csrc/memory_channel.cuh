@@ -1,12 +1,12 @@
 // memory_channel.cuh -- device side of a MemoryChannel between two virtual ranks.
 //
-// MSCCL++ README, "PortChannel and MemoryChannel": a MemoryChannel's methods
-// use GPU threads to read and write the peer's memory directly, which needs
-// many threads for bandwidth.  "On-GPU Communication Interfaces: Channels"
-// gives the method set -- put (copy local -> remote), signal ("I have arrived
-// and all my previous memory operations are done"), flush (previous channel
-// operations complete from the local device's view) and wait (for the peer's
-// signal) -- and the barrier built from them.  get is listed with put in the
+// MSCCL++ README, "PortChannel and MemoryChannel": with a MemoryChannel the
+// calling GPU threads themselves load from and store to the peer's memory, so
+// bandwidth takes many threads.  "On-GPU Communication Interfaces: Channels"
+// gives the method set -- put (local memory into the peer's), signal (tell the
+// peer this point is reached with earlier memory operations finished), flush
+// (earlier channel operations finished as seen from this GPU) and wait (until
+// the peer has signalled) -- and a barrier made of them.  get is listed with put in the
 // project summary ("How It Works").
 //
 // GB300 reading, one GPU, N virtual ranks:

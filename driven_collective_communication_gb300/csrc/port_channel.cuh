@@ -1,13 +1,13 @@
 // port_channel.cuh -- device side of a PortChannel: one GPU thread hands
 // operations to a host-side proxy through a FIFO of triggers.
 //
-// MSCCL++ README, "PortChannel and MemoryChannel": PortChannel methods send a
-// request to a host-side proxy, which runs the transfer (cudaMemcpy* here) or
-// the synchronisation; one GPU thread is enough to call them.  "Host-Side
-// Communication Proxy": the proxy is a background host thread that busy-polls
-// triggers pushed by GPU threads into a FIFO (FifoDeviceHandle::push of a
-// ProxyTrigger with fields fst/snd), and users may install their own handler
-// for custom triggers.
+// MSCCL++ README, "PortChannel and MemoryChannel": a PortChannel call hands
+// the work to a helper on the host, which performs the transfer (cudaMemcpy*
+// here) or the synchronisation, so a single GPU thread can drive it.
+// "Host-Side Communication Proxy": that helper is a host thread that keeps
+// polling a FIFO into which GPU threads place triggers (FifoDeviceHandle::push
+// of a ProxyTrigger with fields fst/snd); applications may replace its trigger
+// handling with their own.
 //
 // Layout and protocol (both sides):
 //  * the FIFO is a ring of 16-byte triggers {fst, snd} in pinned, mapped host

@@ -1,12 +1,12 @@
 // proxy.cu -- PortChannel host proxy: FIFO, proxy thread, and the kernels and
 // C entry points that use PortChannels.
 //
-// MSCCL++ README, "Host-Side Communication Proxy": a background host thread
-// busy-polls triggers that GPU threads push, and carries out what they ask
-// (startProxy / stopProxy around the application's kernels); a custom proxy
-// installs its own trigger handler.  "PortChannel and MemoryChannel": the
-// proxy runs the transfer with cudaMemcpy* (InfiniBand verbs between nodes --
-// not on one GPU) and the synchronisation.
+// MSCCL++ README, "Host-Side Communication Proxy": a host thread keeps
+// checking for triggers that GPU threads have posted and does what each one
+// asks (started and stopped around the application's kernels); a custom
+// proxy replaces the trigger handling.  "PortChannel and MemoryChannel": the
+// proxy performs the transfer with cudaMemcpy* (InfiniBand verbs between
+// nodes -- not on one GPU) and the synchronisation.
 //
 // GB300 reading: the FIFO lives in pinned host memory mapped into the GPU's
 // address space (Grace and the GPU share it coherently over NVLink-C2C); the

@@ -6,12 +6,12 @@
  * of CTAs.  Ranks talk through MemoryChannels -- the memory-mapped channel of
  * the MSCCL++ README ("PortChannel and MemoryChannel"): GPU threads read and
  * write the peer's memory directly, and synchronise with signal/flush/wait
- * ("On-GPU Communication Interfaces: Channels").  Channels are built on the
- * host and copied to the device before the first launch, as that section
- * describes.  The collectives are the standard sum collectives of the MSCCL++
- * abstract, point (3) ("a library of efficient algorithms implementing the
- * standard collective API"); AllReduce is the one the project summary singles
- * out ("Highlighted Details": tensor-parallel LLM serving).
+ * ("On-GPU Communication Interfaces: Channels").  As that section describes,
+ * the host side creates the channels and a device copy of them exists before
+ * the first launch.  The collectives are the usual sum collectives that point
+ * (3) of the MSCCL++ abstract offers as ready-made algorithms; AllReduce is
+ * the one the project summary singles out ("Highlighted Details":
+ * tensor-parallel LLM serving).
  *
  * Conventions for every function below:
  *  - Return value: DCC_OK (0) or a negative dcc_result_t.  dcc_error_string()

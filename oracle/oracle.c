@@ -6,10 +6,9 @@
  * the benchmark use it.  It shares no code, header, table or constant with
  * the CUDA library.
  *
- * What it computes (the standard collective API the MSCCL++ abstract names in
- * its point (3), "a library of efficient algorithms implementing the standard
- * collective API"; the AllReduce use case is in the project summary,
- * "Highlighted Details"):
+ * What it computes (the usual sum collectives, which point (3) of the MSCCL++
+ * abstract offers as a collection of ready-made algorithms; the AllReduce use
+ * case is in the project summary, "Highlighted Details"):
  *
  *   AllReduce      out[i]        = R( x_0[i] + x_1[i] + ... + x_{N-1}[i] )
  *   ReduceScatter  out_r[j]      = R( sum_p x_p[r*m + j] )
