@@ -40,7 +40,10 @@ from driven_collective_communication_gb300.replicas import Dist  # noqa: E402
 GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "allreduce_twoshot_bf16_n8.txt")
-KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "coll_bf16.cu"]
+# what the timed kernel and its launch shape are made of: the roofline's measured
+# traffic is reported only while these files hash to the value in the profile
+KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "coll_bf16.cu",
+                  "dcc_internal.h", "dcc_host.cu", "comm.h"]
 
 
 # ------------------------------------------------------------------ helpers

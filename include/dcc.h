@@ -44,7 +44,7 @@ extern "C" {
 #endif
 
 #define DCC_MAX_RANKS 16            /* virtual ranks per communicator */
-#define DCC_MAX_BLOCKS_PER_RANK 128 /* CTAs per rank in one collective kernel */
+#define DCC_MAX_BLOCKS_PER_RANK 128 /* CTAs per rank of a kernel that synchronises ranks */
 #define DCC_MAX_WINDOWS 8           /* registered windows per (rank, kind) */
 
 typedef struct dcc_comm* dcc_comm_t;
@@ -322,7 +322,9 @@ int dcc_fifo_push(dcc_comm_t c, const uint64_t* fst, const uint64_t* snd, int co
 int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us);
 
 /* CTAs per rank for the collectives; 0 = choose by size (default, or
- * DCC_BLOCKS_PER_RANK from the environment).  Clamped to what fits. */
+ * DCC_BLOCKS_PER_RANK from the environment).  Kernels that synchronise ranks
+ * clamp it to one co-resident wave and DCC_MAX_BLOCKS_PER_RANK; streaming
+ * kernels that never wait otherwise size their grid to cover the work. */
 int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks);
 
 /* AUTO picks ONE_SHOT for messages of at most `bytes` per rank and TWO_SHOT

@@ -565,5 +565,9 @@ def test_auto_selection(dcc):
         dcc.dcc_set_algo_threshold(c.handle, "bf16", 65536)
         assert dcc.dcc_select_algo(c.handle, 32768, "bf16") == "one_shot"
         assert dcc.dcc_select_algo(c.handle, 32769, "bf16") == "two_shot"
+        # streaming two-shot: one 16-byte vector per thread over the shard
         b, t = dcc.dcc_launch_shape(c.handle, W.C4.count, "bf16", "two_shot")
+        assert b * t >= W.C4.count // 8 // 8 and t > 0
+        # a kernel that synchronises ranks stays within one wave and its slots
+        b, t = dcc.dcc_launch_shape(c.handle, W.C4.count, "bf16", "two_shot_scratch")
         assert 1 <= b <= dcc.DCC_MAX_BLOCKS_PER_RANK and t > 0
