@@ -50,11 +50,21 @@ def _stale(target, deps):
 
 
 def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link libdcc.so if any source changed; returns its path."""
+    """Compile and link libdcc.so if any source changed; returns its path.
+    Concurrent callers (e.g. parallel test workers) serialise on a lock file."""
+    import fcntl
     deps = _deps()
     if not force and not _stale(LIB, deps):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale(LIB, deps):  # another process built it meanwhile
+            return LIB
+        return _build_locked(force, verbose, extra_flags)
+
+
+def _build_locked(force, verbose, extra_flags):
     cc = nvcc()
 
     def compile_one(src):

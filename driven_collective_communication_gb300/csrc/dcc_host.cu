@@ -125,6 +125,27 @@ dcc_algo_t resolve_algo(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo
 
 dcc::DevComm dev_view(const dcc_comm* c) { return c->dev; }
 
+// Device address of host memory the GPU can reach directly (pinned and mapped
+// into the device's address space); false for anything else.
+bool device_address(const void* p, size_t bytes, void** dptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer || !at.hostPointer) return false;
+  // the whole range must lie in the same allocation; the runtime maps pinned
+  // allocations contiguously, so checking the last byte is enough
+  cudaPointerAttributes end;
+  if (bytes && (cudaPointerGetAttributes(&end, static_cast<const char*>(p) + bytes - 1) != cudaSuccess ||
+                end.type != cudaMemoryTypeHost)) {
+    cudaGetLastError();
+    return false;
+  }
+  *dptr = at.devicePointer;
+  return true;
+}
+
 struct Shape {
   const void* fn;
   int blocks;
@@ -178,6 +199,9 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   return pick_blocks(c, sh->fn, sh->threads, work, &sh->blocks, 0, 0, one_wave);
 }
 
+int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
+                  dcc_algo_t algo, bool inplace, cudaStream_t s);
+
 int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t count,
                      dcc_dtype_t t, dcc_algo_t a, cudaStream_t s) {
   if (c->sticky != DCC_OK) return c->sticky;
@@ -191,8 +215,15 @@ int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t c
   if (rc != DCC_OK) return rc;
   rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
-  const dcc_algo_t algo = resolve_algo(c, count, t, a, inplace);
+  return run_allreduce(c, send, recv, count, t, resolve_algo(c, count, t, a, inplace), inplace, s);
+}
 
+// Builds the arguments and launches an AllReduce whose buffers are already
+// checked (pointers, alignment, overlaps, channels).
+int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
+                  dcc_algo_t algo, bool inplace, cudaStream_t s) {
+  const size_t bytes = count * elem_bytes(t);
+  int rc;
   dcc::CollArgs args{};
   for (int r = 0; r < c->n; ++r) {
     args.send[r] = send[r];
@@ -348,6 +379,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   }
   c->log = env_flag("DCC_LOG");
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
+  if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
@@ -435,6 +467,30 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
   if (rc != DCC_OK) return rc;
   for (int r = 0; r < c->n; ++r)
     if (!host_send[r] || !host_recv[r]) return DCC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  // Zero copy: when every host buffer is pinned memory the GPU can address,
+  // the two-shot kernel reads the inputs and writes the outputs over the
+  // host link directly (each input byte crosses once, each output byte
+  // once), which keeps both link directions busy with no staging in HBM.
+  // Measured on GB300 for 8 x 256 MiB bf16: 13.5 ms vs 14.8-15.4 ms staged.
+  if (c->zero_copy && (a == DCC_ALGO_AUTO || a == DCC_ALGO_TWO_SHOT)) {
+    void* zs[DCC_MAX_RANKS];
+    void* zr[DCC_MAX_RANKS];
+    bool ok = true;
+    for (int r = 0; r < c->n && ok; ++r)
+      ok = device_address(host_send[r], bytes, &zs[r]) && device_address(host_recv[r], bytes, &zr[r]) &&
+           !((reinterpret_cast<uintptr_t>(zs[r]) | reinterpret_cast<uintptr_t>(zr[r])) & 15u);
+    bool zinplace = false;
+    for (int r = 0; r < c->n && ok; ++r)
+      for (int p = 0; p < c->n && ok; ++p) {
+        if (overlaps(zr[r], bytes, zs[p], bytes)) {
+          ok = r == p && zr[r] == zs[r];
+          zinplace = zinplace || ok;
+        }
+        if (ok && p != r && overlaps(zr[r], bytes, zr[p], bytes)) ok = false;
+      }
+    if (ok) return run_allreduce(c, zs, zr, count, t, DCC_ALGO_TWO_SHOT, zinplace, st);
+  }
   if (!c->pipe_ready) {
     if (cudaStreamCreateWithFlags(&c->pipe_in, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&c->pipe_out, cudaStreamNonBlocking) != cudaSuccess ||
@@ -447,7 +503,6 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
     }
     c->pipe_ready = true;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(s);
   const size_t vw = 16 / eb;
   size_t chunk = kPipeChunkBytes / eb / vw * vw;
   if (chunk < vw) chunk = vw;

@@ -144,14 +144,20 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
                   dcc_dtype_t t, dcc_stream_t s);
 
-/* Host-buffer AllReduce: host_send[r] -> dev_send[r], dcc_allreduce(dev_send,
- * dev_recv), dev_recv[r] -> host_recv[r], as one stream-ordered operation on s.
- * The message is pipelined in 8 MiB-per-rank chunks: chunk i is copied in on
- * the communicator's copy-in stream (one cudaMemcpyAsync per rank), reduced on
- * s, and copied out on its copy-out stream, so both copy directions and the
- * kernels overlap.  The device buffers follow dcc_allreduce's rules; the host
- * buffers (pinned memory for asynchronous copies) must stay valid until s has
- * drained.  Results are the same bits as dcc_allreduce on the whole message. */
+/* Host-buffer AllReduce: host_recv[r] = sum_p host_send[p], as one
+ * stream-ordered operation on s.  Two ways, same bits as dcc_allreduce:
+ *  - zero copy (default when every host buffer is pinned memory the GPU can
+ *    address, algo AUTO or TWO_SHOT; DCC_ZERO_COPY=0 turns it off): the
+ *    two-shot kernel reads the host inputs and writes the host outputs over
+ *    the host link directly; dev_send / dev_recv are checked but not touched;
+ *  - staged: host_send[r] -> dev_send[r], dcc_allreduce(dev_send, dev_recv),
+ *    dev_recv[r] -> host_recv[r], pipelined in 8 MiB-per-rank chunks: chunk i
+ *    is copied in on the communicator's copy-in stream (one cudaMemcpyAsync
+ *    per rank), reduced on s and copied out on its copy-out stream, so both
+ *    copy directions and the kernels overlap.
+ * The device buffers follow dcc_allreduce's rules; the host buffers must stay
+ * valid until s has drained (pageable host memory makes the copies
+ * synchronous). */
 int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* const* host_recv,
                             void* const* dev_send, void* const* dev_recv, size_t count,
                             dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);

@@ -530,15 +530,24 @@ def test_argument_errors(dcc):
         comm.close()
 
 
+@pytest.mark.parametrize("mode", ["zero_copy", "staged", "pageable"])
 @pytest.mark.parametrize("count,inplace", [(300001, False), (3 * 4194304 + 13, False),
                                            (2 * 4194304 + 8, True)])
-def test_allreduce_from_host(dcc, count, inplace):
-    """Host buffers in, host buffers out, pipelined in 8 MiB-per-rank chunks
-    (one chunk; three chunks with a ragged last one; in place)."""
+def test_allreduce_from_host(dcc, count, inplace, mode, monkeypatch):
+    """Host buffers in, host buffers out: zero copy over the host link (pinned
+    buffers), or staged through device buffers and pipelined in 8 MiB-per-rank
+    chunks (forced, or because the host memory is pageable); one chunk, three
+    chunks with a ragged last one, in-place staging."""
     n = 8
+    if mode == "staged":
+        monkeypatch.setenv("DCC_ZERO_COPY", "0")
     w = W.with_count(W.C4, count)
-    xs = [x.pin_memory() for x in W.rank_inputs(w)]
-    outs = [torch.empty_like(x).pin_memory() for x in xs]
+    if mode == "pageable":
+        xs = [x.clone() for x in W.rank_inputs(w)]
+        outs = [torch.empty_like(x) for x in xs]
+    else:
+        xs = [x.pin_memory() for x in W.rank_inputs(w)]
+        outs = [torch.empty_like(x).pin_memory() for x in xs]
     dev_in = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
     dev_out = dev_in if inplace else [torch.empty_like(d) for d in dev_in]
     comm = dcc.Comm(n)
