@@ -650,7 +650,7 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
   const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
                                  : dcc::linear_allreduce_kernel<__half>(c->n);
   const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // 8-row items per rank
-  rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, dcc::kFusedThreads / 32, false);
+  rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
   if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &a};

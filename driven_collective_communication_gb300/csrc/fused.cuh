@@ -11,14 +11,15 @@
 //
 //   y_r[i] = R( sum_p  sum_k W_p[i][k] x_p[k] )   for every rank r
 //
-// Schedule (two-shot, like k_allreduce_twoshot): rank r's warps own shard r of
-// the rows, in groups of 8 rows (one 16-byte output vector).  For each rank p
-// in order, a warp gets the 8 weight rows of W_p and x_p from rank p's memory
-// in 16-byte vectors (lanes stride the row, coalesced), accumulates 8 fp32
-// dot products with fused multiply-adds, reduces them across lanes with a
-// fixed shuffle tree, and adds them to the running sum in rank order.  Lanes
-// 0..N-1 then put the packed vector into the N outputs.  Every output element
-// is computed once, so every rank receives the same bits.
+// Schedule (two-shot, like k_allreduce_twoshot): rank r's CTAs own shard r of
+// the rows, in items of 8 rows (one 16-byte output vector), one item per CTA
+// at a time.  The CTA's warps take the ranks in parallel: warp w gets the 8
+// weight rows of W_p and x_p from rank p = w, w + 8, ... in 16-byte vectors
+// (lanes stride the row, coalesced), accumulates 8 fp32 dot products with
+// fused multiply-adds and reduces them across lanes with a fixed shuffle
+// tree.  One thread per row then adds the ranks' partials in rank order and
+// lanes 0..N-1 put the packed vector into the N outputs.  Every output
+// element is computed once, so every rank receives the same bits.
 //
 // The per-rank dot products are reordered relative to a sequential sum (lane
 // strides and a shuffle tree), so results are exact when every fp32 partial
@@ -67,11 +68,13 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const size_t kv = a.kp / 8;             // 16-byte vectors per weight row
   const size_t items = a.rows / kFusedRows;
+  __shared__ float part_s[DCC_MAX_RANKS][kFusedRows];
   size_t s0, s1;
   shard_vecs(items, n, rank, s0, s1);
-  for (size_t v = s0 + (size_t)blk * nwarps + warp; v < s1; v += (size_t)B * nwarps) {
-    float acc[kFusedRows];
-    for (int p = 0; p < n; ++p) {
+  for (size_t v = s0 + blk; v < s1; v += B) {
+    // warp w computes the partial products of ranks w, w + nwarps, ... for
+    // the item's 8 rows; the ranks' partials meet in shared memory
+    for (int p = warp; p < n; p += nwarps) {
       const uint4* w = static_cast<const uint4*>(a.weight[p]) + v * kFusedRows * kv;
       const uint4* x = static_cast<const uint4*>(a.x[p]);
       float part[kFusedRows];
@@ -99,15 +102,26 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
       }
 #pragma unroll
       for (int r = 0; r < kFusedRows; ++r) {
-        const float s = warp_sum(part[r]);
-        acc[r] = p == 0 ? s : __fadd_rn(acc[r], s);
+        const float sum = warp_sum(part[r]);
+        if (lane == 0) part_s[p][r] = sum;
       }
     }
-    typename L::Acc out;
+    __syncthreads();
+    // one thread per row adds the ranks' partials in rank order; the packed
+    // result goes to all N outputs
+    if (warp == 0) {
+      float acc = 0.0f;
+      if (lane < kFusedRows) {
+        acc = part_s[0][lane];
+        for (int p = 1; p < n; ++p) acc = __fadd_rn(acc, part_s[p][lane]);
+      }
+      typename L::Acc out;
 #pragma unroll
-    for (int r = 0; r < kFusedRows; ++r) out.v[r] = acc[r];
-    const uint4 packed = L::pack(out);
-    for (int q = lane; q < n; q += 32) st_vec(static_cast<uint4*>(a.y[q]) + v, packed);
+      for (int r = 0; r < kFusedRows; ++r) out.v[r] = __shfl_sync(0xffffffffu, acc, r);
+      const uint4 packed = L::pack(out);
+      for (int q = lane; q < n; q += 32) st_vec(static_cast<uint4*>(a.y[q]) + v, packed);
+    }
+    __syncthreads();
   }
 }
 
