@@ -40,10 +40,11 @@ from driven_collective_communication_gb300.replicas import Dist  # noqa: E402
 GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "allreduce_twoshot_bf16_n8.txt")
-# what the timed kernel and its launch shape are made of: the roofline's measured
-# traffic is reported only while these files hash to the value in the profile
+# what the timed kernel is made of: the roofline's measured traffic is reported
+# only while these device sources hash to the value in the profile and the live
+# launch shape (CTAs per rank x threads) equals the profiled one
 KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "coll_bf16.cu",
-                  "dcc_internal.h", "dcc_host.cu", "comm.h"]
+                  "dcc_internal.h"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -65,16 +66,19 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(blocks, threads):
     """DRAM bytes per launch of the timed kernel from the committed ncu summary,
-    or None if the kernel sources changed since the counters were taken."""
+    or None if the kernel or its launch shape changed since the counters were taken."""
     try:
         text = open(PROFILE_TRAFFIC).read()
     except OSError:
         return None
     m = re.search(r"^traffic_bytes_per_full_launch:\s*(\d+)", text, re.M)
     h = re.search(r"^kernel_source_hash:\s*(\w+)", text, re.M)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    sh = re.search(r"^launch_shape:\s*(\d+)\s*x\s*(\d+)", text, re.M)
+    if not m or not h or not sh or h.group(1) != kernel_source_hash():
+        return None
+    if (int(sh.group(1)), int(sh.group(2))) != (blocks, threads):
         return None
     return int(m.group(1))
 
@@ -233,7 +237,7 @@ def run_ours(args, dist):
                    "values": "N(0,1)*(1+r), seed 3+r", "l2": "inputs larger than L2 (2 GiB read per step)",
                    "parallelism": "replicas" if dist.ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(blocks, threads),
                      "algorithmic_bytes": algo_bytes, "peak_source": peak_src,
                      "kernel_ms": round(kernel_ms, 5)},
         "gpu_launches": args.steps,

@@ -38,10 +38,16 @@ inline bool env_flag(const char* name) {
 }
 
 // Messages at or below this many bytes per rank run one-shot under AUTO.
-// Measured on GB300, 8 ranks bf16, CUDA-graph-amortised: one-shot 1.34 us vs
-// two-shot 1.46 us at 16 KiB, 1.60 vs 1.66 us at 32 KiB, even at 64 KiB, and
-// two-shot ahead from 128 KiB (1.79 vs 2.05 us) upwards.
+// Measured on GB300, CUDA-graph-amortised, one-shot vs two-shot (us): 8 ranks
+// bf16 1.48/1.68 at 8 KiB, 1.60/1.72 at 32 KiB, even at 64 KiB, two-shot ahead
+// from 128 KiB (2.09/1.85); 16 ranks 2.03/2.22 at 32 KiB, 2.50/2.26 at 64 KiB.
+// With 2 or 4 ranks the two are level (within 0.05 us) up to 64 KiB and
+// two-shot is ahead from there, so one-shot never pays: threshold 0.
 constexpr size_t kDefaultOneShotMaxBytes = 32 * 1024;
+constexpr int kOneShotMinRanks = 5;
+inline size_t default_one_shot_max(int n_ranks) {
+  return n_ranks >= kOneShotMinRanks ? kDefaultOneShotMaxBytes : 0;
+}
 
 // Threads per CTA of the thread-copy kernels, by work (16-byte vectors per
 // rank): small messages want many small CTAs spread over many SMs (latency),
@@ -77,8 +83,7 @@ struct dcc_comm {
   int blocks_override = 0;
   int threads_override = 0;  // threads per CTA of the thread-copy kernels (0 = by size)
   bool cooperative = true;   // DCC_COOPERATIVE=0: plain launches (diagnostic only)
-  size_t one_shot_max[4] = {dcc_host::kDefaultOneShotMaxBytes, dcc_host::kDefaultOneShotMaxBytes,
-                            dcc_host::kDefaultOneShotMaxBytes, dcc_host::kDefaultOneShotMaxBytes};
+  size_t one_shot_max[4] = {};  // set from the rank count at creation
   int forced_algo = -1;  // DCC_ALGO environment override of AUTO
   // AUTO: messages of at least bulk_min_bytes per rank run large_algo
   size_t bulk_min_bytes = (size_t)1 << 62;

@@ -80,9 +80,6 @@ const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
   }
 }
 
-// CTAs per rank: enough for one vector per thread, at most one full wave of
-// the GPU (co-residency is required when the kernel waits), at most
-// DCC_MAX_BLOCKS_PER_RANK (the semaphore slots).
 // CTAs per rank.  A kernel whose CTAs wait on one another, or rely on running
 // together (one_wave), gets at most one co-resident wave and at most
 // DCC_MAX_BLOCKS_PER_RANK (its semaphore slots).  A streaming kernel that
@@ -328,6 +325,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   dcc_comm* c = new dcc_comm();
   c->n = n_ranks;
   c->device = dev;
+  for (size_t& m : c->one_shot_max) m = dcc_host::default_one_shot_max(n_ranks);
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     delete c;

@@ -333,8 +333,9 @@ int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us);
  * kernels that never wait otherwise size their grid to cover the work. */
 int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks);
 
-/* AUTO picks ONE_SHOT for messages of at most `bytes` per rank and TWO_SHOT
- * above, for this dtype.  Defaults come from the measured crossover. */
+/* AUTO picks ONE_SHOT for out-of-place messages of at most `bytes` per rank
+ * and TWO_SHOT above, for this dtype.  Defaults come from the measured
+ * crossover: 32 KiB with 5 or more ranks, 0 (always two-shot) with 2 to 4. */
 int dcc_set_algo_threshold(dcc_comm_t c, dcc_dtype_t t, size_t bytes);
 
 /* The algorithm AUTO would run for this request (pure host logic). */

@@ -570,6 +570,12 @@ def test_allreduce_from_host(dcc, count, inplace, mode, monkeypatch):
 
 
 def test_auto_selection(dcc):
+    # default crossover: one-shot up to 32 KiB with 8 ranks, never with 2
+    with dcc.Comm(8) as c:
+        assert dcc.dcc_select_algo(c.handle, 16384, "bf16") == "one_shot"
+        assert dcc.dcc_select_algo(c.handle, 16385, "bf16") == "two_shot"
+    with dcc.Comm(2) as c:
+        assert dcc.dcc_select_algo(c.handle, 64, "bf16") == "two_shot"
     with dcc.Comm(8) as c:
         dcc.dcc_set_algo_threshold(c.handle, "bf16", 65536)
         assert dcc.dcc_select_algo(c.handle, 32768, "bf16") == "one_shot"
