@@ -152,13 +152,14 @@ def time_launches(fn, steps, stream):
 
 
 # ------------------------------------------------------------------ oracle CPU leg
-def oracle_sample_run(seconds, elems):
-    """Time the oracle (all host cores) on a prefix of `elems` elements per rank
-    of the large-message workload.  Returns (GB/s algbw, threads, sample text, calls)."""
+def oracle_sample_run(seconds, elems, threads=None):
+    """Time the oracle (all host cores, or `threads`) on a prefix of `elems` elements
+    per rank of the large-message workload.  Returns (GB/s algbw, threads, sample text,
+    seconds per call)."""
     import oracle
     w = W.C4
     xs = [W.to_storage(t) for t in W.rank_inputs(w, device="cpu", count=elems)]
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     oracle.allreduce(xs, "bf16", nthreads=threads)  # warm
     n_calls, t_total = 0, 0.0
     while t_total < seconds:
@@ -240,6 +241,10 @@ def run_ours(args, dist):
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(blocks, threads),
                      "algorithmic_bytes": algo_bytes, "peak_source": peak_src,
                      "kernel_ms": round(kernel_ms, 5)},
+        "latency_us": {"p50": round(statistics.median(per) * 1e3, 2), "min": round(min(per) * 1e3, 2),
+                       "mean": round(kernel_ms * 1e3, 2), "launches": len(per)},
+        # NCCL-tests convention, for comparison with other reports only
+        "busbw_gbs": round(value * 2 * (n - 1) / n, 2),
         "gpu_launches": args.steps,
         "clocks": clk,
     }
@@ -249,8 +254,11 @@ def run_ours(args, dist):
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
         out["other"] = other_workloads(dcc, dev, stream)
         gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
+        gbs1, _, sample1, _ = oracle_sample_run(3.0, args.cpu_elems // 8, threads=1)
         out["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
-                               "kind": "oracle", "sample": sample}
+                               "kind": "oracle", "sample": sample,
+                               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s",
+                                                 "cores": 1, "sample": sample1}}
     comm.close()
     return out
 

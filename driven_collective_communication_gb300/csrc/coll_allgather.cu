@@ -1,4 +1,5 @@
 // coll_allgather.cu -- AllGather kernel table (a bit copy; element type only sets the size).
+#include "allgather.cuh"
 #include "bulk.cuh"
 
 namespace dcc {

@@ -333,44 +333,6 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArg
   }
 }
 
-// ------------------------------------------------------------- AllGather
-// recv[p][q*m + j] = send[q][j]: rank q's CTAs put their input into slot q of
-// every rank's output.  A bit copy of elem_bytes-sized elements.
-template <int NT>
-__global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, int elem_bytes) {
-  const int n = NT > 0 ? NT : dc.n;
-  const int B = a.blocks;
-  const int rank = blockIdx.x / B, blk = blockIdx.x % B;
-  const size_t bytes = a.count * (size_t)elem_bytes;
-  const size_t stride = (size_t)B * blockDim.x;
-  const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
-  if (bytes % 16 == 0) {
-    const size_t nv = bytes / 16;
-    const uint4* src = static_cast<const uint4*>(a.send[rank]);
-    for (size_t v = first; v < nv; v += stride) {
-      const uint4 x = ld_vec(src + v);
-      if constexpr (NT > 0) {
-#pragma unroll
-        for (int p = 0; p < NT; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + (size_t)rank * nv + v, x);
-      } else {
-        for (int p = 0; p < n; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + (size_t)rank * nv + v, x);
-      }
-    }
-  } else if (elem_bytes == 4) {
-    const uint32_t* src = static_cast<const uint32_t*>(a.send[rank]);
-    for (size_t j = first; j < a.count; j += stride) {
-      const uint32_t x = src[j];
-      for (int p = 0; p < n; ++p) static_cast<uint32_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
-    }
-  } else {
-    const uint16_t* src = static_cast<const uint16_t*>(a.send[rank]);
-    for (size_t j = first; j < a.count; j += stride) {
-      const uint16_t x = src[j];
-      for (int p = 0; p < n; ++p) static_cast<uint16_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
-    }
-  }
-}
-
 // ------------------------------------------------------------- kernel tables
 enum KernelKind {
   kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3, kTwoShotBulk = 4, kOneShotLL = 5
@@ -381,7 +343,5 @@ enum KernelKind {
 template <typename T>
 const void* reduce_kernel(int kind, int n);
 
-const void* allgather_kernel(int n);
-const void* allgather_bulk_kernel(int n);
 
 }  // namespace dcc

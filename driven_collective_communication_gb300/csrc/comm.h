@@ -88,7 +88,7 @@ struct dcc_comm {
   // AUTO: messages of at least bulk_min_bytes per rank run large_algo
   size_t bulk_min_bytes = (size_t)1 << 62;
   dcc_algo_t large_algo = DCC_ALGO_TWO_SHOT;
-  bool ag_bulk = true;  // AllGather through the bulk-copy pipeline when aligned and large
+  bool ag_bulk = false;  // DCC_AG_BULK=1: AllGather through the bulk-copy pipeline when aligned and large
   bool zero_copy = true;  // host-buffer AllReduce reads/writes mapped pinned host memory directly
   int sticky = DCC_OK;
   int err_rank = -1, err_peer = -1, err_block = -1;

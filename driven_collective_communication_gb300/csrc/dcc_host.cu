@@ -15,6 +15,7 @@
 #include <unordered_map>
 #include <vector>
 
+#include "allgather.cuh"
 #include "bulk.cuh"
 #include "ll.cuh"
 #include "collectives.cuh"
@@ -602,7 +603,9 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   const void* fn = dcc::allgather_kernel(c->n);
   const size_t work = (sb + 15) / 16;
   const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);
-  rc = pick_blocks(c, fn, threads, work, &args.blocks, 0, 0, false);
+  // vector path: kAgUnroll vectors per thread; element path: one element per thread
+  const size_t per_block = sb % 16 == 0 ? (size_t)dcc::kAgUnroll * threads : (size_t)threads;
+  rc = pick_blocks(c, fn, threads, sb % 16 == 0 ? work : send_count, &args.blocks, 0, per_block, false);
   if (rc != DCC_OK) return rc;
   return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
 }

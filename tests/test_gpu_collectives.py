@@ -167,6 +167,27 @@ def test_allgather_bulk_and_thread_paths_agree(dcc, monkeypatch):
         assert torch.equal(outs["0"][r].view(torch.int16), ref)
 
 
+@pytest.mark.parametrize("n", [6, 8])
+def test_allgather_launch_shapes(dcc, n):
+    """The AllGather's vector path (several vectors in flight per thread) covers
+    every element for any number of CTAs per rank, including a partial chunk."""
+    m = 8 * (4096 * 8 * 3 + 517)  # bf16: 3 full 8-vector x 512-thread chunks + a ragged one
+    xs = [torch.randn(m, device="cuda").to(torch.bfloat16) for _ in range(n)]
+    ref = torch.cat(xs).view(torch.int16)
+    ys = [torch.empty(n * m, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        for blocks in (1, 2, 7, 128, 0):
+            dcc.dcc_set_blocks_per_rank(comm.handle, blocks)
+            for y in ys:
+                y.fill_(float("nan"))
+            comm.allgather(xs, ys)
+            assert comm.check() == dcc.DCC_OK
+            for r in range(n):
+                assert torch.equal(ys[r].view(torch.int16), ref), (blocks, r)
+
+
 def test_launch_shape_does_not_change_bits(dcc):
     """Any number of CTAs per rank returns the same bits (fixed per-element order)."""
     n, count = 8, 123457
