@@ -471,8 +471,9 @@ def other_workloads(dcc, dev, stream):
         out["c5_allgather_port_channel"] = {"ms": round(ms, 4), "hbm_gbs": round(
             (w.bytes_per_rank + 8 * w.bytes_per_rank) / ms / 1e6, 1)}
     # fused row-parallel linear + AllReduce vs per-rank GEMV (cuBLAS) then AllReduce,
-    # tensor-parallel decode shapes: hidden 8192 rows, 8 ranks, kp = 1024 and 3584
-    for kp in (1024, 3584):
+    # tensor-parallel decode shapes: hidden 8192 rows, 8 ranks, kp = 1024, 3584, 8192
+    # (kp >= 3072 runs the bulk-copy kernel)
+    for kp in (1024, 3584, 8192):
         rows = 8192
         g = torch.Generator(device=dev)
         g.manual_seed(5)
@@ -572,7 +573,7 @@ def run_reference(args, dist):
 # ------------------------------------------------------------------ profiling cases
 PROFILE_CASES = ("allreduce_two_shot", "allreduce_two_shot_bulk", "allreduce_one_shot",
                  "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "reduce_scatter",
-                 "allgather", "ring_barrier")
+                 "allgather", "ring_barrier", "linear_allreduce")
 
 
 def run_profile_case(args):
@@ -587,6 +588,25 @@ def run_profile_case(args):
     n = 8
     w = W.with_count(recipe, args.count, n_ranks=n)
     case = args.profile_case
+    if case == "linear_allreduce":  # --count is kp; 8192 rows per rank, bf16
+        rows, kp = 8192, args.count
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(n)]
+        xin = [torch.randn(kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(n)]
+        yf = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        with dcc.Comm(n) as lc:
+            lc.register_all("input", wts)
+            lc.register_all("input", xin)
+            lc.register_all("output", yf)
+            for _ in range(args.warmup + args.steps):
+                dcc.dcc_linear_allreduce(lc.handle, wts, xin, yf, rows, kp, "bf16")
+            torch.cuda.synchronize()
+            rc = lc.check()
+        if rc != dcc.DCC_OK:
+            raise RuntimeError(dcc.dcc_error_string(rc))
+        print(json.dumps({"profile_case": case, "rows": rows, "kp": kp, "launches": args.warmup + args.steps}))
+        return
     xs = W.rank_inputs(w, device=dev)
     comm = dcc.Comm(n, connect="ring" if case == "ring_barrier" else "all")
     if case == "reduce_scatter":

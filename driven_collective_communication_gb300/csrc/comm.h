@@ -63,6 +63,13 @@ inline int threads_for(dcc_algo_t algo, size_t work_vecs_per_rank) {
 // Host-buffer AllReduce: elements per rank per pipeline chunk (8 MiB of bf16).
 constexpr size_t kPipeChunkBytes = 8u << 20;
 
+// Fused linear + AllReduce: rows of at least this many elements per rank
+// stream through the bulk-copy kernel (fused_bulk.cuh), shorter ones through
+// thread loads (fused.cuh).  Measured on GB300, 8 ranks x 8192 rows bf16,
+// thread / bulk (us): kp 2048 52.4 / 62.8, 2560 63.2 / 67.3, 3072 74.7 / 70.7,
+// 4096 97.8 / 80.2, 8192 191 / 150.
+constexpr size_t kFusedBulkMinKp = 3072;
+
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;
 
@@ -88,6 +95,9 @@ struct dcc_comm {
   // AUTO: messages of at least bulk_min_bytes per rank run large_algo
   size_t bulk_min_bytes = (size_t)1 << 62;
   dcc_algo_t large_algo = DCC_ALGO_TWO_SHOT;
+  // fused linear + AllReduce through the bulk-copy kernel: -1 by kp (measured
+  // crossover), 0 never, 1 always (DCC_FUSED_BULK)
+  int fused_bulk = -1;
   bool ag_bulk = false;  // DCC_AG_BULK=1: AllGather through the bulk-copy pipeline when aligned and large
   bool zero_copy = true;  // host-buffer AllReduce reads/writes mapped pinned host memory directly
   int sticky = DCC_OK;

@@ -21,6 +21,7 @@
 #include "collectives.cuh"
 #include "comm.h"
 #include "fused.cuh"
+#include "fused_bulk.cuh"
 #include "sync_kernels.cuh"
 
 namespace {
@@ -282,7 +283,8 @@ int dcc_preload_kernels() {
       for (int kind = dcc::kOneShot; kind <= dcc::kOneShotLL; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
   for (int n : ns) ok &= load(dcc::allgather_kernel(n)) && load(dcc::allgather_bulk_kernel(n));
   for (int n : ns)
-    ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n));
+    ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n)) &&
+          load(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_bulk_kernel<__half>(n));
   ok &= load(dcc::ring_barrier_kernel()) && load(dcc::channel_put_kernel()) && load(dcc::channel_get_kernel());
   return ok ? DCC_OK : DCC_ERR_CUDA;
 }
@@ -379,6 +381,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   c->log = env_flag("DCC_LOG");
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
+  if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_bulk = std::strcmp(v, "0") != 0 ? 1 : 0;
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
@@ -648,13 +651,22 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
   }
   a.rows = rows;
   a.kp = kp;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &a};
+  if (c->fused_bulk > 0 || (c->fused_bulk < 0 && kp >= kFusedBulkMinKp)) {
+    const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(c->n)
+                                   : dcc::linear_allreduce_bulk_kernel<__half>(c->n);
+    const size_t smem = dcc::fused_bulk_smem_bytes();
+    const size_t items = rows / dcc::kFusedBulkRows / (size_t)c->n + 1;  // 2-row items per rank
+    rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, smem, 1, false);  // one item per CTA
+    if (rc != DCC_OK) return rc;
+    return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), smem);
+  }
   const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
                                  : dcc::linear_allreduce_kernel<__half>(c->n);
   const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // 8-row items per rank
   rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
   if (rc != DCC_OK) return rc;
-  dcc::DevComm dc = dev_view(c);
-  void* kargs[] = {&dc, &a};
   return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s));
 }
 

@@ -25,6 +25,13 @@ def dcc():
     return mod
 
 
+@pytest.fixture(params=["thread", "bulk"])
+def path(request, monkeypatch):
+    """Both kernels of the op: thread loads (fused.cuh) and bulk copies (fused_bulk.cuh)."""
+    monkeypatch.setenv("DCC_FUSED_BULK", "1" if request.param == "bulk" else "0")
+    return request.param
+
+
 def run(dcc, ws, xs, rows, kp, dtype):
     n = len(ws)
     dw = [w.cuda() for w in ws]
@@ -44,8 +51,8 @@ def run(dcc, ws, xs, rows, kp, dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("n,rows,kp", [(1, 8, 8), (2, 64, 40), (8, 1032, 1032), (16, 256, 1024),
-                                        (5, 136, 2056), (8, 8192, 64)])
-def test_integer_data_bit_exact(dcc, dtype, n, rows, kp):
+                                        (5, 136, 2056), (8, 8192, 64), (3, 24, 9000), (8, 64, 4096)])
+def test_integer_data_bit_exact(dcc, path, dtype, n, rows, kp):
     g = torch.Generator().manual_seed(n * 1000 + kp)
     ws = [torch.randint(-3, 4, (rows * kp,), generator=g).to(TD[dtype]) for _ in range(n)]
     xs = [torch.randint(-3, 4, (kp,), generator=g).to(TD[dtype]) for _ in range(n)]
@@ -57,7 +64,7 @@ def test_integer_data_bit_exact(dcc, dtype, n, rows, kp):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("n,rows,kp", [(8, 8192, 1024), (8, 512, 3584), (3, 64, 4104)])
-def test_random_data_within_bound(dcc, dtype, n, rows, kp):
+def test_random_data_within_bound(dcc, path, dtype, n, rows, kp):
     g = torch.Generator().manual_seed(7 + n + kp)
     ws = [(torch.randn(rows * kp, generator=g) * 0.05).to(TD[dtype]) for _ in range(n)]
     xs = [torch.randn(kp, generator=g).to(TD[dtype]) for _ in range(n)]
