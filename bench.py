@@ -388,8 +388,47 @@ def other_workloads(dcc, dev, stream):
         ms = statistics.median(per)
         out["c4_bf16_" + algo] = {"ms": round(ms, 4),
                                   "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+    # the optional entry barrier: its cost on the headline size (one co-resident wave)
+    dcc.dcc_set_entry_barrier(comm.handle, True)
+    step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", "two_shot", stream)
+    for _ in range(3):
+        step()
+    per, _ = time_launches(step, 30, stream)
+    dcc.dcc_set_entry_barrier(comm.handle, False)
+    out["c4_bf16_two_shot_entry_barrier"] = {"ms": round(statistics.median(per), 4)}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
+    # ... and on the 16 KiB decode size, CUDA-graph amortised
+    w16 = W.c3(1)
+    with torch.cuda.stream(stream):
+        xs16 = W.rank_inputs(w16, device=dev)
+        ys16 = [torch.empty_like(x) for x in xs16]
+    torch.cuda.synchronize()
+    with dcc.Comm(8) as c16:
+        c16.register_all("input", xs16)
+        c16.register_all("output", ys16)
+        res = {}
+        for on in (False, True):
+            dcc.dcc_set_entry_barrier(c16.handle, on)
+            step = dcc.prepare_allreduce(c16.handle, xs16, ys16, w16.count, "bf16", "two_shot", stream)
+            for _ in range(20):
+                step()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(100):
+                    step()
+            with torch.cuda.stream(stream):
+                g.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(10):
+                    g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            res["with_barrier_us" if on else "without_us"] = round(e0.elapsed_time(e1) * 1e3 / 1000, 2)
+        assert c16.check(stream) == dcc.DCC_OK
+        out["c3_16KiB_two_shot_entry_barrier_graph"] = res
     del xs, ys, scr
     # more ranks and another dtype at the large size (two-shot push, 256 MiB per rank)
     for n_ranks, dtype in ((2, "bf16"), (4, "bf16"), (16, "bf16"), (8, "fp32")):

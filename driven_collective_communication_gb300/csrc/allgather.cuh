@@ -26,12 +26,15 @@ constexpr int kAgUnroll = 8;  // 16-byte vectors each thread has in flight
 
 __device__ __forceinline__ void st_vec_stream(uint4* p, uint4 v) { __stcs(p, v); }
 
-template <int NT>
+template <int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, int elem_bytes) {
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;
   const int rank = blockIdx.x / B, blk = blockIdx.x % B;
   const size_t bytes = a.count * (size_t)elem_bytes;
+  if constexpr (EB) {
+    if (!entry_barrier(dc, rank, n, blk)) return;
+  }
   if (bytes % 16 == 0) {
     // thread t of CTA c covers vectors c*U*T + j*T + t, j < U: every load and
     // store instruction of a warp touches 512 contiguous bytes
@@ -81,8 +84,9 @@ __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, 
   }
 }
 
-// Kernel tables (compile-time N for 1, 2, 4, 8, 16; a runtime-N instance otherwise).
-const void* allgather_kernel(int n);
+// Kernel tables (compile-time N for 1, 2, 4, 8, 16; a runtime-N instance
+// otherwise); eb selects the instance with the entry barrier.
+const void* allgather_kernel(int n, bool eb = false);
 const void* allgather_bulk_kernel(int n);
 
 }  // namespace dcc

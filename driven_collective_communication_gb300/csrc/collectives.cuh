@@ -171,6 +171,24 @@ __device__ __forceinline__ void shard_vecs(size_t nvec, int n, int r, size_t& s0
   s1 = (r == n - 1) ? nvec : s0 + per;
 }
 
+// Optional entry barrier: before touching peer memory, every CTA tells the
+// CTAs of its block slot in the other ranks that its input is ready (signal)
+// and waits until all of them have said the same.  Between GPUs this is what
+// makes a peer's input safe to read; on one GPU stream order already does, so
+// it is off unless the caller asks for it.  The kernels take it as a template
+// flag EB, so the default instances carry no trace of it; EB instances are
+// launched cooperatively with at most one wave, so every CTA they wait for is
+// running.
+__device__ __forceinline__ bool entry_barrier(const DevComm& dc, int rank, int n, int blk) {
+  if (n == 1) return true;
+  unsigned long long expected = 0;
+  const bool waiter = (int)threadIdx.x < n && (int)threadIdx.x != rank;
+  if (waiter) expected = dc.expect[sem_slot(rank, threadIdx.x, blk)];
+  const bool ok = group_barrier(dc, rank, n, blk, expected);
+  if (waiter) dc.expect[sem_slot(rank, threadIdx.x, blk)] = expected;
+  return ok;
+}
+
 // ------------------------------------------------------------- one-shot
 // Every rank gets all N inputs and reduces its whole output.  Out of place no
 // rank writes what another reads, so there is no synchronisation.  In place,
@@ -179,7 +197,7 @@ __device__ __forceinline__ void shard_vecs(size_t nvec, int n, int r, size_t& s0
 // signal/wait barrier ("everyone has read this chunk"), then store.  (Getting
 // the next chunk while the signals travel measured slower on GB300: 0.53 vs
 // 0.43 ms for 8 x 64 MiB int32.)
-template <typename T, int NT>
+template <typename T, int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   const int n = NT > 0 ? NT : dc.n;
@@ -189,6 +207,9 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   const size_t tail0 = nvec * L::VW;
   uint4* out = static_cast<uint4*>(a.recv[rank]);
   using S = typename L::S;
+  if constexpr (EB) {
+    if (!entry_barrier(dc, rank, n, blk)) return;
+  }
 
   if (!a.inplace) {
     const size_t stride = (size_t)B * blockDim.x;
@@ -236,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 // rank r's CTAs touch shard r of any buffer and every thread reads all N
 // values of a vector before writing it anywhere, so in place is safe without
 // synchronisation.  Traffic: N*S read + N*S written in total, the minimum.
-template <typename T, int NT>
+template <typename T, int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   using S = typename L::S;
@@ -246,6 +267,9 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, Coll
   const size_t nvec = a.count / L::VW;
   size_t s0, s1;
   shard_vecs(nvec, n, rank, s0, s1);
+  if constexpr (EB) {
+    if (!entry_barrier(dc, rank, n, blk)) return;
+  }
   const size_t stride = (size_t)B * blockDim.x;
   for (size_t v = s0 + (size_t)blk * blockDim.x + threadIdx.x; v < s1; v += stride) {
     const uint4 r = reduce_vec<T, NT>(a.send, n, v);
@@ -270,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, Coll
 // (r, blk) reads exactly the scratch vectors CTA (q, blk) wrote, so the
 // per-slot barrier is enough.  In place is safe: rank r overwrites shard q of
 // its buffer only after CTA (q, blk) has read it.
-template <typename T, int NT>
+template <typename T, int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   using S = typename L::S;
@@ -285,6 +309,9 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
 
   size_t s0, s1;
   shard_vecs(nvec, n, rank, s0, s1);
+  if constexpr (EB) {
+    if (!entry_barrier(dc, rank, n, blk)) return;
+  }
   uint4* mine = static_cast<uint4*>(a.scratch[rank]);
   for (size_t v = s0 + first; v < s1; v += stride) st_vec(mine + (v - s0), reduce_vec<T, NT>(a.send, n, v));
   if (rank == n - 1 && tail_thread)
@@ -312,13 +339,16 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
 // ------------------------------------------------------------- ReduceScatter
 // recv[r][j] = sum_p send[p][r*m + j].  Rank r's CTAs get shard r of every
 // input.  Vector path when a shard starts on a 16-byte boundary, else scalar.
-template <typename T, int NT>
+template <typename T, int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   using S = typename L::S;
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;
   const int rank = blockIdx.x / B, blk = blockIdx.x % B;
+  if constexpr (EB) {
+    if (!entry_barrier(dc, rank, n, blk)) return;
+  }
   const size_t m = a.count;
   const size_t stride = (size_t)B * blockDim.x;
   const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
@@ -335,7 +365,10 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArg
 
 // ------------------------------------------------------------- kernel tables
 enum KernelKind {
-  kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3, kTwoShotBulk = 4, kOneShotLL = 5
+  kOneShot = 0, kTwoShot = 1, kTwoShotScratch = 2, kReduceScatter = 3, kTwoShotBulk = 4, kOneShotLL = 5,
+  // the same kernels with the entry barrier
+  kOneShotEB = 6, kTwoShotEB = 7, kTwoShotScratchEB = 8, kReduceScatterEB = 9,
+  kNumKernelKinds = 10
 };
 
 // Kernel of `kind` for element type T and n ranks (compile-time N for

@@ -162,10 +162,14 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   const size_t nvec = count / vw;
   int kind;
   size_t work;
+  const bool eb = c->entry_barrier;  // instances with the entry barrier
   switch (algo) {
-    case DCC_ALGO_ONE_SHOT: kind = dcc::kOneShot; work = nvec; break;
-    case DCC_ALGO_TWO_SHOT: kind = dcc::kTwoShot; work = nvec / c->n + 1; break;
-    case DCC_ALGO_TWO_SHOT_SCRATCH: kind = dcc::kTwoShotScratch; work = nvec / c->n + 1; break;
+    case DCC_ALGO_ONE_SHOT: kind = eb ? dcc::kOneShotEB : dcc::kOneShot; work = nvec; break;
+    case DCC_ALGO_TWO_SHOT: kind = eb ? dcc::kTwoShotEB : dcc::kTwoShot; work = nvec / c->n + 1; break;
+    case DCC_ALGO_TWO_SHOT_SCRATCH:
+      kind = eb ? dcc::kTwoShotScratchEB : dcc::kTwoShotScratch;
+      work = nvec / c->n + 1;
+      break;
     case DCC_ALGO_TWO_SHOT_BULK: kind = dcc::kTwoShotBulk; work = nvec / c->n + 1; break;
     case DCC_ALGO_ONE_SHOT_LL: kind = dcc::kOneShotLL; work = nvec; break;
     default: return DCC_ERR_INVALID_ARG;
@@ -173,6 +177,9 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   sh->fn = reduce_kernel_for(t, kind, c->n);
   if (!sh->fn) return DCC_ERR_INVALID_ARG;
   sh->smem = 0;
+  // the entry barrier is built into the thread-copy kernels only
+  if (c->entry_barrier && (algo == DCC_ALGO_ONE_SHOT_LL || algo == DCC_ALGO_TWO_SHOT_BULK))
+    return DCC_ERR_UNSUPPORTED;
   if (algo == DCC_ALGO_ONE_SHOT_LL) {  // fixed launch shape (see ll.cuh)
     if (count * elem_bytes(t) > dcc::kLLMaxBytes) return DCC_ERR_UNSUPPORTED;
     sh->threads = dcc::kLLThreads;
@@ -190,7 +197,7 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   }
   sh->threads = c->threads_override > 0 ? c->threads_override : threads_for(algo, work);
   sh->cooperative = (algo == DCC_ALGO_ONE_SHOT && inplace && c->n > 1) ||
-                    (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1);
+                    (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1) || (c->entry_barrier && c->n > 1);
   if (algo == DCC_ALGO_ONE_SHOT && inplace) work = (nvec + dcc::kInplaceUnroll - 1) / dcc::kInplaceUnroll;
   // one-shot keeps one wave even out of place: every rank reads every input,
   // and the ranks' CTAs reading a region together is what lets L2 serve it
@@ -280,8 +287,10 @@ int dcc_preload_kernels() {
   bool ok = true;
   for (dcc_dtype_t t : types)
     for (int n : ns)
-      for (int kind = dcc::kOneShot; kind <= dcc::kOneShotLL; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
-  for (int n : ns) ok &= load(dcc::allgather_kernel(n)) && load(dcc::allgather_bulk_kernel(n));
+      for (int kind = 0; kind < dcc::kNumKernelKinds; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
+  for (int n : ns)
+    ok &= load(dcc::allgather_kernel(n, false)) && load(dcc::allgather_kernel(n, true)) &&
+          load(dcc::allgather_bulk_kernel(n));
   for (int n : ns)
     ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n)) &&
           load(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_bulk_kernel<__half>(n));
@@ -382,6 +391,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_bulk = std::strcmp(v, "0") != 0 ? 1 : 0;
+  c->entry_barrier = env_flag("DCC_ENTRY_BARRIER");
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
@@ -561,15 +571,17 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
     args.recv[r] = recv[r];
   }
   args.count = recv_count;
-  const void* fn = reduce_kernel_for(t, dcc::kReduceScatter, c->n);
+  // with the entry barrier the CTAs wait on one another: one cooperative wave
+  const bool coop = c->entry_barrier && c->n > 1;
+  const void* fn = reduce_kernel_for(t, coop ? dcc::kReduceScatterEB : dcc::kReduceScatter, c->n);
   const size_t vw = 16 / elem_bytes(t);
   const size_t work = (recv_count + vw - 1) / vw;
   const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);
-  rc = pick_blocks(c, fn, threads, work, &args.blocks, 0, 0, false);
+  rc = pick_blocks(c, fn, threads, work, &args.blocks, 0, 0, coop);
   if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s));
 }
 
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
@@ -596,21 +608,24 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   int eb = (int)elem_bytes(t);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args, &eb};
-  if (c->ag_bulk && sb % 16 == 0 && sb >= kAgBulkMinBytes) {
+  // with the entry barrier the CTAs wait on one another: one cooperative wave
+  // of the thread-copy kernel (the bulk-copy kernel has no entry barrier)
+  const bool coop = c->entry_barrier && c->n > 1;
+  if (!coop && c->ag_bulk && sb % 16 == 0 && sb >= kAgBulkMinBytes) {
     const void* fn = dcc::allgather_bulk_kernel(c->n);
     const size_t smem = dcc::ag_smem_bytes();
     rc = pick_blocks(c, fn, 32, (sb + dcc::kAgTile - 1) / dcc::kAgTile, &args.blocks, smem, 1);
     if (rc != DCC_OK) return rc;
     return launch(fn, args.blocks * c->n, 32, false, kargs, static_cast<cudaStream_t>(s), smem);
   }
-  const void* fn = dcc::allgather_kernel(c->n);
+  const void* fn = dcc::allgather_kernel(c->n, coop);
   const size_t work = (sb + 15) / 16;
   const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);
   // vector path: kAgUnroll vectors per thread; element path: one element per thread
   const size_t per_block = sb % 16 == 0 ? (size_t)dcc::kAgUnroll * threads : (size_t)threads;
-  rc = pick_blocks(c, fn, threads, sb % 16 == 0 ? work : send_count, &args.blocks, 0, per_block, false);
+  rc = pick_blocks(c, fn, threads, sb % 16 == 0 ? work : send_count, &args.blocks, 0, per_block, coop);
   if (rc != DCC_OK) return rc;
-  return launch(fn, args.blocks * c->n, threads, false, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s));
 }
 
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
@@ -795,6 +810,12 @@ int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us) {
 int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks) {
   if (!c || blocks < 0 || blocks > DCC_MAX_BLOCKS_PER_RANK) return DCC_ERR_INVALID_ARG;
   c->blocks_override = blocks;
+  return DCC_OK;
+}
+
+int dcc_set_entry_barrier(dcc_comm_t c, int on) {
+  if (!c) return DCC_ERR_INVALID_ARG;
+  c->entry_barrier = on != 0;
   return DCC_OK;
 }
 

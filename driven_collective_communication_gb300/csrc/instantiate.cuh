@@ -16,6 +16,10 @@ const void* pick_kernel(int kind) {
     case kReduceScatter: return reinterpret_cast<const void*>(&k_reduce_scatter<T, NT>);
     case kTwoShotBulk: return reinterpret_cast<const void*>(&k_allreduce_twoshot_bulk<T, NT>);
     case kOneShotLL: return reinterpret_cast<const void*>(&k_allreduce_oneshot_ll<T, NT>);
+    case kOneShotEB: return reinterpret_cast<const void*>(&k_allreduce_oneshot<T, NT, true>);
+    case kTwoShotEB: return reinterpret_cast<const void*>(&k_allreduce_twoshot<T, NT, true>);
+    case kTwoShotScratchEB: return reinterpret_cast<const void*>(&k_allreduce_twoshot_scratch<T, NT, true>);
+    case kReduceScatterEB: return reinterpret_cast<const void*>(&k_reduce_scatter<T, NT, true>);
     default: return nullptr;
   }
 }

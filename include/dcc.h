@@ -336,6 +336,19 @@ int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us);
  * kernels that never wait otherwise size their grid to cover the work. */
 int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks);
 
+/* Entry barrier (off by default; also DCC_ENTRY_BARRIER=1 in the environment
+ * at creation).  When on, every CTA of the AllReduce (ONE_SHOT, TWO_SHOT,
+ * TWO_SHOT_SCRATCH), ReduceScatter and AllGather kernels first signals the
+ * CTAs of its block slot in every other rank ("my input is ready") and waits
+ * for their signals before it touches peer memory -- the step a multi-GPU
+ * collective needs before reading a peer's input (MSCCL++ README, "Channels":
+ * signal/wait).  On one GPU stream order already orders the ranks' inputs
+ * before the kernel, so the barrier only adds its cost.  Those kernels then
+ * launch cooperatively with at most one wave of CTAs; ONE_SHOT_LL and
+ * TWO_SHOT_BULK have no entry barrier and return DCC_ERR_UNSUPPORTED while it
+ * is on.  A wait that runs out is reported by dcc_comm_check. */
+int dcc_set_entry_barrier(dcc_comm_t c, int on);
+
 /* AUTO picks ONE_SHOT for out-of-place messages of at most `bytes` per rank
  * and TWO_SHOT above, for this dtype.  Defaults come from the measured
  * crossover: 32 KiB with 5 or more ranks, 0 (always two-shot) with 2 to 4. */

@@ -99,6 +99,7 @@ def test_null_communicator_is_rejected(dcc):
         ("dcc_set_wait_timeout_us", None, 10),
         ("dcc_set_blocks_per_rank", None, 1),
         ("dcc_set_algo_threshold", None, 1, 1024),
+        ("dcc_set_entry_barrier", None, 1),
         ("dcc_select_algo", None, 4, 1, ctypes.byref(i)),
         ("dcc_debug_skip_signal", None, 0),
         ("dcc_launch_shape", None, 4, 1, 0, ctypes.byref(i), ctypes.byref(i)),

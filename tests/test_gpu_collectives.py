@@ -503,6 +503,84 @@ def test_lost_signal_times_out_cleanly(dcc):
         assert torch.all(a[0] == 2)
 
 
+# ---------------------------------------------------------------- entry barrier
+@pytest.mark.parametrize("n", [2, 5, 8, 16])
+def test_entry_barrier_same_bits_and_counts(dcc, n):
+    """With the entry barrier on, every thread-copy AllReduce, the ReduceScatter
+    and the AllGather return the oracle's bits, and each launch adds exactly one
+    signal from every rank to every other rank on every block slot it used."""
+    count = 8 * n * 1000 + 3 * n  # ragged: several vectors per shard plus a tail
+    w = W.with_count(W.C4, count, n_ranks=n)
+    xs = W.rank_inputs(w)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16")
+    arena = Arena(dcc, n, count)
+    try:
+        h = arena.comm.handle
+        dcc.dcc_set_entry_barrier(h, True)
+        before, _ = dcc.dcc_comm_read_semaphores(h, n, block=0)
+        launches = 0
+        for algo in ("one_shot", "two_shot", "two_shot_scratch"):
+            for inplace in (False, True):
+                outs = run_allreduce(dcc, arena, xs, "bf16", algo, inplace)
+                launches += 1
+                assert all(same(o, expect, "bf16") for o in outs), (algo, inplace)
+        # block slot 0 took part in every launch: one entry signal per ordered pair each,
+        # plus the scratch kernel's phase barrier and the in-place one-shot's chunk barriers
+        after, expected = dcc.dcc_comm_read_semaphores(h, n, block=0)
+        off = ~np.eye(n, dtype=bool)
+        assert np.all(after[off] - before[off] >= launches)
+        assert np.array_equal(after, expected)  # every signal was waited for
+        # bulk and LL have no entry barrier
+        send = arena.view(arena.inp, "bf16", count)
+        for algo in ("two_shot_bulk", "one_shot_ll"):
+            with pytest.raises(dcc.DccError) as e:
+                dcc.dcc_allreduce(h, send, send, count, "bf16", algo)
+            assert e.value.code == dcc.DCC_ERR_UNSUPPORTED
+        assert arena.comm.check() == dcc.DCC_OK
+    finally:
+        arena.close()
+    # ReduceScatter and AllGather through the entry barrier
+    m = count // n
+    rs_in = [x[: m * n].cuda() for x in xs]
+    rs_out = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ag_out = [torch.empty(m * n, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", rs_in)
+        comm.register_all("output", rs_out)
+        comm.register_all("output", ag_out)
+        dcc.dcc_set_entry_barrier(comm.handle, True)
+        b0, _ = dcc.dcc_comm_read_semaphores(comm.handle, n, block=0)
+        comm.reduce_scatter(rs_in, rs_out)
+        comm.allgather(rs_out, ag_out)
+        assert comm.check() == dcc.DCC_OK
+        b1, e1 = dcc.dcc_comm_read_semaphores(comm.handle, n, block=0)
+        off = ~np.eye(n, dtype=bool)
+        assert np.all(b1[off] - b0[off] == 2) and np.array_equal(b1, e1)
+        host = [W.to_storage(x.cpu()) for x in rs_in]
+        full = oracle.allreduce(host, "bf16")
+        for r in range(n):
+            assert same(W.to_storage(rs_out[r]), full[r * m:(r + 1) * m], "bf16")
+            assert same(W.to_storage(ag_out[r]), full, "bf16")
+
+
+def test_entry_barrier_lost_signal_times_out(dcc):
+    """The two-shot push has no wait of its own; with the entry barrier a rank
+    that never signals makes the launch report DCC_ERR_TIMEOUT."""
+    n = 4
+    comm = dcc.Comm(n)
+    try:
+        bufs = [torch.ones(50000, dtype=torch.float32, device="cuda") for _ in range(n)]
+        comm.register_all("input", bufs)
+        dcc.dcc_set_wait_timeout_us(comm.handle, 50000)
+        dcc.dcc_set_entry_barrier(comm.handle, True)
+        dcc.dcc_debug_skip_signal(comm.handle, 2)
+        comm.allreduce(bufs, bufs, algo="two_shot")
+        assert comm.check() == dcc.DCC_ERR_TIMEOUT
+        assert dcc.dcc_comm_error_detail(comm.handle)[1] == 2
+    finally:
+        comm.close()
+
+
 # ---------------------------------------------------------------- host-side errors on a device
 def test_argument_errors(dcc):
     n = 2
