@@ -314,6 +314,7 @@ def sweep_c3(dcc, dev, stream):
                 step()
             per, _ = time_launches(step, 1000, stream)
             p50 = statistics.median(per) * 1e3
+            p_min, p_mean = min(per) * 1e3, statistics.mean(per) * 1e3
             # host cost of one call (launch included), no device wait in between
             stream.synchronize()
             t = time.perf_counter()
@@ -337,7 +338,8 @@ def sweep_c3(dcc, dev, stream):
                 e1.record(stream)
             e1.synchronize()
             graph_us = e0.elapsed_time(e1) * 1e3 / (10 * reps)
-            row[algo] = {"p50_us": round(p50, 2), "host_us_per_call": round(host_us, 2),
+            row[algo] = {"p50_us": round(p50, 2), "min_us": round(p_min, 2), "mean_us": round(p_mean, 2),
+                         "host_us_per_call": round(host_us, 2),
                          "graph_us": round(graph_us, 2),
                          "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
         if w.bytes_per_rank <= dcc.DCC_LL_MAX_BYTES:  # in place: barrier one-shot vs LL
@@ -398,6 +400,22 @@ def other_workloads(dcc, dev, stream):
     out["c4_bf16_two_shot_entry_barrier"] = {"ms": round(statistics.median(per), 4)}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
+    # the 2-rank fp32 1 MiB one-shot (a latency case: 4 MiB of traffic sits in L2)
+    w1 = W.C1
+    with torch.cuda.stream(stream):
+        xs1 = W.rank_inputs(w1, device=dev)
+        ys1 = [torch.empty_like(x) for x in xs1]
+    torch.cuda.synchronize()
+    with dcc.Comm(2) as c1:
+        c1.register_all("input", xs1)
+        c1.register_all("output", ys1)
+        step = dcc.prepare_allreduce(c1.handle, xs1, ys1, w1.count, "fp32", "one_shot", stream)
+        for _ in range(20):
+            step()
+        per, _ = time_launches(step, 200, stream)
+        assert c1.check(stream) == dcc.DCC_OK
+        out["c1_fp32_n2_1MiB_one_shot"] = {"p50_us": round(statistics.median(per) * 1e3, 2),
+                                           "min_us": round(min(per) * 1e3, 2)}
     # ... and on the 16 KiB decode size, CUDA-graph amortised
     w16 = W.c3(1)
     with torch.cuda.stream(stream):

@@ -140,7 +140,10 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
 
 /* AllGather: recv[p][q*send_count + j] = send[q][j] for all p, q, j < send_count.
  * recv[p] holds N*send_count elements.  Ranges must not overlap.  A bit copy:
- * t only fixes the element size. */
+ * t only fixes the element size.  Thread copies with eight 16-byte loads in
+ * flight per thread and evict-first stores; DCC_AG_BULK=1 in the environment
+ * at communicator creation sends inputs of at least 64 KiB per rank (a
+ * multiple of 16 bytes) through the bulk-copy (TMA) kernel instead. */
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
                   dcc_dtype_t t, dcc_stream_t s);
 
