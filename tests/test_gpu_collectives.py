@@ -94,8 +94,8 @@ def run_allreduce(dcc, arena, xs_host, dtype, algo, inplace, offset=0):
 # ---------------------------------------------------------------- small parity sweep
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16])
 def test_allreduce_parity_sweep(dcc, n):
-    """All dtypes x algorithms x in/out-of-place x counts (empty, 1 element,
-    below one vector, ragged, several CTAs' worth + tail) against the oracle."""
+    """All dtypes x algorithms x in/out-of-place x counts (1 element, below one
+    vector, ragged, several CTAs' worth + tail) against the oracle."""
     counts = [1, 5, 8, 16 * n + 3, 3 * 512 * 8 + 5, 70001]
     arena = Arena(dcc, n, max(counts))
     try:
@@ -111,6 +111,28 @@ def test_allreduce_parity_sweep(dcc, n):
                             assert same(outs[r], expect, dtype), (dtype, count, algo, inplace, r)
     finally:
         arena.close()
+
+
+def test_empty_inputs_are_no_ops(dcc):
+    """count 0: every entry point returns OK, launches nothing and leaves the
+    outputs as they were."""
+    n = 4
+    xs = [torch.full((64,), float(r + 1), device="cuda") for r in range(n)]
+    ys = [torch.full((64 * n,), -7.0, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        h = comm.handle
+        for algo in ("auto", "one_shot", "two_shot", "two_shot_bulk", "one_shot_ll"):
+            dcc.dcc_allreduce(h, xs, ys, 0, "fp32", algo)
+        dcc.dcc_reduce_scatter(h, xs, ys, 0, "fp32")
+        dcc.dcc_allgather(h, xs, ys, 0, "fp32")
+        dcc.dcc_linear_allreduce(h, xs, xs, ys, 0, 8, "bf16")
+        assert comm.check() == dcc.DCC_OK
+    for y in ys:
+        assert torch.all(y == -7.0)
+    for r in range(n):
+        assert torch.all(xs[r] == r + 1)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
