@@ -114,21 +114,26 @@ struct dcc_comm {
 
 namespace dcc_host {
 
-// Makes the communicator's device current for the scope of a call.
+// Makes the communicator's device current for the scope of a call (and puts
+// the caller's device back only if it had to change it).
 class DeviceScope {
  public:
   explicit DeviceScope(int dev) {
     if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
-    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+    if (prev_ != dev) {
+      ok_ = cudaSetDevice(dev) == cudaSuccess;
+      changed_ = ok_ && prev_ >= 0;
+    }
   }
   ~DeviceScope() {
-    if (prev_ >= 0) cudaSetDevice(prev_);
+    if (changed_) cudaSetDevice(prev_);
   }
   bool ok() const { return ok_; }
 
  private:
   int prev_ = -1;
   bool ok_ = true;
+  bool changed_ = false;
 };
 
 // Resident CTAs per SM of `fn` with `threads` threads and `smem` bytes of
