@@ -10,14 +10,18 @@
 //
 // GB300 reading: the FIFO lives in pinned host memory mapped into the GPU's
 // address space (Grace and the GPU share it coherently over NVLink-C2C); the
-// proxy issues cudaMemcpyAsync device-to-device on a copy engine and reports
-// signals and flushes back with 64-bit value writes (cuStreamWriteValue64)
-// into device memory that the GPU polls, all on one proxy stream, so stream
-// order alone puts every signal and flush behind the copies before it.  Every
+// proxy issues cudaMemcpyAsync device-to-device on the copy engines and
+// reports signals and flushes back with 64-bit value writes
+// (cuStreamWriteValue64) into device memory that the GPU polls.  Copies and
+// signals to rank d go to proxy stream d % K, so stream order puts every
+// signal behind the copies of its channel, and K copy engines work at once; a
+// flush is written after every stream's earlier work (events).  K is 4 by
+// default (DCC_PROXY_STREAMS, 1..8): measured on GB300 for the 8 x 8 MiB fp16
+// AllGather, 0.573 / 0.345 / 0.253 / 0.281 ms with K = 1 / 2 / 4 / 8.  Every
 // wait on either side is bounded.
 //
-// The kernels that push triggers keep running while the proxy's stream works
-// for them.  If the GPU multiplexes the proxy stream onto the same hardware
+// The kernels that push triggers keep running while the proxy's streams work
+// for them.  If the GPU multiplexes a proxy stream onto the same hardware
 // queue as the pushing kernel's stream (an application with more streams than
 // CUDA_DEVICE_MAX_CONNECTIONS), the proxy's work queues behind that kernel and
 // its waits run out: run PortChannel code with enough connections.
@@ -39,6 +43,7 @@ namespace {
 
 constexpr unsigned long long kFifoCapacity = 1024;
 constexpr int kMaxCustom = 32;
+constexpr int kMaxProxyStreams = 8;
 
 typedef CUresult (*WriteValue64Fn)(CUstream, CUdeviceptr, cuuint64_t, unsigned int);
 
@@ -57,7 +62,13 @@ struct ProxyState {
   // device words: head | done | sem[kSemSlots*kSemWords] | expect[kSemSlots]
   unsigned long long* d_words = nullptr;
   dcc::PortDev dev{};
-  cudaStream_t stream = nullptr;  // copies, signals and flushes, in FIFO order
+  // Copies and signals to rank d go to streams[d % nstreams], in FIFO order
+  // per stream; a flush is written on streams[0] after the work of every
+  // stream that had some since the previous flush (events).
+  int nstreams = 4;
+  cudaStream_t streams[kMaxProxyStreams] = {};
+  cudaEvent_t events[kMaxProxyStreams] = {};
+  bool dirty[kMaxProxyStreams] = {};
   unsigned long long sig_count[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
   WriteValue64Fn write_value = nullptr;
   dcc_trigger_handler_t handler = nullptr;
@@ -167,7 +178,9 @@ void handle(dcc_comm* c, ProxyState& P, unsigned long long fst, unsigned long lo
     set_error(P, DCC_ERR_INVALID_ARG);
     return;
   }
-  cudaStream_t st = P.stream;
+  const int k = dst % P.nstreams;
+  cudaStream_t st = P.streams[k];
+  if (fst & (dcc::kTrigPut | dcc::kTrigSignal)) P.dirty[k] = true;
   if (fst & dcc::kTrigPut) {
     char *d = nullptr, *s = nullptr;
     if (!window_range(c, dst, DCC_BUF_OUTPUT, dst_off, bytes, &d) ||
@@ -183,8 +196,15 @@ void handle(dcc_comm* c, ProxyState& P, unsigned long long fst, unsigned long lo
     if (P.write_value((CUstream)st, addr, v, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
       set_error(P, DCC_ERR_CUDA);
   }
-  if (fst & dcc::kTrigFlush) {  // in stream order after everything issued so far
-    if (P.write_value((CUstream)st, (CUdeviceptr)P.dev.done, seq + 1, CU_STREAM_WRITE_VALUE_DEFAULT) !=
+  if (fst & dcc::kTrigFlush) {  // after everything issued so far, on every stream
+    for (int j = 1; j < P.nstreams; ++j) {
+      if (!P.dirty[j]) continue;
+      if (cudaEventRecord(P.events[j], P.streams[j]) != cudaSuccess ||
+          cudaStreamWaitEvent(P.streams[0], P.events[j], 0) != cudaSuccess)
+        set_error(P, DCC_ERR_CUDA);
+      P.dirty[j] = false;
+    }
+    if (P.write_value((CUstream)P.streams[0], (CUdeviceptr)P.dev.done, seq + 1, CU_STREAM_WRITE_VALUE_DEFAULT) !=
         CUDA_SUCCESS)
       set_error(P, DCC_ERR_CUDA);
   }
@@ -229,7 +249,10 @@ int ensure_proxy(dcc_comm* c) {
     cudaGetLastError();
     if (P->h_fifo) cudaFreeHost(P->h_fifo);
     if (P->d_words) cudaFree(P->d_words);
-    if (P->stream) cudaStreamDestroy(P->stream);
+    for (int j = 0; j < kMaxProxyStreams; ++j) {
+      if (P->streams[j]) cudaStreamDestroy(P->streams[j]);
+      if (P->events[j]) cudaEventDestroy(P->events[j]);
+    }
     delete P;
     return code;
   };
@@ -252,9 +275,15 @@ int ensure_proxy(dcc_comm* c) {
   if (cudaMalloc(&P->d_words, words * sizeof(unsigned long long)) != cudaSuccess ||
       cudaMemset(P->d_words, 0, words * sizeof(unsigned long long)) != cudaSuccess)
     return fail(DCC_ERR_CUDA);
-  if (cudaStreamCreateWithFlags(&P->stream, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess)
-    return fail(DCC_ERR_CUDA);
+  if (const char* v = std::getenv("DCC_PROXY_STREAMS")) {
+    const int k = std::atoi(v);
+    if (k >= 1 && k <= kMaxProxyStreams) P->nstreams = k;
+  }
+  for (int j = 0; j < P->nstreams; ++j)
+    if (cudaStreamCreateWithFlags(&P->streams[j], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&P->events[j], cudaEventDisableTiming) != cudaSuccess)
+      return fail(DCC_ERR_CUDA);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(DCC_ERR_CUDA);
   P->dev.slots = reinterpret_cast<dcc::ProxyTrigger*>(P->d_fifo);
   P->dev.tail = reinterpret_cast<unsigned long long*>(P->d_fifo + kFifoCapacity * sizeof(dcc::ProxyTrigger));
   P->dev.head = P->d_words;
@@ -288,7 +317,10 @@ void dcc_proxy_release(dcc_comm* c) {
     P->running = false;
   }
   cudaDeviceSynchronize();
-  if (P->stream) cudaStreamDestroy(P->stream);
+  for (int j = 0; j < kMaxProxyStreams; ++j) {
+    if (P->streams[j]) cudaStreamDestroy(P->streams[j]);
+    if (P->events[j]) cudaEventDestroy(P->events[j]);
+  }
   cudaFree(P->d_words);
   cudaFreeHost(P->h_fifo);
   cudaGetLastError();
@@ -338,7 +370,7 @@ int dcc_proxy_stop(dcc_comm_t c) {
   P.stop.store(true, std::memory_order_release);
   P.thread.join();
   P.running = false;
-  cudaStreamSynchronize(P.stream);
+  for (int j = 0; j < P.nstreams; ++j) cudaStreamSynchronize(P.streams[j]);
   return P.error.load();
 }
 

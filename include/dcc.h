@@ -268,12 +268,15 @@ int dcc_comm_read_semaphores(dcc_comm_t c, int block, uint64_t* inbound, uint64_
 /* thread of the communicator pops them and carries them out: PUT = a      */
 /* cudaMemcpyAsync device-to-device on a copy engine from the source rank's */
 /* first INPUT window to the destination rank's first OUTPUT window; SIGNAL */
-/* and FLUSH = value writes the GPU polls (bounded), all on one proxy       */
-/* stream in FIFO order.  A trigger whose fst is non-zero with bit 63 clear */
-/* is a custom trigger for the installed handler.  Windows must not change  */
-/* while the proxy runs.  The GPU must not multiplex the proxy's stream     */
-/* onto the hardware queue of a kernel that waits for it: with many streams */
-/* set CUDA_DEVICE_MAX_CONNECTIONS=32 before the CUDA context exists.       */
+/* and FLUSH = value writes the GPU polls (bounded).  Copies and signals to */
+/* rank d run in FIFO order on proxy stream d % K (K = 4, or               */
+/* DCC_PROXY_STREAMS = 1..8 at the proxy's first start), so K copy engines  */
+/* work at once; a FLUSH is written after every stream's earlier work.  A   */
+/* trigger whose fst is non-zero with bit 63 clear is a custom trigger for  */
+/* the installed handler.  Windows must not change while the proxy runs.    */
+/* The GPU must not multiplex a proxy stream onto the hardware queue of a   */
+/* kernel that waits for it: with many streams set                          */
+/* CUDA_DEVICE_MAX_CONNECTIONS=32 before the CUDA context exists.           */
 /* ------------------------------------------------------------------------ */
 
 typedef void (*dcc_trigger_handler_t)(uint64_t fst, uint64_t snd, void* user);

@@ -24,7 +24,7 @@ def dcc():
     return mod
 
 
-def test_port_put_signal_flush(dcc):
+def test_port_put_signal_flush(dcc, proxy_streams):
     n = 4
     with dcc.Comm(n) as comm:
         ins = [torch.arange(8192, dtype=torch.int32, device="cuda") + 100000 * r for r in range(n)]
@@ -47,8 +47,15 @@ def test_port_put_signal_flush(dcc):
         assert rc == dcc.DCC_OK and processed == 4 and custom == 0  # 2 puts + 2 flushes
 
 
+@pytest.fixture(params=[1, 4])
+def proxy_streams(request, monkeypatch):
+    """The proxy with one stream, and with copies spread over four (the default)."""
+    monkeypatch.setenv("DCC_PROXY_STREAMS", str(request.param))
+    return request.param
+
+
 @pytest.mark.parametrize("n,m", [(8, 4096), (8, 4194304), (3, 1000 * 8), (16, 65536)])
-def test_port_allgather_matches_oracle_and_memory_channel(dcc, n, m):
+def test_port_allgather_matches_oracle_and_memory_channel(dcc, proxy_streams, n, m):
     w = W.with_count(W.C5, n * m, n_ranks=n)
     xs = [x[:m].cuda() for x in W.rank_inputs(w)]
     port_out = [torch.full((n * m,), float("nan"), dtype=torch.float16, device="cuda") for _ in range(n)]
@@ -73,7 +80,7 @@ def test_port_allgather_matches_oracle_and_memory_channel(dcc, n, m):
         assert torch.equal(port_out[r].view(torch.int16), mem_out[r].view(torch.int16))
 
 
-def test_fifo_wraps_around(dcc):
+def test_fifo_wraps_around(dcc, proxy_streams):
     """Many more triggers than FIFO slots (1024): flow control on the tail."""
     n, m = 8, 2048
     xs = [torch.randn(m, device="cuda").half() for _ in range(n)]
