@@ -525,6 +525,59 @@ def test_lost_signal_times_out_cleanly(dcc):
         assert torch.all(a[0] == 2)
 
 
+# ---------------------------------------------------------------- beyond 32-bit element indices
+def test_more_than_2_31_elements_per_rank(dcc):
+    """4 GiB + 26 bytes of bf16 per rank (2^31 + 13 elements): 64-bit index
+    arithmetic on the device and in the launch shapes.  Sampled windows (random
+    ones, both sides of element 2^31 and the ragged tail) are checked against
+    the oracle run on those elements.  Inputs are filled and outputs cleared
+    in 2^24-element slices, and samples are read back as contiguous slices, so
+    every torch operation stays small."""
+    n, count, chunk = 2, 2 ** 31 + 13, 2 ** 24
+    free, _ = torch.cuda.mem_get_info()
+    if free < 24 * 2 ** 30:
+        pytest.skip("needs 24 GiB of free device memory")
+    pat = ((torch.arange(chunk, device="cuda") % 251) - 125).to(torch.bfloat16)
+    xs = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    for r, x in enumerate(xs):
+        src = pat * (r + 1)
+        for a in range(0, count, chunk):
+            b = min(count, a + chunk)
+            x[a:b].copy_(src[: b - a])
+    ys = [torch.empty_like(x) for x in xs]
+
+    def clear(t):
+        for a in range(0, count, chunk):
+            t[a: min(count, a + chunk)].zero_()
+
+    rng = np.random.default_rng(5)
+    windows = [(int(o), 64) for o in np.sort(rng.integers(0, count - 64, 48))]
+    windows += [(2 ** 31 - 64, count - (2 ** 31 - 64)), (count - 40, 40)]  # up to the last element
+    assert all(0 <= o and o + k <= count for o, k in windows)
+
+    def sample(t):
+        return np.concatenate([W.to_storage(t[o: o + k].cpu()) for o, k in windows])
+
+    expect = oracle.allreduce([sample(x) for x in xs], "bf16")
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        for algo in ("one_shot", "two_shot"):
+            for y in ys:
+                clear(y)
+            comm.allreduce(xs, ys, algo=algo)
+            assert comm.check() == dcc.DCC_OK
+            for r in range(n):
+                assert same(sample(ys[r]), expect, "bf16"), (algo, r)
+        # in place through the two-shot push
+        comm.allreduce(xs, xs, algo="two_shot")
+        assert comm.check() == dcc.DCC_OK
+        for r in range(n):
+            assert same(sample(xs[r]), expect, "bf16"), ("in place", r)
+    del xs, ys
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- entry barrier
 @pytest.mark.parametrize("n", [2, 5, 8, 16])
 def test_entry_barrier_same_bits_and_counts(dcc, n):
