@@ -32,6 +32,13 @@
  *    given type, native (little-endian) storage; bf16 and fp16 are raw 16-bit
  *    IEEE patterns.  Data pointers must be 16-byte aligned.
  *  - Threading: a communicator is not thread-safe; serialise calls on it.
+ *  - Concurrency on the GPU: kernels that synchronise ranks (in-place
+ *    ONE_SHOT, TWO_SHOT_SCRATCH, ONE_SHOT_LL, the ring barrier, the channel
+ *    primitives, anything with the entry barrier on) use the communicator's
+ *    semaphores and waiter counts; two of them must not run at the same time
+ *    on one communicator (issue them on one stream, or use one communicator
+ *    per stream).  Kernels that never wait (out-of-place ONE_SHOT, TWO_SHOT,
+ *    ReduceScatter, AllGather, the fused linear layer) may overlap freely.
  */
 #ifndef DCC_H
 #define DCC_H
