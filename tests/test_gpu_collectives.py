@@ -482,6 +482,61 @@ def test_graph_replay_keeps_epochs(dcc):
         arena.close()
 
 
+def test_graph_replay_of_rs_ag_fused_and_entry_barrier(dcc):
+    """ReduceScatter, AllGather (plain and through the entry barrier) and both
+    fused linear-layer kernels captured into one CUDA graph and replayed: the
+    same bits as the oracle after every replay."""
+    n, m = 8, 4104
+    g = torch.Generator().manual_seed(11)
+    xs = [torch.randn(n * m, generator=g).to(torch.bfloat16).cuda() for _ in range(n)]
+    rs = [torch.empty(m, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ag = [torch.empty(n * m, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    rs_eb = [torch.empty_like(t) for t in rs]
+    ag_eb = [torch.empty_like(t) for t in ag]
+    rows = 64
+    lin = {}
+    for kp in (1024, 4096):  # thread-load kernel and bulk-copy kernel
+        ws = [torch.randint(-3, 4, (rows * kp,), generator=g).to(torch.bfloat16).cuda() for _ in range(n)]
+        xv = [torch.randint(-3, 4, (kp,), generator=g).to(torch.bfloat16).cuda() for _ in range(n)]
+        yv = [torch.empty(rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        lin[kp] = (ws, xv, yv)
+    host = [W.to_storage(x.cpu()) for x in xs]
+    full = oracle.allreduce(host, "bf16")
+    with dcc.Comm(n) as comm, dcc.Comm(n) as comm_eb:
+        for c, (r_, a_) in ((comm, (rs, ag)), (comm_eb, (rs_eb, ag_eb))):
+            c.register_all("input", xs)
+            c.register_all("output", r_)
+            c.register_all("output", a_)
+        for ws, xv, yv in lin.values():
+            comm.register_all("input", ws)
+            comm.register_all("input", xv)
+            comm.register_all("output", yv)
+        dcc.dcc_set_entry_barrier(comm_eb.handle, True)
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            dcc.dcc_reduce_scatter(comm.handle, xs, rs, m, "bf16", stream=s)
+            dcc.dcc_allgather(comm.handle, rs, ag, m, "bf16", stream=s)
+            dcc.dcc_reduce_scatter(comm_eb.handle, xs, rs_eb, m, "bf16", stream=s)
+            dcc.dcc_allgather(comm_eb.handle, rs_eb, ag_eb, m, "bf16", stream=s)
+            for kp, (ws, xv, yv) in lin.items():
+                dcc.dcc_linear_allreduce(comm.handle, ws, xv, yv, rows, kp, "bf16", stream=s)
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert comm.check() == dcc.DCC_OK and comm_eb.check() == dcc.DCC_OK
+    for r in range(n):
+        for got_rs, got_ag in ((rs, ag), (rs_eb, ag_eb)):
+            assert same(W.to_storage(got_rs[r]), full[r * m:(r + 1) * m], "bf16")
+            assert same(W.to_storage(got_ag[r]), full, "bf16")
+    for kp, (ws, xv, yv) in lin.items():
+        expect = oracle.linear_allreduce([W.to_storage(w.cpu()) for w in ws], [W.to_storage(x.cpu()) for x in xv],
+                                         "bf16", rows, kp)
+        for r in range(n):
+            assert np.array_equal(W.to_storage(yv[r]), expect), (kp, r)
+
+
 def test_lost_signal_times_out_cleanly(dcc):
     """A rank that never signals makes its peers' waits run out: the kernel
     records DCC_ERR_TIMEOUT and returns; the GPU stays usable."""
