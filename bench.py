@@ -629,7 +629,8 @@ def run_reference(args, dist):
 
 # ------------------------------------------------------------------ profiling cases
 PROFILE_CASES = ("allreduce_two_shot", "allreduce_two_shot_bulk", "allreduce_one_shot",
-                 "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "reduce_scatter",
+                 "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "allreduce_one_shot_ll",
+                 "reduce_scatter",
                  "allgather", "ring_barrier", "linear_allreduce")
 
 
