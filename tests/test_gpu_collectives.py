@@ -319,6 +319,31 @@ def test_c4_bf16_n8_256MiB_sampled(dcc):
         comm.close()
 
 
+@pytest.mark.parametrize("n,dtype", [(2, "bf16"), (4, "bf16"), (16, "bf16"), (8, "fp32")])
+def test_256MiB_per_rank_other_rank_counts_and_fp32_sampled(dcc, n, dtype):
+    """The other full-size AllReduces the benchmark times (256 MiB per rank, AUTO):
+    sampled elements against the oracle and every rank's output identical."""
+    recipe = W.C4 if dtype == "bf16" else W.C1
+    count = (256 << 20) // W.ELEM_BYTES[dtype]
+    w = W.with_count(recipe, count, n_ranks=n)
+    xs = W.rank_inputs(w, device="cuda")
+    recv = [torch.empty_like(x) for x in xs]
+    idx = sampled_indices(count, n, k=50000)
+    assert idx.min() >= 0 and idx.max() < count
+    idx_t = torch.from_numpy(idx).cuda()
+    expect = oracle.allreduce([W.to_storage(x[idx_t]) for x in xs], dtype)
+    bits = torch.int16 if dtype == "bf16" else torch.int32
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", xs)
+        comm.register_all("output", recv)
+        comm.allreduce(xs, recv, algo="auto")
+        assert comm.check() == dcc.DCC_OK
+    for r in range(1, n):
+        assert torch.equal(recv[r].view(bits), recv[0].view(bits)), r
+    for r in (0, n - 1):
+        assert same(W.to_storage(recv[r][idx_t]), expect, dtype), r
+
+
 def test_c5_fp16_reduce_scatter_and_allgather_full(dcc):
     w = W.C5
     n = 8
