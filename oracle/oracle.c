@@ -144,6 +144,38 @@ static float widen(const void* buf, size_t i, int dtype)
     }
 }
 
+/* binary64 -> fp16 / bf16 with one round-to-nearest-even, from the IEEE-754
+ * formats: p significant bits (implicit one included), exponents emin..emax,
+ * subnormals down to 2^(emin - p + 1), overflow to infinity at the midpoint
+ * above the largest finite value.  Used where a result is defined as a
+ * binary64 value rounded once to the 16-bit output type. */
+static uint16_t f64_to_half_once(double v, int dtype)
+{
+    const int p = dtype == ORC_FP16 ? 11 : 8, emin = dtype == ORC_FP16 ? -14 : -126,
+              emax = dtype == ORC_FP16 ? 15 : 127, bias = dtype == ORC_FP16 ? 15 : 127;
+    const uint16_t sign = signbit(v) ? 0x8000u : 0u, exp_all = dtype == ORC_FP16 ? 0x7C00u : 0x7F80u;
+    if (isnan(v)) return (uint16_t)(sign | exp_all | (dtype == ORC_FP16 ? 0x0200u : 0x0040u));
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | exp_all);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);             /* a in [2^(e2-1), 2^e2) */
+    int e = e2 - 1;
+    if (e < emin) e = emin;          /* subnormals share the smallest quantum */
+    double q = ldexp(1.0, e - (p - 1));
+    double n = a / q;                /* exact: a power-of-two scaling */
+    double fl = floor(n);
+    double r = n - fl;               /* exact */
+    if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    long k = (long)fl;               /* quanta, <= 2^p */
+    const long one = 1L << (p - 1);
+    if (k == 0) return sign;
+    if (e == emin && k < one) return (uint16_t)(sign | (uint16_t)k);   /* subnormal */
+    if (k == 2 * one) { k = one; e += 1; }                             /* next binade */
+    if (e > emax) return (uint16_t)(sign | exp_all);                   /* overflow */
+    return (uint16_t)(sign | (uint16_t)((e + bias) << (p - 1)) | (uint16_t)(k - one));
+}
+
 static void narrow_store(void* buf, size_t i, float v, int dtype)
 {
     switch (dtype) {
@@ -295,7 +327,7 @@ int orc_linear_allreduce(int n, const void* const* w, const void* const* x, size
         for (int p = 0; p < n; ++p)
             for (size_t k = 0; k < kp; ++k)
                 acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);
-        narrow_store(out, i, (float)acc, dtype);
+        ((uint16_t*)out)[i] = f64_to_half_once(acc, dtype);
     }
     return 0;
 }

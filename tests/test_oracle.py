@@ -379,16 +379,52 @@ def test_linear_allreduce_closed_forms(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_allreduce_rounds_once(dtype):
+    """The binary64 sum is rounded once to the output type.  Hand-derived cases
+    where rounding through binary32 first would land on a tie and round to
+    even, but the exact sum lies just above the tie:
+      bf16: 1 + 2^-8 + 2^-30 -> 1 + 2^-7 (0x3F81); via binary32 -> 1.0 (0x3F80)
+      fp16: 1 + 2^-11 + 2^-14 * 2^-14 -> 1 + 2^-10 (0x3C01); via binary32 -> 1.0
+    plus the same with the sign flipped, a subnormal result and an overflow."""
+    if dtype == "bf16":
+        w, x, want = [0x3F80, 0x3B80, 0x3080], [0x3F80, 0x3F80, 0x3F80], 0x3F81  # 1, 2^-8, 2^-30
+        sub_w, sub_x, sub_want = [0x0380], [0x3A80], 0x0008       # 2^-120 * 2^-10 = 2^-130 = 8 quanta of 2^-133
+        big, inf = 0x7F7F, 0x7F80                                   # largest finite, infinity
+    else:
+        w, x, want = [0x3C00, 0x1000, 0x0400], [0x3C00, 0x3C00, 0x0400], 0x3C01  # 1, 2^-11, 2^-14
+        sub_w, sub_x, sub_want = [0x0400], [0x1400], 0x0001        # 2^-14 * 2^-10 = 2^-24
+        big, inf = 0x7BFF, 0x7C00                                   # 65504, infinity
+
+    def run(wv, xv):
+        return int(oracle.linear_allreduce([np.array(wv, np.uint16)], [np.array(xv, np.uint16)], dtype,
+                                           1, len(wv))[0])
+
+    assert run(w, x) == want
+    assert run([v | 0x8000 for v in w], x) == want | 0x8000
+    # exact ties go to even: 1 + half a quantum -> 1; 1 + 1.5 quanta -> 1 + 2 quanta
+    one = 0x3C00 if dtype == "fp16" else 0x3F80
+    half_q = 0x1000 if dtype == "fp16" else 0x3B80           # 2^-11 / 2^-8
+    q = 0x1400 if dtype == "fp16" else 0x3C00                # 2^-10 / 2^-7
+    assert run([one, half_q], [one, one]) == one
+    assert run([one, q, half_q], [one, one, one]) == one + 2
+    assert run(sub_w, sub_x) == sub_want
+    assert run([big, big], [0x3C00 if dtype == "fp16" else 0x3F80] * 2) == inf
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_linear_allreduce_matches_float64_matmul(dtype):
     """Against numpy's float64 matrix product of the concatenated shards,
-    rounded once to the output type (a library routine, not the oracle's loop)."""
+    rounded once to the output type by the pure-Python brute force's generic
+    rounding (a library product and an independent rounding, not the oracle's
+    loop)."""
     n, rows, kp = 3, 24, 40
     rng = np.random.default_rng(2)
     ws = [W.to_storage(torch.randn(rows * kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
     xs = [W.to_storage(torch.randn(kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
     a = np.concatenate([storage_to_float(w, dtype).reshape(rows, kp) for w in ws], axis=1)
     x = np.concatenate([storage_to_float(v, dtype) for v in xs])
-    ref = W.to_storage(torch.from_numpy(a @ x).float().to(W.TORCH_DTYPES[dtype]))
+    ref = np.array([brute.encode(brute.round_ieee(float(v), *brute.FORMATS[dtype]), dtype) for v in a @ x],
+                   np.uint16)
     got = oracle.linear_allreduce(ws, xs, dtype, rows, kp)
     # the fp64 sums of a float64 matmul may differ from the oracle's loop in the
     # last bits of binary64; after rounding to 16 bits they agree except at

@@ -41,6 +41,10 @@ MUTANTS = {
     "ring_wrong_neighbour": ("(s == (d + n - 1) % n)", "(s == (d + 1) % n)"),
     "linear_drops_rank_weight": ("acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);",
                                  "acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p ? p - 1 : 0], k, dtype);"),
+    "linear_rounds_through_fp32": ("((uint16_t*)out)[i] = f64_to_half_once(acc, dtype);",
+                                   "((uint16_t*)out)[i] = f64_to_half_once((double)(float)acc, dtype);"),
+    "half_once_ties_up": ("if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;\n    long k = (long)fl;               /* quanta, <= 2^p */",
+                          "if (r >= 0.5) fl += 1.0;\n    long k = (long)fl;               /* quanta, <= 2^p */"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
