@@ -66,7 +66,7 @@ typedef enum {
   DCC_ERR_CUDA = -5,           /* a CUDA runtime call failed */
   DCC_ERR_LAUNCH = -6,         /* the grid cannot be co-resident on this GPU */
   DCC_ERR_TIMEOUT = -7,        /* a device wait gave up (sticky for the communicator) */
-  DCC_ERR_UNSUPPORTED = -8     /* valid request this build does not implement */
+  DCC_ERR_UNSUPPORTED = -8     /* valid request the library does not implement */
 } dcc_result_t;
 
 typedef enum { DCC_INT32 = 0, DCC_FP32 = 1, DCC_FP16 = 2, DCC_BF16 = 3 } dcc_dtype_t;
