@@ -715,7 +715,7 @@ def main():
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "int32", "fp32"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no sweep, e2e, CPU leg)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
