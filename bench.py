@@ -257,6 +257,7 @@ def run_ours(args, dist):
     if dist.rank == 0 and not args.quick:
         out["e2e"] = e2e_host(dcc, comm, xs, ys, w, args, stream)
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
+        out["graph_node_floor_us"] = graph_node_floor(stream)
         out["other"] = other_workloads(dcc, dev, stream)
         gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
         gbs1, _, sample1, _ = oracle_sample_run(3.0, args.cpu_elems // 8, threads=1)
@@ -296,6 +297,28 @@ def e2e_host(dcc, comm, xs, ys, w, args, stream):
     return {"value": round(w.bytes_per_rank / (ms / 1e3) / GB, 3), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
             "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3), "steps": steps}
+
+
+def graph_node_floor(stream, reps=100):
+    """Time per node of a CUDA graph of near-empty kernels (torch's spin kernel
+    with a zero count): the launch floor under the graph-amortised latencies."""
+    for _ in range(10):
+        torch.cuda._sleep(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            torch.cuda._sleep(0)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return round(e0.elapsed_time(e1) * 1e3 / (10 * reps), 3)
 
 
 def sweep_c3(dcc, dev, stream):
