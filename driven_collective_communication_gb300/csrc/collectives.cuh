@@ -31,7 +31,7 @@
 namespace dcc {
 
 constexpr int kThreads = 512;       // threads per CTA of the data kernels
-constexpr int kInplaceUnroll = 4;   // vectors per thread per chunk, in-place one-shot
+constexpr int kInplaceUnroll = 4;   // most vectors per thread per chunk, in-place one-shot
 
 // ------------------------------------------------------------- element lanes
 template <typename T>
@@ -223,7 +223,11 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   unsigned long long expected = 0;
   const bool waiter = (int)threadIdx.x < n && (int)threadIdx.x != rank;
   if (waiter) expected = dc.expect[sem_slot(rank, threadIdx.x, blk)];
-  const size_t chunk = (size_t)kInplaceUnroll * blockDim.x;
+  // U vectors per thread per chunk: 1 for small messages (one chunk per CTA,
+  // all loads of a thread in flight at once), kInplaceUnroll for large ones
+  // (fewer chunks, so fewer barrier rounds)
+  const int U = a.unroll > 0 && a.unroll < kInplaceUnroll ? a.unroll : kInplaceUnroll;
+  const size_t chunk = (size_t)U * blockDim.x;
   const size_t nchunks = (nvec + chunk - 1) / chunk;
   bool ok = true;
   for (size_t c = blk; c < nchunks; c += B) {
@@ -231,14 +235,14 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (v < nvec) res[u] = reduce_vec<T, NT>(a.send, n, v);
+      if (u < U && v < nvec) res[u] = reduce_vec<T, NT>(a.send, n, v);
     }
     ok = group_barrier(dc, rank, n, blk, expected);
     if (!ok) break;
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (v < nvec) st_vec(out + v, res[u]);
+      if (u < U && v < nvec) st_vec(out + v, res[u]);
     }
   }
   if (ok && blk == 0 && tail0 < a.count) {  // same on every rank: all slot-0 CTAs take part

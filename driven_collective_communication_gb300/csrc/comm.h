@@ -99,6 +99,7 @@ struct dcc_comm {
   // crossover), 0 never, 1 always (DCC_FUSED_BULK)
   int fused_bulk = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier
+  int inplace_unroll = 0;      // DCC_INPLACE_UNROLL: force the in-place one-shot's vectors per thread
   bool ag_bulk = false;  // DCC_AG_BULK=1: AllGather through the bulk-copy pipeline when aligned and large
   bool zero_copy = true;  // host-buffer AllReduce reads/writes mapped pinned host memory directly
   int sticky = DCC_OK;

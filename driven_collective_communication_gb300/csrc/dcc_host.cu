@@ -151,6 +151,7 @@ struct Shape {
   int threads;
   bool cooperative;
   size_t smem;
+  int unroll = 0;  // in-place one-shot: vectors per thread per chunk
 };
 
 // The compile-time rank count a kernel table holds for n (0 = runtime-N instance).
@@ -198,7 +199,14 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   sh->threads = c->threads_override > 0 ? c->threads_override : threads_for(algo, work);
   sh->cooperative = (algo == DCC_ALGO_ONE_SHOT && inplace && c->n > 1) ||
                     (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1) || (c->entry_barrier && c->n > 1);
-  if (algo == DCC_ALGO_ONE_SHOT && inplace) work = (nvec + dcc::kInplaceUnroll - 1) / dcc::kInplaceUnroll;
+  if (algo == DCC_ALGO_ONE_SHOT && inplace) {
+    // one vector per thread while one chunk per CTA covers the message within
+    // the CTA cap (a single barrier round, every load in flight at once), else
+    // kInplaceUnroll vectors per thread and fewer barrier rounds
+    sh->unroll = c->inplace_unroll > 0 ? c->inplace_unroll
+                 : nvec <= (size_t)DCC_MAX_BLOCKS_PER_RANK * sh->threads ? 1 : dcc::kInplaceUnroll;
+    work = (nvec + sh->unroll - 1) / sh->unroll;
+  }
   // one-shot keeps one wave even out of place: every rank reads every input,
   // and the ranks' CTAs reading a region together is what lets L2 serve it
   const bool one_wave = sh->cooperative || algo == DCC_ALGO_ONE_SHOT;
@@ -255,6 +263,7 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
   rc = allreduce_shape(c, count, t, algo, inplace, &sh);
   if (rc != DCC_OK) return rc;
   args.blocks = sh.blocks;
+  args.unroll = sh.unroll;
   if (c->log)
     std::fprintf(stderr, "dcc_allreduce: n=%d count=%zu dtype=%d algo=%d inplace=%d blocks/rank=%d\n",
                  c->n, count, (int)t, (int)algo, (int)inplace, sh.blocks);
@@ -391,6 +400,10 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_bulk = std::strcmp(v, "0") != 0 ? 1 : 0;
+  if (const char* v = std::getenv("DCC_INPLACE_UNROLL")) {
+    const int u = std::atoi(v);
+    if (u >= 1 && u <= dcc::kInplaceUnroll) c->inplace_unroll = u;
+  }
   c->entry_barrier = env_flag("DCC_ENTRY_BARRIER");
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;

@@ -57,6 +57,7 @@ struct CollArgs {
   size_t count;   // elements: per-rank buffer (AllReduce), recv_count (RS), send_count (AG)
   int blocks;     // CTAs per rank
   int inplace;    // some rank has send == recv
+  int unroll;     // in-place one-shot: vectors per thread per chunk (1..4; 0 = 4)
 };
 
 // Arguments of the primitive (put/get) kernels.
