@@ -9,7 +9,8 @@
 // Packets are written and polled with relaxed GPU-scope accesses: only GPU
 // threads read them, and on GB300 (whose host CPU may cache GPU memory
 // coherently) the system-scope volatile forms measured 4.6 us per 16 KiB
-// AllReduce against 3.8 us.
+// AllReduce against 3.8 us (3.6 us once missing packets are re-polled in one
+// round rather than peer by peer).
 //
 // Rank r first publishes its input as packets into its own LL buffer (a
 // library-owned allocation, so no caller data can look like a flag), then gets
@@ -103,18 +104,23 @@ __device__ __forceinline__ bool ll_reduce(const DevComm& dc, int n, int rank, in
       if (p != rank && !(lo[p].y == flag && lo[p].w == flag && hi[p].y == flag && hi[p].w == flag))
         missing |= 1u << p;
     if (missing) {
+      // re-poll: issue the loads of every packet still missing, then examine
+      // them, so one round costs one L2 round trip however many are missing
       const unsigned long long t0 = global_timer_ns();
       for (unsigned it = 1; missing; ++it) {
 #pragma unroll
         for (int p = 0; p < NT; ++p) {
           if (!(missing & (1u << p))) continue;
           const uint4* pk = reinterpret_cast<const uint4*>(dc.ll_buf + (size_t)p * kLLBufBytes) + 2 * v;
-          uint32_t a, b, c, d;
-          if (ld_ll(pk, flag, a, b) && ld_ll(pk + 1, flag, c, d)) {
-            lo[p].x = a; lo[p].z = b; hi[p].x = c; hi[p].z = d;
-            missing &= ~(1u << p);
-          }
+          asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(lo[p].x), "=r"(lo[p].y), "=r"(lo[p].z), "=r"(lo[p].w) : "l"(pk) : "memory");
+          asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(hi[p].x), "=r"(hi[p].y), "=r"(hi[p].z), "=r"(hi[p].w) : "l"(pk + 1) : "memory");
         }
+#pragma unroll
+        for (int p = 0; p < NT; ++p)
+          if ((missing & (1u << p)) && lo[p].y == flag && lo[p].w == flag && hi[p].y == flag && hi[p].w == flag)
+            missing &= ~(1u << p);
         if (missing && (it & 31u) == 0) {
           if (ld_relaxed_gpu(dc.status) != 0ull) return false;
           if (global_timer_ns() - t0 > dc.timeout_ns) {
