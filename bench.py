@@ -557,7 +557,7 @@ def other_workloads(dcc, dev, stream):
             (w.bytes_per_rank + 8 * w.bytes_per_rank) / ms / 1e6, 1)}
     # fused row-parallel linear + AllReduce vs per-rank GEMV (cuBLAS) then AllReduce,
     # tensor-parallel decode shapes: hidden 8192 rows, 8 ranks, kp = 1024, 3584, 8192
-    # (kp >= 3072 runs the bulk-copy kernel)
+    # (kp >= 3584 runs the bulk-copy kernel)
     for kp in (1024, 3584, 8192):
         rows = 8192
         g = torch.Generator(device=dev)

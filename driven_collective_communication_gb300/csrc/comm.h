@@ -66,9 +66,9 @@ constexpr size_t kPipeChunkBytes = 8u << 20;
 // Fused linear + AllReduce: rows of at least this many elements per rank
 // stream through the bulk-copy kernel (fused_bulk.cuh), shorter ones through
 // thread loads (fused.cuh).  Measured on GB300, 8 ranks x 8192 rows bf16,
-// thread / bulk (us): kp 2048 52.4 / 62.8, 2560 63.2 / 67.3, 3072 74.7 / 70.7,
-// 4096 97.8 / 80.2, 8192 191 / 150.
-constexpr size_t kFusedBulkMinKp = 3072;
+// thread / bulk (us): kp 2048 46.7 / 62.7, 2560 58.9 / 67.2, 3072 68.0 / 70.6,
+// 3584 79.1 / 75.1, 4096 87.3 / 80.5, 8192 169 / 152.
+constexpr size_t kFusedBulkMinKp = 3584;
 
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;

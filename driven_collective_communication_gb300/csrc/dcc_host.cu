@@ -646,7 +646,7 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
   if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
   if (c->sticky != DCC_OK) return c->sticky;
   if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
-  if (rows % dcc::kFusedRows || kp % 8) return DCC_ERR_UNSUPPORTED;
+  if (rows % 8 || kp % 8) return DCC_ERR_UNSUPPORTED;  // the documented shape rule
   if (rows == 0 || kp == 0) return DCC_OK;
   const size_t eb = 2;
   if (rows > ((size_t)1 << 40) / kp) return DCC_ERR_INVALID_ARG;
@@ -692,7 +692,7 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
   }
   const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
                                  : dcc::linear_allreduce_kernel<__half>(c->n);
-  const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // 8-row items per rank
+  const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // items per rank
   rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
   if (rc != DCC_OK) return rc;
   return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s));

@@ -12,14 +12,18 @@
 //   y_r[i] = R( sum_p  sum_k W_p[i][k] x_p[k] )   for every rank r
 //
 // Schedule (two-shot, like k_allreduce_twoshot): rank r's CTAs own shard r of
-// the rows, in items of 8 rows (one 16-byte output vector), one item per CTA
-// at a time.  The CTA's warps take the ranks in parallel: warp w gets the 8
-// weight rows of W_p and x_p from rank p = w, w + 8, ... in 16-byte vectors
-// (lanes stride the row, coalesced), accumulates 8 fp32 dot products with
-// fused multiply-adds and reduces them across lanes with a fixed shuffle
-// tree.  One thread per row then adds the ranks' partials in rank order and
-// lanes 0..N-1 put the packed vector into the N outputs.  Every output
-// element is computed once, so every rank receives the same bits.
+// the rows, in items of kFusedRows rows, one item per CTA at a time.  The
+// CTA's warps take the ranks in parallel: warp w gets the item's rows of W_p
+// and x_p from rank p = w, w + 8, ... in 16-byte vectors, kFusedVecs per lane
+// and row per round so that a row's loads of one round are all in flight
+// (lanes stride the row, coalesced), accumulates fp32 dot products with fused
+// multiply-adds and reduces them across lanes with a fixed shuffle tree.  One
+// thread per row then adds the ranks' partials in rank order and lanes
+// 0..N-1 put the packed rows into the N outputs.  Every output element is
+// computed once, so every rank receives the same bits.  Measured on GB300 (8
+// ranks x 8192 rows): two-row items with four vectors per lane per round
+// beat eight-row items with two by 7-9 % at kp 2048-2560 and match them at
+// kp 1024; more rows per item or fewer vectors per round were slower.
 //
 // The per-rank dot products are reordered relative to a sequential sum (lane
 // strides and a shuffle tree), so results are exact when every fp32 partial
@@ -31,7 +35,8 @@
 namespace dcc {
 
 constexpr int kFusedThreads = 256;
-constexpr int kFusedRows = 8;  // output rows per warp item: one 16-byte vector
+constexpr int kFusedRows = 2;  // output rows per item: one 4-byte packed store per rank
+constexpr int kFusedVecs = 4;  // 16-byte vectors per lane and row per round
 
 struct LinearArgs {
   const void* weight[DCC_MAX_RANKS];  // rows x kp, row-major
@@ -62,64 +67,59 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, LinearArgs a) {
   using L = Lanes<T>;
+  constexpr int R = kFusedRows, V = kFusedVecs;
+  static_assert(R == 2, "the epilogue packs two rows per item");
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;
   const int rank = blockIdx.x / B, blk = blockIdx.x % B;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const size_t kv = a.kp / 8;             // 16-byte vectors per weight row
-  const size_t items = a.rows / kFusedRows;
-  __shared__ float part_s[DCC_MAX_RANKS][kFusedRows];
+  const size_t kv = a.kp / 8;  // 16-byte vectors per weight row
+  const size_t items = a.rows / R;
+  __shared__ float part_s[DCC_MAX_RANKS][R];
   size_t s0, s1;
   shard_vecs(items, n, rank, s0, s1);
   for (size_t v = s0 + blk; v < s1; v += B) {
     // warp w computes the partial products of ranks w, w + nwarps, ... for
-    // the item's 8 rows; the ranks' partials meet in shared memory
+    // the item's rows; the ranks' partials meet in shared memory
     for (int p = warp; p < n; p += nwarps) {
-      const uint4* w = static_cast<const uint4*>(a.weight[p]) + v * kFusedRows * kv;
+      const uint4* w = static_cast<const uint4*>(a.weight[p]) + v * R * kv;
       const uint4* x = static_cast<const uint4*>(a.x[p]);
-      float part[kFusedRows];
+      float part[R];
 #pragma unroll
-      for (int r = 0; r < kFusedRows; ++r) part[r] = 0.0f;
-      size_t k = lane;
-      for (; k + 32 < kv; k += 64) {  // two vectors per lane in flight per row
-        const uint4 x0 = ld_vec(x + k), x1 = ld_vec(x + k + 32);
-        uint4 w0[kFusedRows], w1[kFusedRows];
+      for (int r = 0; r < R; ++r) part[r] = 0.0f;
+      for (size_t k0 = 0; k0 < kv; k0 += 32 * V) {
+        uint4 wv[R][V], xv[V];
 #pragma unroll
-        for (int r = 0; r < kFusedRows; ++r) {
-          w0[r] = ld_vec(w + r * kv + k);
-          w1[r] = ld_vec(w + r * kv + k + 32);
+        for (int j = 0; j < V; ++j) {
+          const size_t k = k0 + j * 32 + lane;
+          const bool in = k < kv;
+          xv[j] = in ? ld_vec(x + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int r = 0; r < R; ++r) wv[r][j] = in ? ld_vec(w + r * kv + k) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int r = 0; r < kFusedRows; ++r) {
-          dot8_acc<T>(part[r], w0[r], x0);
-          dot8_acc<T>(part[r], w1[r], x1);
-        }
-      }
-      if (k < kv) {
-        const uint4 x0 = ld_vec(x + k);
+        for (int j = 0; j < V; ++j)
 #pragma unroll
-        for (int r = 0; r < kFusedRows; ++r) dot8_acc<T>(part[r], ld_vec(w + r * kv + k), x0);
+          for (int r = 0; r < R; ++r) dot8_acc<T>(part[r], wv[r][j], xv[j]);
       }
 #pragma unroll
-      for (int r = 0; r < kFusedRows; ++r) {
+      for (int r = 0; r < R; ++r) {
         const float sum = warp_sum(part[r]);
         if (lane == 0) part_s[p][r] = sum;
       }
     }
     __syncthreads();
     // one thread per row adds the ranks' partials in rank order; the packed
-    // result goes to all N outputs
+    // rows go to all N outputs
     if (warp == 0) {
       float acc = 0.0f;
-      if (lane < kFusedRows) {
+      if (lane < R) {
         acc = part_s[0][lane];
         for (int p = 1; p < n; ++p) acc = __fadd_rn(acc, part_s[p][lane]);
       }
-      typename L::Acc out;
-#pragma unroll
-      for (int r = 0; r < kFusedRows; ++r) out.v[r] = __shfl_sync(0xffffffffu, acc, r);
-      const uint4 packed = L::pack(out);
-      for (int q = lane; q < n; q += 32) st_vec(static_cast<uint4*>(a.y[q]) + v, packed);
+      const float y0 = __shfl_sync(0xffffffffu, acc, 0), y1 = __shfl_sync(0xffffffffu, acc, 1);
+      const uint32_t packed = L::narrow2(y0, y1);
+      for (int q = lane; q < n; q += 32) static_cast<uint32_t*>(a.y[q])[v] = packed;
     }
     __syncthreads();
   }

@@ -183,7 +183,7 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
  * registered, outputs disjoint from every input.  The dot products use a
  * fixed lane/shuffle order: exact when every fp32 partial sum is exact, else
  * within the fp32 dot-product error bound before the final rounding.  Rows of
- * at least 3072 elements stream their weights through shared memory with
+ * at least 3584 elements stream their weights through shared memory with
  * bulk copies (TMA), shorter ones through thread loads; DCC_FUSED_BULK=1 / 0
  * in the environment at communicator creation forces one or the other. */
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
