@@ -562,6 +562,64 @@ def test_graph_replay_of_rs_ag_fused_and_entry_barrier(dcc):
             assert np.array_equal(W.to_storage(yv[r]), expect), (kp, r)
 
 
+def test_concurrent_streams(dcc):
+    """Kernels that never wait overlap freely on one communicator (two streams,
+    two-shot push and ReduceScatter/AllGather on separate buffers), and two
+    communicators run their synchronising kernels (in-place one-shot, two-shot
+    via scratch) on two streams at the same time: every result as the oracle's."""
+    n, count = 8, 3 * 4096 + 24
+    g = torch.Generator().manual_seed(21)
+    host = [torch.randint(-8, 9, (count,), generator=g).float() for _ in range(n)]
+    expect = oracle.allreduce([W.to_storage(h) for h in host], "fp32")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def bufs():
+        return [h.cuda() for h in host], [torch.empty(count, device="cuda") for _ in range(n)]
+
+    # one communicator, two streams, wait-free kernels on disjoint buffers
+    (xa, ya), (xb, yb) = bufs(), bufs()
+    m = count // n
+    rs = [torch.empty(m, device="cuda") for _ in range(n)]
+    ag = [torch.empty(m * n, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        for t in (xa, xb):
+            comm.register_all("input", t)
+        for t in (ya, yb, rs, ag):
+            comm.register_all("output", t)
+        torch.cuda.synchronize()
+        for _ in range(20):
+            dcc.dcc_allreduce(comm.handle, xa, ya, count, "fp32", "two_shot", stream=s1)
+            dcc.dcc_reduce_scatter(comm.handle, xb, rs, m, "fp32", stream=s2)
+            dcc.dcc_allgather(comm.handle, rs, ag, m, "fp32", stream=s2)
+        torch.cuda.synchronize()
+        assert comm.check() == dcc.DCC_OK
+    for r in range(n):
+        assert same(W.to_storage(ya[r]), expect, "fp32")
+        assert same(W.to_storage(ag[r]), expect[: m * n], "fp32")
+    # two communicators, two streams, synchronising kernels at the same time:
+    # a ring barrier then an in-place one-shot on one, two-shots via scratch on
+    # the other (neither waits on the other's semaphores)
+    (xc, _), (xd, yd) = bufs(), bufs()
+    scr = [torch.empty(count, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as c1, dcc.Comm(n) as c2:
+        c1.register_all("input", xc)
+        c2.register_all("input", xd)
+        c2.register_all("output", yd)
+        c2.register_all("scratch", scr)
+        torch.cuda.synchronize()
+        c1.ring_barrier(2000, stream=s1)
+        dcc.dcc_allreduce(c1.handle, xc, xc, count, "fp32", "one_shot", stream=s1)
+        for _ in range(20):
+            dcc.dcc_allreduce(c2.handle, xd, yd, count, "fp32", "two_shot_scratch", stream=s2)
+        torch.cuda.synchronize()
+        assert c1.check() == dcc.DCC_OK and c2.check() == dcc.DCC_OK
+        inbound, expected = dcc.dcc_comm_read_semaphores(c1.handle, n)
+        assert np.array_equal(inbound, expected)
+    for r in range(n):
+        assert same(W.to_storage(xc[r]), expect, "fp32")
+        assert same(W.to_storage(yd[r]), expect, "fp32")
+
+
 def test_lost_signal_times_out_cleanly(dcc):
     """A rank that never signals makes its peers' waits run out: the kernel
     records DCC_ERR_TIMEOUT and returns; the GPU stays usable."""
