@@ -335,7 +335,10 @@ def sweep_c3(dcc, dev, stream):
         comm.register_all("input", xs)
         comm.register_all("output", ys)
         h = comm.handle
-        row = {"tokens": tokens, "bytes_per_rank": w.bytes_per_rank}
+        # a working set (2 N S) that fits in L2 is a latency case, not an HBM-roofline one
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        row = {"tokens": tokens, "bytes_per_rank": w.bytes_per_rank,
+               "working_set_in_l2": 2 * 8 * w.bytes_per_rank <= l2, "l2_bytes": l2}
         for algo in ("one_shot", "two_shot"):
             step = dcc.prepare_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
             for _ in range(50):
