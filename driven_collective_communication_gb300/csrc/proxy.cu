@@ -17,8 +17,12 @@
 // signal behind the copies of its channel, and K copy engines work at once; a
 // flush is written after every stream's earlier work (events).  K is 4 by
 // default (DCC_PROXY_STREAMS, 1..8): measured on GB300 for the 8 x 8 MiB fp16
-// AllGather, 0.573 / 0.345 / 0.253 / 0.281 ms with K = 1 / 2 / 4 / 8.  Every
-// wait on either side is bounded.
+// AllGather, 0.573 / 0.345 / 0.253 / 0.281 ms with K = 1 / 2 / 4 / 8.  Signal
+// writes queue per stream and go out together (one batch of stream memory
+// operations) when the FIFO runs empty, after 256 triggers, or before a flush
+// or a custom trigger: fewer host calls when one thread issues everything
+// (K = 1: 0.573 -> 0.473 ms), the same with K = 4, where the copy engines
+// bound it.  Every wait on either side is bounded.
 //
 // The kernels that push triggers keep running while the proxy's streams work
 // for them.  If the GPU multiplexes a proxy stream onto the same hardware
@@ -31,6 +35,7 @@
 #include <atomic>
 #include <chrono>
 #include <thread>
+#include <vector>
 
 #include "comm.h"
 #include "port_channel.cuh"
@@ -46,6 +51,8 @@ constexpr int kMaxCustom = 32;
 constexpr int kMaxProxyStreams = 8;
 
 typedef CUresult (*WriteValue64Fn)(CUstream, CUdeviceptr, cuuint64_t, unsigned int);
+typedef CUresult (*BatchMemOpFn)(CUstream, unsigned int, CUstreamBatchMemOpParams*, unsigned int);
+constexpr int kMaxTakePerRound = 256;  // triggers the proxy takes from the FIFO in one round
 
 }  // namespace
 
@@ -71,6 +78,10 @@ struct ProxyState {
   bool dirty[kMaxProxyStreams] = {};
   unsigned long long sig_count[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
   WriteValue64Fn write_value = nullptr;
+  BatchMemOpFn batch_mem_op = nullptr;
+  // signal writes waiting to be issued, per stream: the values go out together
+  // (one stream memory-operation batch per stream) after the round's copies
+  std::vector<CUstreamBatchMemOpParams> pending[kMaxProxyStreams];
   dcc_trigger_handler_t handler = nullptr;
   void* user = nullptr;
   std::atomic<unsigned long long> processed{0}, custom{0};
@@ -150,6 +161,25 @@ bool window_range(const dcc_comm* c, int rank, int kind, size_t off, size_t byte
   return true;
 }
 
+// Issue the signal writes queued on each stream: a single write as is, several
+// as one batch of stream memory operations (in queue order).
+void issue_pending_signals(ProxyState& P) {
+  for (int k = 0; k < P.nstreams; ++k) {
+    std::vector<CUstreamBatchMemOpParams>& q = P.pending[k];
+    if (q.empty()) continue;
+    CUresult r = CUDA_SUCCESS;
+    if (q.size() == 1 || !P.batch_mem_op) {
+      for (size_t i = 0; i < q.size() && r == CUDA_SUCCESS; ++i)
+        r = P.write_value((CUstream)P.streams[k], q[i].writeValue.address, q[i].writeValue.value64,
+                          CU_STREAM_WRITE_VALUE_DEFAULT);
+    } else {
+      r = P.batch_mem_op((CUstream)P.streams[k], (unsigned)q.size(), q.data(), 0);
+    }
+    if (r != CUDA_SUCCESS) set_error(P, DCC_ERR_CUDA);
+    q.clear();
+  }
+}
+
 void handle(dcc_comm* c, ProxyState& P, unsigned long long fst, unsigned long long snd,
             unsigned long long seq) {
   P.processed.fetch_add(1, std::memory_order_relaxed);
@@ -168,6 +198,7 @@ void handle(dcc_comm* c, ProxyState& P, unsigned long long fst, unsigned long lo
   } log_on_exit{c, seq, fst, snd, t_start};
   if (!(fst & dcc::kTrigBuiltin)) {
     P.custom.fetch_add(1, std::memory_order_relaxed);
+    issue_pending_signals(P);  // the handler sees every earlier trigger carried out
     if (P.handler) P.handler(fst, snd, P.user);
     return;
   }
@@ -190,13 +221,18 @@ void handle(dcc_comm* c, ProxyState& P, unsigned long long fst, unsigned long lo
       set_error(P, DCC_ERR_CUDA);
     }
   }
-  if (fst & dcc::kTrigSignal) {
+  if (fst & dcc::kTrigSignal) {  // queued behind this stream's copies of the round
     const unsigned long long v = ++P.sig_count[dst][src];
-    CUdeviceptr addr = (CUdeviceptr)(P.dev.sem + dcc::sem_slot(dst, src, 0) * dcc::kSemWords);
-    if (P.write_value((CUstream)st, addr, v, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
-      set_error(P, DCC_ERR_CUDA);
+    CUstreamBatchMemOpParams op;
+    std::memset(&op, 0, sizeof op);
+    op.writeValue.operation = CU_STREAM_MEM_OP_WRITE_VALUE_64;
+    op.writeValue.address = (CUdeviceptr)(P.dev.sem + dcc::sem_slot(dst, src, 0) * dcc::kSemWords);
+    op.writeValue.value64 = v;
+    op.writeValue.flags = CU_STREAM_WRITE_VALUE_DEFAULT;
+    P.pending[k].push_back(op);
   }
   if (fst & dcc::kTrigFlush) {  // after everything issued so far, on every stream
+    issue_pending_signals(P);
     for (int j = 1; j < P.nstreams; ++j) {
       if (!P.dirty[j]) continue;
       if (cudaEventRecord(P.events[j], P.streams[j]) != cudaSuccess ||
@@ -215,6 +251,7 @@ void proxy_loop(dcc_comm* c) {
   cudaSetDevice(c->device);
   unsigned long long tail = __atomic_load_n(P.h_tail, __ATOMIC_ACQUIRE);
   unsigned idle = 0;
+  int taken = 0;  // triggers handled since the queued signal writes last went out
   bool draining = false;
   std::chrono::steady_clock::time_point deadline;
   for (;;) {
@@ -230,6 +267,11 @@ void proxy_loop(dcc_comm* c) {
     dcc::ProxyTrigger* s = P.h_slots + (tail % kFifoCapacity);
     const unsigned long long fst = __atomic_load_n(&s->fst, __ATOMIC_ACQUIRE);
     if (fst == 0) {
+      // the FIFO is empty for now: the round's queued signals go out
+      if (taken) {
+        issue_pending_signals(P);
+        taken = 0;
+      }
       if (++idle > 4096) std::this_thread::yield();
       continue;
     }
@@ -239,7 +281,12 @@ void proxy_loop(dcc_comm* c) {
     const unsigned long long seq = tail++;
     __atomic_store_n(P.h_tail, tail, __ATOMIC_RELEASE);
     handle(c, P, fst, snd, seq);
+    if (++taken >= kMaxTakePerRound) {  // a steady stream of triggers still gets its signals
+      issue_pending_signals(P);
+      taken = 0;
+    }
   }
+  issue_pending_signals(P);
 }
 
 int ensure_proxy(dcc_comm* c) {
@@ -263,6 +310,12 @@ int ensure_proxy(dcc_comm* c) {
       q != cudaDriverEntryPointSuccess || !fn)
     return fail(DCC_ERR_CUDA);
   P->write_value = reinterpret_cast<WriteValue64Fn>(fn);
+  void* fb = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuStreamBatchMemOp", &fb, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fb)
+    P->batch_mem_op = reinterpret_cast<BatchMemOpFn>(fb);
+  else
+    cudaGetLastError();  // single writes then
   const size_t fifo_bytes = kFifoCapacity * sizeof(dcc::ProxyTrigger) + 64;
   if (cudaHostAlloc(reinterpret_cast<void**>(&P->h_fifo), fifo_bytes, cudaHostAllocMapped) != cudaSuccess)
     return fail(DCC_ERR_CUDA);
