@@ -135,6 +135,49 @@ def test_empty_inputs_are_no_ops(dcc):
         assert torch.all(xs[r] == r + 1)
 
 
+def test_random_configurations_match_oracle(dcc, monkeypatch):
+    """Two hundred seeded random mixes of rank count (compiled and runtime-N instances),
+    element count, dtype, algorithm, in/out of place, CTAs per rank, threads
+    per CTA and the entry barrier, each against the oracle bit for bit."""
+    rng = np.random.default_rng(2026)
+    checked = 0
+    for case in range(200):
+        n = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16]))
+        dtype = str(rng.choice(sorted(RECIPES)))
+        count = int(rng.integers(1, 60000))
+        algo = str(rng.choice(ALGOS))
+        inplace = bool(rng.integers(0, 2))
+        blocks = int(rng.choice([0, 1, 3, 17, 128]))
+        threads = int(rng.choice([0, 64, 96, 256]))
+        entry_barrier = bool(rng.integers(0, 4) == 0)
+        if threads:
+            monkeypatch.setenv("DCC_THREADS", str(threads))
+        else:
+            monkeypatch.delenv("DCC_THREADS", raising=False)
+        w = W.with_count(RECIPES[dtype], count, n_ranks=n)
+        xs = W.rank_inputs(w)
+        expect = oracle.allreduce([W.to_storage(x) for x in xs], dtype)
+        arena = Arena(dcc, n, count)
+        try:
+            h = arena.comm.handle
+            dcc.dcc_set_blocks_per_rank(h, blocks)
+            dcc.dcc_set_entry_barrier(h, entry_barrier)
+            what = (case, n, dtype, count, algo, inplace, blocks, threads, entry_barrier)
+            if entry_barrier and algo in ("two_shot_bulk", "one_shot_ll"):
+                send = arena.view(arena.inp, dtype, count)
+                with pytest.raises(dcc.DccError) as e:
+                    dcc.dcc_allreduce(h, send, send, count, dtype, algo)
+                assert e.value.code == dcc.DCC_ERR_UNSUPPORTED, what
+                continue
+            outs = run_allreduce(dcc, arena, xs, dtype, algo, inplace)
+            for r in range(n if outs is not None else 0):
+                assert same(outs[r], expect, dtype), (what, r)
+            checked += outs is not None
+        finally:
+            arena.close()
+    assert checked >= 150, checked  # most draws run (the rest are the rejected combinations)
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 def test_allreduce_special_values(dcc, dtype):
     """Raw random bit patterns: subnormals (no flush to zero), signed zeros,
