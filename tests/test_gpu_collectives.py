@@ -442,6 +442,43 @@ def test_reduce_scatter_allgather_ragged(dcc, n, count, dtype):
         comm.close()
 
 
+def test_random_rs_ag_configurations_match_oracle(dcc, monkeypatch):
+    """A hundred seeded random mixes of rank count, per-rank element count (16-byte
+    vector path and element path), dtype, CTAs per rank, threads per CTA and the
+    entry barrier for the ReduceScatter followed by the AllGather."""
+    rng = np.random.default_rng(77)
+    for case in range(100):
+        n = int(rng.choice([1, 2, 3, 4, 5, 8, 9, 16]))
+        dtype = str(rng.choice(sorted(RECIPES)))
+        m = int(rng.integers(1, 9000))
+        blocks = int(rng.choice([0, 1, 5, 128]))
+        threads = int(rng.choice([0, 64, 160, 512]))
+        entry_barrier = bool(rng.integers(0, 3) == 0)
+        if threads:
+            monkeypatch.setenv("DCC_THREADS", str(threads))
+        else:
+            monkeypatch.delenv("DCC_THREADS", raising=False)
+        w = W.with_count(RECIPES[dtype], m * n, n_ranks=n)
+        host = W.rank_inputs(w)
+        xs = [x.cuda() for x in host]
+        rs = [torch.empty(m, dtype=xs[0].dtype, device="cuda") for _ in range(n)]
+        ag = [torch.empty(m * n, dtype=xs[0].dtype, device="cuda") for _ in range(n)]
+        with dcc.Comm(n) as comm:
+            comm.register_all("input", xs)
+            comm.register_all("output", rs)
+            comm.register_all("output", ag)
+            dcc.dcc_set_blocks_per_rank(comm.handle, blocks)
+            dcc.dcc_set_entry_barrier(comm.handle, entry_barrier)
+            comm.reduce_scatter(xs, rs)
+            comm.allgather(rs, ag)
+            assert comm.check() == dcc.DCC_OK
+        full = oracle.allreduce([W.to_storage(x) for x in host], dtype)
+        what = (case, n, dtype, m, blocks, threads, entry_barrier)
+        for r in range(n):
+            assert same(W.to_storage(rs[r]), full[r * m:(r + 1) * m], dtype), (what, r)
+            assert same(W.to_storage(ag[r]), full, dtype), (what, r)
+
+
 # ---------------------------------------------------------------- synchronisation
 @pytest.mark.parametrize("n", [1, 2, 8, 16])
 def test_ring_barrier_counts(dcc, n):
