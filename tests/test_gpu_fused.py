@@ -62,6 +62,25 @@ def test_integer_data_bit_exact(dcc, path, dtype, n, rows, kp):
     assert np.array_equal(got, expect)
 
 
+def test_random_shapes_bit_exact(dcc, monkeypatch):
+    """Sixty seeded random mixes of rank count, rows, kp, dtype and kernel
+    (thread loads / bulk copies) on small-integer data: exact against the oracle."""
+    rng = np.random.default_rng(31)
+    for case in range(60):
+        n = int(rng.choice([1, 2, 3, 5, 8, 9, 16]))
+        rows = 8 * int(rng.integers(1, 40))
+        kp = 8 * int(rng.integers(1, 1150))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        monkeypatch.setenv("DCC_FUSED_BULK", str(int(rng.integers(0, 2))))
+        g = torch.Generator().manual_seed(1000 + case)
+        ws = [torch.randint(-3, 4, (rows * kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+        xs = [torch.randint(-3, 4, (kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+        got = run(dcc, ws, xs, rows, kp, dtype)
+        expect = oracle.linear_allreduce([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                         dtype, rows, kp)
+        assert np.array_equal(got, expect), (case, n, rows, kp, dtype)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("n,rows,kp", [(8, 8192, 1024), (8, 512, 3584), (3, 64, 4104)])
 def test_random_data_within_bound(dcc, path, dtype, n, rows, kp):
