@@ -200,11 +200,16 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   sh->cooperative = (algo == DCC_ALGO_ONE_SHOT && inplace && c->n > 1) ||
                     (algo == DCC_ALGO_TWO_SHOT_SCRATCH && c->n > 1) || (c->entry_barrier && c->n > 1);
   if (algo == DCC_ALGO_ONE_SHOT && inplace) {
-    // one vector per thread while one chunk per CTA covers the message within
-    // the CTA cap (a single barrier round, every load in flight at once), else
-    // kInplaceUnroll vectors per thread and fewer barrier rounds
-    sh->unroll = c->inplace_unroll > 0 ? c->inplace_unroll
-                 : nvec <= (size_t)DCC_MAX_BLOCKS_PER_RANK * sh->threads ? 1 : dcc::kInplaceUnroll;
+    // one vector per thread while one chunk per CTA of the co-resident grid
+    // covers the message (a single barrier round, every load in flight at
+    // once), else kInplaceUnroll vectors per thread and fewer barrier rounds
+    sh->unroll = c->inplace_unroll;
+    if (sh->unroll <= 0) {
+      int b1 = 0;
+      const int rc = pick_blocks(c, sh->fn, sh->threads, nvec, &b1, 0, 0, true);
+      if (rc != DCC_OK) return rc;
+      sh->unroll = (size_t)b1 * sh->threads >= nvec ? 1 : dcc::kInplaceUnroll;
+    }
     work = (nvec + sh->unroll - 1) / sh->unroll;
   }
   // one-shot keeps one wave even out of place: every rank reads every input,
