@@ -1,7 +1,7 @@
 // fused.cuh -- row-parallel linear layer fused with the sum AllReduce.
 //
-// The project summary ("How It Works") counts communication-to-computation
-// overlap among the channel interfaces' uses, and its "Highlighted Details"
+// The project summary ("How It Works") counts overlapping communication with
+// computation among the channel interfaces' uses, and its "Highlighted Details"
 // single out AllReduce for tensor-parallel LLM serving.  In a tensor-parallel
 // decode step a row-parallel layer leaves rank p with the partial product
 // W_p x_p of its slice of the contraction dimension, and the AllReduce sums

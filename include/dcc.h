@@ -173,7 +173,7 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
                             dcc_dtype_t t, dcc_algo_t a, dcc_stream_t s);
 
 /* Row-parallel linear layer fused with the AllReduce (tensor-parallel decode;
- * the project summary's communication-to-computation overlap): rank p holds
+ * the project summary's overlap of communication with computation): rank p holds
  * weight[p] (rows x kp, row-major) and x[p] (kp elements), and every rank
  * receives y[r][i] = R(sum_p sum_k weight[p][i*kp + k] * x[p][k]), i < rows.
  * One kernel: rank r's CTAs compute shard r of the rows, getting every rank's
