@@ -12,7 +12,9 @@ clocks sampled during the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
-("replicas only": the virtual-rank path has no exchange between GPUs).
+("replicas only": the virtual-rank path has no exchange between GPUs); the
+headline and the end-to-end number are timed on all replicas together, the
+single-GPU extras (sweeps, other workloads, the CPU leg) run at N = 1 only.
 """
 import argparse
 import hashlib
@@ -254,8 +256,9 @@ def run_ours(args, dist):
         "clocks": clk,
     }
 
-    if dist.rank == 0 and not args.quick:
-        out["e2e"] = e2e_host(dcc, comm, xs, ys, w, args, stream)
+    if not args.quick:  # every replica, timed together
+        out["e2e"] = e2e_host(dcc, comm, xs, ys, w, args, stream, dist)
+    if dist.ws == 1 and not args.quick:  # single-GPU extras and the CPU leg (N = 1 only)
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
         out["graph_node_floor_us"] = graph_node_floor(stream)
         out["other"] = other_workloads(dcc, dev, stream)
@@ -269,9 +272,10 @@ def run_ours(args, dist):
     return out
 
 
-def e2e_host(dcc, comm, xs, ys, w, args, stream):
+def e2e_host(dcc, comm, xs, ys, w, args, stream, dist):
     """The same AllReduce through dcc_allreduce_from_host: pinned host inputs
-    copied in, the collective, outputs copied back -- all inside the timing."""
+    copied in, the collective, outputs copied back -- all inside the timing.
+    Every replica runs it between barriers; the job takes the slowest."""
     hin = [x.cpu().pin_memory() for x in xs]
     hout = [torch.empty_like(t).pin_memory() for t in hin]
     h = comm.handle
@@ -283,6 +287,7 @@ def e2e_host(dcc, comm, xs, ys, w, args, stream):
         step()
     stream.synchronize()
     steps = max(3, min(10, args.steps // 100))
+    dist.barrier()
     t0 = time.perf_counter()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -291,10 +296,12 @@ def e2e_host(dcc, comm, xs, ys, w, args, stream):
         step()
     ev1.record(stream)
     ev1.synchronize()
-    ms = ev0.elapsed_time(ev1) / steps
     wall = (time.perf_counter() - t0) / steps
-    nbytes = w.n_ranks * w.bytes_per_rank
-    return {"value": round(w.bytes_per_rank / (ms / 1e3) / GB, 3), "unit": "GB/s",
+    dist.barrier()
+    ms = dist.max(ev0.elapsed_time(ev1) / steps)
+    wall = dist.max(wall)
+    nbytes = dist.ws * w.n_ranks * w.bytes_per_rank  # every replica's inputs in and outputs out
+    return {"value": round(dist.ws * w.bytes_per_rank / (ms / 1e3) / GB, 3), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
             "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3), "steps": steps}
 
