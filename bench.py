@@ -261,6 +261,7 @@ def run_ours(args, dist):
     if dist.ws == 1 and not args.quick:  # single-GPU extras and the CPU leg (N = 1 only)
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
         out["graph_node_floor_us"] = graph_node_floor(stream)
+        out["sweep_large"] = sweep_large(dcc, dev, stream)
         out["other"] = other_workloads(dcc, dev, stream)
         gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
         gbs1, _, sample1, _ = oracle_sample_run(3.0, args.cpu_elems // 8, threads=1)
@@ -304,6 +305,35 @@ def e2e_host(dcc, comm, xs, ys, w, args, stream, dist):
     return {"value": round(dist.ws * w.bytes_per_rank / (ms / 1e3) / GB, 3), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
             "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3), "steps": steps}
+
+
+def sweep_large(dcc, dev, stream):
+    """algbw and fraction of the HBM roofline vs message size above L2: the
+    8-rank bf16 AllReduce (AUTO) at 16 MiB .. 1 GiB per rank, inputs N(0,1)*(1+r)."""
+    peak, _ = measured_peaks()
+    res = []
+    for mib in (16, 64, 256, 1024):
+        count = (mib << 20) // 2
+        w = W.with_count(W.C4, count)
+        with torch.cuda.stream(stream):
+            xs = W.rank_inputs(w, device=dev)
+            ys = [torch.empty_like(x) for x in xs]
+        torch.cuda.synchronize()
+        with dcc.Comm(8) as c:
+            c.register_all("input", xs)
+            c.register_all("output", ys)
+            step = dcc.prepare_allreduce(c.handle, xs, ys, count, "bf16", "auto", stream)
+            for _ in range(3):
+                step()
+            per, _ = time_launches(step, 20, stream)
+            assert c.check(stream) == dcc.DCC_OK
+        ms = statistics.median(per)
+        hbm = 2 * 8 * (mib << 20) / ms / 1e6
+        res.append({"bytes_per_rank": mib << 20, "ms": round(ms, 4),
+                    "algbw_gbs": round((mib << 20) / ms / 1e6, 1), "hbm_gbs_2NS": round(hbm, 1),
+                    "roofline_frac": round(hbm / peak, 4)})
+        del xs, ys
+    return res
 
 
 def graph_node_floor(stream, reps=100):
