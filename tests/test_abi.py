@@ -162,3 +162,17 @@ def test_product_path_does_not_touch_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert not pat.search(text), os.path.join(dirpath, fn)
+
+
+def test_readme_c_example_compiles(tmp_path):
+    """The C usage example in the README compiles against include/dcc.h."""
+    text = open(os.path.join(ROOT, "README.md")).read()
+    m = re.search(r"```c\n(.*?)```", text, re.S)
+    assert m, "no C example in the README"
+    src = tmp_path / "example.c"
+    src.write_text(m.group(1) + "\nint main(void) { return 0; }\n")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, "-c", str(src), "-o", str(tmp_path / "example.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
