@@ -1,4 +1,4 @@
-"""CPU oracle for the sum collectives -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the collectives -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product library never loads it and
@@ -41,9 +41,11 @@ def _load():
         lib.orc_convert_to_f32.argtypes = [vp, vp, sz, i32]
         lib.orc_convert_from_f32.argtypes = [vp, vp, sz, i32]
         lib.orc_linear_allreduce.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, sz, i32, vp]
+        lib.orc_allreduce_op.argtypes = [i32, ctypes.POINTER(vp), vp, sz, i32, i32]
         for name in ("orc_allreduce", "orc_allreduce_at", "orc_allreduce_mt",
                      "orc_reduce_scatter", "orc_allgather", "orc_ring_barrier_counts",
-                     "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce"):
+                     "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce",
+                     "orc_allreduce_op"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -77,6 +79,19 @@ def allreduce(xs, dtype, nthreads=1):
     else:
         rc = lib.orc_allreduce(len(arrs), ptrs, out.ctypes.data, n, DTYPES[dtype])
     _ok(rc, "allreduce")
+    return out
+
+
+OPS = {"max": 1, "min": 2}
+
+
+def allreduce_op(xs, dtype, op):
+    """out[i] = the IEEE maximum / minimum over ranks (in order 0..N-1) of xs[p][i];
+    op is "max" or "min" (the sum is ``allreduce``)."""
+    lib = _load()
+    arrs, ptrs, n = _inputs(xs, dtype)
+    out = np.empty(n, dtype=STORAGE[dtype])
+    _ok(lib.orc_allreduce_op(len(arrs), ptrs, out.ctypes.data, n, DTYPES[dtype], OPS[op]), "allreduce_op")
     return out
 
 

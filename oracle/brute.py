@@ -95,6 +95,40 @@ def encode(v, dtype):
     return bits | (0x8000 if neg else 0)
 
 
+def _max_ieee(a, b):
+    """IEEE 754-2019 maximum of two Python floats: NaN wins, -0 < +0."""
+    if a != a or b != b:
+        return float("nan")
+    if a == b:
+        return b if math.copysign(1.0, a) < 0 else a
+    return a if a > b else b
+
+
+def _min_ieee(a, b):
+    if a != a or b != b:
+        return float("nan")
+    if a == b:
+        return a if math.copysign(1.0, a) < 0 else b
+    return a if a < b else b
+
+
+def allreduce_op_elem(values, dtype, op):
+    """MAX / MIN over ranks in order 0..N-1 of the decoded values; int32 as integers."""
+    if dtype == "int32":
+        vals = [int(v) for v in values]
+        return max(vals) if op == "max" else min(vals)
+    f = _max_ieee if op == "max" else _min_ieee
+    acc = decode(values[0], dtype)
+    for v in values[1:]:
+        acc = f(acc, decode(v, dtype))
+    return acc
+
+
+def allreduce_op(xs, dtype, op):
+    n = len(xs[0])
+    return [allreduce_op_elem([x[i] for x in xs], dtype, op) for i in range(n)]
+
+
 def allreduce_elem(values, dtype):
     """One output element from the N ranks' raw values at that index."""
     if dtype == "int32":

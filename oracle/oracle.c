@@ -22,6 +22,11 @@
  *     in fp32 with IEEE round-to-nearest-even after every add, subnormals
  *     kept; R rounds the fp32 sum once to the output type (RNE);
  *   - int32 accumulates with two's-complement wraparound.
+ * MAX / MIN AllReduce (orc_allreduce_op) is not on the pages, which speak of
+ * sum reductions only; it follows the IEEE 754-2019 maximum / minimum
+ * operations in rank order: a NaN operand gives the canonical quiet NaN
+ * (positive, top mantissa bit set), -0 orders below +0, and int32 takes the
+ * integer maximum / minimum.
  * The widening/narrowing routines below are written from the IEEE-754
  * binary16 format and from bfloat16 being the top 16 bits of binary32.
  *
@@ -216,6 +221,52 @@ int orc_allreduce(int n, const void* const* in, void* out, size_t count, int dty
 {
     if (check_args(n, in, dtype) || (count && !out)) return -1;
     for (size_t i = 0; i < count; ++i) reduce_one(n, in, i, out, i, dtype);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* AllReduce with MAX or MIN: an extension the pages do not define.  Plain */
+/* reading: the ranks' values combine in rank order 0..N-1 starting from   */
+/* x_0 with the IEEE 754-2019 maximum / minimum operations -- a NaN        */
+/* operand gives NaN, and -0 orders below +0.  16-bit inputs widen exactly */
+/* to binary32 and the result is one of the inputs (or NaN), so storing it */
+/* rounds nothing.  int32 takes the integer maximum / minimum.             */
+/* ---------------------------------------------------------------------- */
+#define ORC_OP_MAX 1
+#define ORC_OP_MIN 2
+
+static float max_ieee(float a, float b)
+{
+    if (isnan(a) || isnan(b)) return NAN;
+    if (a == b) return signbit(a) ? b : a;   /* equal values, or +0 and -0: +0 wins */
+    return a > b ? a : b;
+}
+
+static float min_ieee(float a, float b)
+{
+    if (isnan(a) || isnan(b)) return NAN;
+    if (a == b) return signbit(a) ? a : b;   /* -0 wins */
+    return a < b ? a : b;
+}
+
+int orc_allreduce_op(int n, const void* const* in, void* out, size_t count, int dtype, int op)
+{
+    if (check_args(n, in, dtype) || (count && !out) || (op != ORC_OP_MAX && op != ORC_OP_MIN)) return -1;
+    for (size_t i = 0; i < count; ++i) {
+        if (dtype == ORC_INT32) {
+            int32_t acc = ((const int32_t*)in[0])[i];
+            for (int p = 1; p < n; ++p) {
+                const int32_t v = ((const int32_t*)in[p])[i];
+                acc = op == ORC_OP_MAX ? (v > acc ? v : acc) : (v < acc ? v : acc);
+            }
+            ((int32_t*)out)[i] = acc;
+            continue;
+        }
+        float acc = widen(in[0], i, dtype);
+        for (int p = 1; p < n; ++p)
+            acc = op == ORC_OP_MAX ? max_ieee(acc, widen(in[p], i, dtype)) : min_ieee(acc, widen(in[p], i, dtype));
+        narrow_store(out, i, acc, dtype);
+    }
     return 0;
 }
 

@@ -432,3 +432,93 @@ def test_linear_allreduce_matches_float64_matmul(dtype):
     # ties, which random normal data does not produce
     assert np.array_equal(got, ref)
     del rng
+
+
+# --------------------------------------------------------------------- MAX / MIN
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+def test_max_min_closed_forms(dtype, n):
+    """Rank r filled with r: max N-1, min 0; rank r filled with -r: max 0,
+    min -(N-1); one rank is the identity."""
+    m = 37
+    up = [np.full(m, value_to_storage(r, dtype)) for r in range(n)]
+    down = [np.full(m, value_to_storage(-r, dtype)) for r in range(n)]
+    assert np.all(storage_to_float(oracle.allreduce_op(up, dtype, "max"), dtype) == n - 1)
+    assert np.all(storage_to_float(oracle.allreduce_op(up, dtype, "min"), dtype) == 0)
+    assert np.all(storage_to_float(oracle.allreduce_op(down, dtype, "max"), dtype) == 0)
+    assert np.all(storage_to_float(oracle.allreduce_op(down, dtype, "min"), dtype) == -(n - 1))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_max_min_ieee_special_cases(dtype):
+    """Hand cases of the IEEE 754-2019 maximum / minimum: a NaN operand gives
+    NaN in either position; max(-0, +0) = +0 and min = -0 in both orders;
+    infinities order; a subnormal is above zero."""
+    nan, inf = float("nan"), float("inf")
+    tiny = {"fp32": 1e-45, "fp16": 2.0 ** -24, "bf16": 2.0 ** -133}[dtype]
+    cases = [((-0.0, 0.0), 0.0, -0.0), ((0.0, -0.0), 0.0, -0.0), ((nan, 1.0), nan, nan),
+             ((1.0, nan), nan, nan), ((-inf, 3.0), 3.0, -inf), ((inf, -inf), inf, -inf),
+             ((tiny, 0.0), tiny, 0.0), ((-2.0, -0.0, 5.0), 5.0, -2.0)]
+
+    def bits(v):
+        s = value_to_storage(v, dtype)
+        return int(np.asarray(s).view(np.uint32 if dtype == "fp32" else np.uint16))
+
+    for vals, want_max, want_min in cases:
+        xs = [np.array([value_to_storage(v, dtype)]) for v in vals]
+        for op, want in (("max", want_max), ("min", want_min)):
+            got = oracle.allreduce_op(xs, dtype, op)
+            g = float(storage_to_float(got, dtype)[0])
+            if math.isnan(want):
+                assert math.isnan(g), (vals, op)
+            else:
+                gb = int(np.asarray(got).view(np.uint32 if dtype == "fp32" else np.uint16)[0])
+                assert gb == bits(want), (vals, op, hex(gb))
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("op", ["max", "min"])
+@pytest.mark.parametrize("n", [1, 2, 5, 8])
+def test_max_min_brute_force_bit_equal(dtype, op, n):
+    """The pure-Python brute force and the C oracle agree bit for bit on random
+    raw patterns with NaN, infinities, subnormals and signed zeros."""
+    rng = np.random.default_rng(300 + n)
+    m = 301
+    xs = [random_raw(rng, dtype, m * 2, specials=True)[:m] for _ in range(n)]
+    m = min(len(x) for x in xs)
+    xs = [x[:m] for x in xs]
+    if dtype == "fp32":
+        for x in xs:
+            x[rng.random(m) < 0.03] = np.nan
+    got = oracle.allreduce_op(xs, dtype, op)
+    ref = brute.allreduce_op(xs, dtype, op)
+    for i in range(m):
+        r = ref[i]
+        if dtype == "int32":
+            assert int(got[i]) == r
+        elif dtype == "fp32":
+            g = float(got[i])
+            if math.isnan(r):
+                assert math.isnan(g)
+            else:
+                assert g == r and math.copysign(1, g) == math.copysign(1, r), (i, g, r)
+        else:
+            g = int(got[i])
+            if math.isnan(r):
+                assert math.isnan(brute.decode(g, dtype))
+            else:
+                assert g == brute.encode(r, dtype), (i, hex(g), r)
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+def test_max_min_match_numpy_on_finite_data(dtype):
+    """Against numpy's maximum / minimum reductions (a library routine) on
+    finite data, compared by value."""
+    rng = np.random.default_rng(9)
+    m, n = 2000, 8
+    xs = [random_raw(rng, dtype, m * 2)[:m] for _ in range(n)]
+    m = min(len(x) for x in xs)
+    xs = [x[:m] for x in xs]
+    stack = np.stack([storage_to_float(x, dtype) for x in xs])
+    assert np.array_equal(storage_to_float(oracle.allreduce_op(xs, dtype, "max"), dtype), stack.max(axis=0))
+    assert np.array_equal(storage_to_float(oracle.allreduce_op(xs, dtype, "min"), dtype), stack.min(axis=0))

@@ -45,6 +45,16 @@ MUTANTS = {
                                    "((uint16_t*)out)[i] = f64_to_half_once((double)(float)acc, dtype);"),
     "half_once_ties_up": ("if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;\n    long k = (long)fl;               /* quanta, <= 2^p */",
                           "if (r >= 0.5) fl += 1.0;\n    long k = (long)fl;               /* quanta, <= 2^p */"),
+    "max_drops_nan": ("if (isnan(a) || isnan(b)) return NAN;\n    if (a == b) return signbit(a) ? b : a;",
+                      "if (isnan(a)) return b;\n    if (isnan(b)) return a;\n    if (a == b) return signbit(a) ? b : a;"),
+    "max_signed_zero_first_wins": ("if (a == b) return signbit(a) ? b : a;", "if (a == b) return a;"),
+    "min_signed_zero_wrong": ("if (a == b) return signbit(a) ? a : b;", "if (a == b) return signbit(a) ? b : a;"),
+    "op_max_min_swapped": ("acc = op == ORC_OP_MAX ? max_ieee(acc, widen(in[p], i, dtype)) : min_ieee(acc, widen(in[p], i, dtype));",
+                           "acc = op == ORC_OP_MAX ? min_ieee(acc, widen(in[p], i, dtype)) : max_ieee(acc, widen(in[p], i, dtype));"),
+    "op_int_drops_last_rank": ("for (int p = 1; p < n; ++p) {\n                const int32_t v",
+                               "for (int p = 1; p < n - 1; ++p) {\n                const int32_t v"),
+    "op_skips_rank_0": ("float acc = widen(in[0], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op",
+                        "float acc = widen(in[n - 1], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
