@@ -24,9 +24,9 @@
  *   - int32 accumulates with two's-complement wraparound.
  * MAX / MIN AllReduce (orc_allreduce_op) is not on the pages, which speak of
  * sum reductions only; it follows the IEEE 754-2019 maximum / minimum
- * operations in rank order: a NaN operand gives the canonical quiet NaN
- * (positive, top mantissa bit set), -0 orders below +0, and int32 takes the
- * integer maximum / minimum.
+ * operations in rank order: a NaN in any rank gives the canonical quiet NaN
+ * (positive, top mantissa bit set; for every N, one rank included), -0
+ * orders below +0, and int32 takes the integer maximum / minimum.
  * The widening/narrowing routines below are written from the IEEE-754
  * binary16 format and from bfloat16 being the top 16 bits of binary32.
  *
@@ -265,6 +265,7 @@ int orc_allreduce_op(int n, const void* const* in, void* out, size_t count, int 
         float acc = widen(in[0], i, dtype);
         for (int p = 1; p < n; ++p)
             acc = op == ORC_OP_MAX ? max_ieee(acc, widen(in[p], i, dtype)) : min_ieee(acc, widen(in[p], i, dtype));
+        if (isnan(acc)) acc = NAN;   /* canonical at N = 1 too, where no operation ran */
         narrow_store(out, i, acc, dtype);
     }
     return 0;

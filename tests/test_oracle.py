@@ -522,3 +522,23 @@ def test_max_min_match_numpy_on_finite_data(dtype):
     stack = np.stack([storage_to_float(x, dtype) for x in xs])
     assert np.array_equal(storage_to_float(oracle.allreduce_op(xs, dtype, "max"), dtype), stack.max(axis=0))
     assert np.array_equal(storage_to_float(oracle.allreduce_op(xs, dtype, "min"), dtype), stack.min(axis=0))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_max_min_nan_is_canonical(dtype, n):
+    """A NaN in any rank -- signalling, negative or with a payload -- gives
+    the canonical quiet NaN bits, for one rank as for several."""
+    canon = {"fp32": 0x7fc00000, "fp16": 0x7e00, "bf16": 0x7fc0}[dtype]
+    nans = {"fp32": [0xffc00001, 0x7f800001, 0xff812345], "fp16": [0xfe01, 0x7c01, 0xfd55],
+            "bf16": [0xffc1, 0x7f81, 0xff95]}[dtype]
+    store = np.uint32 if dtype == "fp32" else np.uint16
+    for bits in nans:
+        for where in range(n):
+            cols = [np.array([0x3c00 if dtype == "fp16" else (0x3f80 if dtype == "bf16" else 0x3f800000)],
+                             dtype=store) for _ in range(n)]
+            cols[where] = np.array([bits], dtype=store)
+            xs = [c.view(np.float32) if dtype == "fp32" else c for c in cols]
+            for op in ("max", "min"):
+                got = oracle.allreduce_op(xs, dtype, op)
+                assert int(np.asarray(got).view(store)[0]) == canon, (hex(bits), where, op)

@@ -55,6 +55,7 @@ MUTANTS = {
                                "for (int p = 1; p < n - 1; ++p) {\n                const int32_t v"),
     "op_skips_rank_0": ("float acc = widen(in[0], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op",
                         "float acc = widen(in[n - 1], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op"),
+    "op_nan_not_canonical_at_one_rank": ("if (isnan(acc)) acc = NAN;   /* canonical", "if (0) acc = NAN;   /* canonical"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
