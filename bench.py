@@ -45,7 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "allreduce_twoshot_bf16_n8.txt")
 # what the timed kernel is made of: the roofline's measured traffic is reported
 # only while these device sources hash to the value in the profile and the live
-# launch shape (CTAs per rank x threads) equals the profiled one
+# launch shape (CTAs per rank x threads) equals the profiled one.  reduce_ops.cuh
+# is left out on purpose: it holds only the MAX / MIN combiners, which the
+# timed sum instance does not instantiate
 KERNEL_SOURCES = ["collectives.cuh", "memory_channel.cuh", "instantiate.cuh", "coll_bf16.cu",
                   "dcc_internal.h"]
 
@@ -458,6 +460,15 @@ def other_workloads(dcc, dev, stream):
         ms = statistics.median(per)
         out["c4_bf16_" + algo] = {"ms": round(ms, 4),
                                   "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+    # MAX / MIN on the headline size (AUTO: the two-shot push kernels, raw-bit combines)
+    for op in ("max", "min"):
+        def step(op=op):
+            dcc.dcc_allreduce_op(comm.handle, xs, ys, w.count, "bf16", op, "auto", stream)
+        for _ in range(3):
+            step()
+        per, _ = time_launches(step, 30, stream)
+        ms = statistics.median(per)
+        out["c4_bf16_" + op] = {"ms": round(ms, 4), "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
     # the optional entry barrier: its cost on the headline size (one co-resident wave)
     dcc.dcc_set_entry_barrier(comm.handle, True)
     step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", "two_shot", stream)

@@ -24,7 +24,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=fal
 
 SOURCES = ["dcc_host.cu", "sync_kernels.cu", "coll_allgather.cu",
            "coll_int32.cu", "coll_fp32.cu", "coll_fp16.cu", "coll_bf16.cu", "noalloc.cu",
-           "proxy.cu", "coll_fused_bulk.cu"]
+           "proxy.cu", "coll_fused_bulk.cu", "coll_max.cu", "coll_min.cu"]
 
 
 def nvcc():

@@ -1,5 +1,7 @@
 // collectives.cuh -- sum AllReduce (one-shot, two-shot push, two-shot via
-// scratch), ReduceScatter and AllGather kernels for N virtual ranks.
+// scratch) and ReduceScatter kernels for N virtual ranks; the one-shot,
+// two-shot push and ReduceScatter kernels also take MAX / MIN (template
+// parameter OP, combiners in reduce_ops.cuh).
 //
 // The collectives are the standard ones of the MSCCL++ abstract, point (3);
 // the AllReduce is the tensor-parallel serving case of the project summary's
@@ -27,6 +29,7 @@
 #include <cstring>
 
 #include "memory_channel.cuh"
+#include "reduce_ops.cuh"
 
 namespace dcc {
 
@@ -134,10 +137,12 @@ template <>
 struct Lanes<__half> : HalfLanes<__half2, F16Ops> {};
 
 // ------------------------------------------------------------- reductions
-// Sum of vector v over the N ranks' buffers src[0..N-1], rank order.  With a
-// compile-time N all N gets are issued before the first add.
-template <typename T, int NT>
+// Sum (or, with OP, MAX / MIN: reduce_ops.cuh) of vector v over the N ranks'
+// buffers src[0..N-1], rank order.  With a compile-time N all N gets are
+// issued before the first add.
+template <typename T, int NT, int OP = kOpSum>
 __device__ __forceinline__ uint4 reduce_vec(void* const* src, int n, size_t v) {
+  if constexpr (OP != kOpSum) return pick_ranks_vec<T, NT, OP>(src, n, v);
   using L = Lanes<T>;
   typename L::Acc acc;
   if constexpr (NT > 0) {
@@ -154,10 +159,11 @@ __device__ __forceinline__ uint4 reduce_vec(void* const* src, int n, size_t v) {
   return L::pack(acc);
 }
 
-template <typename T>
+template <typename T, int OP = kOpSum>
 __device__ __forceinline__ typename Lanes<T>::S reduce_scalar(void* const* src, int n, size_t i) {
   using L = Lanes<T>;
   using S = typename L::S;
+  if constexpr (OP != kOpSum) return pick_ranks_scalar<T, OP, S>(src, n, i);
   typename L::SAcc acc = L::sinit(static_cast<const S*>(src[0])[i]);
   for (int p = 1; p < n; ++p) acc = L::sadd(acc, static_cast<const S*>(src[p])[i]);
   return L::spack(acc);
@@ -197,7 +203,7 @@ __device__ __forceinline__ bool entry_barrier(const DevComm& dc, int rank, int n
 // signal/wait barrier ("everyone has read this chunk"), then store.  (Getting
 // the next chunk while the signals travel measured slower on GB300: 0.53 vs
 // 0.43 ms for 8 x 64 MiB int32.)
-template <typename T, int NT, bool EB = false>
+template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   const int n = NT > 0 ? NT : dc.n;
@@ -214,9 +220,9 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   if (!a.inplace) {
     const size_t stride = (size_t)B * blockDim.x;
     for (size_t v = (size_t)blk * blockDim.x + threadIdx.x; v < nvec; v += stride)
-      st_vec(out + v, reduce_vec<T, NT>(a.send, n, v));
+      st_vec(out + v, reduce_vec<T, NT, OP>(a.send, n, v));
     if (blk == 0 && tail0 + threadIdx.x < a.count)
-      static_cast<S*>(a.recv[rank])[tail0 + threadIdx.x] = reduce_scalar<T>(a.send, n, tail0 + threadIdx.x);
+      static_cast<S*>(a.recv[rank])[tail0 + threadIdx.x] = reduce_scalar<T, OP>(a.send, n, tail0 + threadIdx.x);
     return;
   }
 
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (u < U && v < nvec) res[u] = reduce_vec<T, NT>(a.send, n, v);
+      if (u < U && v < nvec) res[u] = reduce_vec<T, NT, OP>(a.send, n, v);
     }
     ok = group_barrier(dc, rank, n, blk, expected);
     if (!ok) break;
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   if (ok && blk == 0 && tail0 < a.count) {  // same on every rank: all slot-0 CTAs take part
     const size_t i = tail0 + threadIdx.x;
     S r{};
-    if (i < a.count) r = reduce_scalar<T>(a.send, n, i);
+    if (i < a.count) r = reduce_scalar<T, OP>(a.send, n, i);
     ok = group_barrier(dc, rank, n, blk, expected);
     if (ok && i < a.count) static_cast<S*>(a.recv[rank])[i] = r;
   }
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 // rank r's CTAs touch shard r of any buffer and every thread reads all N
 // values of a vector before writing it anywhere, so in place is safe without
 // synchronisation.  Traffic: N*S read + N*S written in total, the minimum.
-template <typename T, int NT, bool EB = false>
+template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   using S = typename L::S;
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, Coll
   }
   const size_t stride = (size_t)B * blockDim.x;
   for (size_t v = s0 + (size_t)blk * blockDim.x + threadIdx.x; v < s1; v += stride) {
-    const uint4 r = reduce_vec<T, NT>(a.send, n, v);
+    const uint4 r = reduce_vec<T, NT, OP>(a.send, n, v);
     if constexpr (NT > 0) {
 #pragma unroll
       for (int p = 0; p < NT; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + v, r);
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, Coll
   }
   const size_t i = nvec * L::VW + threadIdx.x;
   if (rank == n - 1 && blk == 0 && i < a.count) {
-    const S r = reduce_scalar<T>(a.send, n, i);
+    const S r = reduce_scalar<T, OP>(a.send, n, i);
     for (int p = 0; p < n; ++p) static_cast<S*>(a.recv[p])[i] = r;
   }
 }
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
 // ------------------------------------------------------------- ReduceScatter
 // recv[r][j] = sum_p send[p][r*m + j].  Rank r's CTAs get shard r of every
 // input.  Vector path when a shard starts on a 16-byte boundary, else scalar.
-template <typename T, int NT, bool EB = false>
+template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArgs a) {
   using L = Lanes<T>;
   using S = typename L::S;
@@ -359,11 +365,11 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArg
   if ((m * sizeof(S)) % 16 == 0) {
     const size_t nv = m / L::VW, base = (size_t)rank * nv;
     uint4* out = static_cast<uint4*>(a.recv[rank]);
-    for (size_t v = first; v < nv; v += stride) st_vec(out + v, reduce_vec<T, NT>(a.send, n, base + v));
+    for (size_t v = first; v < nv; v += stride) st_vec(out + v, reduce_vec<T, NT, OP>(a.send, n, base + v));
   } else {
     S* out = static_cast<S*>(a.recv[rank]);
     const size_t base = (size_t)rank * m;
-    for (size_t j = first; j < m; j += stride) out[j] = reduce_scalar<T>(a.send, n, base + j);
+    for (size_t j = first; j < m; j += stride) out[j] = reduce_scalar<T, OP>(a.send, n, base + j);
   }
 }
 
@@ -379,6 +385,13 @@ enum KernelKind {
 // 1..8 and 16, a runtime-N instance otherwise).
 template <typename T>
 const void* reduce_kernel(int kind, int n);
+
+// MAX / MIN kernels (OP = kOpMax or kOpMin) of kind kOneShot, kTwoShot or
+// kReduceScatter (compile-time N for 2, 4, 8 and 16 ranks, a runtime-N
+// instance otherwise) and of the matching entry-barrier kinds (runtime-N
+// instances only); nullptr for other kinds.
+template <typename T, int OP>
+const void* reduce_op_kernel(int kind, int n);
 
 
 }  // namespace dcc

@@ -82,6 +82,26 @@ const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
   }
 }
 
+// Kernel of `kind` for reduction op (DCC_OP_SUM / MAX / MIN); MAX and MIN
+// exist for the one-shot, two-shot push and ReduceScatter kinds only.
+const void* op_kernel_for(dcc_dtype_t t, int op, int kind, int n) {
+  if (op == DCC_OP_SUM) return reduce_kernel_for(t, kind, n);
+  const bool mx = op == DCC_OP_MAX;
+  if (!mx && op != DCC_OP_MIN) return nullptr;
+  switch (t) {
+    case DCC_INT32:
+      return mx ? dcc::reduce_op_kernel<int32_t, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<int32_t, dcc::kOpMin>(kind, n);
+    case DCC_FP32:
+      return mx ? dcc::reduce_op_kernel<float, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<float, dcc::kOpMin>(kind, n);
+    case DCC_FP16:
+      return mx ? dcc::reduce_op_kernel<__half, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<__half, dcc::kOpMin>(kind, n);
+    case DCC_BF16:
+      return mx ? dcc::reduce_op_kernel<__nv_bfloat16, dcc::kOpMax>(kind, n)
+                : dcc::reduce_op_kernel<__nv_bfloat16, dcc::kOpMin>(kind, n);
+    default: return nullptr;
+  }
+}
+
 // CTAs per rank.  A kernel whose CTAs wait on one another, or rely on running
 // together (one_wave), gets at most one co-resident wave and at most
 // DCC_MAX_BLOCKS_PER_RANK (its semaphore slots).  A streaming kernel that
@@ -158,7 +178,8 @@ struct Shape {
 int compiled_n(int n) { return (n >= 1 && n <= 8) || n == 16 ? n : 0; }
 
 int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t algo, bool inplace,
-                    Shape* sh) {
+                    Shape* sh, int op = DCC_OP_SUM) {
+  if (op != DCC_OP_SUM && algo != DCC_ALGO_ONE_SHOT && algo != DCC_ALGO_TWO_SHOT) return DCC_ERR_UNSUPPORTED;
   const size_t vw = 16 / elem_bytes(t);
   const size_t nvec = count / vw;
   int kind;
@@ -175,7 +196,7 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
     case DCC_ALGO_ONE_SHOT_LL: kind = dcc::kOneShotLL; work = nvec; break;
     default: return DCC_ERR_INVALID_ARG;
   }
-  sh->fn = reduce_kernel_for(t, kind, c->n);
+  sh->fn = op_kernel_for(t, op, kind, c->n);
   if (!sh->fn) return DCC_ERR_INVALID_ARG;
   sh->smem = 0;
   // the entry barrier is built into the thread-copy kernels only
@@ -219,12 +240,23 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
 }
 
 int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
-                  dcc_algo_t algo, bool inplace, cudaStream_t s);
+                  dcc_algo_t algo, bool inplace, cudaStream_t s, int op = DCC_OP_SUM);
+
+// MAX / MIN run on the one-shot and two-shot push kernels: AUTO keeps the
+// size-based choice between those two and takes two-shot where it would pick
+// another schedule; an explicit other schedule is unsupported.
+dcc_algo_t resolve_op_algo(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a, bool inplace,
+                           int op) {
+  const dcc_algo_t r = resolve_algo(c, count, t, a, inplace);
+  if (op == DCC_OP_SUM || a != DCC_ALGO_AUTO || r == DCC_ALGO_ONE_SHOT) return r;
+  return DCC_ALGO_TWO_SHOT;
+}
 
 int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t count,
-                     dcc_dtype_t t, dcc_algo_t a, cudaStream_t s) {
+                     dcc_dtype_t t, dcc_algo_t a, cudaStream_t s, int op = DCC_OP_SUM) {
   if (c->sticky != DCC_OK) return c->sticky;
   if (elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (op != DCC_OP_SUM && op != DCC_OP_MAX && op != DCC_OP_MIN) return DCC_ERR_INVALID_ARG;
   if (a < DCC_ALGO_AUTO || a > DCC_ALGO_ONE_SHOT_LL) return DCC_ERR_INVALID_ARG;
   if (count == 0) return DCC_OK;
   const size_t bytes = count * elem_bytes(t);
@@ -234,13 +266,13 @@ int allreduce_launch(dcc_comm* c, void* const* send, void* const* recv, size_t c
   if (rc != DCC_OK) return rc;
   rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
-  return run_allreduce(c, send, recv, count, t, resolve_algo(c, count, t, a, inplace), inplace, s);
+  return run_allreduce(c, send, recv, count, t, resolve_op_algo(c, count, t, a, inplace, op), inplace, s, op);
 }
 
 // Builds the arguments and launches an AllReduce whose buffers are already
 // checked (pointers, alignment, overlaps, channels).
 int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
-                  dcc_algo_t algo, bool inplace, cudaStream_t s) {
+                  dcc_algo_t algo, bool inplace, cudaStream_t s, int op) {
   const size_t bytes = count * elem_bytes(t);
   int rc;
   dcc::CollArgs args{};
@@ -265,13 +297,13 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
     }
   }
   Shape sh;
-  rc = allreduce_shape(c, count, t, algo, inplace, &sh);
+  rc = allreduce_shape(c, count, t, algo, inplace, &sh, op);
   if (rc != DCC_OK) return rc;
   args.blocks = sh.blocks;
   args.unroll = sh.unroll;
   if (c->log)
-    std::fprintf(stderr, "dcc_allreduce: n=%d count=%zu dtype=%d algo=%d inplace=%d blocks/rank=%d\n",
-                 c->n, count, (int)t, (int)algo, (int)inplace, sh.blocks);
+    std::fprintf(stderr, "dcc_allreduce: n=%d count=%zu dtype=%d op=%d algo=%d inplace=%d blocks/rank=%d\n",
+                 c->n, count, (int)t, op, (int)algo, (int)inplace, sh.blocks);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
   return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative && c->cooperative, kargs, s, sh.smem);
@@ -301,7 +333,10 @@ int dcc_preload_kernels() {
   bool ok = true;
   for (dcc_dtype_t t : types)
     for (int n : ns)
-      for (int kind = 0; kind < dcc::kNumKernelKinds; ++kind) ok &= load(reduce_kernel_for(t, kind, n));
+      for (int kind = 0; kind < dcc::kNumKernelKinds; ++kind) {
+        ok &= load(reduce_kernel_for(t, kind, n));
+        ok &= load(op_kernel_for(t, DCC_OP_MAX, kind, n)) && load(op_kernel_for(t, DCC_OP_MIN, kind, n));
+      }
   for (int n : ns)
     ok &= load(dcc::allgather_kernel(n, false)) && load(dcc::allgather_kernel(n, true)) &&
           load(dcc::allgather_bulk_kernel(n));
@@ -473,6 +508,14 @@ int dcc_allreduce(dcc_comm_t c, void* const* send, void* const* recv, size_t cou
   return allreduce_launch(c, send, recv, count, t, a, static_cast<cudaStream_t>(s));
 }
 
+int dcc_allreduce_op(dcc_comm_t c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
+                     dcc_red_op_t op, dcc_algo_t a, dcc_stream_t s) {
+  if (!c) return DCC_ERR_INVALID_ARG;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  return allreduce_launch(c, send, recv, count, t, a, static_cast<cudaStream_t>(s), (int)op);
+}
+
 // The message is cut into chunks of whole vectors.  Chunk i's inputs are
 // copied in on the copy-in stream, reduced on the caller's stream once they
 // have landed, and copied out on the copy-out stream once reduced, so the two
@@ -570,7 +613,13 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
 
 int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
                        dcc_dtype_t t, dcc_stream_t s) {
+  return dcc_reduce_scatter_op(c, send, recv, recv_count, t, DCC_OP_SUM, s);
+}
+
+int dcc_reduce_scatter_op(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
+                          dcc_dtype_t t, dcc_red_op_t op, dcc_stream_t s) {
   if (!c || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  if (op != DCC_OP_SUM && op != DCC_OP_MAX && op != DCC_OP_MIN) return DCC_ERR_INVALID_ARG;
   if (c->sticky != DCC_OK) return c->sticky;
   if (recv_count == 0) return DCC_OK;
   DeviceScope ds(c->device);
@@ -591,7 +640,8 @@ int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_
   args.count = recv_count;
   // with the entry barrier the CTAs wait on one another: one cooperative wave
   const bool coop = c->entry_barrier && c->n > 1;
-  const void* fn = reduce_kernel_for(t, coop ? dcc::kReduceScatterEB : dcc::kReduceScatter, c->n);
+  const void* fn = op_kernel_for(t, (int)op, coop ? dcc::kReduceScatterEB : dcc::kReduceScatter, c->n);
+  if (!fn) return DCC_ERR_INVALID_ARG;
   const size_t vw = 16 / elem_bytes(t);
   const size_t work = (recv_count + vw - 1) / vw;
   const int threads = c->threads_override > 0 ? c->threads_override : threads_for(DCC_ALGO_TWO_SHOT, work);

@@ -45,6 +45,8 @@ DCC_MAX_BLOCKS_PER_RANK = 128
 DTYPE_CODES = {"int32": DCC_INT32, "fp32": DCC_FP32, "fp16": DCC_FP16, "bf16": DCC_BF16}
 TORCH_CODES = {torch.int32: DCC_INT32, torch.float32: DCC_FP32, torch.float16: DCC_FP16,
                torch.bfloat16: DCC_BF16}
+DCC_OP_SUM, DCC_OP_MAX, DCC_OP_MIN = 0, 1, 2
+OP_CODES = {"sum": DCC_OP_SUM, "max": DCC_OP_MAX, "min": DCC_OP_MIN}
 ALGO_CODES = {"auto": DCC_ALGO_AUTO, "one_shot": DCC_ALGO_ONE_SHOT, "two_shot": DCC_ALGO_TWO_SHOT,
               "two_shot_scratch": DCC_ALGO_TWO_SHOT_SCRATCH, "two_shot_bulk": DCC_ALGO_TWO_SHOT_BULK,
               "one_shot_ll": DCC_ALGO_ONE_SHOT_LL}
@@ -64,6 +66,8 @@ _SIGS = {
     "dcc_memory_channel_make": [_vp, _i, _i],
     "dcc_allreduce": [_vp, _PP, _PP, _sz, _i, _i, _vp],
     "dcc_reduce_scatter": [_vp, _PP, _PP, _sz, _i, _vp],
+    "dcc_allreduce_op": [_vp, _PP, _PP, _sz, _i, _i, _i, _vp],
+    "dcc_reduce_scatter_op": [_vp, _PP, _PP, _sz, _i, _i, _vp],
     "dcc_allgather": [_vp, _PP, _PP, _sz, _i, _vp],
     "dcc_allreduce_from_host": [_vp, _PP, _PP, _PP, _PP, _sz, _i, _i, _vp],
     "dcc_ring_barrier": [_vp, _i, _vp],
@@ -186,6 +190,18 @@ def dcc_allreduce(comm, send, recv, count, dtype, algo="auto", stream=None):
 def dcc_reduce_scatter(comm, send, recv, recv_count, dtype, stream=None):
     return _check(_lib.dcc_reduce_scatter(comm, _ptrs(send), _ptrs(recv), recv_count, _dtype(dtype),
                                           _stream(stream)), "dcc_reduce_scatter")
+
+
+def dcc_allreduce_op(comm, send, recv, count, dtype, op, algo="auto", stream=None):
+    return _check(_lib.dcc_allreduce_op(comm, _ptrs(send), _ptrs(recv), count, _dtype(dtype),
+                                        _code(OP_CODES, op, "op"), _code(ALGO_CODES, algo, "algo"),
+                                        _stream(stream)), "dcc_allreduce_op")
+
+
+def dcc_reduce_scatter_op(comm, send, recv, recv_count, dtype, op, stream=None):
+    return _check(_lib.dcc_reduce_scatter_op(comm, _ptrs(send), _ptrs(recv), recv_count, _dtype(dtype),
+                                             _code(OP_CODES, op, "op"), _stream(stream)),
+                  "dcc_reduce_scatter_op")
 
 
 def dcc_allgather(comm, send, recv, send_count, dtype, stream=None):
@@ -398,6 +414,13 @@ class Comm:
 
     def reduce_scatter(self, send, recv, stream=None):
         dcc_reduce_scatter(self.handle, send, recv, recv[0].numel(), send[0].dtype, stream)
+
+    def allreduce_op(self, send, recv=None, op="sum", algo="auto", stream=None):
+        recv = send if recv is None else recv
+        dcc_allreduce_op(self.handle, send, recv, send[0].numel(), send[0].dtype, op, algo, stream)
+
+    def reduce_scatter_op(self, send, recv, op="sum", stream=None):
+        dcc_reduce_scatter_op(self.handle, send, recv, recv[0].numel(), send[0].dtype, op, stream)
 
     def allgather(self, send, recv, stream=None):
         dcc_allgather(self.handle, send, recv, send[0].numel(), send[0].dtype, stream)

@@ -71,6 +71,11 @@ typedef enum {
 
 typedef enum { DCC_INT32 = 0, DCC_FP32 = 1, DCC_FP16 = 2, DCC_BF16 = 3 } dcc_dtype_t;
 
+/* Reduction of dcc_allreduce_op / dcc_reduce_scatter_op.  SUM is the
+ * reduction of the pages' collectives; MAX and MIN are not on the pages and
+ * follow the IEEE 754-2019 maximum / minimum operations (see dcc_allreduce_op). */
+typedef enum { DCC_OP_SUM = 0, DCC_OP_MAX = 1, DCC_OP_MIN = 2 } dcc_red_op_t;
+
 typedef enum {
   DCC_ALGO_AUTO = 0,   /* pick by message size from the measured crossover table */
   DCC_ALGO_ONE_SHOT = 1, /* every rank gets all N inputs and reduces its whole output */
@@ -125,7 +130,8 @@ int dcc_register_buffer(dcc_comm_t c, int rank, dcc_buf_kind_t kind, void* dev_p
 int dcc_memory_channel_make(dcc_comm_t c, int src_rank, int dst_rank);
 
 /* ------------------------------------------------------------------------ */
-/* Collectives (sum).  Per element, ranks are added in order 0..N-1 starting */
+/* Collectives (sum; MAX / MIN through the _op calls).  Per element, ranks  */
+/* are added in order 0..N-1 starting                                       */
 /* from rank 0's value; fp32/fp16/bf16 accumulate in fp32 and round once    */
 /* (round-to-nearest-even) to the output type; int32 wraps.  Results are    */
 /* therefore the same bits for every algorithm and every launch shape.      */
@@ -144,6 +150,27 @@ int dcc_allreduce(dcc_comm_t c, void* const* send, void* const* recv, size_t cou
  * send[p] holds N*recv_count elements.  Ranges must not overlap. */
 int dcc_reduce_scatter(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
                        dcc_dtype_t t, dcc_stream_t s);
+
+/* AllReduce with a chosen reduction: recv[r][i] = op over p of send[p][i],
+ * ranks combined in order 0..N-1.  DCC_OP_SUM is exactly dcc_allreduce.
+ * DCC_OP_MAX / DCC_OP_MIN: the MSCCL++ pages describe sum collectives only;
+ * these take the IEEE 754-2019 maximum / minimum -- a NaN in any rank gives
+ * the type's canonical quiet NaN (fp32 0x7fc00000, fp16 0x7e00, bf16 0x7fc0),
+ * -0 orders below +0, and otherwise the result is the bits of the largest /
+ * smallest input (no rounding); int32 takes the signed maximum / minimum.
+ * They run on the ONE_SHOT and TWO_SHOT schedules: AUTO picks between those
+ * two by size as for the sum (two-shot where the sum would take another
+ * schedule); any other explicit algo returns DCC_ERR_UNSUPPORTED.  Buffers,
+ * in-place rules and errors as dcc_allreduce; an op outside dcc_red_op_t is
+ * INVALID_ARG. */
+int dcc_allreduce_op(dcc_comm_t c, void* const* send, void* const* recv, size_t count,
+                     dcc_dtype_t t, dcc_red_op_t op, dcc_algo_t a, dcc_stream_t s);
+
+/* ReduceScatter with a chosen reduction (same semantics as dcc_allreduce_op):
+ * recv[r][j] = op over p of send[p][r*recv_count + j].  DCC_OP_SUM is exactly
+ * dcc_reduce_scatter. */
+int dcc_reduce_scatter_op(dcc_comm_t c, void* const* send, void* const* recv, size_t recv_count,
+                          dcc_dtype_t t, dcc_red_op_t op, dcc_stream_t s);
 
 /* AllGather: recv[p][q*send_count + j] = send[q][j] for all p, q, j < send_count.
  * recv[p] holds N*send_count elements.  Ranges must not overlap.  A bit copy:
