@@ -42,6 +42,8 @@ from driven_collective_communication_gb300.replicas import Dist  # noqa: E402
 
 GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
+# large messages (each launch >= tens of microseconds): warm-ups and timed launches per point
+LARGE_WARMUP, LARGE_STEPS = 20, 50
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "allreduce_twoshot_bf16_n8.txt")
 # what the timed kernel is made of: the roofline's measured traffic is reported
 # only while these device sources hash to the value in the profile and the live
@@ -141,6 +143,11 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(rows),
                 "power_w_max": max(power) if power else None}
+
+
+def spread(per):
+    """min and mean of per-launch times (ms) beside the median a result reports as "ms"."""
+    return {"min_ms": round(min(per), 4), "mean_ms": round(statistics.fmean(per), 4)}
 
 
 def time_launches(fn, steps, stream):
@@ -325,13 +332,13 @@ def sweep_large(dcc, dev, stream):
             c.register_all("input", xs)
             c.register_all("output", ys)
             step = dcc.prepare_allreduce(c.handle, xs, ys, count, "bf16", "auto", stream)
-            for _ in range(3):
+            for _ in range(LARGE_WARMUP):
                 step()
-            per, _ = time_launches(step, 20, stream)
+            per, _ = time_launches(step, LARGE_STEPS, stream)
             assert c.check(stream) == dcc.DCC_OK
         ms = statistics.median(per)
         hbm = 2 * 8 * (mib << 20) / ms / 1e6
-        res.append({"bytes_per_rank": mib << 20, "ms": round(ms, 4),
+        res.append({"bytes_per_rank": mib << 20, "ms": round(ms, 4), **spread(per),
                     "algbw_gbs": round((mib << 20) / ms / 1e6, 1), "hbm_gbs_2NS": round(hbm, 1),
                     "roofline_frac": round(hbm / peak, 4)})
         del xs, ys
@@ -454,29 +461,29 @@ def other_workloads(dcc, dev, stream):
     comm.register_all("scratch", scr)
     for algo in ("two_shot", "two_shot_bulk", "two_shot_scratch", "one_shot"):
         step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", algo, stream)
-        for _ in range(3):
+        for _ in range(LARGE_WARMUP):
             step()
-        per, _ = time_launches(step, 30, stream)
+        per, _ = time_launches(step, LARGE_STEPS, stream)
         ms = statistics.median(per)
-        out["c4_bf16_" + algo] = {"ms": round(ms, 4),
+        out["c4_bf16_" + algo] = {"ms": round(ms, 4), **spread(per),
                                   "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
     # MAX / MIN on the headline size (AUTO: the two-shot push kernels, raw-bit combines)
     for op in ("max", "min"):
         def step(op=op):
             dcc.dcc_allreduce_op(comm.handle, xs, ys, w.count, "bf16", op, "auto", stream)
-        for _ in range(3):
+        for _ in range(LARGE_WARMUP):
             step()
-        per, _ = time_launches(step, 30, stream)
+        per, _ = time_launches(step, LARGE_STEPS, stream)
         ms = statistics.median(per)
-        out["c4_bf16_" + op] = {"ms": round(ms, 4), "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+        out["c4_bf16_" + op] = {"ms": round(ms, 4), **spread(per), "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
     # the optional entry barrier: its cost on the headline size (one co-resident wave)
     dcc.dcc_set_entry_barrier(comm.handle, True)
     step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", "two_shot", stream)
-    for _ in range(3):
+    for _ in range(LARGE_WARMUP):
         step()
-    per, _ = time_launches(step, 30, stream)
+    per, _ = time_launches(step, LARGE_STEPS, stream)
     dcc.dcc_set_entry_barrier(comm.handle, False)
-    out["c4_bf16_two_shot_entry_barrier"] = {"ms": round(statistics.median(per), 4)}
+    out["c4_bf16_two_shot_entry_barrier"] = {"ms": round(statistics.median(per), 4), **spread(per)}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
     # the 2-rank fp32 1 MiB one-shot (a latency case: 4 MiB of traffic sits in L2)
@@ -540,13 +547,13 @@ def other_workloads(dcc, dev, stream):
             cn.register_all("input", xs)
             cn.register_all("output", ys)
             step = dcc.prepare_allreduce(cn.handle, xs, ys, count, dtype, "auto", stream)
-            for _ in range(3):
+            for _ in range(LARGE_WARMUP):
                 step()
-            per, _ = time_launches(step, 20, stream)
+            per, _ = time_launches(step, LARGE_STEPS, stream)
             assert cn.check(stream) == dcc.DCC_OK
         ms = statistics.median(per)
         out["allreduce_%s_n%d_256MiB" % (dtype, n_ranks)] = {
-            "ms": round(ms, 4), "algbw_gbs": round((256 << 20) / ms / 1e6, 1),
+            "ms": round(ms, 4), **spread(per), "algbw_gbs": round((256 << 20) / ms / 1e6, 1),
             "hbm_gbs_2NS": round(2 * n_ranks * (256 << 20) / ms / 1e6, 1)}
         del xs, ys
     w = W.C2
@@ -558,11 +565,11 @@ def other_workloads(dcc, dev, stream):
     for algo in ("one_shot", "two_shot"):
         def step():
             dcc.dcc_allreduce(comm.handle, xs, xs, w.count, "int32", algo, stream)
-        for _ in range(3):
+        for _ in range(LARGE_WARMUP):
             step()
-        per, _ = time_launches(step, 20, stream)
+        per, _ = time_launches(step, LARGE_STEPS, stream)
         ms = statistics.median(per)
-        out["c2_int32_inplace_" + algo] = {"ms": round(ms, 4),
+        out["c2_int32_inplace_" + algo] = {"ms": round(ms, 4), **spread(per),
                                            "algbw_gbs": round(w.bytes_per_rank / ms / 1e6, 2),
                                            "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
     assert comm.check(stream) == dcc.DCC_OK
@@ -584,11 +591,11 @@ def other_workloads(dcc, dev, stream):
              8 * w.bytes_per_rank + w.bytes_per_rank),
             ("c5_allgather", lambda: dcc.dcc_allgather(comm.handle, rs, ag, m, "fp16", stream),
              w.bytes_per_rank + 8 * w.bytes_per_rank)):
-        for _ in range(3):
+        for _ in range(LARGE_WARMUP):
             fn()
-        per, _ = time_launches(fn, 20, stream)
+        per, _ = time_launches(fn, LARGE_STEPS, stream)
         ms = statistics.median(per)
-        out[name] = {"ms": round(ms, 4), "hbm_gbs": round(nbytes / ms / 1e6, 1),
+        out[name] = {"ms": round(ms, 4), **spread(per), "hbm_gbs": round(nbytes / ms / 1e6, 1),
                      "algorithmic_bytes": nbytes}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
@@ -598,13 +605,13 @@ def other_workloads(dcc, dev, stream):
         pc.register_all("output", ag)
         dcc.dcc_proxy_start(pc.handle)
         fn = lambda: dcc.dcc_port_allgather(pc.handle, rs, ag, m, "fp16", stream)  # noqa: E731
-        for _ in range(3):
+        for _ in range(LARGE_WARMUP):
             fn()
-        per, _ = time_launches(fn, 10, stream)
+        per, _ = time_launches(fn, LARGE_STEPS, stream)
         assert pc.check(stream) == dcc.DCC_OK
         assert dcc.dcc_proxy_stop(pc.handle) == dcc.DCC_OK
         ms = statistics.median(per)
-        out["c5_allgather_port_channel"] = {"ms": round(ms, 4), "hbm_gbs": round(
+        out["c5_allgather_port_channel"] = {"ms": round(ms, 4), **spread(per), "hbm_gbs": round(
             (w.bytes_per_rank + 8 * w.bytes_per_rank) / ms / 1e6, 1)}
     # fused row-parallel linear + AllReduce vs per-rank GEMV (cuBLAS) then AllReduce,
     # tensor-parallel decode shapes: hidden 8192 rows, 8 ranks, kp = 1024, 3584, 8192
