@@ -167,6 +167,34 @@ def time_launches(fn, steps, stream):
     return per, t0.elapsed_time(t1)
 
 
+def time_launches_queued(fn, steps, stream, batch=100, hold_cycles=5_000_000):
+    """Per-launch CUDA-event durations (ms) with the host kept out of them: a
+    bounded spin kernel (torch's sleep kernel, hold_cycles SM cycles, about
+    2.4 ms at 2.07 GHz) holds the stream while the host queues a batch of
+    (event, launch, event), so the launches then run back to back and each
+    pair of events brackets one launch as the device runs it.  Also returns
+    whether every batch was fully queued before its hold ended."""
+    per, queued_ok = [], True
+    for b0 in range(0, steps, batch):
+        nb = min(batch, steps - b0)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(nb)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(nb)]
+        h0 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            h0.record(stream)
+            torch.cuda._sleep(hold_cycles)
+            t = time.perf_counter()
+            for i in range(nb):
+                starts[i].record(stream)
+                fn()
+                ends[i].record(stream)
+            host_ms = (time.perf_counter() - t) * 1e3
+        ends[-1].synchronize()
+        queued_ok &= host_ms < h0.elapsed_time(starts[0])
+        per += [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    return per, queued_ok
+
+
 # ------------------------------------------------------------------ oracle CPU leg
 def oracle_sample_run(seconds, elems, threads=None):
     """Time the oracle (all host cores, or `threads`) on a prefix of `elems` elements
@@ -368,8 +396,11 @@ def graph_node_floor(stream, reps=100):
 
 
 def sweep_c3(dcc, dev, stream):
-    """Decode-shaped sizes: per-launch p50 (events) and CUDA-graph-amortised us
-    per algorithm.  Steady state: the 8 x 16 KiB..4 MiB inputs stay in L2."""
+    """Decode-shaped sizes, per algorithm: per-launch p50 / min / mean (CUDA
+    events, launches queued ahead of the device so the host's submission time
+    is not inside them), the same host-paced (one launch at a time from
+    Python), the host cost per call, and the CUDA-graph-amortised us.  Steady
+    state: the 8 x 16 KiB..4 MiB inputs stay in L2."""
     res = []
     for tokens in W.C3_TOKENS:
         w = W.c3(tokens)
@@ -389,9 +420,10 @@ def sweep_c3(dcc, dev, stream):
             step = dcc.prepare_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
             for _ in range(50):
                 step()
-            per, _ = time_launches(step, 1000, stream)
+            per, queued_ok = time_launches_queued(step, 1000, stream)
             p50 = statistics.median(per) * 1e3
             p_min, p_mean = min(per) * 1e3, statistics.mean(per) * 1e3
+            eager, _ = time_launches(step, 1000, stream)
             # host cost of one call (launch included), no device wait in between
             stream.synchronize()
             t = time.perf_counter()
@@ -416,6 +448,8 @@ def sweep_c3(dcc, dev, stream):
             e1.synchronize()
             graph_us = e0.elapsed_time(e1) * 1e3 / (10 * reps)
             row[algo] = {"p50_us": round(p50, 2), "min_us": round(p_min, 2), "mean_us": round(p_mean, 2),
+                         "queued_ahead": bool(queued_ok),
+                         "host_paced_p50_us": round(statistics.median(eager) * 1e3, 2),
                          "host_us_per_call": round(host_us, 2),
                          "graph_us": round(graph_us, 2),
                          "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
