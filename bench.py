@@ -195,6 +195,40 @@ def time_launches_queued(fn, steps, stream, batch=100, hold_cycles=5_000_000):
     return per, queued_ok
 
 
+def time_queued_span(fn, launches, stream, hold_cycles=5_000_000, rounds=5):
+    """Device time per launch (us) of `launches` eager launches queued back to
+    back behind the same hold as time_launches_queued, with one pair of events
+    around the whole run instead of a pair per launch (an event between two
+    launches makes the second wait for the first to drain).  Median over
+    `rounds` runs."""
+    out = []
+    for _ in range(rounds):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(hold_cycles)
+            e0.record(stream)
+            for _ in range(launches):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / launches)
+    return statistics.median(out)
+
+
+def eager_floor(stream):
+    """The same per-launch measures for an empty kernel (torch's sleep kernel
+    with a zero count): what an eager launch costs the device by itself."""
+    empty = lambda: torch.cuda._sleep(0)  # noqa: E731
+    with torch.cuda.stream(stream):
+        for _ in range(50):
+            empty()
+        per, queued_ok = time_launches_queued(empty, 1000, stream)
+    return {"event_bracketed_p50_us": round(statistics.median(per) * 1e3, 2),
+            "event_bracketed_min_us": round(min(per) * 1e3, 2), "queued_ahead": bool(queued_ok),
+            "back_to_back_us": round(time_queued_span(empty, 100, stream), 2)}
+
+
 # ------------------------------------------------------------------ oracle CPU leg
 def oracle_sample_run(seconds, elems, threads=None):
     """Time the oracle (all host cores, or `threads`) on a prefix of `elems` elements
@@ -298,6 +332,7 @@ def run_ours(args, dist):
     if dist.ws == 1 and not args.quick:  # single-GPU extras and the CPU leg (N = 1 only)
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
         out["graph_node_floor_us"] = graph_node_floor(stream)
+        out["eager_launch_floor"] = eager_floor(stream)
         out["sweep_large"] = sweep_large(dcc, dev, stream)
         out["other"] = other_workloads(dcc, dev, stream)
         gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
@@ -424,6 +459,7 @@ def sweep_c3(dcc, dev, stream):
             p50 = statistics.median(per) * 1e3
             p_min, p_mean = min(per) * 1e3, statistics.mean(per) * 1e3
             eager, _ = time_launches(step, 1000, stream)
+            span_us = time_queued_span(step, 100, stream)
             # host cost of one call (launch included), no device wait in between
             stream.synchronize()
             t = time.perf_counter()
@@ -450,6 +486,7 @@ def sweep_c3(dcc, dev, stream):
             row[algo] = {"p50_us": round(p50, 2), "min_us": round(p_min, 2), "mean_us": round(p_mean, 2),
                          "queued_ahead": bool(queued_ok),
                          "host_paced_p50_us": round(statistics.median(eager) * 1e3, 2),
+                         "back_to_back_us": round(span_us, 2),
                          "host_us_per_call": round(host_us, 2),
                          "graph_us": round(graph_us, 2),
                          "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
