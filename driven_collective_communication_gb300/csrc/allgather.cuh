@@ -28,6 +28,7 @@ __device__ __forceinline__ void st_vec_stream(uint4* p, uint4 v) { __stcs(p, v);
 
 template <int NT, bool EB = false>
 __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, int elem_bytes) {
+  pdl_prologue();
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;
   const int rank = blockIdx.x / B, blk = blockIdx.x % B;

@@ -127,6 +127,7 @@ __device__ __forceinline__ uint4 reduce_stage(const uint4* in, int n, uint32_t v
 // refills the stage.  The CTA's tiles are t = blk, blk + B, ... of the shard.
 template <typename T, int NT>
 __global__ void __launch_bounds__(kBulkThreads, 1) k_allreduce_twoshot_bulk(DevComm dc, CollArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   using S = typename L::S;
   constexpr int ST = bulk_stages(NT > 0 ? NT : DCC_MAX_RANKS);
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_allreduce_twoshot_bulk(DevC
 // Requires m * elem_bytes to be a multiple of 16 (host checks).
 template <int NT>
 __global__ void __launch_bounds__(32, 1) k_allgather_bulk(DevComm dc, CollArgs a, int elem_bytes) {
+  pdl_prologue();
   if (threadIdx.x != 0) return;
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;

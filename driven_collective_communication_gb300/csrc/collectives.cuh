@@ -205,6 +205,7 @@ __device__ __forceinline__ bool entry_barrier(const DevComm& dc, int rank, int n
 // 0.43 ms for 8 x 64 MiB int32.)
 template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   const int n = NT > 0 ? NT : dc.n;
   const int B = a.blocks;
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 // synchronisation.  Traffic: N*S read + N*S written in total, the minimum.
 template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, CollArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   using S = typename L::S;
   const int n = NT > 0 ? NT : dc.n;
@@ -351,6 +353,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
 // input.  Vector path when a shard starts on a 16-byte boundary, else scalar.
 template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   using S = typename L::S;
   const int n = NT > 0 ? NT : dc.n;

@@ -99,6 +99,7 @@ struct dcc_comm {
   // crossover), 0 never, 1 always (DCC_FUSED_BULK)
   int fused_bulk = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier
+  bool pdl = true;             // DCC_PDL / dcc_set_pdl: programmatic dependent launch of the wait-free kernels
   int inplace_unroll = 0;      // DCC_INPLACE_UNROLL: force the in-place one-shot's vectors per thread
   bool ag_bulk = false;  // DCC_AG_BULK=1: AllGather through the bulk-copy pipeline when aligned and large
   bool zero_copy = true;  // host-buffer AllReduce reads/writes mapped pinned host memory directly
@@ -205,8 +206,11 @@ inline int check_buffers(const dcc_comm* c, void* const* send, size_t send_bytes
   return DCC_OK;
 }
 
+// pdl: launch with programmatic stream serialization (only kernels that open
+// with pdl_prologue() and whose CTAs never wait on one another; never together
+// with a cooperative launch).
 inline int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s,
-           size_t smem = 0) {
+           size_t smem = 0, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
@@ -216,6 +220,11 @@ inline int launch(const void* fn, int grid, int threads, bool cooperative, void*
   if (cooperative) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }

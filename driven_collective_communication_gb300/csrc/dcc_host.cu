@@ -306,7 +306,11 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
                  c->n, count, (int)t, op, (int)algo, (int)inplace, sh.blocks);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative && c->cooperative, kargs, s, sh.smem);
+  // programmatic dependent launch for the schedules whose CTAs never wait on
+  // one another (out-of-place one-shot, two-shot push, bulk two-shot)
+  const bool pdl = c->pdl && !sh.cooperative &&
+                   (algo == DCC_ALGO_ONE_SHOT || algo == DCC_ALGO_TWO_SHOT || algo == DCC_ALGO_TWO_SHOT_BULK);
+  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative && c->cooperative, kargs, s, sh.smem, pdl);
 }
 
 }  // namespace
@@ -445,6 +449,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
     if (u >= 1 && u <= dcc::kInplaceUnroll) c->inplace_unroll = u;
   }
   c->entry_barrier = env_flag("DCC_ENTRY_BARRIER");
+  if (const char* v = std::getenv("DCC_PDL")) c->pdl = std::strcmp(v, "0") != 0;
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
@@ -649,7 +654,8 @@ int dcc_reduce_scatter_op(dcc_comm_t c, void* const* send, void* const* recv, si
   if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s), 0,
+                c->pdl && !coop);
 }
 
 int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t send_count,
@@ -684,7 +690,7 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
     const size_t smem = dcc::ag_smem_bytes();
     rc = pick_blocks(c, fn, 32, (sb + dcc::kAgTile - 1) / dcc::kAgTile, &args.blocks, smem, 1);
     if (rc != DCC_OK) return rc;
-    return launch(fn, args.blocks * c->n, 32, false, kargs, static_cast<cudaStream_t>(s), smem);
+    return launch(fn, args.blocks * c->n, 32, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl);
   }
   const void* fn = dcc::allgather_kernel(c->n, coop);
   const size_t work = (sb + 15) / 16;
@@ -693,7 +699,8 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   const size_t per_block = sb % 16 == 0 ? (size_t)dcc::kAgUnroll * threads : (size_t)threads;
   rc = pick_blocks(c, fn, threads, sb % 16 == 0 ? work : send_count, &args.blocks, 0, per_block, coop);
   if (rc != DCC_OK) return rc;
-  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s), 0,
+                c->pdl && !coop);
 }
 
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
@@ -743,14 +750,14 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
     const size_t items = rows / dcc::kFusedBulkRows / (size_t)c->n + 1;  // 2-row items per rank
     rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, smem, 1, false);  // one item per CTA
     if (rc != DCC_OK) return rc;
-    return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), smem);
+    return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl);
   }
   const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
                                  : dcc::linear_allreduce_kernel<__half>(c->n);
   const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // items per rank
   rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
   if (rc != DCC_OK) return rc;
-  return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s));
+  return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), 0, c->pdl);
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {
@@ -878,6 +885,12 @@ int dcc_set_wait_timeout_us(dcc_comm_t c, uint64_t us) {
 int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks) {
   if (!c || blocks < 0 || blocks > DCC_MAX_BLOCKS_PER_RANK) return DCC_ERR_INVALID_ARG;
   c->blocks_override = blocks;
+  return DCC_OK;
+}
+
+int dcc_set_pdl(dcc_comm_t c, int on) {
+  if (!c) return DCC_ERR_INVALID_ARG;
+  c->pdl = on != 0;
   return DCC_OK;
 }
 

@@ -66,6 +66,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, LinearArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   constexpr int R = kFusedRows, V = kFusedVecs;
   static_assert(R == 2, "the epilogue packs two rows per item");

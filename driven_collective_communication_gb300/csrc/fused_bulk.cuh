@@ -48,6 +48,7 @@ __host__ __device__ constexpr size_t fused_bulk_smem_bytes() {
 
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm dc, LinearArgs a) {
+  pdl_prologue();
   using L = Lanes<T>;
   constexpr int RI = kFusedBulkRows, ST = kFusedBulkStages;
   constexpr int ROWB = kFusedBulkChunk * 2;

@@ -60,6 +60,18 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 
 // 16-byte vector accesses.  Peer data that another CTA wrote in this kernel is
 // read at L2 (ld.global.cg) so that no stale L1 line can be returned.
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may begin launching while the kernel before it on the stream
+// is still finishing; griddepcontrol.wait then blocks until that kernel has
+// completed and its memory operations are visible, so it must come before
+// any access to global memory.  launch_dependents lets the next such kernel
+// begin launching (it waits in turn).  Both are no-ops in a launch without
+// the attribute.  Only kernels whose CTAs never wait on one another take it.
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ld_vec(const uint4* p) { return *p; }
 __device__ __forceinline__ uint4 ld_vec_l2(const uint4* p) { return __ldcg(p); }
 __device__ __forceinline__ void st_vec(uint4* p, uint4 v) { *p = v; }

@@ -80,6 +80,7 @@ _SIGS = {
     "dcc_set_blocks_per_rank": [_vp, _i],
     "dcc_set_algo_threshold": [_vp, _i, _sz],
     "dcc_set_entry_barrier": [_vp, _i],
+    "dcc_set_pdl": [_vp, _i],
     "dcc_select_algo": [_vp, _sz, _i, ctypes.POINTER(_i)],
     "dcc_debug_skip_signal": [_vp, _i],
     "dcc_launch_shape": [_vp, _sz, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
@@ -267,6 +268,10 @@ def dcc_set_blocks_per_rank(comm, blocks):
 
 def dcc_set_entry_barrier(comm, on):
     return _check(_lib.dcc_set_entry_barrier(comm, 1 if on else 0), "dcc_set_entry_barrier")
+
+
+def dcc_set_pdl(comm, on):
+    return _check(_lib.dcc_set_pdl(comm, 1 if on else 0), "dcc_set_pdl")
 
 
 def dcc_set_algo_threshold(comm, dtype, nbytes):

@@ -389,6 +389,19 @@ int dcc_set_blocks_per_rank(dcc_comm_t c, int blocks);
  * is on.  A wait that runs out is reported by dcc_comm_check. */
 int dcc_set_entry_barrier(dcc_comm_t c, int on);
 
+/* Programmatic dependent launch (on by default; DCC_PDL=0 in the environment
+ * at creation turns it off).  The kernels whose CTAs never wait on one
+ * another -- out-of-place ONE_SHOT, TWO_SHOT, TWO_SHOT_BULK, ReduceScatter,
+ * AllGather and the fused linear layer, each without the entry barrier -- are
+ * launched with programmatic stream serialization: the launch may begin while
+ * the previous kernel on the stream is still finishing, and the kernel's
+ * first instruction waits until that kernel has completed and its writes are
+ * visible, so stream order is kept.  This hides most of the gap between
+ * dependent launches (the next kernel must be launched the same way to gain
+ * from it in turn).  Synchronising kernels always launch in plain stream
+ * order.  Errors: INVALID_ARG (c NULL). */
+int dcc_set_pdl(dcc_comm_t c, int on);
+
 /* AUTO picks ONE_SHOT for out-of-place messages of at most `bytes` per rank
  * and TWO_SHOT above, for this dtype.  Defaults come from the measured
  * crossover: 32 KiB with 5 or more ranks, 0 (always two-shot) with 2 to 4. */

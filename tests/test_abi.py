@@ -89,6 +89,8 @@ def test_null_communicator_is_rejected(dcc):
         ("dcc_allreduce", None, arr, arr, 4, 1, 0, None),
         ("dcc_reduce_scatter", None, arr, arr, 4, 1, None),
         ("dcc_allgather", None, arr, arr, 4, 1, None),
+        ("dcc_allreduce_op", None, arr, arr, 4, 1, 1, 0, None),
+        ("dcc_reduce_scatter_op", None, arr, arr, 4, 1, 1, None),
         ("dcc_allreduce_from_host", None, arr, arr, arr, arr, 4, 1, 0, None),
         ("dcc_ring_barrier", None, 1, None),
         ("dcc_comm_check", None, None),
@@ -100,6 +102,7 @@ def test_null_communicator_is_rejected(dcc):
         ("dcc_set_blocks_per_rank", None, 1),
         ("dcc_set_algo_threshold", None, 1, 1024),
         ("dcc_set_entry_barrier", None, 1),
+        ("dcc_set_pdl", None, 1),
         ("dcc_select_algo", None, 4, 1, ctypes.byref(i)),
         ("dcc_debug_skip_signal", None, 0),
         ("dcc_launch_shape", None, 4, 1, 0, ctypes.byref(i), ctypes.byref(i)),
