@@ -230,6 +230,26 @@ def eager_floor(stream):
 
 
 # ------------------------------------------------------------------ oracle CPU leg
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def oracle_sample_run(seconds, elems, threads=None):
     """Time the oracle (all host cores, or `threads`) on a prefix of `elems` elements
     per rank of the large-message workload.  Returns (GB/s algbw, threads, sample text,
@@ -338,7 +358,7 @@ def run_ours(args, dist):
         gbs, cores, sample, _ = oracle_sample_run(args.cpu_seconds, args.cpu_elems)
         gbs1, _, sample1, _ = oracle_sample_run(3.0, args.cpu_elems // 8, threads=1)
         out["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
-                               "kind": "oracle", "sample": sample,
+                               "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
                                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s",
                                                  "cores": 1, "sample": sample1}}
     comm.close()
@@ -778,7 +798,7 @@ def run_reference(args, dist):
         "config": {"workload": w.name, "n_ranks": 8, "elem": "bf16", "accumulate": "f32",
                    "count_per_rank": w.count, "sample_elems_per_rank": elems},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
