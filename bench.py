@@ -418,12 +418,16 @@ def sweep_large(dcc, dev, stream):
             for _ in range(LARGE_WARMUP):
                 step()
             per, _ = time_launches(step, LARGE_STEPS, stream)
+            # launches queued back to back (no event in between, so consecutive
+            # launches overlap through programmatic dependent launch)
+            b2b_ms = time_queued_span(step, 20, stream) / 1e3
             assert c.check(stream) == dcc.DCC_OK
         ms = statistics.median(per)
         hbm = 2 * 8 * (mib << 20) / ms / 1e6
         res.append({"bytes_per_rank": mib << 20, "ms": round(ms, 4), **spread(per),
                     "algbw_gbs": round((mib << 20) / ms / 1e6, 1), "hbm_gbs_2NS": round(hbm, 1),
-                    "roofline_frac": round(hbm / peak, 4)})
+                    "roofline_frac": round(hbm / peak, 4), "back_to_back_ms": round(b2b_ms, 4),
+                    "back_to_back_roofline_frac": round(2 * 8 * (mib << 20) / b2b_ms / 1e6 / peak, 4)})
         del xs, ys
     return res
 
@@ -590,9 +594,12 @@ def other_workloads(dcc, dev, stream):
         for _ in range(20):
             step()
         per, _ = time_launches(step, 200, stream)
+        b2b_us = time_queued_span(step, 100, stream)
         assert c1.check(stream) == dcc.DCC_OK
         out["c1_fp32_n2_1MiB_one_shot"] = {"p50_us": round(statistics.median(per) * 1e3, 2),
-                                           "min_us": round(min(per) * 1e3, 2)}
+                                           "min_us": round(min(per) * 1e3, 2),
+                                           "mean_us": round(statistics.fmean(per) * 1e3, 2),
+                                           "back_to_back_us": round(b2b_us, 2)}
     # ... and on the 16 KiB decode size, CUDA-graph amortised
     w16 = W.c3(1)
     with torch.cuda.stream(stream):
