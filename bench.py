@@ -814,7 +814,7 @@ def run_reference(args, dist):
 # ------------------------------------------------------------------ profiling cases
 PROFILE_CASES = ("allreduce_two_shot", "allreduce_two_shot_bulk", "allreduce_one_shot",
                  "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "allreduce_one_shot_ll",
-                 "reduce_scatter",
+                 "allreduce_two_shot_max", "reduce_scatter",
                  "allgather", "ring_barrier", "linear_allreduce")
 
 
@@ -867,10 +867,14 @@ def run_profile_case(args):
         algo = case[len("allreduce_"):]
         inplace = algo.endswith("_inplace")
         algo = algo.replace("_inplace", "")
+        op = "sum"
+        for o in ("max", "min"):
+            if algo.endswith("_" + o):
+                op, algo = o, algo[: -len(o) - 1]
         ys = xs if inplace else [torch.empty_like(x) for x in xs]
         if algo == "two_shot_scratch":
             comm.register_all("scratch", [torch.empty_like(x) for x in xs])
-        fn = lambda: dcc.dcc_allreduce(comm.handle, xs, ys, w.count, args.dtype, algo)  # noqa: E731
+        fn = lambda: dcc.dcc_allreduce_op(comm.handle, xs, ys, w.count, args.dtype, op, algo)  # noqa: E731
     if case != "ring_barrier":
         comm.register_all("input", xs)
         if ys is not xs:
