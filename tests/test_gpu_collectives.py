@@ -138,7 +138,8 @@ def test_empty_inputs_are_no_ops(dcc):
 def test_random_configurations_match_oracle(dcc, monkeypatch):
     """Two hundred seeded random mixes of rank count (compiled and runtime-N instances),
     element count, dtype, algorithm, in/out of place, CTAs per rank, threads
-    per CTA and the entry barrier, each against the oracle bit for bit."""
+    per CTA, the entry barrier and programmatic dependent launch, each against
+    the oracle bit for bit."""
     rng = np.random.default_rng(2026)
     checked = 0
     for case in range(200):
@@ -150,6 +151,7 @@ def test_random_configurations_match_oracle(dcc, monkeypatch):
         blocks = int(rng.choice([0, 1, 3, 17, 128]))
         threads = int(rng.choice([0, 64, 96, 256]))
         entry_barrier = bool(rng.integers(0, 4) == 0)
+        pdl = bool(rng.integers(0, 2))
         if threads:
             monkeypatch.setenv("DCC_THREADS", str(threads))
         else:
@@ -162,7 +164,8 @@ def test_random_configurations_match_oracle(dcc, monkeypatch):
             h = arena.comm.handle
             dcc.dcc_set_blocks_per_rank(h, blocks)
             dcc.dcc_set_entry_barrier(h, entry_barrier)
-            what = (case, n, dtype, count, algo, inplace, blocks, threads, entry_barrier)
+            dcc.dcc_set_pdl(h, pdl)
+            what = (case, n, dtype, count, algo, inplace, blocks, threads, entry_barrier, pdl)
             if entry_barrier and algo in ("two_shot_bulk", "one_shot_ll"):
                 send = arena.view(arena.inp, dtype, count)
                 with pytest.raises(dcc.DccError) as e:

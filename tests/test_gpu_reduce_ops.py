@@ -278,3 +278,77 @@ def test_op_full_size_sampled(dcc):
             assert bool(hit.all())
             for r in range(1, n):
                 assert torch.equal(ys[r].view(torch.int16), ys[0].view(torch.int16))
+
+
+def test_random_op_configurations_match_oracle(dcc, monkeypatch):
+    """150 seeded random mixes of rank count (compiled and runtime-N
+    instances), element count, dtype, MAX / MIN, schedule, in / out of place,
+    CTAs per rank, threads per CTA, entry barrier and programmatic dependent
+    launch, on raw inputs with specials, each against the oracle bit for bit."""
+    rng = np.random.default_rng(4242)
+    for case in range(150):
+        n = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16]))
+        dtype = str(rng.choice(DTYPES))
+        count = int(rng.integers(1, 60000))
+        op = str(rng.choice(OPS))
+        algo = str(rng.choice(["auto", "one_shot", "two_shot"]))
+        inplace = bool(rng.integers(0, 2))
+        blocks = int(rng.choice([0, 1, 3, 17, 128]))
+        threads = int(rng.choice([0, 64, 96, 256]))
+        entry_barrier = bool(rng.integers(0, 4) == 0)
+        pdl = bool(rng.integers(0, 2))
+        if threads:
+            monkeypatch.setenv("DCC_THREADS", str(threads))
+        else:
+            monkeypatch.delenv("DCC_THREADS", raising=False)
+        xs = raw_inputs(9000 + case, dtype, n, count)
+        expect = oracle.allreduce_op(xs, dtype, op)
+        arena = Arena(dcc, n, count * 4)
+        try:
+            h = arena.comm.handle
+            dcc.dcc_set_blocks_per_rank(h, blocks)
+            dcc.dcc_set_entry_barrier(h, entry_barrier)
+            dcc.dcc_set_pdl(h, pdl)
+            outs = run_op(dcc, arena, xs, dtype, op, algo, inplace)
+            what = (case, n, dtype, count, op, algo, inplace, blocks, threads, entry_barrier, pdl)
+            for r in range(n):
+                assert bits_equal(outs[r], expect, dtype), (what, r)
+        finally:
+            arena.close()
+
+
+def test_random_op_reduce_scatter_configurations(dcc, monkeypatch):
+    """60 seeded random ReduceScatter mixes (rank count, shard size on and off
+    16-byte boundaries, dtype, MAX / MIN, CTAs per rank, threads, entry
+    barrier, programmatic dependent launch) against the oracle."""
+    rng = np.random.default_rng(4343)
+    for case in range(60):
+        n = int(rng.choice([2, 3, 4, 5, 8, 9, 16]))
+        dtype = str(rng.choice(DTYPES))
+        m = int(rng.integers(1, 9000))
+        op = str(rng.choice(OPS))
+        blocks = int(rng.choice([0, 1, 5, 64]))
+        threads = int(rng.choice([0, 64, 256]))
+        if threads:
+            monkeypatch.setenv("DCC_THREADS", str(threads))
+        else:
+            monkeypatch.delenv("DCC_THREADS", raising=False)
+        xs = raw_inputs(7000 + case, dtype, n, m * n)
+        expect = oracle.allreduce_op(xs, dtype, op)
+        arena = Arena(dcc, n, m * n * 4)
+        try:
+            h = arena.comm.handle
+            dcc.dcc_set_blocks_per_rank(h, blocks)
+            dcc.dcc_set_entry_barrier(h, bool(rng.integers(0, 4) == 0))
+            dcc.dcc_set_pdl(h, bool(rng.integers(0, 2)))
+            send = arena.view(arena.inp, dtype, m * n)
+            recv = arena.view(arena.out, dtype, m)
+            for r in range(n):
+                send[r].copy_(to_device(xs[r], dtype))
+                recv[r].zero_()
+            dcc.dcc_reduce_scatter_op(h, send, recv, m, dtype, op)
+            assert arena.comm.check() == dcc.DCC_OK
+            for r in range(n):
+                assert bits_equal(recv[r], expect[r * m:(r + 1) * m], dtype), (case, n, dtype, m, op, r)
+        finally:
+            arena.close()
