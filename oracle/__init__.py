@@ -42,10 +42,12 @@ def _load():
         lib.orc_convert_from_f32.argtypes = [vp, vp, sz, i32]
         lib.orc_linear_allreduce.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, sz, i32, vp]
         lib.orc_allreduce_op.argtypes = [i32, ctypes.POINTER(vp), vp, sz, i32, i32]
+        lib.orc_linear_allreduce_residual.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                      ctypes.POINTER(vp), sz, sz, i32, vp]
         for name in ("orc_allreduce", "orc_allreduce_at", "orc_allreduce_mt",
                      "orc_reduce_scatter", "orc_allgather", "orc_ring_barrier_counts",
                      "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce",
-                     "orc_allreduce_op"):
+                     "orc_allreduce_op", "orc_linear_allreduce_residual"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -171,6 +173,29 @@ def linear_allreduce(ws, xs, dtype, rows, kp):
     _ok(lib.orc_linear_allreduce(len(warrs), wp, xp, rows, kp, DTYPES[dtype], out.ctypes.data),
         "linear_allreduce")
     return out
+
+
+def linear_allreduce_residual(ws, xs, res, dtype, rows, kp):
+    """y_q[i] = R(sum_p sum_k W_p[i, k] x_p[k] + res_q[i]) for every rank q: the
+    row-parallel linear layer + AllReduce with a residual per output rank,
+    added before the one rounding.  Returns the N outputs as a list."""
+    lib = _load()
+    if dtype not in ("fp16", "bf16"):
+        raise ValueError("fp16 or bf16 only")
+    warrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in ws]
+    xarrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in xs]
+    rarrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in res]
+    n = len(warrs)
+    if (len(xarrs) != n or len(rarrs) != n or any(len(a) != rows * kp for a in warrs)
+            or any(len(a) != kp for a in xarrs) or any(len(a) != rows for a in rarrs)):
+        raise ValueError("shapes")
+    wp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in warrs])
+    xp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in xarrs])
+    rp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in rarrs])
+    out = np.empty(n * rows, dtype=np.uint16)
+    _ok(lib.orc_linear_allreduce_residual(n, wp, xp, rp, rows, kp, DTYPES[dtype], out.ctypes.data),
+        "linear_allreduce_residual")
+    return [out[q * rows:(q + 1) * rows].copy() for q in range(n)]
 
 
 def library_path():

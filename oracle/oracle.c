@@ -369,17 +369,48 @@ int orc_ring_barrier_counts(int n, uint64_t iters, uint64_t* counts)
 /* in binary64 (for the small-integer inputs the tests pin it with, exactly */
 /* the real sum), then rounded once to the output type.                     */
 /* ---------------------------------------------------------------------- */
+/* row i of the layer: sum_p sum_k W_p[i][k] * x_p[k] in binary64 */
+static double layer_row(int n, const void* const* w, const void* const* x, size_t i, size_t kp, int dtype)
+{
+    double acc = 0.0;
+    for (int p = 0; p < n; ++p)
+        for (size_t k = 0; k < kp; ++k)
+            acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);
+    return acc;
+}
+
 int orc_linear_allreduce(int n, const void* const* w, const void* const* x, size_t rows, size_t kp,
                          int dtype, void* out)
 {
     if (n < 1 || !w || !x || (rows && !out) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
     for (int p = 0; p < n; ++p) if (!w[p] || !x[p]) return -1;
     for (size_t i = 0; i < rows; ++i) {
-        double acc = 0.0;
-        for (int p = 0; p < n; ++p)
-            for (size_t k = 0; k < kp; ++k)
-                acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);
+        const double acc = layer_row(n, w, x, i, kp, dtype);
         ((uint16_t*)out)[i] = f64_to_half_once(acc, dtype);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* The same layer with a residual added for each output rank (the          */
+/* tensor-parallel residual stream: h_q <- h_q + the layer's AllReduced    */
+/* output).  Reading taken: the residual joins the binary64 sum before the */
+/* single rounding,                                                        */
+/*   y_q[i] = R( sum_p sum_k W_p[i][k] * x_p[k] + res_q[i] ),              */
+/* res_q has rows elements of the same type; out holds the N outputs one  */
+/* after another (rank q's at out + q * rows).                             */
+/* ---------------------------------------------------------------------- */
+int orc_linear_allreduce_residual(int n, const void* const* w, const void* const* x,
+                                  const void* const* res, size_t rows, size_t kp, int dtype, void* out)
+{
+    if (n < 1 || !w || !x || !res || (rows && !out) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    for (int p = 0; p < n; ++p) if (!w[p] || !x[p] || !res[p]) return -1;
+    for (size_t i = 0; i < rows; ++i) {
+        const double acc = layer_row(n, w, x, i, kp, dtype);
+        for (int q = 0; q < n; ++q) {
+            const double y = acc + (double)widen(res[q], i, dtype);
+            ((uint16_t*)out)[(size_t)q * rows + i] = f64_to_half_once(y, dtype);
+        }
     }
     return 0;
 }

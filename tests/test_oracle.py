@@ -434,6 +434,75 @@ def test_linear_allreduce_matches_float64_matmul(dtype):
     del rng
 
 
+# --------------------------------------------------------------------- linear layer + residual
+def _small_ints(rng, dtype, lo, hi, size):
+    return np.array([value_to_storage(int(v), dtype) for v in rng.integers(lo, hi + 1, size=size)], np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_residual_closed_forms(dtype):
+    """Zero weights leave each rank its own residual; a zero residual gives the
+    layer without one; on small-integer data output q minus output 0 is
+    residual q minus residual 0; (+0) + (-0) is +0."""
+    n, rows, kp = 4, 16, 32
+    rng = np.random.default_rng(11)
+    zero = value_to_storage(0, dtype)
+    ws0 = [np.full(rows * kp, zero, np.uint16) for _ in range(n)]
+    xs = [_small_ints(rng, dtype, -3, 3, kp) for _ in range(n)]
+    res = [_small_ints(rng, dtype, -50, 50, rows) for _ in range(n)]
+    for q, y in enumerate(oracle.linear_allreduce_residual(ws0, xs, res, dtype, rows, kp)):
+        assert np.array_equal(storage_to_float(y, dtype), storage_to_float(res[q], dtype))
+    ws = [_small_ints(rng, dtype, -3, 3, rows * kp) for _ in range(n)]
+    zres = [np.full(rows, zero, np.uint16) for _ in range(n)]
+    plain = oracle.linear_allreduce(ws, xs, dtype, rows, kp)
+    for y in oracle.linear_allreduce_residual(ws, xs, zres, dtype, rows, kp):
+        assert np.array_equal(y, plain)
+    ys = oracle.linear_allreduce_residual(ws, xs, res, dtype, rows, kp)
+    base = storage_to_float(plain, dtype)
+    for q in range(n):
+        assert np.array_equal(storage_to_float(ys[q], dtype), base + storage_to_float(res[q], dtype))
+    negz = [np.full(rows, 0x8000, np.uint16) for _ in range(n)]
+    for y in oracle.linear_allreduce_residual(ws0, xs, negz, dtype, rows, kp):
+        assert np.all(y == 0)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_residual_rounds_once(dtype):
+    """The residual joins the exact sum before the one rounding.  Hand cases
+    where rounding the layer first would leave an exact tie (to even, 1.0):
+      bf16: layer 1 + 2^-30, residual 2^-8 -> 1 + 2^-7 (0x3F81)
+      fp16: layer 1 + 2^-24, residual 2^-11 -> 1 + 2^-10 (0x3C01)"""
+    if dtype == "bf16":
+        w, x, r, want = [0x3F80, 0x3080], [0x3F80, 0x3F80], 0x3B80, 0x3F81   # 1, 2^-30; 2^-8
+    else:
+        w, x, r, want = [0x3C00, 0x0C00], [0x3C00, 0x0C00], 0x1000, 0x3C01   # 1, 2^-12 * 2^-12; 2^-11
+    ys = oracle.linear_allreduce_residual([np.array(w, np.uint16)], [np.array(x, np.uint16)],
+                                          [np.array([r], np.uint16)], dtype, 1, len(w))
+    assert int(ys[0][0]) == want
+    ys = oracle.linear_allreduce_residual([np.array([v | 0x8000 for v in w], np.uint16)], [np.array(x, np.uint16)],
+                                          [np.array([r | 0x8000], np.uint16)], dtype, 1, len(w))
+    assert int(ys[0][0]) == want | 0x8000
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_residual_matches_float64_matmul(dtype):
+    """Against numpy's float64 product of the concatenated shards plus each
+    rank's residual, rounded once by the brute force's generic rounding."""
+    n, rows, kp = 3, 24, 40
+    ws = [W.to_storage(torch.randn(rows * kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    xs = [W.to_storage(torch.randn(kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    res = [W.to_storage(torch.randn(rows).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    a = np.concatenate([storage_to_float(w, dtype).reshape(rows, kp) for w in ws], axis=1)
+    x = np.concatenate([storage_to_float(v, dtype) for v in xs])
+    layer = a @ x
+    ys = oracle.linear_allreduce_residual(ws, xs, res, dtype, rows, kp)
+    for q in range(n):
+        exact = layer + storage_to_float(res[q], dtype).astype(np.float64)
+        ref = np.array([brute.encode(brute.round_ieee(float(v), *brute.FORMATS[dtype]), dtype) for v in exact],
+                       np.uint16)
+        assert np.array_equal(ys[q], ref), q
+
+
 # --------------------------------------------------------------------- MAX / MIN
 @pytest.mark.parametrize("dtype", ALL_DTYPES)
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16])

@@ -56,6 +56,14 @@ MUTANTS = {
     "op_skips_rank_0": ("float acc = widen(in[0], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op",
                         "float acc = widen(in[n - 1], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op"),
     "op_nan_not_canonical_at_one_rank": ("if (isnan(acc)) acc = NAN;   /* canonical", "if (0) acc = NAN;   /* canonical"),
+    "residual_of_rank_0": ("const double y = acc + (double)widen(res[q], i, dtype);",
+                           "const double y = acc + (double)widen(res[0], i, dtype);"),
+    "residual_dropped": ("const double y = acc + (double)widen(res[q], i, dtype);",
+                         "const double y = acc + 0.0 * (double)widen(res[q], i, dtype);"),
+    "residual_after_rounding_the_layer": (
+        "const double y = acc + (double)widen(res[q], i, dtype);",
+        "const double y = (double)(dtype == ORC_FP16 ? orc_f16_to_f32(f64_to_half_once(acc, dtype))"
+        " : orc_bf16_to_f32(f64_to_half_once(acc, dtype))) + (double)widen(res[q], i, dtype);"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
