@@ -351,6 +351,81 @@ int dcc_preload_kernels() {
   return ok ? DCC_OK : DCC_ERR_CUDA;
 }
 
+namespace {
+
+// The fused layer with (residual != nullptr) or without a residual per output
+// rank.  Residual q is rows elements like y; it may be y[q] itself (in place)
+// but must not partially overlap y[q] nor overlap any other output.
+int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
+                  size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+  if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
+  if (rows % 8 || kp % 8) return DCC_ERR_UNSUPPORTED;  // the documented shape rule
+  if (rows == 0 || kp == 0) return DCC_OK;
+  const size_t eb = 2;
+  if (rows > ((size_t)1 << 40) / kp) return DCC_ERR_INVALID_ARG;
+  const size_t wb = rows * kp * eb, xb = kp * eb, yb = rows * eb;
+  for (int r = 0; r < c->n; ++r) {
+    if (!weight[r] || !x[r] || !y[r]) return DCC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(weight[r]) | reinterpret_cast<uintptr_t>(x[r]) |
+         reinterpret_cast<uintptr_t>(y[r])) & 15u)
+      return DCC_ERR_MISALIGNED;
+    const void* ptrs[3] = {weight[r], x[r], y[r]};
+    const size_t lens[3] = {wb, xb, yb};
+    for (int j = 0; j < 3; ++j)
+      if (!in_window(c, r, DCC_BUF_INPUT, ptrs[j], lens[j]) && !in_window(c, r, DCC_BUF_OUTPUT, ptrs[j], lens[j]))
+        return DCC_ERR_NOT_REGISTERED;
+  }
+  for (int r = 0; r < c->n; ++r)
+    for (int p = 0; p < c->n; ++p) {
+      if (overlaps(y[r], yb, weight[p], wb) || overlaps(y[r], yb, x[p], xb)) return DCC_ERR_INVALID_ARG;
+      if (p != r && overlaps(y[r], yb, y[p], yb)) return DCC_ERR_INVALID_ARG;
+    }
+  if (residual) {
+    for (int r = 0; r < c->n; ++r) {
+      if (!residual[r]) return DCC_ERR_INVALID_ARG;
+      if (reinterpret_cast<uintptr_t>(residual[r]) & 15u) return DCC_ERR_MISALIGNED;
+      if (!in_window(c, r, DCC_BUF_INPUT, residual[r], yb) && !in_window(c, r, DCC_BUF_OUTPUT, residual[r], yb))
+        return DCC_ERR_NOT_REGISTERED;
+      for (int p = 0; p < c->n; ++p)
+        if (overlaps(residual[r], yb, y[p], yb) && !(p == r && residual[r] == y[r])) return DCC_ERR_INVALID_ARG;
+    }
+  }
+  int rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  dcc::LinearArgs a{};
+  for (int r = 0; r < c->n; ++r) {
+    a.weight[r] = weight[r];
+    a.x[r] = x[r];
+    a.residual[r] = residual ? residual[r] : nullptr;
+    a.y[r] = y[r];
+  }
+  a.rows = rows;
+  a.kp = kp;
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&dc, &a};
+  if (c->fused_bulk > 0 || (c->fused_bulk < 0 && kp >= kFusedBulkMinKp)) {
+    const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(c->n)
+                                   : dcc::linear_allreduce_bulk_kernel<__half>(c->n);
+    const size_t smem = dcc::fused_bulk_smem_bytes();
+    const size_t items = rows / dcc::kFusedBulkRows / (size_t)c->n + 1;  // 2-row items per rank
+    rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, smem, 1, false);  // one item per CTA
+    if (rc != DCC_OK) return rc;
+    return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl);
+  }
+  const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
+                                 : dcc::linear_allreduce_kernel<__half>(c->n);
+  const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // items per rank
+  rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
+  if (rc != DCC_OK) return rc;
+  return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), 0, c->pdl);
+}
+
+}  // namespace
+
 // ====================================================================== C ABI
 extern "C" {
 
@@ -703,61 +778,16 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
                 c->pdl && !coop);
 }
 
+
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
                          size_t kp, dcc_dtype_t t, dcc_stream_t s) {
-  if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
-  if (c->sticky != DCC_OK) return c->sticky;
-  if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
-  if (rows % 8 || kp % 8) return DCC_ERR_UNSUPPORTED;  // the documented shape rule
-  if (rows == 0 || kp == 0) return DCC_OK;
-  const size_t eb = 2;
-  if (rows > ((size_t)1 << 40) / kp) return DCC_ERR_INVALID_ARG;
-  const size_t wb = rows * kp * eb, xb = kp * eb, yb = rows * eb;
-  for (int r = 0; r < c->n; ++r) {
-    if (!weight[r] || !x[r] || !y[r]) return DCC_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(weight[r]) | reinterpret_cast<uintptr_t>(x[r]) |
-         reinterpret_cast<uintptr_t>(y[r])) & 15u)
-      return DCC_ERR_MISALIGNED;
-    const void* ptrs[3] = {weight[r], x[r], y[r]};
-    const size_t lens[3] = {wb, xb, yb};
-    for (int j = 0; j < 3; ++j)
-      if (!in_window(c, r, DCC_BUF_INPUT, ptrs[j], lens[j]) && !in_window(c, r, DCC_BUF_OUTPUT, ptrs[j], lens[j]))
-        return DCC_ERR_NOT_REGISTERED;
-  }
-  for (int r = 0; r < c->n; ++r)
-    for (int p = 0; p < c->n; ++p) {
-      if (overlaps(y[r], yb, weight[p], wb) || overlaps(y[r], yb, x[p], xb)) return DCC_ERR_INVALID_ARG;
-      if (p != r && overlaps(y[r], yb, y[p], yb)) return DCC_ERR_INVALID_ARG;
-    }
-  int rc = check_channels_all_pairs(c);
-  if (rc != DCC_OK) return rc;
-  DeviceScope ds(c->device);
-  if (!ds.ok()) return DCC_ERR_CUDA;
-  dcc::LinearArgs a{};
-  for (int r = 0; r < c->n; ++r) {
-    a.weight[r] = weight[r];
-    a.x[r] = x[r];
-    a.y[r] = y[r];
-  }
-  a.rows = rows;
-  a.kp = kp;
-  dcc::DevComm dc = dev_view(c);
-  void* kargs[] = {&dc, &a};
-  if (c->fused_bulk > 0 || (c->fused_bulk < 0 && kp >= kFusedBulkMinKp)) {
-    const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(c->n)
-                                   : dcc::linear_allreduce_bulk_kernel<__half>(c->n);
-    const size_t smem = dcc::fused_bulk_smem_bytes();
-    const size_t items = rows / dcc::kFusedBulkRows / (size_t)c->n + 1;  // 2-row items per rank
-    rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, smem, 1, false);  // one item per CTA
-    if (rc != DCC_OK) return rc;
-    return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl);
-  }
-  const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_kernel<__nv_bfloat16>(c->n)
-                                 : dcc::linear_allreduce_kernel<__half>(c->n);
-  const size_t items = rows / dcc::kFusedRows / (size_t)c->n + 1;  // items per rank
-  rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
-  if (rc != DCC_OK) return rc;
-  return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), 0, c->pdl);
+  return linear_launch(c, weight, x, nullptr, y, rows, kp, t, s);
+}
+
+int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual,
+                                  void* const* y, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+  if (!residual) return DCC_ERR_INVALID_ARG;
+  return linear_launch(c, weight, x, residual, y, rows, kp, t, s);
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {

@@ -11,6 +11,10 @@
 //
 //   y_r[i] = R( sum_p  sum_k W_p[i][k] x_p[k] )   for every rank r
 //
+// optionally with a residual per output rank joining the sum before the
+// rounding, y_r[i] = R( ... + res_r[i] ) (the tensor-parallel residual
+// stream update h <- h + layer(h), in place when res_r is y_r).
+//
 // Schedule (two-shot, like k_allreduce_twoshot): rank r's CTAs own shard r of
 // the rows, in items of kFusedRows rows, one item per CTA at a time.  The
 // CTA's warps take the ranks in parallel: warp w gets the item's rows of W_p
@@ -39,9 +43,10 @@ constexpr int kFusedRows = 2;  // output rows per item: one 4-byte packed store 
 constexpr int kFusedVecs = 4;  // 16-byte vectors per lane and row per round
 
 struct LinearArgs {
-  const void* weight[DCC_MAX_RANKS];  // rows x kp, row-major
-  const void* x[DCC_MAX_RANKS];       // kp
-  void* y[DCC_MAX_RANKS];             // rows
+  const void* weight[DCC_MAX_RANKS];    // rows x kp, row-major
+  const void* x[DCC_MAX_RANKS];         // kp
+  const void* residual[DCC_MAX_RANKS];  // rows per output rank, or all null (no residual)
+  void* y[DCC_MAX_RANKS];               // rows
   size_t rows, kp;
   int blocks;
 };
@@ -58,6 +63,25 @@ __device__ __forceinline__ void dot8_acc(float& acc, uint4 w, uint4 x) {
   }
 }
 
+// Puts item v's two rows (fp32 sums y0, y1) into the N outputs: one packed
+// rounding shared by every rank, or with residuals R(y + residual_q) for
+// output q, the residual joining the fp32 sum before the one rounding.  The
+// same thread reads residual q and writes output q, so they may be the same
+// buffer (the in-place residual-stream update).
+template <typename T>
+__device__ __forceinline__ void put_rows(const LinearArgs& a, int n, int lane, size_t v, float y0, float y1) {
+  using L = Lanes<T>;
+  if (a.residual[0] == nullptr) {
+    const uint32_t packed = L::narrow2(y0, y1);
+    for (int q = lane; q < n; q += 32) static_cast<uint32_t*>(a.y[q])[v] = packed;
+  } else {
+    for (int q = lane; q < n; q += 32) {
+      const float2 r = L::widen2(static_cast<const uint32_t*>(a.residual[q])[v]);
+      static_cast<uint32_t*>(a.y[q])[v] = L::narrow2(__fadd_rn(y0, r.x), __fadd_rn(y1, r.y));
+    }
+  }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -67,7 +91,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, LinearArgs a) {
   pdl_prologue();
-  using L = Lanes<T>;
   constexpr int R = kFusedRows, V = kFusedVecs;
   static_assert(R == 2, "the epilogue packs two rows per item");
   const int n = NT > 0 ? NT : dc.n;
@@ -119,8 +142,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
         for (int p = 1; p < n; ++p) acc = __fadd_rn(acc, part_s[p][lane]);
       }
       const float y0 = __shfl_sync(0xffffffffu, acc, 0), y1 = __shfl_sync(0xffffffffu, acc, 1);
-      const uint32_t packed = L::narrow2(y0, y1);
-      for (int q = lane; q < n; q += 32) static_cast<uint32_t*>(a.y[q])[v] = packed;
+      put_rows<T>(a, n, lane, v, y0, y1);
     }
     // kept even after the CTA's last item: skipping it there measured slower
     // on GB300 (32.4 vs 26.2 us at 8 ranks x 8192 rows x kp 1024)

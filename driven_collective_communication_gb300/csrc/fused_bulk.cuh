@@ -2,7 +2,7 @@
 // with its weight stream staged in shared memory by the bulk copy engine
 // (TMA, non-tensor cp.async.bulk), for long rows.
 //
-//   y_r[i] = R( sum_p  sum_k W_p[i][k] x_p[k] )   for every rank r
+//   y_r[i] = R( sum_p  sum_k W_p[i][k] x_p[k] [+ res_r[i]] )   for every rank r
 //
 // A matrix-vector product streams its weights once, so it is bound by how
 // many bytes each SM keeps in flight.  Loads into registers cannot keep
@@ -49,7 +49,6 @@ __host__ __device__ constexpr size_t fused_bulk_smem_bytes() {
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm dc, LinearArgs a) {
   pdl_prologue();
-  using L = Lanes<T>;
   constexpr int RI = kFusedBulkRows, ST = kFusedBulkStages;
   constexpr int ROWB = kFusedBulkChunk * 2;
   constexpr int NW = kFusedThreads / 32, PARTS = NW / RI;
@@ -143,8 +142,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
         }
       }
       const float y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 1);
-      const uint32_t packed = L::narrow2(y0, y1);
-      for (int q = lane; q < n; q += 32) static_cast<uint32_t*>(a.y[q])[v] = packed;
+      put_rows<T>(a, n, lane, v, y0, y1);
     }
     __syncthreads();  // part_s is rewritten by the next item
   }

@@ -95,6 +95,7 @@ _SIGS = {
     "dcc_fifo_push": [_vp, _vp, _vp, _i, _vp],
     "dcc_proxy_state": [_vp, _vp, _i],
     "dcc_linear_allreduce": [_vp, _PP, _PP, _PP, _sz, _sz, _i, _vp],
+    "dcc_linear_allreduce_residual": [_vp, _PP, _PP, _PP, _PP, _sz, _sz, _i, _vp],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -221,6 +222,12 @@ def dcc_allreduce_from_host(comm, host_send, host_recv, dev_send, dev_recv, coun
 def dcc_linear_allreduce(comm, weight, x, y, rows, kp, dtype, stream=None):
     return _check(_lib.dcc_linear_allreduce(comm, _ptrs(weight), _ptrs(x), _ptrs(y), rows, kp,
                                             _dtype(dtype), _stream(stream)), "dcc_linear_allreduce")
+
+
+def dcc_linear_allreduce_residual(comm, weight, x, residual, y, rows, kp, dtype, stream=None):
+    return _check(_lib.dcc_linear_allreduce_residual(comm, _ptrs(weight), _ptrs(x), _ptrs(residual), _ptrs(y),
+                                                     rows, kp, _dtype(dtype), _stream(stream)),
+                  "dcc_linear_allreduce_residual")
 
 
 def dcc_ring_barrier(comm, iters, stream=None):

@@ -216,6 +216,17 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
                          size_t kp, dcc_dtype_t t, dcc_stream_t s);
 
+/* The same layer with a residual per output rank (the tensor-parallel
+ * residual stream, h <- h + layer(h)): y[r][i] = R( sum_p sum_k W_p[i][k]
+ * x_p[k] + residual[r][i] ).  The residual joins the fp32 sum before the one
+ * rounding (the reading taken for the fused epilogue; the pages give none).
+ * residual[r] holds rows elements of t, registered and 16-byte aligned like
+ * y[r]; residual[r] == y[r] updates the residual in place, any other overlap
+ * with an output is rejected.  Shapes, kernels, results on small-integer data
+ * and errors as dcc_linear_allreduce; residual NULL is INVALID_ARG. */
+int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual,
+                                  void* const* y, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s);
+
 /* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
  * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
  * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One

@@ -5,6 +5,8 @@ the oracle bit for bit whatever its internal order.  Random data are held to
 the fp32 dot-product bound: |acc - exact| <= (kp + N) * 2^-24 * sum|w x| before
 one rounding to the output type, i.e. |y - y_oracle| <= 2 (kp + N) 2^-24 S + ulp.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -125,3 +127,129 @@ def test_argument_errors(dcc):
             dcc.dcc_linear_allreduce(h, ws, xs, [ws[0][:rows], ys[1]], rows, kp, "bf16")
         assert e.value.code == dcc.DCC_ERR_INVALID_ARG
         assert comm.check() == dcc.DCC_OK
+
+
+# ------------------------------------------------------------------ residual epilogue
+def run_residual(dcc, ws, xs, res, rows, kp, dtype, inplace):
+    """dcc_linear_allreduce_residual; in place the residual buffers are the outputs.
+    Returns every rank's output as raw storage."""
+    n = len(ws)
+    dw = [w.cuda() for w in ws]
+    dx = [x.cuda() for x in xs]
+    dr = [r.cuda() for r in res]
+    dy = dr if inplace else [torch.full((rows,), float("nan"), dtype=TD[dtype], device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", dw)
+        for r in range(n):
+            comm.register(r, "input", dx[r])
+        comm.register_all("output", dy)
+        if not inplace:
+            comm.register_all("input", dr)
+        dcc.dcc_linear_allreduce_residual(comm.handle, dw, dx, dr, dy, rows, kp, dtype)
+        assert comm.check() == dcc.DCC_OK
+    return [W.to_storage(y) for y in dy]
+
+
+def small_int_case(seed, n, rows, kp, dtype):
+    g = torch.Generator().manual_seed(seed)
+    ws = [torch.randint(-3, 4, (rows * kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randint(-3, 4, (kp,), generator=g).to(TD[dtype]) for _ in range(n)]
+    res = [torch.randint(-100, 101, (rows,), generator=g).to(TD[dtype]) for _ in range(n)]
+    return ws, xs, res
+
+
+def residual_expect(ws, xs, res, dtype, rows, kp):
+    return oracle.linear_allreduce_residual([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                            [W.to_storage(r) for r in res], dtype, rows, kp)
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,rows,kp", [(1, 8, 8), (2, 64, 40), (8, 1032, 1032), (16, 256, 1024),
+                                        (3, 24, 9000), (8, 64, 4096)])
+def test_residual_integer_data_bit_exact(dcc, path, dtype, n, rows, kp, inplace):
+    """Each rank's own residual (they differ) joins the sum before the rounding:
+    exact against the oracle on small-integer data, in and out of place."""
+    ws, xs, res = small_int_case(n * 7 + kp, n, rows, kp, dtype)
+    expect = residual_expect(ws, xs, res, dtype, rows, kp)
+    got = run_residual(dcc, ws, xs, res, rows, kp, dtype, inplace)
+    for q in range(n):
+        assert np.array_equal(got[q], expect[q]), q
+
+
+def test_residual_random_shapes_bit_exact(dcc, monkeypatch):
+    """Thirty seeded random mixes of rank count, rows, kp, dtype, kernel and
+    in / out of place with residuals, small-integer data, exact."""
+    rng = np.random.default_rng(37)
+    for case in range(30):
+        n = int(rng.choice([1, 2, 3, 5, 8, 16]))
+        rows = 8 * int(rng.integers(1, 40))
+        kp = 8 * int(rng.integers(1, 1150))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        inplace = bool(rng.integers(0, 2))
+        monkeypatch.setenv("DCC_FUSED_BULK", str(int(rng.integers(0, 2))))
+        ws, xs, res = small_int_case(2000 + case, n, rows, kp, dtype)
+        expect = residual_expect(ws, xs, res, dtype, rows, kp)
+        got = run_residual(dcc, ws, xs, res, rows, kp, dtype, inplace)
+        for q in range(n):
+            assert np.array_equal(got[q], expect[q]), (case, n, rows, kp, dtype, inplace, q)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_residual_random_data_within_bound(dcc, path, dtype):
+    """Random data: within the fp32 bound of the layer plus the residual term,
+    |y - y_oracle| <= 2 (kp + N + 1) 2^-24 (sum|w x| + |res|) + ulp."""
+    n, rows, kp = 8, 1024, 1024
+    g = torch.Generator().manual_seed(77)
+    ws = [(torch.randn(rows * kp, generator=g) * 0.05).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randn(kp, generator=g).to(TD[dtype]) for _ in range(n)]
+    res = [torch.randn(rows, generator=g).to(TD[dtype]) for _ in range(n)]
+    expect = residual_expect(ws, xs, res, dtype, rows, kp)
+    got = run_residual(dcc, ws, xs, res, rows, kp, dtype, False)
+    s = sum(np.abs(w.double().numpy().reshape(rows, kp)) @ np.abs(x.double().numpy()) for w, x in zip(ws, xs))
+    for q in range(n):
+        gf = W.from_storage(got[q], dtype).double().numpy()
+        ef = W.from_storage(expect[q], dtype).double().numpy()
+        big = np.maximum(np.abs(gf), np.abs(ef))
+        if dtype == "bf16":
+            ulp = np.exp2(np.floor(np.log2(np.maximum(big, 2.0 ** -126))) - 7)
+        else:
+            ulp = np.abs(np.spacing(big.astype(np.float16)).astype(np.float64))
+        bound = 2 * (kp + n + 1) * 2.0 ** -24 * (s + np.abs(res[q].double().numpy())) + ulp
+        assert np.all(np.abs(gf - ef) <= bound), q
+        assert np.mean(got[q] == expect[q]) > 0.98
+
+
+def test_residual_argument_errors(dcc):
+    """Residual overlapping another rank's output or part of its own, not
+    registered, misaligned, or a NULL array: rejected, nothing launched."""
+    n, rows, kp = 2, 16, 16
+    ws = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    xs = [torch.zeros(kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ys = [torch.full((rows + 64,), 5.0, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    rs = [torch.zeros(rows + 64, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    loose = torch.zeros(rows, dtype=torch.bfloat16, device="cuda")
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", ws)
+        comm.register_all("input", xs)
+        comm.register_all("output", ys)
+        comm.register_all("input", rs)
+        comm.register(0, "input", ys[1])  # so that the overlap check, not the window check, decides
+        h = comm.handle
+        y = [t[:rows] for t in ys]
+        cases = [([ys[1][:rows], rs[1][:rows]], dcc.DCC_ERR_INVALID_ARG),     # rank 0's residual is rank 1's output
+                 ([ys[0][8:8 + rows], rs[1][:rows]], dcc.DCC_ERR_INVALID_ARG),  # part of its own output
+                 ([loose, rs[1][:rows]], dcc.DCC_ERR_NOT_REGISTERED),
+                 ([rs[0][1:1 + rows], rs[1][:rows]], dcc.DCC_ERR_MISALIGNED)]
+        for res, code in cases:
+            with pytest.raises(dcc.DccError) as e:
+                dcc.dcc_linear_allreduce_residual(h, ws, xs, res, y, rows, kp, "bf16")
+            assert e.value.code == code
+        P = ctypes.c_void_p * n
+        rc = dcc.raw_call("dcc_linear_allreduce_residual", h, P(*[w.data_ptr() for w in ws]),
+                          P(*[x.data_ptr() for x in xs]), None, P(*[t.data_ptr() for t in y]), rows, kp, 3, None)
+        assert rc == dcc.DCC_ERR_INVALID_ARG
+        assert comm.check() == dcc.DCC_OK
+    torch.cuda.synchronize()
+    for t in ys:
+        assert torch.all(t == 5.0)
