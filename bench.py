@@ -723,13 +723,17 @@ def other_workloads(dcc, dev, stream):
         yf = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         part = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         ysep = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        hres = [torch.zeros(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]  # residual stream
         with dcc.Comm(8) as lc:
             lc.register_all("input", wts)
             lc.register_all("input", xin)
             lc.register_all("output", yf)
             lc.register_all("input", part)
             lc.register_all("output", ysep)
+            lc.register_all("output", hres)
             fused = lambda: dcc.dcc_linear_allreduce(lc.handle, wts, xin, yf, rows, kp, "bf16", stream)  # noqa
+            fused_res = lambda: dcc.dcc_linear_allreduce_residual(  # noqa: E731  h <- h + layer, in place
+                lc.handle, wts, xin, hres, hres, rows, kp, "bf16", stream)
             ar = dcc.prepare_allreduce(lc.handle, part, ysep, rows, "bf16", "auto", stream)
 
             def unfused():
@@ -738,7 +742,8 @@ def other_workloads(dcc, dev, stream):
                         torch.matmul(wts[r], xin[r], out=part[r])
                 ar()
             res = {}
-            for name, fn in (("fused", fused), ("gemv_then_allreduce", unfused)):
+            for name, fn in (("fused", fused), ("fused_residual_inplace", fused_res),
+                             ("gemv_then_allreduce", unfused)):
                 for _ in range(5):
                     fn()
                 g2 = torch.cuda.CUDAGraph()
@@ -759,7 +764,7 @@ def other_workloads(dcc, dev, stream):
                 res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
             assert lc.check(stream) == dcc.DCC_OK
         out["linear_allreduce_bf16_n8_rows8192_kp%d" % kp] = res
-        del wts, xin, yf, part, ysep
+        del wts, xin, yf, part, ysep, hres
     with dcc.Comm(8, connect="ring") as ring:
         ring.ring_barrier(100, stream)
         e0 = torch.cuda.Event(enable_timing=True)
