@@ -63,22 +63,31 @@ __device__ __forceinline__ void dot8_acc(float& acc, uint4 w, uint4 x) {
   }
 }
 
+static_assert(DCC_MAX_RANKS <= 32, "lane q of warp 0 serves output rank q");
+
+// Lane q < N of warp 0: residual q's two rows of item v (0 without
+// residuals).  Loaded when the item starts, so that the load overlaps the
+// weight stream instead of adding a memory round trip to the epilogue.
+__device__ __forceinline__ uint32_t load_residual(const LinearArgs& a, int n, int lane, size_t v) {
+  return a.residual[0] != nullptr && lane < n ? static_cast<const uint32_t*>(a.residual[lane])[v] : 0u;
+}
+
 // Puts item v's two rows (fp32 sums y0, y1) into the N outputs: one packed
 // rounding shared by every rank, or with residuals R(y + residual_q) for
-// output q, the residual joining the fp32 sum before the one rounding.  The
-// same thread reads residual q and writes output q, so they may be the same
-// buffer (the in-place residual-stream update).
+// output q (res: the word load_residual returned), the residual joining the
+// fp32 sum before the one rounding.  The same thread reads residual q and
+// writes output q, so they may be the same buffer (the in-place
+// residual-stream update).
 template <typename T>
-__device__ __forceinline__ void put_rows(const LinearArgs& a, int n, int lane, size_t v, float y0, float y1) {
+__device__ __forceinline__ void put_rows(const LinearArgs& a, int n, int lane, size_t v, float y0, float y1,
+                                         uint32_t res) {
   using L = Lanes<T>;
   if (a.residual[0] == nullptr) {
     const uint32_t packed = L::narrow2(y0, y1);
-    for (int q = lane; q < n; q += 32) static_cast<uint32_t*>(a.y[q])[v] = packed;
-  } else {
-    for (int q = lane; q < n; q += 32) {
-      const float2 r = L::widen2(static_cast<const uint32_t*>(a.residual[q])[v]);
-      static_cast<uint32_t*>(a.y[q])[v] = L::narrow2(__fadd_rn(y0, r.x), __fadd_rn(y1, r.y));
-    }
+    if (lane < n) static_cast<uint32_t*>(a.y[lane])[v] = packed;
+  } else if (lane < n) {
+    const float2 r = L::widen2(res);
+    static_cast<uint32_t*>(a.y[lane])[v] = L::narrow2(__fadd_rn(y0, r.x), __fadd_rn(y1, r.y));
   }
 }
 
@@ -103,6 +112,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
   size_t s0, s1;
   shard_vecs(items, n, rank, s0, s1);
   for (size_t v = s0 + blk; v < s1; v += B) {
+    const uint32_t res = warp == 0 ? load_residual(a, n, lane, v) : 0u;
     // warp w computes the partial products of ranks w, w + nwarps, ... for
     // the item's rows; the ranks' partials meet in shared memory
     for (int p = warp; p < n; p += nwarps) {
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
         for (int p = 1; p < n; ++p) acc = __fadd_rn(acc, part_s[p][lane]);
       }
       const float y0 = __shfl_sync(0xffffffffu, acc, 0), y1 = __shfl_sync(0xffffffffu, acc, 1);
-      put_rows<T>(a, n, lane, v, y0, y1);
+      put_rows<T>(a, n, lane, v, y0, y1, res);
     }
     // kept even after the CTA's last item: skipping it there measured slower
     // on GB300 (32.4 vs 26.2 us at 8 ranks x 8192 rows x kp 1024)

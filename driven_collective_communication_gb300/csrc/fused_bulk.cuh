@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
     for (int u = 0; u < ST; ++u) issue_next(iv, it);
 
   for (size_t v = s0 + (size_t)blk; v < s1 && !failed; v += (size_t)B) {
+    const uint32_t res = warp == 0 ? load_residual(a, n, lane, v) : 0u;
     float acc = 0.0f;
     for (int t = 0; t < ntiles; ++t, ++g) {
       const int u = (int)(g % ST), p = t / nch, c = t % nch;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
         }
       }
       const float y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 1);
-      put_rows<T>(a, n, lane, v, y0, y1);
+      put_rows<T>(a, n, lane, v, y0, y1, res);
     }
     __syncthreads();  // part_s is rewritten by the next item
   }
