@@ -692,9 +692,18 @@ def other_workloads(dcc, dev, stream):
         for _ in range(LARGE_WARMUP):
             fn()
         per, _ = time_launches(fn, LARGE_STEPS, stream)
+        b2b_ms = time_queued_span(fn, 50, stream) / 1e3
         ms = statistics.median(per)
         out[name] = {"ms": round(ms, 4), **spread(per), "hbm_gbs": round(nbytes / ms / 1e6, 1),
-                     "algorithmic_bytes": nbytes}
+                     "algorithmic_bytes": nbytes, "back_to_back_ms": round(b2b_ms, 4),
+                     "back_to_back_hbm_gbs": round(nbytes / b2b_ms / 1e6, 1)}
+    # the two halves as one stream-ordered pair (RS then AG of its output), back to back
+    def rs_ag():
+        dcc.dcc_reduce_scatter(comm.handle, xs, rs, m, "fp16", stream)
+        dcc.dcc_allgather(comm.handle, rs, ag, m, "fp16", stream)
+    b2b_ms = time_queued_span(rs_ag, 50, stream) / 1e3
+    out["c5_reduce_scatter_then_allgather_back_to_back"] = {
+        "ms": round(b2b_ms, 4), "hbm_gbs": round(2 * 9 * w.bytes_per_rank / b2b_ms / 1e6, 1)}
     assert comm.check(stream) == dcc.DCC_OK
     comm.close()
     # the same AllGather through PortChannels: the host proxy drives copy engines
