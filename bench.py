@@ -570,7 +570,8 @@ def other_workloads(dcc, dev, stream):
             step()
         per, _ = time_launches(step, LARGE_STEPS, stream)
         ms = statistics.median(per)
-        out["c4_bf16_" + op] = {"ms": round(ms, 4), **spread(per), "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
+        out["c4_bf16_" + op] = {"ms": round(ms, 4), **spread(per),
+                                "hbm_gbs_2NS": round(2 * 8 * w.bytes_per_rank / ms / 1e6, 1)}
     # the optional entry barrier: its cost on the headline size (one co-resident wave)
     dcc.dcc_set_entry_barrier(comm.handle, True)
     step = dcc.prepare_allreduce(comm.handle, xs, ys, w.count, "bf16", "two_shot", stream)

@@ -82,6 +82,11 @@ const void* reduce_kernel_for(dcc_dtype_t t, int kind, int n) {
   }
 }
 
+template <typename T>
+const void* op_kernel_of(bool mx, int kind, int n) {
+  return mx ? dcc::reduce_op_kernel<T, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<T, dcc::kOpMin>(kind, n);
+}
+
 // Kernel of `kind` for reduction op (DCC_OP_SUM / MAX / MIN); MAX and MIN
 // exist for the one-shot, two-shot push and ReduceScatter kinds only.
 const void* op_kernel_for(dcc_dtype_t t, int op, int kind, int n) {
@@ -89,15 +94,10 @@ const void* op_kernel_for(dcc_dtype_t t, int op, int kind, int n) {
   const bool mx = op == DCC_OP_MAX;
   if (!mx && op != DCC_OP_MIN) return nullptr;
   switch (t) {
-    case DCC_INT32:
-      return mx ? dcc::reduce_op_kernel<int32_t, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<int32_t, dcc::kOpMin>(kind, n);
-    case DCC_FP32:
-      return mx ? dcc::reduce_op_kernel<float, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<float, dcc::kOpMin>(kind, n);
-    case DCC_FP16:
-      return mx ? dcc::reduce_op_kernel<__half, dcc::kOpMax>(kind, n) : dcc::reduce_op_kernel<__half, dcc::kOpMin>(kind, n);
-    case DCC_BF16:
-      return mx ? dcc::reduce_op_kernel<__nv_bfloat16, dcc::kOpMax>(kind, n)
-                : dcc::reduce_op_kernel<__nv_bfloat16, dcc::kOpMin>(kind, n);
+    case DCC_INT32: return op_kernel_of<int32_t>(mx, kind, n);
+    case DCC_FP32: return op_kernel_of<float>(mx, kind, n);
+    case DCC_FP16: return op_kernel_of<__half>(mx, kind, n);
+    case DCC_BF16: return op_kernel_of<__nv_bfloat16>(mx, kind, n);
     default: return nullptr;
   }
 }
@@ -346,7 +346,8 @@ int dcc_preload_kernels() {
           load(dcc::allgather_bulk_kernel(n));
   for (int n : ns)
     ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n)) &&
-          load(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_bulk_kernel<__half>(n));
+          load(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) &&
+          load(dcc::linear_allreduce_bulk_kernel<__half>(n));
   ok &= load(dcc::ring_barrier_kernel()) && load(dcc::channel_put_kernel()) && load(dcc::channel_get_kernel());
   return ok ? DCC_OK : DCC_ERR_CUDA;
 }
