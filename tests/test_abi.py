@@ -47,6 +47,15 @@ def test_library_exports_every_declared_symbol(dcc):
         assert getattr(lib, f) is not None
 
 
+def test_every_exported_symbol_is_declared(dcc):
+    """The boundary is exactly the header: no dcc_* entry point is exported
+    without a declaration (and its documentation) in include/dcc.h."""
+    out = subprocess.run(["nm", "-D", "--defined-only", dcc.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (dcc_\w+)$", out, flags=re.M))
+    assert exported <= set(declared_functions()), sorted(exported - set(declared_functions()))
+
+
 def test_sm103a_code_only(dcc):
     """The library carries sm_103a device code (listed by the toolkit's cuobjdump -lelf)."""
     r = subprocess.run(["cuobjdump", "-lelf", dcc.LIB_PATH], capture_output=True, text=True)
