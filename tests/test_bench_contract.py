@@ -26,6 +26,7 @@ def _check(line, n):
     assert line["config"]["workload"] == "allreduce_bf16_n8_256MiB"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert isinstance(cb.get("cpu_model"), str) and cb["cpu_model"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
@@ -46,3 +47,11 @@ def test_reference_arm_two_ranks_rank0_only():
                   "--gpus", "2", "--steps", "3", "--warmup", "3", "--ref-elems", "65536"], env=env)
     assert len(lines) == 1
     _check(lines[0], 2)
+
+
+def test_timing_helpers_on_the_host():
+    """The pure helpers of the bench: min / mean beside the median, and the CPU model."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.spread([3.0, 1.0, 2.0]) == {"min_ms": 1.0, "mean_ms": 2.0}
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
