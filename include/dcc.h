@@ -39,6 +39,13 @@
  *    on one communicator (issue them on one stream, or use one communicator
  *    per stream).  Kernels that never wait (out-of-place ONE_SHOT, TWO_SHOT,
  *    ReduceScatter, AllGather, the fused linear layer) may overlap freely.
+ *  - Stream order with programmatic dependent launch: the kernels that never
+ *    wait launch so that they may begin while the previous kernel on the
+ *    stream finishes, and wait on the device for it to complete before they
+ *    touch memory (dcc_set_pdl); the order a stream gives is kept either way.
+ *  - Reductions: the sum everywhere; MAX and MIN through dcc_allreduce_op /
+ *    dcc_reduce_scatter_op; the fused layer optionally adds a residual per
+ *    rank (dcc_linear_allreduce_residual).
  */
 #ifndef DCC_H
 #define DCC_H
