@@ -42,7 +42,10 @@ inline bool env_flag(const char* name) {
 // bf16 1.48/1.68 at 8 KiB, 1.60/1.72 at 32 KiB, even at 64 KiB, two-shot ahead
 // from 128 KiB (2.09/1.85); 16 ranks 2.03/2.22 at 32 KiB, 2.50/2.26 at 64 KiB.
 // With 2 or 4 ranks the two are level (within 0.05 us) up to 64 KiB and
-// two-shot is ahead from there, so one-shot never pays: threshold 0.
+// two-shot is ahead from there, so one-shot never pays: threshold 0.  The
+// threshold is in bytes and the same for every dtype: at 8 ranks fp32, int32,
+// fp16 and bf16 all have one-shot leading or level up to 32 KiB and two-shot
+// ahead from 128 KiB (e.g. fp32 1.28/1.44 at 32 KiB, 1.88/1.58 at 128 KiB).
 constexpr size_t kDefaultOneShotMaxBytes = 32 * 1024;
 constexpr int kOneShotMinRanks = 5;
 inline size_t default_one_shot_max(int n_ranks) {
