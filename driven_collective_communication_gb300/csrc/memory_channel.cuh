@@ -58,8 +58,6 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
-// 16-byte vector accesses.  Peer data that another CTA wrote in this kernel is
-// read at L2 (ld.global.cg) so that no stale L1 line can be returned.
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialization may begin launching while the kernel before it on the stream
 // is still finishing; griddepcontrol.wait then blocks until that kernel has
@@ -72,6 +70,8 @@ __device__ __forceinline__ void pdl_prologue() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 16-byte vector accesses.  Peer data that another CTA wrote in this kernel is
+// read at L2 (ld.global.cg) so that no stale L1 line can be returned.
 __device__ __forceinline__ uint4 ld_vec(const uint4* p) { return *p; }
 __device__ __forceinline__ uint4 ld_vec_l2(const uint4* p) { return __ldcg(p); }
 __device__ __forceinline__ void st_vec(uint4* p, uint4 v) { *p = v; }
