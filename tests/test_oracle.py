@@ -504,6 +504,27 @@ def test_linear_residual_matches_float64_matmul(dtype):
 
 
 # --------------------------------------------------------------------- MAX / MIN
+def test_golden_max_min():
+    """Hand-derived MAX / MIN cases (tests/golden/max_min_cases.txt, IEEE 754-2019
+    maximum / minimum): signed zeros both ways, NaN in any position and at one
+    rank (canonical quiet NaN), infinities against the largest finite values,
+    subnormals, several ranks, signed int32."""
+    n = 0
+    for line in _golden_lines("max_min_cases.txt"):
+        dtype, op, vals, want = line.split()[:4]
+        bits = [int(v, 16) for v in vals.split(",")]
+        if dtype in ("fp32", "int32"):
+            raw = [np.array([b], np.uint32) for b in bits]
+            xs = [r.view(np.float32) if dtype == "fp32" else r.view(np.int32) for r in raw]
+            got = int(np.asarray(oracle.allreduce_op(xs, dtype, op)).view(np.uint32)[0])
+        else:
+            xs = [np.array([b], np.uint16) for b in bits]
+            got = int(np.asarray(oracle.allreduce_op(xs, dtype, op))[0])
+        assert got == int(want, 16), line
+        n += 1
+    assert n >= 30
+
+
 @pytest.mark.parametrize("dtype", ALL_DTYPES)
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
 def test_max_min_closed_forms(dtype, n):
