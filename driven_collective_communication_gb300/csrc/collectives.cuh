@@ -84,11 +84,7 @@ struct HalfLanes {
   struct Acc { float v[8]; };
   using S = uint16_t;  // raw storage bits
   using SAcc = float;
-  __device__ static float2 widen2(uint32_t w) {
-    H2 h;
-    memcpy(&h, &w, 4);
-    return Ops::to_float2(h);
-  }
+  __device__ static float2 widen2(uint32_t w) { return Ops::widen2(w); }
   __device__ static uint32_t narrow2(float lo, float hi) {
     H2 h = Ops::from_floats(lo, hi);
     uint32_t w;
@@ -122,12 +118,20 @@ struct HalfLanes {
   __device__ static S spack(SAcc a) { return (uint16_t)(narrow2(a, 0.0f) & 0xFFFFu); }
 };
 
+// bf16 is the upper half of binary32, so widening places the 16 bits there
+// (two integer operations, exact for every pattern); fp16 converts.
 struct Bf16Ops {
-  __device__ static float2 to_float2(__nv_bfloat162 h) { return __bfloat1622float2(h); }
+  __device__ static float2 widen2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
   __device__ static __nv_bfloat162 from_floats(float lo, float hi) { return __floats2bfloat162_rn(lo, hi); }
 };
 struct F16Ops {
-  __device__ static float2 to_float2(__half2 h) { return __half22float2(h); }
+  __device__ static float2 widen2(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+  }
   __device__ static __half2 from_floats(float lo, float hi) { return __floats2half2_rn(lo, hi); }
 };
 
