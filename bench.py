@@ -361,8 +361,46 @@ def run_ours(args, dist):
                                "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
                                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s",
                                                  "cores": 1, "sample": sample1}}
+        out["crossover_n8"] = crossover_sweep(dcc, dev, stream)[8]
+        # compact figures last, so that a reader keeping only the end of the line has them
+        out["summary"] = summary(dcc, out)
+        out["latency_16KiB_us"] = latency_16k(dcc, out)
     comm.close()
     return out
+
+
+def latency_16k(dcc, out):
+    """The metric's latency half: 8 ranks x 16 KiB bf16 (1 token x 8192) under AUTO."""
+    row = next(r for r in out["sweep_c3"] if r["tokens"] == 1)
+    algo = row["auto_algo"]
+    m = row[algo]
+    return {"algo": algo, "p50_event": m["p50_us"], "min_event": m["min_us"],
+            "back_to_back": m["back_to_back_us"], "graph": m["graph_us"],
+            "host_us_per_call": m["host_us_per_call"],
+            "graph_node_floor": out["graph_node_floor_us"],
+            "eager_floor_p50_event": out["eager_launch_floor"]["event_bracketed_p50_us"],
+            "eager_floor_back_to_back": out["eager_launch_floor"]["back_to_back_us"]}
+
+
+def summary(dcc, out):
+    """Short figures of the extras (the detail is in the keys before)."""
+    from driven_collective_communication_gb300 import build
+    o = out["other"]
+    table = build.load_auto_table()
+    cross = {t: v["one_shot_max_bytes"] for t, v in out["crossover_n8"].items()}
+    return {
+        "crossover_n8_bytes": cross,
+        "crossover_n8_matches_compiled_table": all(table[8][t] == b for t, b in cross.items()),
+        "c2_int32_inplace_ms": {"one_shot": o["c2_int32_inplace_one_shot"]["ms"],
+                                "two_shot": o["c2_int32_inplace_two_shot"]["ms"]},
+        "c2_one_shot_roofline_frac": round(o["c2_int32_inplace_one_shot"]["hbm_gbs_2NS"]
+                                           / measured_peaks()[0], 3),
+        "c5_rs_ag_ms": [o["c5_reduce_scatter"]["ms"], o["c5_allgather"]["ms"]],
+        "ring_barrier_per_hop_us": o["c5_ring_barrier"]["per_hop_us"],
+        "fused_kp1024_us": o["linear_allreduce_bf16_n8_rows8192_kp1024"]["fused_us"],
+        "fused_kp1024_weight_frac": round(o["linear_allreduce_bf16_n8_rows8192_kp1024"]["fused_weight_gbs"]
+                                          / measured_peaks()[0], 3),
+    }
 
 
 def e2e_host(dcc, comm, xs, ys, w, args, stream, dist):
@@ -454,6 +492,106 @@ def graph_node_floor(stream, reps=100):
     return round(e0.elapsed_time(e1) * 1e3 / (10 * reps), 3)
 
 
+def graph_us(step, stream, reps=100, replays=10):
+    """Device time per call of `step` inside a CUDA graph of `reps` calls,
+    replayed `replays` times after one untimed replay (steady state)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            step()
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (replays * reps)
+
+
+CROSSOVER_SIZES = tuple(k << 10 for k in (4, 8, 16, 32, 64, 128, 256))
+DTYPE_RECIPES = {"int32": W.C2, "fp32": W.C1, "fp16": W.C5, "bf16": W.C4}
+
+
+def crossover_rule(sizes, t_one, t_two):
+    """Largest measured size s with one-shot no slower than two-shot at every
+    measured size up to s; 0 if two-shot is faster at the smallest size."""
+    best = 0
+    for s, a, b in zip(sizes, t_one, t_two):
+        if a > b:
+            break
+        best = s
+    return best
+
+
+def crossover_sweep(dcc, dev, stream, ranks=(8,), dtypes=("int32", "fp32", "fp16", "bf16"),
+                    sizes=CROSSOVER_SIZES, repeats=3):
+    """Out-of-place AllReduce, one-shot vs two-shot, CUDA-graph-amortised us per
+    call (median of `repeats` graphs) at each size, per rank count and dtype;
+    returns {n: {dtype: {"sizes", "one_shot_us", "two_shot_us", "one_shot_max_bytes"}}}."""
+    res = {}
+    for n in ranks:
+        res[n] = {}
+        for dtype in dtypes:
+            eb = W.ELEM_BYTES[dtype]
+            w = W.with_count(DTYPE_RECIPES[dtype], max(sizes) // eb, n_ranks=n)
+            with torch.cuda.stream(stream):
+                xs = W.rank_inputs(w, device=dev)
+                ys = [torch.empty_like(x) for x in xs]
+            torch.cuda.synchronize()
+            t = {"one_shot": [], "two_shot": []}
+            with dcc.Comm(n) as c:
+                c.register_all("input", xs)
+                c.register_all("output", ys)
+                for size in sizes:
+                    count = size // eb
+                    for algo in ("one_shot", "two_shot"):
+                        step = dcc.prepare_allreduce(c.handle, xs, ys, count, dtype, algo, stream)
+                        for _ in range(20):
+                            step()
+                        t[algo].append(statistics.median(graph_us(step, stream) for _ in range(repeats)))
+                assert c.check(stream) == dcc.DCC_OK
+            res[n][dtype] = {"sizes": list(sizes),
+                             "one_shot_us": [round(v, 3) for v in t["one_shot"]],
+                             "two_shot_us": [round(v, 3) for v in t["two_shot"]],
+                             "one_shot_max_bytes": crossover_rule(sizes, t["one_shot"], t["two_shot"])}
+            del xs, ys
+    return res
+
+
+def write_auto_table(args):
+    """Measure the crossover for every rank count 2..16 and dtype and write the
+    tuning JSON that the library build compiles in (1 rank: no choice, 0)."""
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    sweep = crossover_sweep(dcc, dev, stream, ranks=tuple(range(2, 17)))
+    table = {"1": {t: 0 for t in build.DTYPE_ORDER}}
+    for n, per in sweep.items():
+        table[str(n)] = {t: per[t]["one_shot_max_bytes"] for t in build.DTYPE_ORDER}
+    props = torch.cuda.get_device_properties(dev)
+    doc = {
+        "what": "largest out-of-place AllReduce message, in bytes per rank, that DCC_ALGO_AUTO runs "
+                "one-shot (above it: two-shot), per rank count and element type",
+        "rule": "one-shot up to the largest measured size s such that one-shot took no longer than "
+                "two-shot at every measured size up to s (CUDA-graph-amortised time per AllReduce, "
+                "median of repeats); 0 when two-shot is faster already at the smallest size",
+        "source": "python bench.py --write-auto-table on %s (%d SMs), %s" % (
+            props.name, props.multi_processor_count, time.strftime("%Y-%m-%d")),
+        "one_shot_max_bytes": table,
+        "timings_us": {str(n): per for n, per in sweep.items()},
+    }
+    with open(args.write_auto_table, "w") as f:
+        json.dump(doc, f, indent=1)
+    print(json.dumps({"auto_table": args.write_auto_table,
+                      "one_shot_max_bytes": {n: table[n] for n in sorted(table, key=int)}}))
+
+
 def sweep_c3(dcc, dev, stream):
     """Decode-shaped sizes, per algorithm: per-launch p50 / min / mean (CUDA
     events, launches queued ahead of the device so the host's submission time
@@ -474,7 +612,8 @@ def sweep_c3(dcc, dev, stream):
         # a working set (2 N S) that fits in L2 is a latency case, not an HBM-roofline one
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         row = {"tokens": tokens, "bytes_per_rank": w.bytes_per_rank,
-               "working_set_in_l2": 2 * 8 * w.bytes_per_rank <= l2, "l2_bytes": l2}
+               "working_set_in_l2": 2 * 8 * w.bytes_per_rank <= l2, "l2_bytes": l2,
+               "auto_algo": dcc.dcc_select_algo(h, w.count, "bf16")}
         for algo in ("one_shot", "two_shot"):
             step = dcc.prepare_allreduce(h, xs, ys, w.count, "bf16", algo, stream)
             for _ in range(50):
@@ -491,48 +630,20 @@ def sweep_c3(dcc, dev, stream):
                 step()
             host_us = (time.perf_counter() - t) * 1e3
             stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            reps = 100
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(reps):
-                    step()
-            with torch.cuda.stream(stream):  # replay() launches on the current stream
-                g.replay()
-                stream.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(10):
-                    g.replay()
-                e1.record(stream)
-            e1.synchronize()
-            graph_us = e0.elapsed_time(e1) * 1e3 / (10 * reps)
+            g_us = graph_us(step, stream)
             row[algo] = {"p50_us": round(p50, 2), "min_us": round(p_min, 2), "mean_us": round(p_mean, 2),
                          "queued_ahead": bool(queued_ok),
                          "host_paced_p50_us": round(statistics.median(eager) * 1e3, 2),
                          "back_to_back_us": round(span_us, 2),
                          "host_us_per_call": round(host_us, 2),
-                         "graph_us": round(graph_us, 2),
-                         "algbw_gbs_graph": round(w.bytes_per_rank / (graph_us * 1e-6) / GB, 2)}
+                         "graph_us": round(g_us, 2),
+                         "algbw_gbs_graph": round(w.bytes_per_rank / (g_us * 1e-6) / GB, 2)}
         if w.bytes_per_rank <= dcc.DCC_LL_MAX_BYTES:  # in place: barrier one-shot vs LL
             for algo in ("one_shot", "one_shot_ll"):
                 step = dcc.prepare_allreduce(h, xs, xs, w.count, "bf16", algo, stream)
                 for _ in range(20):
                     step()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for _ in range(100):
-                        step()
-                with torch.cuda.stream(stream):
-                    g.replay()
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    for _ in range(10):
-                        g.replay()
-                    e1.record(stream)
-                e1.synchronize()
-                row[algo + "_inplace"] = {"graph_us": round(e0.elapsed_time(e1) * 1e3 / 1000, 2)}
+                row[algo + "_inplace"] = {"graph_us": round(graph_us(step, stream), 2)}
         assert comm.check(stream) == dcc.DCC_OK
         comm.close()
         res.append(row)
@@ -919,11 +1030,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-elems", type=int, default=1 << 24)
     ap.add_argument("--ref-elems", type=int, default=1 << 22)
+    ap.add_argument("--write-auto-table", default=None, metavar="PATH",
+                    help="measure the one-shot/two-shot crossover for 2..16 ranks and write the tuning JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.profile_case:
         run_profile_case(args)
+        return
+    if args.write_auto_table:
+        write_auto_table(args)
         return
     dist = Dist()
     try:

@@ -12,6 +12,7 @@
 
 #include "dcc.h"
 #include "dcc_internal.h"
+#include "dcc_tuning.h"
 
 struct ProxyState;  // proxy.cu
 struct dcc_comm;
@@ -37,19 +38,12 @@ inline bool env_flag(const char* name) {
   return v && *v && std::strcmp(v, "0") != 0;
 }
 
-// Messages at or below this many bytes per rank run one-shot under AUTO.
-// Measured on GB300, CUDA-graph-amortised, one-shot vs two-shot (us): 8 ranks
-// bf16 1.48/1.68 at 8 KiB, 1.60/1.72 at 32 KiB, even at 64 KiB, two-shot ahead
-// from 128 KiB (2.09/1.85); 16 ranks 2.03/2.22 at 32 KiB, 2.50/2.26 at 64 KiB.
-// With 2 or 4 ranks the two are level (within 0.05 us) up to 64 KiB and
-// two-shot is ahead from there, so one-shot never pays: threshold 0.  The
-// threshold is in bytes and the same for every dtype: at 8 ranks fp32, int32,
-// fp16 and bf16 all have one-shot leading or level up to 32 KiB and two-shot
-// ahead from 128 KiB (e.g. fp32 1.28/1.44 at 32 KiB, 1.88/1.58 at 128 KiB).
-constexpr size_t kDefaultOneShotMaxBytes = 32 * 1024;
-constexpr int kOneShotMinRanks = 5;
-inline size_t default_one_shot_max(int n_ranks) {
-  return n_ranks >= kOneShotMinRanks ? kDefaultOneShotMaxBytes : 0;
+// Messages at or below this many bytes per rank run one-shot under AUTO, by
+// rank count and dtype: the measured crossover table (the JSON file under
+// tuning/, turned into dcc_tuning.h by the build).
+inline size_t default_one_shot_max(int n_ranks, dcc_dtype_t t) {
+  if (n_ranks < 1 || n_ranks > DCC_MAX_RANKS || (int)t < 0 || (int)t > 3) return 0;
+  return (size_t)kOneShotMaxTable[n_ranks][(int)t];
 }
 
 // Threads per CTA of the thread-copy kernels, by work (16-byte vectors per
@@ -92,7 +86,6 @@ struct dcc_comm {
   dcc::DevComm dev{};
   int blocks_override = 0;
   int threads_override = 0;  // threads per CTA of the thread-copy kernels (0 = by size)
-  bool cooperative = true;   // DCC_COOPERATIVE=0: plain launches (diagnostic only)
   size_t one_shot_max[4] = {};  // set from the rank count at creation
   int forced_algo = -1;  // DCC_ALGO environment override of AUTO
   // AUTO: messages of at least bulk_min_bytes per rank run large_algo

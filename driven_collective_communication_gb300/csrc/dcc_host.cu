@@ -310,7 +310,33 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
   // one another (out-of-place one-shot, two-shot push, bulk two-shot)
   const bool pdl = c->pdl && !sh.cooperative &&
                    (algo == DCC_ALGO_ONE_SHOT || algo == DCC_ALGO_TWO_SHOT || algo == DCC_ALGO_TWO_SHOT_BULK);
-  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative && c->cooperative, kargs, s, sh.smem, pdl);
+  return launch(sh.fn, sh.blocks * c->n, sh.threads, sh.cooperative, kargs, s, sh.smem, pdl);
+}
+
+}  // namespace
+
+namespace {
+
+// Calls visit(fn) for every kernel of the library's collectives, fused layer
+// and MemoryChannel primitives; stops at the first false.
+template <typename F>
+bool visit_kernels(F&& visit) {
+  const dcc_dtype_t types[] = {DCC_INT32, DCC_FP32, DCC_FP16, DCC_BF16};
+  const int ns[] = {1, 2, 3, 4, 5, 6, 7, 8, 16, 9};  // 9: the runtime-N instances
+  auto v = [&](const void* fn) { return !fn || visit(fn); };
+  for (dcc_dtype_t t : types)
+    for (int n : ns)
+      for (int kind = 0; kind < dcc::kNumKernelKinds; ++kind)
+        if (!v(reduce_kernel_for(t, kind, n)) || !v(op_kernel_for(t, DCC_OP_MAX, kind, n)) ||
+            !v(op_kernel_for(t, DCC_OP_MIN, kind, n)))
+          return false;
+  for (int n : ns)
+    if (!v(dcc::allgather_kernel(n, false)) || !v(dcc::allgather_kernel(n, true)) ||
+        !v(dcc::allgather_bulk_kernel(n)) || !v(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) ||
+        !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
+        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)))
+      return false;
+  return v(dcc::ring_barrier_kernel()) && v(dcc::channel_put_kernel()) && v(dcc::channel_get_kernel());
 }
 
 }  // namespace
@@ -324,31 +350,14 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
 int dcc_preload_kernels() {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  const dcc_dtype_t types[] = {DCC_INT32, DCC_FP32, DCC_FP16, DCC_BF16};
-  const int ns[] = {1, 2, 3, 4, 5, 6, 7, 8, 16, 9};  // 9: the runtime-N instances
   cudaFuncAttributes attr;
-  auto load = [&](const void* fn) {
-    if (fn && cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+  const bool ok = visit_kernels([&](const void* fn) {
+    if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
     return true;
-  };
-  bool ok = true;
-  for (dcc_dtype_t t : types)
-    for (int n : ns)
-      for (int kind = 0; kind < dcc::kNumKernelKinds; ++kind) {
-        ok &= load(reduce_kernel_for(t, kind, n));
-        ok &= load(op_kernel_for(t, DCC_OP_MAX, kind, n)) && load(op_kernel_for(t, DCC_OP_MIN, kind, n));
-      }
-  for (int n : ns)
-    ok &= load(dcc::allgather_kernel(n, false)) && load(dcc::allgather_kernel(n, true)) &&
-          load(dcc::allgather_bulk_kernel(n));
-  for (int n : ns)
-    ok &= load(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) && load(dcc::linear_allreduce_kernel<__half>(n)) &&
-          load(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) &&
-          load(dcc::linear_allreduce_bulk_kernel<__half>(n));
-  ok &= load(dcc::ring_barrier_kernel()) && load(dcc::channel_put_kernel()) && load(dcc::channel_get_kernel());
+  });
   return ok ? DCC_OK : DCC_ERR_CUDA;
 }
 
@@ -445,7 +454,27 @@ const char* dcc_error_string(int code) {
   }
 }
 
-const char* dcc_version(void) { return "dcc 0.1 (sm_103a)"; }
+const char* dcc_version(void) { return "dcc 0.2 (sm_103a)"; }
+
+int dcc_kernel_binary_version(int* version) {
+  if (!version) return DCC_ERR_INVALID_ARG;
+  int seen = 0;
+  bool mixed = false;
+  const bool ok = visit_kernels([&](const void* fn) {
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (seen && attr.binaryVersion != seen) mixed = true;
+    seen = attr.binaryVersion;
+    return true;
+  });
+  if (!ok) return DCC_ERR_CUDA;
+  if (mixed) return DCC_ERR_UNSUPPORTED;
+  *version = seen;
+  return DCC_OK;
+}
 
 int dcc_shard_range(size_t count, int n_ranks, int rank, size_t eb, size_t* begin, size_t* end) {
   if (n_ranks < 1 || n_ranks > DCC_MAX_RANKS || rank < 0 || rank >= n_ranks || !begin || !end)
@@ -466,7 +495,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   dcc_comm* c = new dcc_comm();
   c->n = n_ranks;
   c->device = dev;
-  for (size_t& m : c->one_shot_max) m = dcc_host::default_one_shot_max(n_ranks);
+  for (int t = 0; t < 4; ++t) c->one_shot_max[t] = dcc_host::default_one_shot_max(n_ranks, (dcc_dtype_t)t);
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     delete c;
@@ -505,7 +534,6 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
     if (us > 0) c->dev.timeout_ns = us * 1000ull;
   }
   if (const char* v = std::getenv("DCC_BLOCKS_PER_RANK")) c->blocks_override = std::atoi(v);
-  if (const char* v = std::getenv("DCC_COOPERATIVE")) c->cooperative = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_THREADS")) {
     const int t = std::atoi(v);
     if (t >= 32 && t <= dcc::kThreads && t % 32 == 0) c->threads_override = t;
@@ -730,7 +758,7 @@ int dcc_reduce_scatter_op(dcc_comm_t c, void* const* send, void* const* recv, si
   if (rc != DCC_OK) return rc;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args};
-  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s), 0,
+  return launch(fn, args.blocks * c->n, threads, coop, kargs, static_cast<cudaStream_t>(s), 0,
                 c->pdl && !coop);
 }
 
@@ -775,7 +803,7 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
   const size_t per_block = sb % 16 == 0 ? (size_t)dcc::kAgUnroll * threads : (size_t)threads;
   rc = pick_blocks(c, fn, threads, sb % 16 == 0 ? work : send_count, &args.blocks, 0, per_block, coop);
   if (rc != DCC_OK) return rc;
-  return launch(fn, args.blocks * c->n, threads, coop && c->cooperative, kargs, static_cast<cudaStream_t>(s), 0,
+  return launch(fn, args.blocks * c->n, threads, coop, kargs, static_cast<cudaStream_t>(s), 0,
                 c->pdl && !coop);
 }
 
@@ -934,6 +962,12 @@ int dcc_set_entry_barrier(dcc_comm_t c, int on) {
 int dcc_set_algo_threshold(dcc_comm_t c, dcc_dtype_t t, size_t bytes) {
   if (!c || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
   c->one_shot_max[t] = bytes;
+  return DCC_OK;
+}
+
+int dcc_auto_threshold(int n_ranks, dcc_dtype_t t, size_t* bytes) {
+  if (!bytes || n_ranks < 1 || n_ranks > DCC_MAX_RANKS || elem_bytes(t) == 0) return DCC_ERR_INVALID_ARG;
+  *bytes = dcc_host::default_one_shot_max(n_ranks, t);
   return DCC_OK;
 }
 

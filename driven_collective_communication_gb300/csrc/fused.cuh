@@ -97,9 +97,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Asks L2 to fetch [p, p + bytes) from memory (bytes a multiple of 16, p
+// 16-byte aligned).  A prefetch returns no data to the thread, so it may be
+// issued before the programmatic-dependent-launch wait: whatever the previous
+// kernel writes later still lands in L2, which the loads after the wait read.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, LinearArgs a) {
-  pdl_prologue();
   constexpr int R = kFusedRows, V = kFusedVecs;
   static_assert(R == 2, "the epilogue packs two rows per item");
   const int n = NT > 0 ? NT : dc.n;
@@ -111,6 +118,14 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
   __shared__ float part_s[DCC_MAX_RANKS][R];
   size_t s0, s1;
   shard_vecs(items, n, rank, s0, s1);
+  // The weight rows of the CTA's first item start their way into L2 while the
+  // previous kernel on the stream may still be finishing (launched with
+  // programmatic dependent launch, this CTA can start before it ends); the
+  // rows are contiguous per rank, one prefetch per rank.
+  if (lane == 0 && s0 + blk < s1 && R * kv * 16 <= 0xffffffffu)
+    for (int p = warp; p < n; p += nwarps)
+      prefetch_l2(static_cast<const uint4*>(a.weight[p]) + (s0 + blk) * R * kv, (uint32_t)(R * kv * 16));
+  pdl_prologue();
   for (size_t v = s0 + blk; v < s1; v += B) {
     const uint32_t res = warp == 0 ? load_residual(a, n, lane, v) : 0u;
     // warp w computes the partial products of ranks w, w + nwarps, ... for

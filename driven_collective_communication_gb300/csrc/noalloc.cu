@@ -15,6 +15,14 @@
 //
 // The kernel is the communicator path's k_allreduce_twoshot_scratch,
 // unchanged: only where its memory comes from differs.
+//
+// No per-call clearing: in a call that completes, every semaphore slot the
+// kernel uses receives exactly one signal and is waited on exactly once, so
+// each slot's signal count equals its waiter count again afterwards, whatever
+// the rank count or launch shape of the next call.  Only a wait that ran out
+// breaks that balance; it also records itself in the status word, and
+// dcc_noalloc_check, which reports it, zeroes the whole synchronisation part
+// of the array so that the next call starts balanced.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,7 +39,7 @@ namespace {
 constexpr size_t kSemBytes = dcc::kSemSlots * dcc::kSemWords * sizeof(unsigned long long);
 constexpr size_t kExpectBytes = dcc::kSemSlots * sizeof(unsigned long long);
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kSyncBytes = kSemBytes + kExpectBytes + kStatusBytes;  // cleared every call
+constexpr size_t kSyncBytes = kSemBytes + kExpectBytes + kStatusBytes;
 constexpr size_t kArrayBytes = kSyncBytes + (size_t)DCC_NOALLOC_MAX_BYTES;
 constexpr int kMaxDevices = 64;
 
@@ -40,30 +48,46 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_array[kArrayBytes];
 
 std::mutex g_mu;
-unsigned char* g_base[kMaxDevices] = {};  // device address of g_noalloc_array per device
-int g_sms[kMaxDevices] = {};
+struct DeviceState {
+  unsigned char* base = nullptr;  // device address of g_noalloc_array on this device
+  int sms = 0;
+  unsigned long long timeout_ns = 0;
+  int skip_signal_rank = -1;
+  int per_sm[4][DCC_MAX_RANKS + 1] = {};  // resident CTAs per SM by (dtype, n); 0 = not yet queried
+};
+DeviceState g_dev[kMaxDevices];
 
 // Once per device, with that device current: resolve the array's device
-// address (no allocation happens here; the array already exists).
-int setup_device(int dev, unsigned char** base, int* sms) {
+// address (no allocation happens here; the array already exists), zero its
+// synchronisation part, and read the wait limit and the test knob from the
+// environment.
+int setup_device(int dev, DeviceState** out) {
   if (dev < 0 || dev >= kMaxDevices) return DCC_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_base[dev]) {
+  DeviceState& d = g_dev[dev];
+  if (!d.base) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_array) != cudaSuccess || !p) {
       cudaGetLastError();
       return DCC_ERR_CUDA;
     }
     int n_sms = 0;
-    if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaMemset(p, 0, kSyncBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
       cudaGetLastError();
       return DCC_ERR_CUDA;
     }
-    g_base[dev] = static_cast<unsigned char*>(p);
-    g_sms[dev] = n_sms;
+    d.timeout_ns = 2000000ull * 1000ull;
+    if (const char* v = std::getenv("DCC_WAIT_TIMEOUT_US")) {
+      const unsigned long long us = std::strtoull(v, nullptr, 10);
+      if (us > 0) d.timeout_ns = us * 1000ull;
+    }
+    // test knob: this rank sends no signals, so its peers' waits run out
+    if (const char* v = std::getenv("DCC_NOALLOC_SKIP_SIGNAL")) d.skip_signal_rank = std::atoi(v);
+    d.sms = n_sms;
+    d.base = static_cast<unsigned char*>(p);
   }
-  *base = g_base[dev];
-  *sms = g_sms[dev];
+  *out = &d;
   return DCC_OK;
 }
 
@@ -117,19 +141,27 @@ extern "C" int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const
     cudaGetLastError();
     return DCC_ERR_CUDA;
   }
-  unsigned char* base = nullptr;
-  int sms = 0;
-  int rc = setup_device(dev, &base, &sms);
+  DeviceState* d = nullptr;
+  int rc = setup_device(dev, &d);
   if (rc != DCC_OK) return rc;
+  unsigned char* base = d->base;
 
   const void* fn = scratch_kernel(t, n_ranks);
-  int per_sm = 0;
-  if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, dcc::kThreads, 0) !=
-                 cudaSuccess) {
-    cudaGetLastError();
-    return DCC_ERR_CUDA;
+  if (!fn) return DCC_ERR_INVALID_ARG;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    per_sm = d->per_sm[t][n_ranks];
   }
-  int bmax = per_sm * sms / n_ranks;
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, dcc::kThreads, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return DCC_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    d->per_sm[t][n_ranks] = per_sm;
+  }
+  int bmax = per_sm * d->sms / n_ranks;
   if (bmax > DCC_MAX_BLOCKS_PER_RANK) bmax = DCC_MAX_BLOCKS_PER_RANK;
   if (bmax < 1) return DCC_ERR_LAUNCH;
   const size_t vw = 16 / eb;
@@ -139,12 +171,8 @@ extern "C" int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const
 
   dcc::DevComm dc{};
   dc.n = n_ranks;
-  dc.skip_signal_rank = -1;
-  dc.timeout_ns = 2000000ull * 1000ull;
-  if (const char* v = std::getenv("DCC_WAIT_TIMEOUT_US")) {
-    const unsigned long long us = std::strtoull(v, nullptr, 10);
-    if (us > 0) dc.timeout_ns = us * 1000ull;
-  }
+  dc.skip_signal_rank = d->skip_signal_rank;
+  dc.timeout_ns = d->timeout_ns;
   dc.sem = reinterpret_cast<unsigned long long*>(base);
   dc.expect = reinterpret_cast<unsigned long long*>(base + kSemBytes);
   dc.status = reinterpret_cast<unsigned long long*>(base + kSemBytes + kExpectBytes);
@@ -162,12 +190,6 @@ extern "C" int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const
   a.inplace = inplace ? 1 : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(s);
-  // Counters, waiter counts and status start at zero for every call: the
-  // array keeps whatever the previous call (on any stream) left there.
-  if (cudaMemsetAsync(base, 0, kSyncBytes, st) != cudaSuccess) {
-    cudaGetLastError();
-    return DCC_ERR_CUDA;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(blocks * n_ranks));
   cfg.blockDim = dim3((unsigned)dcc::kThreads);
@@ -188,4 +210,32 @@ extern "C" int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const
     return DCC_ERR_CUDA;
   }
   return DCC_OK;
+}
+
+extern "C" int dcc_noalloc_check(dcc_stream_t s, int* rank, int* peer, int* block) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  DeviceState* d = nullptr;
+  const int rc = setup_device(dev, &d);
+  if (rc != DCC_OK) return rc;
+  unsigned long long st = 0;
+  unsigned char* status = d->base + kSemBytes + kExpectBytes;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(s)) != cudaSuccess ||
+      cudaMemcpy(&st, status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  if (st == 0) return DCC_OK;
+  if (rank) *rank = (int)((st >> 8) & 0xFF);
+  if (peer) *peer = (int)((st >> 16) & 0xFF);
+  if (block) *block = (int)((st >> 24) & 0xFFFF);
+  // the semaphores are unbalanced after a wait gave up: start again from zero
+  if (cudaMemset(d->base, 0, kSyncBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_CUDA;
+  }
+  return DCC_ERR_TIMEOUT;
 }

@@ -354,7 +354,7 @@ int require_running(const dcc_comm* c) {
 }
 
 int port_launch(dcc_comm* c, const void* fn, int grid, void** args, cudaStream_t s) {
-  return dcc_host::launch(fn, grid, 32, c->cooperative, args, s);
+  return dcc_host::launch(fn, grid, 32, true, args, s);
 }
 
 }  // namespace

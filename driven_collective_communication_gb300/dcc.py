@@ -82,10 +82,13 @@ _SIGS = {
     "dcc_set_entry_barrier": [_vp, _i],
     "dcc_set_pdl": [_vp, _i],
     "dcc_select_algo": [_vp, _sz, _i, ctypes.POINTER(_i)],
+    "dcc_auto_threshold": [_i, _i, ctypes.POINTER(_sz)],
     "dcc_debug_skip_signal": [_vp, _i],
     "dcc_launch_shape": [_vp, _sz, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "dcc_shard_range": [_sz, _i, _i, _sz, ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
     "dcc_allreduce_noalloc": [_i, _PP, _PP, _sz, _i, _vp],
+    "dcc_noalloc_check": [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)],
+    "dcc_kernel_binary_version": [ctypes.POINTER(_i)],
     "dcc_proxy_start": [_vp],
     "dcc_proxy_stop": [_vp],
     "dcc_proxy_set_handler": [_vp, _vp, _vp],
@@ -292,6 +295,14 @@ def dcc_select_algo(comm, count, dtype):
     return {v: k for k, v in ALGO_CODES.items()}[out.value]
 
 
+def dcc_auto_threshold(n_ranks, dtype):
+    """Default one-shot threshold (bytes per rank) for n_ranks and dtype: the
+    compiled crossover table (pure host logic)."""
+    out = _sz()
+    _check(_lib.dcc_auto_threshold(n_ranks, _dtype(dtype), ctypes.byref(out)), "dcc_auto_threshold")
+    return out.value
+
+
 def dcc_debug_skip_signal(comm, rank):
     return _check(_lib.dcc_debug_skip_signal(comm, int(rank)), "dcc_debug_skip_signal")
 
@@ -317,7 +328,24 @@ def dcc_allreduce_noalloc(n_ranks, send, recv, count, dtype, stream=None):
                   "dcc_allreduce_noalloc")
 
 
+def dcc_noalloc_check(stream=None):
+    """Status of the allocation-free AllReduce on the current device: returns
+    (code, rank, peer, block); code is DCC_OK or DCC_ERR_TIMEOUT (see dcc.h)."""
+    r, p, b = _i(-1), _i(-1), _i(-1)
+    rc = _lib.dcc_noalloc_check(_stream(stream), ctypes.byref(r), ctypes.byref(p), ctypes.byref(b))
+    if rc not in (DCC_OK, DCC_ERR_TIMEOUT):
+        raise DccError(rc, "dcc_noalloc_check")
+    return rc, r.value, p.value, b.value
+
+
 DCC_NOALLOC_MAX_BYTES = 4 << 20
+
+
+def dcc_kernel_binary_version():
+    """binaryVersion of the library's kernels on the current device (103 = sm_103a)."""
+    v = _i()
+    _check(_lib.dcc_kernel_binary_version(ctypes.byref(v)), "dcc_kernel_binary_version")
+    return v.value
 
 TRIGGER_HANDLER = ctypes.CFUNCTYPE(None, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p)
 _handlers = {}  # keeps the ctypes callbacks alive per communicator

@@ -272,19 +272,33 @@ const char* dcc_error_string(int code);
  * lives in one fixed device array of DCC_NOALLOC_MAX_BYTES plus 1.25 MiB that
  * every GPU that loads the library holds until the process exits.
  *  - Never allocates: no cudaMalloc/cudaFree or other allocating call.
- *  - The first call on a device resolves that array's device address for the
- *    device (once); make that first call before any stream capture.
- *  - Every call clears the array's synchronisation part on s before its
- *    kernel; calls share the array, so calls that overlap on the GPU (on
- *    different streams, or on several host threads) race and must not be
- *    issued.
+ *  - The first call on a device (of this function or dcc_noalloc_check) sets
+ *    that device up once: it resolves the array's device address, zeroes its
+ *    synchronisation part and synchronises the device; make that first call
+ *    before any stream capture.  Later calls only launch the kernel.
+ *  - Calls share the array: calls that overlap on the GPU (on different
+ *    streams, or from several host threads) race and must not be issued.
+ *    Nothing is cleared between calls: a call that completes leaves every
+ *    semaphore it used balanced (as many waits as signals), which is all the
+ *    next call needs.
  *  - A device wait that runs out (the same bounded waits as the communicator
- *    path) leaves that call's outputs incomplete; there is no communicator to
- *    report it through.
+ *    path; limit DCC_WAIT_TIMEOUT_US, read at set-up) leaves that call's
+ *    outputs incomplete and records the failure in the array's status word.
+ *    It stays recorded, and outputs of later calls carry no guarantee, until
+ *    dcc_noalloc_check has reported it.
  * Errors: INVALID_ARG (n_ranks, NULL, dtype, overlap), MISALIGNED,
  * UNSUPPORTED (count * element size > DCC_NOALLOC_MAX_BYTES), LAUNCH, CUDA. */
 int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const* recv, size_t count,
                           dcc_dtype_t t, dcc_stream_t s);
+
+/* Failure report of dcc_allreduce_noalloc on the current device.  Synchronises
+ * s (the stream of the calls to check), reads the array's status word (a copy
+ * into host memory; nothing is allocated) and returns DCC_OK, or
+ * DCC_ERR_TIMEOUT with the rank, peer and block of the first wait that gave up
+ * (any pointer may be NULL).  After a failure it zeroes the array's
+ * synchronisation part (and synchronises the device), so the next call starts
+ * clean.  Errors: CUDA. */
+int dcc_noalloc_check(dcc_stream_t s, int* rank, int* peer, int* block);
 
 /* ------------------------------------------------------------------------ */
 /* MemoryChannel primitives on their own (README, "On-GPU Communication     */
@@ -421,9 +435,16 @@ int dcc_set_entry_barrier(dcc_comm_t c, int on);
 int dcc_set_pdl(dcc_comm_t c, int on);
 
 /* AUTO picks ONE_SHOT for out-of-place messages of at most `bytes` per rank
- * and TWO_SHOT above, for this dtype.  Defaults come from the measured
- * crossover: 32 KiB with 5 or more ranks, 0 (always two-shot) with 2 to 4. */
+ * and TWO_SHOT above, for this dtype, on this communicator.  The default is
+ * dcc_auto_threshold(n_ranks, t). */
 int dcc_set_algo_threshold(dcc_comm_t c, dcc_dtype_t t, size_t bytes);
+
+/* The default of that threshold for a communicator of n_ranks (1..16) and
+ * dtype t: the measured crossover table compiled into the library (one-shot
+ * up to the largest measured size at which it was never slower than
+ * two-shot, CUDA-graph-amortised, on GB300).  Pure host logic, no GPU.
+ * Errors: INVALID_ARG (n_ranks, t, bytes NULL). */
+int dcc_auto_threshold(int n_ranks, dcc_dtype_t t, size_t* bytes);
 
 /* The algorithm AUTO would run for this request (pure host logic). */
 int dcc_select_algo(dcc_comm_t c, size_t count, dcc_dtype_t t, dcc_algo_t* out);
@@ -445,6 +466,14 @@ int dcc_shard_range(size_t count, int n_ranks, int rank, size_t elem_bytes, size
 
 /* Library version string (static storage). */
 const char* dcc_version(void);
+
+/* Compute capability the library's device code was built for, as the CUDA
+ * runtime reports it for every kernel of the library on the current device
+ * (binaryVersion, e.g. 103 for sm_103a).  *version receives it when all
+ * kernels agree.  Errors: INVALID_ARG (version NULL), CUDA (no device, or a
+ * kernel that cannot load), UNSUPPORTED (kernels built for different
+ * architectures). */
+int dcc_kernel_binary_version(int* version);
 
 #ifdef __cplusplus
 }

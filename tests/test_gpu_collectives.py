@@ -6,6 +6,8 @@ the same bits (the tolerance of the method -- 1e-6*N*max|x| for fp32, 1 ulp of
 the output type for fp16/bf16 -- is only needed for other orders and is never
 used here).  int32 is exact by definition.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -326,29 +328,24 @@ def test_c3_bf16_decode_sizes(dcc, tokens):
         arena.close()
 
 
-def sampled_indices(count, n, k=200000, seed=0):
-    """Random indices plus every shard boundary neighbourhood and the tail."""
-    rng = np.random.default_rng(seed)
-    idx = [rng.integers(0, count, size=k)]
-    for r in range(n + 1):
-        b = (count // n) * r
-        idx.append(np.arange(max(0, b - 9), min(count, b + 9)))
-    idx.append(np.arange(max(0, count - 17), count))
-    return np.unique(np.concatenate(idx))
+def host_bits(t):
+    """A device tensor's raw storage on the host, as unsigned integers (a view,
+    no conversion), for whole-buffer bit comparisons."""
+    a = W.to_storage(t)
+    return a.view(np.uint16) if a.itemsize == 2 else a.view(np.uint32)
 
 
-def test_c4_bf16_n8_256MiB_sampled(dcc):
+def test_c4_bf16_n8_256MiB_full(dcc):
     """Full size, the launch configuration the benchmark times (AUTO) and every
-    other large-message schedule, checked on sampled elements one by one and by
-    the identical-ranks invariant over every element."""
+    other large-message schedule: all 8 x 134,217,728 outputs of every rank
+    compared bit for bit with the oracle (threaded over the host cores), and
+    every rank's output identical on the device."""
     w = W.C4
     xs = W.rank_inputs(w, device="cuda")
     recv = [torch.empty_like(x) for x in xs]
     comm = dcc.Comm(8)
-    idx = sampled_indices(w.count, 8)
-    idx_t = torch.from_numpy(idx).cuda()
-    host = [W.to_storage(x[idx_t]) for x in xs]
-    expect = oracle.allreduce(host, "bf16")  # elementwise: sampled columns
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], "bf16", nthreads=os.cpu_count() or 1)
+    expect = expect.view(np.uint16)
     try:
         comm.register_all("input", xs)
         comm.register_all("output", recv)
@@ -359,25 +356,24 @@ def test_c4_bf16_n8_256MiB_sampled(dcc):
             assert comm.check() == dcc.DCC_OK
             for r in range(1, 8):
                 assert torch.equal(recv[r].view(torch.int16), recv[0].view(torch.int16)), algo
-            for r in (0, 3, 7):
-                assert same(W.to_storage(recv[r][idx_t]), expect, "bf16"), (algo, r)
+            for r in range(8):
+                got = host_bits(recv[r])
+                assert np.array_equal(got, expect), (algo, r, int(np.count_nonzero(got != expect)))
     finally:
         comm.close()
 
 
 @pytest.mark.parametrize("n,dtype", [(2, "bf16"), (4, "bf16"), (16, "bf16"), (8, "fp32")])
-def test_256MiB_per_rank_other_rank_counts_and_fp32_sampled(dcc, n, dtype):
+def test_256MiB_per_rank_other_rank_counts_and_fp32_full(dcc, n, dtype):
     """The other full-size AllReduces the benchmark times (256 MiB per rank, AUTO):
-    sampled elements against the oracle and every rank's output identical."""
+    every element of every rank's output against the oracle, bit for bit."""
     recipe = W.C4 if dtype == "bf16" else W.C1
     count = (256 << 20) // W.ELEM_BYTES[dtype]
     w = W.with_count(recipe, count, n_ranks=n)
     xs = W.rank_inputs(w, device="cuda")
     recv = [torch.empty_like(x) for x in xs]
-    idx = sampled_indices(count, n, k=50000)
-    assert idx.min() >= 0 and idx.max() < count
-    idx_t = torch.from_numpy(idx).cuda()
-    expect = oracle.allreduce([W.to_storage(x[idx_t]) for x in xs], dtype)
+    expect = oracle.allreduce([W.to_storage(x) for x in xs], dtype, nthreads=os.cpu_count() or 1)
+    expect = expect.view(np.uint16 if dtype == "bf16" else np.uint32)
     bits = torch.int16 if dtype == "bf16" else torch.int32
     with dcc.Comm(n) as comm:
         comm.register_all("input", xs)
@@ -386,8 +382,9 @@ def test_256MiB_per_rank_other_rank_counts_and_fp32_sampled(dcc, n, dtype):
         assert comm.check() == dcc.DCC_OK
     for r in range(1, n):
         assert torch.equal(recv[r].view(bits), recv[0].view(bits)), r
-    for r in (0, n - 1):
-        assert same(W.to_storage(recv[r][idx_t]), expect, dtype), r
+    for r in range(n):
+        got = host_bits(recv[r])
+        assert np.array_equal(got, expect), (r, int(np.count_nonzero(got != expect)))
 
 
 def test_c5_fp16_reduce_scatter_and_allgather_full(dcc):
@@ -965,12 +962,17 @@ def test_allreduce_from_host(dcc, count, inplace, mode, monkeypatch):
 
 
 def test_auto_selection(dcc):
-    # default crossover: one-shot up to 32 KiB with 8 ranks, never with 2
-    with dcc.Comm(8) as c:
-        assert dcc.dcc_select_algo(c.handle, 16384, "bf16") == "one_shot"
-        assert dcc.dcc_select_algo(c.handle, 16385, "bf16") == "two_shot"
-    with dcc.Comm(2) as c:
-        assert dcc.dcc_select_algo(c.handle, 64, "bf16") == "two_shot"
+    """AUTO follows the measured crossover table (the tuning JSON) for every
+    rank count and dtype, and a per-communicator override moves it."""
+    from driven_collective_communication_gb300 import build
+    table = build.load_auto_table()
+    for n in (1, 2, 3, 4, 5, 8, 12, 16):
+        with dcc.Comm(n) as c:
+            for t, eb in (("int32", 4), ("fp32", 4), ("fp16", 2), ("bf16", 2)):
+                lim = table[n][t] // eb  # elements
+                if lim:
+                    assert dcc.dcc_select_algo(c.handle, lim, t) == "one_shot", (n, t)
+                assert dcc.dcc_select_algo(c.handle, lim + 1, t) == "two_shot", (n, t)
     with dcc.Comm(8) as c:
         dcc.dcc_set_algo_threshold(c.handle, "bf16", 65536)
         assert dcc.dcc_select_algo(c.handle, 32768, "bf16") == "one_shot"

@@ -241,43 +241,29 @@ def test_op_with_entry_barrier(dcc, n):
         arena.close()
 
 
-def test_op_full_size_sampled(dcc):
+def test_op_full_size(dcc):
     """8 ranks x 256 MiB bf16 (the sum benchmark's size), MAX and MIN through
     AUTO (two-shot at this size), in the launch configuration the library
-    picks; sampled windows checked against the oracle, and a property that
-    holds everywhere: every output equals one rank's input or is NaN."""
+    picks; every element of every rank's output against the oracle, bit for
+    bit (NaN inputs give the canonical NaN on both sides)."""
     n, count = 8, 134217728
-    win, nwin = 4096, 16
-    rng = np.random.default_rng(2024)
-    starts = np.concatenate([[0, count - win], rng.integers(0, count - win, size=nwin - 2)])
-    assert starts.min() >= 0 and starts.max() + win <= count  # windows in bounds (host check)
     g = torch.Generator(device="cuda")
     g.manual_seed(11)
     xs = [torch.randn(count, generator=g, device="cuda").to(torch.bfloat16) for _ in range(n)]
     xs[3][::1000] = float("nan")
     xs[5][7::997] = -0.0
     ys = [torch.empty_like(x) for x in xs]
+    host = [to_host_bits(x, "bf16") for x in xs]
     with dcc.Comm(n) as comm:
         comm.register_all("input", xs)
         comm.register_all("output", ys)
         for op in OPS:
             comm.allreduce_op(xs, ys, op=op)
             assert comm.check() == dcc.DCC_OK
-            for s in starts:
-                sl = slice(int(s), int(s) + win)
-                ins = [to_host_bits(x[sl], "bf16") for x in xs]
-                expect = oracle.allreduce_op(ins, "bf16", op)
-                for r in (0, 4, 7):
-                    assert bits_equal(ys[r][sl], expect, "bf16"), (op, int(s), r)
-            # the reduction picks one input's bits (or NaN) everywhere
-            hit = torch.zeros(count, dtype=torch.bool, device="cuda")
-            yb = ys[6].view(torch.int16)
-            for x in xs:
-                hit |= yb == x.view(torch.int16)
-            hit |= torch.isnan(ys[6])
-            assert bool(hit.all())
-            for r in range(1, n):
-                assert torch.equal(ys[r].view(torch.int16), ys[0].view(torch.int16))
+            expect = oracle.allreduce_op(host, "bf16", op)
+            for r in range(n):
+                got = to_host_bits(ys[r], "bf16")
+                assert np.array_equal(got, expect), (op, r, int(np.count_nonzero(got != expect)))
 
 
 def test_random_op_configurations_match_oracle(dcc, monkeypatch):
