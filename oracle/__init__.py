@@ -44,10 +44,12 @@ def _load():
         lib.orc_allreduce_op.argtypes = [i32, ctypes.POINTER(vp), vp, sz, i32, i32]
         lib.orc_linear_allreduce_residual.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                       ctypes.POINTER(vp), sz, sz, i32, vp]
+        lib.orc_linear_allreduce_tokens.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, sz, sz,
+                                                    i32, vp]
         for name in ("orc_allreduce", "orc_allreduce_at", "orc_allreduce_mt",
                      "orc_reduce_scatter", "orc_allgather", "orc_ring_barrier_counts",
                      "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce",
-                     "orc_allreduce_op", "orc_linear_allreduce_residual"):
+                     "orc_allreduce_op", "orc_linear_allreduce_residual", "orc_linear_allreduce_tokens"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -196,6 +198,27 @@ def linear_allreduce_residual(ws, xs, res, dtype, rows, kp):
     _ok(lib.orc_linear_allreduce_residual(n, wp, xp, rp, rows, kp, DTYPES[dtype], out.ctypes.data),
         "linear_allreduce_residual")
     return [out[q * rows:(q + 1) * rows].copy() for q in range(n)]
+
+
+def linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp):
+    """Y[t, i] = R(sum_p sum_k W_p[i, k] X_p[t, k]) for rank weights ws[p]
+    (rows*kp, row-major) and inputs xs[p] (tokens*kp, row-major): the
+    row-parallel linear layer + AllReduce over a batch of tokens.  Returns
+    tokens*rows elements, row-major (token t's outputs contiguous)."""
+    lib = _load()
+    if dtype not in ("fp16", "bf16"):
+        raise ValueError("fp16 or bf16 only")
+    warrs = [np.ascontiguousarray(a, dtype=np.uint16).ravel() for a in ws]
+    xarrs = [np.ascontiguousarray(a, dtype=np.uint16).ravel() for a in xs]
+    if (len(warrs) != len(xarrs) or any(len(a) != rows * kp for a in warrs)
+            or any(len(a) != tokens * kp for a in xarrs)):
+        raise ValueError("shapes")
+    wp = (ctypes.c_void_p * len(warrs))(*[a.ctypes.data for a in warrs])
+    xp = (ctypes.c_void_p * len(xarrs))(*[a.ctypes.data for a in xarrs])
+    out = np.empty(tokens * rows, dtype=np.uint16)
+    _ok(lib.orc_linear_allreduce_tokens(len(warrs), wp, xp, tokens, rows, kp, DTYPES[dtype], out.ctypes.data),
+        "linear_allreduce_tokens")
+    return out
 
 
 def library_path():

@@ -392,6 +392,31 @@ int orc_linear_allreduce(int n, const void* const* w, const void* const* x, size
 }
 
 /* ---------------------------------------------------------------------- */
+/* The same layer for a batch of tokens (a multi-token decode step): x_p    */
+/* holds tokens x kp elements, row-major, token t's slice of the            */
+/* contraction dimension at x_p + t*kp, and                                 */
+/*   y[t][i] = R( sum_p sum_k W_p[i][k] * x_p[t][k] ),  t < tokens,        */
+/* out is tokens x rows, row-major (token t's hidden vector at out +        */
+/* t*rows).  Binary64 sum of the exact products, one rounding, exactly as   */
+/* for a single token.                                                      */
+/* ---------------------------------------------------------------------- */
+int orc_linear_allreduce_tokens(int n, const void* const* w, const void* const* x, size_t tokens,
+                                size_t rows, size_t kp, int dtype, void* out)
+{
+    if (n < 1 || !w || !x || (tokens && rows && !out) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    for (int p = 0; p < n; ++p) if (!w[p] || !x[p]) return -1;
+    for (size_t t = 0; t < tokens; ++t)
+        for (size_t i = 0; i < rows; ++i) {
+            double acc = 0.0;
+            for (int p = 0; p < n; ++p)
+                for (size_t k = 0; k < kp; ++k)
+                    acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);
+            ((uint16_t*)out)[t * rows + i] = f64_to_half_once(acc, dtype);
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* The same layer with a residual added for each output rank (the          */
 /* tensor-parallel residual stream: h_q <- h_q + the layer's AllReduced    */
 /* output).  Reading taken: the residual joins the binary64 sum before the */

@@ -434,6 +434,57 @@ def test_linear_allreduce_matches_float64_matmul(dtype):
     del rng
 
 
+# --------------------------------------------------------------------- linear layer, many tokens
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_tokens_each_token_is_the_single_token_layer(dtype):
+    """Token t of the batched layer is the one-token layer applied to token t's
+    slice of every rank's input, and lands at row t of the output (checks the
+    token offsets of the inputs and of the output)."""
+    n, tokens, rows, kp = 3, 5, 12, 24
+    rng = np.random.default_rng(11)
+    ws = [_small_ints(rng, dtype, -3, 3, rows * kp) for _ in range(n)]
+    xs = [_small_ints(rng, dtype, -2, 2, tokens * kp) for _ in range(n)]
+    got = oracle.linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp).reshape(tokens, rows)
+    for t in range(tokens):
+        one = oracle.linear_allreduce(ws, [x[t * kp:(t + 1) * kp] for x in xs], dtype, rows, kp)
+        assert np.array_equal(got[t], one), t
+    # the tokens differ, so a mix-up of rows would show
+    assert len({tuple(r) for r in got}) == tokens
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_tokens_closed_forms(dtype):
+    """All-ones weights with token t's inputs all equal to t+1 give N*kp*(t+1)
+    in every row of token t; a rank whose inputs are all zero drops out."""
+    n, tokens, rows, kp = 4, 6, 8, 16
+    one = value_to_storage(1, dtype)
+    ws = [np.full(rows * kp, one, np.uint16) for _ in range(n)]
+    xs = [np.concatenate([np.full(kp, value_to_storage(t + 1, dtype), np.uint16) for t in range(tokens)])
+          for _ in range(n)]
+    got = storage_to_float(oracle.linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp), dtype)
+    assert np.array_equal(got.reshape(tokens, rows), np.repeat(np.arange(1, tokens + 1)[:, None] * n * kp, rows, 1))
+    xs[2] = np.full(tokens * kp, value_to_storage(0, dtype), np.uint16)
+    got = storage_to_float(oracle.linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp), dtype)
+    assert np.array_equal(got.reshape(tokens, rows),
+                          np.repeat(np.arange(1, tokens + 1)[:, None] * (n - 1) * kp, rows, 1))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_tokens_matches_float64_matmul(dtype):
+    """Against numpy's float64 matrix product X_cat @ W_cat^T of the
+    concatenated shards, rounded once by the brute force's generic rounding."""
+    n, tokens, rows, kp = 3, 7, 20, 32
+    ws = [W.to_storage(torch.randn(rows * kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    xs = [W.to_storage(torch.randn(tokens * kp).to(W.TORCH_DTYPES[dtype])) for _ in range(n)]
+    a = np.concatenate([storage_to_float(w, dtype).reshape(rows, kp) for w in ws], axis=1)
+    x = np.concatenate([storage_to_float(v, dtype).reshape(tokens, kp) for v in xs], axis=1)
+    prod = x @ a.T  # tokens x rows
+    ref = np.array([brute.encode(brute.round_ieee(float(v), *brute.FORMATS[dtype]), dtype) for v in prod.ravel()],
+                   np.uint16)
+    got = oracle.linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp)
+    assert np.array_equal(got, ref)
+
+
 # --------------------------------------------------------------------- linear layer + residual
 def _small_ints(rng, dtype, lo, hi, size):
     return np.array([value_to_storage(int(v), dtype) for v in rng.integers(lo, hi + 1, size=size)], np.uint16)

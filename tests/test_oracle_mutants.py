@@ -64,6 +64,12 @@ MUTANTS = {
         "const double y = acc + (double)widen(res[q], i, dtype);",
         "const double y = (double)(dtype == ORC_FP16 ? orc_f16_to_f32(f64_to_half_once(acc, dtype))"
         " : orc_bf16_to_f32(f64_to_half_once(acc, dtype))) + (double)widen(res[q], i, dtype);"),
+    "tokens_ignore_token_offset": ("(double)widen(x[p], t * kp + k, dtype);",
+                                   "(double)widen(x[p], k, dtype);"),
+    "tokens_output_transposed": ("((uint16_t*)out)[t * rows + i] = f64_to_half_once(acc, dtype);",
+                                 "((uint16_t*)out)[i * tokens + t] = f64_to_half_once(acc, dtype);"),
+    "tokens_drop_last_rank": ("            for (int p = 0; p < n; ++p)\n                for (size_t k = 0; k < kp; ++k)\n                    acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);",
+                              "            for (int p = 0; p < n - 1; ++p)\n                for (size_t k = 0; k < kp; ++k)\n                    acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
