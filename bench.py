@@ -516,18 +516,21 @@ DTYPE_RECIPES = {"int32": W.C2, "fp32": W.C1, "fp16": W.C5, "bf16": W.C4}
 
 
 def crossover_rule(sizes, t_one, t_two):
-    """Largest measured size s with one-shot no slower than two-shot at every
-    measured size up to s; 0 if two-shot is faster at the smallest size."""
-    best = 0
+    """The threshold (0 or a measured size) that minimises the summed time over
+    the measured sizes when every size up to it runs one-shot and every larger
+    one two-shot; ties go to the smaller threshold.  Summing over the sizes
+    keeps one noisy point from moving the threshold the way a first-loss rule
+    would."""
+    best, best_gain, gain = 0, 0.0, 0.0
     for s, a, b in zip(sizes, t_one, t_two):
-        if a > b:
-            break
-        best = s
+        gain += b - a  # time saved by running every size up to s one-shot
+        if gain > best_gain + 1e-9:
+            best, best_gain = s, gain
     return best
 
 
 def crossover_sweep(dcc, dev, stream, ranks=(8,), dtypes=("int32", "fp32", "fp16", "bf16"),
-                    sizes=CROSSOVER_SIZES, repeats=3):
+                    sizes=CROSSOVER_SIZES, repeats=5):
     """Out-of-place AllReduce, one-shot vs two-shot, CUDA-graph-amortised us per
     call (median of `repeats` graphs) at each size, per rank count and dtype;
     returns {n: {dtype: {"sizes", "one_shot_us", "two_shot_us", "one_shot_max_bytes"}}}."""
@@ -561,28 +564,52 @@ def crossover_sweep(dcc, dev, stream, ranks=(8,), dtypes=("int32", "fp32", "fp16
     return res
 
 
+def combine_sweeps(paths):
+    """Mean timings of several sweeps (tuning JSONs written by --write-auto-table)
+    and the thresholds the rule gives for the mean: single sweeps differ by a
+    few hundredths of a microsecond, as much as one-shot and two-shot differ
+    near the crossover."""
+    docs = [json.load(open(p)) for p in paths]
+    sweep = {}
+    for n in docs[0]["timings_us"]:
+        sweep[int(n)] = {}
+        for t, r in docs[0]["timings_us"][n].items():
+            rows = [d["timings_us"][n][t] for d in docs]
+            one = [statistics.fmean(v) for v in zip(*[x["one_shot_us"] for x in rows])]
+            two = [statistics.fmean(v) for v in zip(*[x["two_shot_us"] for x in rows])]
+            sweep[int(n)][t] = {"sizes": r["sizes"], "one_shot_us": [round(v, 3) for v in one],
+                                "two_shot_us": [round(v, 3) for v in two],
+                                "one_shot_max_bytes": crossover_rule(r["sizes"], one, two)}
+    return sweep, "mean of %d sweeps: %s" % (len(docs), "; ".join(d["source"] for d in docs))
+
+
 def write_auto_table(args):
-    """Measure the crossover for every rank count 2..16 and dtype and write the
-    tuning JSON that the library build compiles in (1 rank: no choice, 0)."""
+    """Measure the crossover for every rank count 2..16 and dtype (or combine
+    earlier sweeps, --combine) and write the tuning JSON that the library
+    build compiles in (1 rank: no choice, 0)."""
     from driven_collective_communication_gb300 import build
-    build.build()
-    from driven_collective_communication_gb300 import dcc
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    stream = torch.cuda.Stream(device=dev)
-    sweep = crossover_sweep(dcc, dev, stream, ranks=tuple(range(2, 17)))
+    if args.combine:
+        sweep, source = combine_sweeps(args.combine)
+    else:
+        build.build()
+        from driven_collective_communication_gb300 import dcc
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        stream = torch.cuda.Stream(device=dev)
+        sweep = crossover_sweep(dcc, dev, stream, ranks=tuple(range(2, 17)))
+        props = torch.cuda.get_device_properties(dev)
+        source = "python bench.py --write-auto-table on %s (%d SMs), %s" % (
+            props.name, props.multi_processor_count, time.strftime("%Y-%m-%d"))
     table = {"1": {t: 0 for t in build.DTYPE_ORDER}}
     for n, per in sweep.items():
         table[str(n)] = {t: per[t]["one_shot_max_bytes"] for t in build.DTYPE_ORDER}
-    props = torch.cuda.get_device_properties(dev)
     doc = {
         "what": "largest out-of-place AllReduce message, in bytes per rank, that DCC_ALGO_AUTO runs "
                 "one-shot (above it: two-shot), per rank count and element type",
-        "rule": "one-shot up to the largest measured size s such that one-shot took no longer than "
-                "two-shot at every measured size up to s (CUDA-graph-amortised time per AllReduce, "
-                "median of repeats); 0 when two-shot is faster already at the smallest size",
-        "source": "python bench.py --write-auto-table on %s (%d SMs), %s" % (
-            props.name, props.multi_processor_count, time.strftime("%Y-%m-%d")),
+        "rule": "the threshold (0 or a measured size) that minimises the time summed over the measured "
+                "sizes when every size up to it runs one-shot and every larger one two-shot "
+                "(CUDA-graph-amortised time per AllReduce, median of repeats)",
+        "source": source,
         "one_shot_max_bytes": table,
         "timings_us": {str(n): per for n, per in sweep.items()},
     }
@@ -886,18 +913,25 @@ def other_workloads(dcc, dev, stream):
             assert lc.check(stream) == dcc.DCC_OK
         out["linear_allreduce_bf16_n8_rows8192_kp%d" % kp] = res
         del wts, xin, yf, part, ysep, hres
-    with dcc.Comm(8, connect="ring") as ring:
-        ring.ring_barrier(100, stream)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ring.ring_barrier(W.BARRIER_ITERS, stream)
-        e1.record(stream)
-        e1.synchronize()
-        assert ring.check(stream) == dcc.DCC_OK
+    # the ring barrier: default transport (8 ranks: one cluster, distributed
+    # shared memory) and the global-memory semaphores (DCC_RING_CLUSTER=0)
+    for key, env in (("c5_ring_barrier", None), ("c5_ring_barrier_l2_semaphores", "0")):
+        if env is not None:
+            os.environ["DCC_RING_CLUSTER"] = env
+        try:
+            with dcc.Comm(8, connect="ring") as ring:
+                ring.ring_barrier(100, stream)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                ring.ring_barrier(W.BARRIER_ITERS, stream)
+                e1.record(stream)
+                e1.synchronize()
+                assert ring.check(stream) == dcc.DCC_OK
+        finally:
+            os.environ.pop("DCC_RING_CLUSTER", None)
         us = e0.elapsed_time(e1) * 1e3 / W.BARRIER_ITERS
-        out["c5_ring_barrier"] = {"iters": W.BARRIER_ITERS, "round_trip_us": round(us, 3),
-                                  "per_hop_us": round(us / 8, 3)}
+        out[key] = {"iters": W.BARRIER_ITERS, "round_trip_us": round(us, 3), "per_hop_us": round(us / 8, 3)}
     return out
 
 
@@ -1032,6 +1066,8 @@ def main():
     ap.add_argument("--ref-elems", type=int, default=1 << 22)
     ap.add_argument("--write-auto-table", default=None, metavar="PATH",
                     help="measure the one-shot/two-shot crossover for 2..16 ranks and write the tuning JSON")
+    ap.add_argument("--combine", nargs="+", default=None, metavar="SWEEP",
+                    help="with --write-auto-table: average earlier sweeps instead of measuring")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

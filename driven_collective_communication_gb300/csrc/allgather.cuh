@@ -47,22 +47,21 @@ __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, 
       uint4 x[kAgUnroll];
 #pragma unroll
       for (int j = 0; j < kAgUnroll; ++j)
-        if (v0 + j * T < nv) x[j] = ld_vec(src + v0 + j * T);
+        if (v0 + j * T < nv)
+          x[j] = in_bounds(dc, a, kBufSend, rank, (v0 + j * T) * 16, 16) ? ld_vec(src + v0 + j * T)
+                                                                         : make_uint4(0, 0, 0, 0);
+      auto put = [&](int p) {
+        uint4* d = static_cast<uint4*>(a.recv[p]) + dst_off;
+#pragma unroll
+        for (int j = 0; j < kAgUnroll; ++j)
+          if (v0 + j * T < nv && in_bounds(dc, a, kBufRecv, p, (dst_off + v0 + j * T) * 16, 16))
+            st_vec_stream(d + v0 + j * T, x[j]);
+      };
       if constexpr (NT > 0) {
 #pragma unroll
-        for (int p = 0; p < NT; ++p) {
-          uint4* d = static_cast<uint4*>(a.recv[p]) + dst_off;
-#pragma unroll
-          for (int j = 0; j < kAgUnroll; ++j)
-            if (v0 + j * T < nv) st_vec_stream(d + v0 + j * T, x[j]);
-        }
+        for (int p = 0; p < NT; ++p) put(p);
       } else {
-        for (int p = 0; p < n; ++p) {
-          uint4* d = static_cast<uint4*>(a.recv[p]) + dst_off;
-#pragma unroll
-          for (int j = 0; j < kAgUnroll; ++j)
-            if (v0 + j * T < nv) st_vec_stream(d + v0 + j * T, x[j]);
-        }
+        for (int p = 0; p < n; ++p) put(p);
       }
     }
     return;
@@ -70,19 +69,15 @@ __global__ void __launch_bounds__(kThreads) k_allgather(DevComm dc, CollArgs a, 
   // inputs whose size is not a whole number of 16-byte vectors: element copies
   const size_t stride = (size_t)B * blockDim.x;
   const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
-  if (elem_bytes == 4) {
-    const uint32_t* src = static_cast<const uint32_t*>(a.send[rank]);
+  auto copy = [&](auto zero) {
+    using E = decltype(zero);
     for (size_t j = first; j < a.count; j += stride) {
-      const uint32_t x = src[j];
-      for (int p = 0; p < n; ++p) static_cast<uint32_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
+      const E x = get_elem<E>(dc, a, rank, j);
+      for (int p = 0; p < n; ++p) put_elem<E>(dc, a, p, (size_t)rank * a.count + j, x);
     }
-  } else {
-    const uint16_t* src = static_cast<const uint16_t*>(a.send[rank]);
-    for (size_t j = first; j < a.count; j += stride) {
-      const uint16_t x = src[j];
-      for (int p = 0; p < n; ++p) static_cast<uint16_t*>(a.recv[p])[(size_t)rank * a.count + j] = x;
-    }
-  }
+  };
+  if (elem_bytes == 4) copy(uint32_t{0});
+  else copy(uint16_t{0});
 }
 
 // Kernel tables (compile-time N for 1, 2, 4, 8, 16; a runtime-N instance

@@ -153,10 +153,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_allreduce_twoshot_bulk(DevC
   auto issue = [&](size_t k) {  // thread 0
     const int s = (int)(k % ST);
     const uint32_t bytes = tile_bytes(k);
-    mbar_arrive_expect_tx(&full[s], bytes * (uint32_t)n);
-    for (int p = 0; p < n; ++p)
-      bulk_load(in_base + ((size_t)s * n + p) * kBulkTile,
-                static_cast<const char*>(a.send[p]) + base + tile_off(k), bytes, &full[s]);
+    bool ok = true;  // bounds-checked build: a tile with a load outside its window loads nothing
+    for (int p = 0; p < n; ++p) ok = in_bounds(dc, a, kBufSend, p, base + tile_off(k), bytes) && ok;
+    mbar_arrive_expect_tx(&full[s], ok ? bytes * (uint32_t)n : 0u);
+    if (ok)
+      for (int p = 0; p < n; ++p)
+        bulk_load(in_base + ((size_t)s * n + p) * kBulkTile,
+                  static_cast<const char*>(a.send[p]) + base + tile_off(k), bytes, &full[s]);
   };
 
   if (threadIdx.x == 0) {
@@ -184,7 +187,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_allreduce_twoshot_bulk(DevC
     if (__syncthreads_or(failed)) break;
     if (threadIdx.x == 0) {
       const void* out = out_base + (size_t)s * kBulkTile;
-      for (int p = 0; p < n; ++p) bulk_store(static_cast<char*>(a.recv[p]) + base + tile_off(k), out, bytes);
+      for (int p = 0; p < n; ++p)
+        if (in_bounds(dc, a, kBufRecv, p, base + tile_off(k), bytes))
+          bulk_store(static_cast<char*>(a.recv[p]) + base + tile_off(k), out, bytes);
       bulk_commit();
       if (k + ST < mine) issue(k + ST);
     }
@@ -197,8 +202,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_allreduce_twoshot_bulk(DevC
   }
   const size_t i = nvec * L::VW + threadIdx.x;
   if (!failed && rank == n - 1 && blk == 0 && i < a.count) {
-    const S r = reduce_scalar<T>(a.send, n, i);
-    for (int p = 0; p < n; ++p) static_cast<S*>(a.recv[p])[i] = r;
+    const S r = reduce_scalar<T>(dc, a, n, i);
+    for (int p = 0; p < n; ++p) put_elem<S>(dc, a, p, i, r);
   }
 }
 
@@ -227,8 +232,9 @@ __global__ void __launch_bounds__(32, 1) k_allgather_bulk(DevComm dc, CollArgs a
   };
   auto issue = [&](size_t k) {
     const int s = (int)(k % kAgStages);
-    mbar_arrive_expect_tx(&full[s], len(k));
-    bulk_load(stage + (size_t)s * kAgTile, static_cast<const char*>(a.send[rank]) + off(k), len(k), &full[s]);
+    const bool ok = in_bounds(dc, a, kBufSend, rank, off(k), len(k));  // bounds-checked build
+    mbar_arrive_expect_tx(&full[s], ok ? len(k) : 0u);
+    if (ok) bulk_load(stage + (size_t)s * kAgTile, static_cast<const char*>(a.send[rank]) + off(k), len(k), &full[s]);
   };
   for (int s = 0; s < kAgStages; ++s) mbar_init(&full[s], 1);
   fence_mbar_init();
@@ -242,7 +248,8 @@ __global__ void __launch_bounds__(32, 1) k_allgather_bulk(DevComm dc, CollArgs a
       break;
     }
     for (int p = 0; p < n; ++p)
-      bulk_store(static_cast<char*>(a.recv[p]) + (size_t)rank * bytes + off(k), stage + (size_t)s * kAgTile, len(k));
+      if (in_bounds(dc, a, kBufRecv, p, (size_t)rank * bytes + off(k), len(k)))
+        bulk_store(static_cast<char*>(a.recv[p]) + (size_t)rank * bytes + off(k), stage + (size_t)s * kAgTile, len(k));
     bulk_commit();
     // refill the stage of the previous tile once its stores have read it
     if (k >= 1 && k - 1 + kAgStages < mine) {

@@ -141,35 +141,60 @@ template <>
 struct Lanes<__half> : HalfLanes<__half2, F16Ops> {};
 
 // ------------------------------------------------------------- reductions
+// get of vector v from rank p's input (a zero vector where the bounds-checked
+// build finds it outside the rank's window)
+__device__ __forceinline__ uint4 get_vec(const DevComm& dc, const CollArgs& a, int p, size_t v) {
+  return in_bounds(dc, a, kBufSend, p, v * 16, 16) ? ld_vec(static_cast<const uint4*>(a.send[p]) + v)
+                                                   : make_uint4(0, 0, 0, 0);
+}
+
+// put of vector v into buffer KIND (kBufRecv, kBufScratch) of rank p
+template <int KIND>
+__device__ __forceinline__ void put_vec(const DevComm& dc, const CollArgs& a, int p, size_t v, uint4 x) {
+  void* dst = KIND == kBufScratch ? a.scratch[p] : a.recv[p];
+  if (in_bounds(dc, a, KIND, p, v * 16, 16)) st_vec(static_cast<uint4*>(dst) + v, x);
+}
+
+// get / put of element i (the sub-vector tail and the element paths)
+template <typename S>
+__device__ __forceinline__ S get_elem(const DevComm& dc, const CollArgs& a, int p, size_t i) {
+  return in_bounds(dc, a, kBufSend, p, i * sizeof(S), sizeof(S)) ? static_cast<const S*>(a.send[p])[i] : S{};
+}
+template <typename S>
+__device__ __forceinline__ void put_elem(const DevComm& dc, const CollArgs& a, int p, size_t i, S x) {
+  if (in_bounds(dc, a, kBufRecv, p, i * sizeof(S), sizeof(S))) static_cast<S*>(a.recv[p])[i] = x;
+}
+
 // Sum (or, with OP, MAX / MIN: reduce_ops.cuh) of vector v over the N ranks'
-// buffers src[0..N-1], rank order.  With a compile-time N all N gets are
+// inputs a.send[0..N-1], rank order.  With a compile-time N all N gets are
 // issued before the first add.
 template <typename T, int NT, int OP = kOpSum>
-__device__ __forceinline__ uint4 reduce_vec(void* const* src, int n, size_t v) {
-  if constexpr (OP != kOpSum) return pick_ranks_vec<T, NT, OP>(src, n, v);
+__device__ __forceinline__ uint4 reduce_vec(const DevComm& dc, const CollArgs& a, int n, size_t v) {
+  if constexpr (OP != kOpSum) return pick_ranks_vec<T, NT, OP>(dc, a, n, v);
   using L = Lanes<T>;
   typename L::Acc acc;
   if constexpr (NT > 0) {
     uint4 x[NT];
 #pragma unroll
-    for (int p = 0; p < NT; ++p) x[p] = ld_vec(static_cast<const uint4*>(src[p]) + v);
+    for (int p = 0; p < NT; ++p) x[p] = get_vec(dc, a, p, v);
     L::init(acc, x[0]);
 #pragma unroll
     for (int p = 1; p < NT; ++p) L::add(acc, x[p]);
   } else {
-    L::init(acc, ld_vec(static_cast<const uint4*>(src[0]) + v));
-    for (int p = 1; p < n; ++p) L::add(acc, ld_vec(static_cast<const uint4*>(src[p]) + v));
+    L::init(acc, get_vec(dc, a, 0, v));
+    for (int p = 1; p < n; ++p) L::add(acc, get_vec(dc, a, p, v));
   }
   return L::pack(acc);
 }
 
 template <typename T, int OP = kOpSum>
-__device__ __forceinline__ typename Lanes<T>::S reduce_scalar(void* const* src, int n, size_t i) {
+__device__ __forceinline__ typename Lanes<T>::S reduce_scalar(const DevComm& dc, const CollArgs& a, int n,
+                                                             size_t i) {
   using L = Lanes<T>;
   using S = typename L::S;
-  if constexpr (OP != kOpSum) return pick_ranks_scalar<T, OP, S>(src, n, i);
-  typename L::SAcc acc = L::sinit(static_cast<const S*>(src[0])[i]);
-  for (int p = 1; p < n; ++p) acc = L::sadd(acc, static_cast<const S*>(src[p])[i]);
+  if constexpr (OP != kOpSum) return pick_ranks_scalar<T, OP, S>(dc, a, n, i);
+  typename L::SAcc acc = L::sinit(get_elem<S>(dc, a, 0, i));
+  for (int p = 1; p < n; ++p) acc = L::sadd(acc, get_elem<S>(dc, a, p, i));
   return L::spack(acc);
 }
 
@@ -216,7 +241,6 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   const int rank = blockIdx.x / B, blk = blockIdx.x % B;
   const size_t nvec = a.count / L::VW;
   const size_t tail0 = nvec * L::VW;
-  uint4* out = static_cast<uint4*>(a.recv[rank]);
   using S = typename L::S;
   if constexpr (EB) {
     if (!entry_barrier(dc, rank, n, blk)) return;
@@ -225,9 +249,9 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   if (!a.inplace) {
     const size_t stride = (size_t)B * blockDim.x;
     for (size_t v = (size_t)blk * blockDim.x + threadIdx.x; v < nvec; v += stride)
-      st_vec(out + v, reduce_vec<T, NT, OP>(a.send, n, v));
+      put_vec<kBufRecv>(dc, a, rank, v, reduce_vec<T, NT, OP>(dc, a, n, v));
     if (blk == 0 && tail0 + threadIdx.x < a.count)
-      static_cast<S*>(a.recv[rank])[tail0 + threadIdx.x] = reduce_scalar<T, OP>(a.send, n, tail0 + threadIdx.x);
+      put_elem<S>(dc, a, rank, tail0 + threadIdx.x, reduce_scalar<T, OP>(dc, a, n, tail0 + threadIdx.x));
     return;
   }
 
@@ -246,22 +270,22 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (u < U && v < nvec) res[u] = reduce_vec<T, NT, OP>(a.send, n, v);
+      if (u < U && v < nvec) res[u] = reduce_vec<T, NT, OP>(dc, a, n, v);
     }
     ok = group_barrier(dc, rank, n, blk, expected);
     if (!ok) break;
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (u < U && v < nvec) st_vec(out + v, res[u]);
+      if (u < U && v < nvec) put_vec<kBufRecv>(dc, a, rank, v, res[u]);
     }
   }
   if (ok && blk == 0 && tail0 < a.count) {  // same on every rank: all slot-0 CTAs take part
     const size_t i = tail0 + threadIdx.x;
     S r{};
-    if (i < a.count) r = reduce_scalar<T, OP>(a.send, n, i);
+    if (i < a.count) r = reduce_scalar<T, OP>(dc, a, n, i);
     ok = group_barrier(dc, rank, n, blk, expected);
-    if (ok && i < a.count) static_cast<S*>(a.recv[rank])[i] = r;
+    if (ok && i < a.count) put_elem<S>(dc, a, rank, i, r);
   }
   if (waiter) dc.expect[sem_slot(rank, threadIdx.x, blk)] = expected;
 }
@@ -288,18 +312,18 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot(DevComm dc, Coll
   }
   const size_t stride = (size_t)B * blockDim.x;
   for (size_t v = s0 + (size_t)blk * blockDim.x + threadIdx.x; v < s1; v += stride) {
-    const uint4 r = reduce_vec<T, NT, OP>(a.send, n, v);
+    const uint4 r = reduce_vec<T, NT, OP>(dc, a, n, v);
     if constexpr (NT > 0) {
 #pragma unroll
-      for (int p = 0; p < NT; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + v, r);
+      for (int p = 0; p < NT; ++p) put_vec<kBufRecv>(dc, a, p, v, r);
     } else {
-      for (int p = 0; p < n; ++p) st_vec(static_cast<uint4*>(a.recv[p]) + v, r);
+      for (int p = 0; p < n; ++p) put_vec<kBufRecv>(dc, a, p, v, r);
     }
   }
   const size_t i = nvec * L::VW + threadIdx.x;
   if (rank == n - 1 && blk == 0 && i < a.count) {
-    const S r = reduce_scalar<T, OP>(a.send, n, i);
-    for (int p = 0; p < n; ++p) static_cast<S*>(a.recv[p])[i] = r;
+    const S r = reduce_scalar<T, OP>(dc, a, n, i);
+    for (int p = 0; p < n; ++p) put_elem<S>(dc, a, p, i, r);
   }
 }
 
@@ -329,9 +353,12 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
     if (!entry_barrier(dc, rank, n, blk)) return;
   }
   uint4* mine = static_cast<uint4*>(a.scratch[rank]);
-  for (size_t v = s0 + first; v < s1; v += stride) st_vec(mine + (v - s0), reduce_vec<T, NT>(a.send, n, v));
-  if (rank == n - 1 && tail_thread)
-    reinterpret_cast<S*>(mine + (s1 - s0))[threadIdx.x] = reduce_scalar<T>(a.send, n, tail_i);
+  for (size_t v = s0 + first; v < s1; v += stride) put_vec<kBufScratch>(dc, a, rank, v - s0, reduce_vec<T, NT>(dc, a, n, v));
+  if (rank == n - 1 && tail_thread) {
+    const S r = reduce_scalar<T>(dc, a, n, tail_i);
+    if (in_bounds(dc, a, kBufScratch, rank, (s1 - s0) * 16 + threadIdx.x * sizeof(S), sizeof(S)))
+      reinterpret_cast<S*>(mine + (s1 - s0))[threadIdx.x] = r;
+  }
 
   unsigned long long expected = 0;
   const bool waiter = (int)threadIdx.x < n && (int)threadIdx.x != rank;
@@ -340,15 +367,23 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_twoshot_scratch(DevComm 
   if (waiter) dc.expect[sem_slot(rank, threadIdx.x, blk)] = expected;
   if (!ok) return;
 
-  uint4* out = static_cast<uint4*>(a.recv[rank]);
   for (int q = 0; q < n; ++q) {
     size_t q0, q1;
     shard_vecs(nvec, n, q, q0, q1);
     MemoryChannel ch = MemoryChannel::make(dc, rank, q, blk, a.scratch[q], nullptr);
-    for (size_t v = q0 + first; v < q1; v += stride) st_vec(out + v, ld_vec_l2(reinterpret_cast<const uint4*>(ch.remote_src) + (v - q0)));
-    if (q == n - 1 && tail_thread)
-      static_cast<S*>(a.recv[rank])[tail_i] = __ldcg(reinterpret_cast<const S*>(
-          reinterpret_cast<const uint4*>(ch.remote_src) + (q1 - q0)) + threadIdx.x);
+    for (size_t v = q0 + first; v < q1; v += stride) {
+      const uint4 x = in_bounds(dc, a, kBufScratch, q, (v - q0) * 16, 16)
+                          ? ld_vec_l2(reinterpret_cast<const uint4*>(ch.remote_src) + (v - q0))
+                          : make_uint4(0, 0, 0, 0);
+      put_vec<kBufRecv>(dc, a, rank, v, x);
+    }
+    if (q == n - 1 && tail_thread) {
+      const size_t off = (q1 - q0) * 16 + threadIdx.x * sizeof(S);
+      const S x = in_bounds(dc, a, kBufScratch, q, off, sizeof(S))
+                      ? __ldcg(reinterpret_cast<const S*>(ch.remote_src + off))
+                      : S{};
+      put_elem<S>(dc, a, rank, tail_i, x);
+    }
   }
 }
 
@@ -371,12 +406,10 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(DevComm dc, CollArg
   const size_t first = (size_t)blk * blockDim.x + threadIdx.x;
   if ((m * sizeof(S)) % 16 == 0) {
     const size_t nv = m / L::VW, base = (size_t)rank * nv;
-    uint4* out = static_cast<uint4*>(a.recv[rank]);
-    for (size_t v = first; v < nv; v += stride) st_vec(out + v, reduce_vec<T, NT, OP>(a.send, n, base + v));
+    for (size_t v = first; v < nv; v += stride) put_vec<kBufRecv>(dc, a, rank, v, reduce_vec<T, NT, OP>(dc, a, n, base + v));
   } else {
-    S* out = static_cast<S*>(a.recv[rank]);
     const size_t base = (size_t)rank * m;
-    for (size_t j = first; j < m; j += stride) out[j] = reduce_scalar<T, OP>(a.send, n, base + j);
+    for (size_t j = first; j < m; j += stride) put_elem<S>(dc, a, rank, j, reduce_scalar<T, OP>(dc, a, n, base + j));
   }
 }
 

@@ -96,6 +96,7 @@ struct dcc_comm {
   int fused_bulk = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier
   bool pdl = true;             // DCC_PDL / dcc_set_pdl: programmatic dependent launch of the wait-free kernels
+  bool ring_cluster = true;    // DCC_RING_CLUSTER=0: the ring barrier through L2 even when the ranks fit one cluster
   int inplace_unroll = 0;      // DCC_INPLACE_UNROLL: force the in-place one-shot's vectors per thread
   bool ag_bulk = false;  // DCC_AG_BULK=1: AllGather through the bulk-copy pipeline when aligned and large
   bool zero_copy = true;  // host-buffer AllReduce reads/writes mapped pinned host memory directly
@@ -202,18 +203,39 @@ inline int check_buffers(const dcc_comm* c, void* const* send, size_t send_bytes
   return DCC_OK;
 }
 
+// Bounds-checked build (DCC_CHECK_BOUNDS): the bytes a kernel may touch from
+// pointer `rank` of buffer `kind` -- the call's own range, which the host
+// checks already lies inside a registered window.  A no-op otherwise.
+template <typename A>
+inline void set_extent(A& a, int kind, int rank, size_t bytes) {
+#if DCC_CHECK_BOUNDS
+  a.ext[kind][rank] = bytes;
+#else
+  (void)a; (void)kind; (void)rank; (void)bytes;
+#endif
+}
+
 // pdl: launch with programmatic stream serialization (only kernels that open
 // with pdl_prologue() and whose CTAs never wait on one another; never together
 // with a cooperative launch).
+// cluster > 0: thread-block clusters of that many CTAs along x (grid a
+// multiple of it; never together with the other two).
 inline int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s,
-           size_t smem = 0, bool pdl = false) {
+           size_t smem = 0, bool pdl = false, int cluster = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if (cooperative) {
+  if (cluster > 0) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else if (cooperative) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;

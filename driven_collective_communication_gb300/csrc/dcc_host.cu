@@ -282,6 +282,10 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
   }
   args.count = count;
   args.inplace = inplace ? 1 : 0;
+  for (int r = 0; r < c->n; ++r) {
+    set_extent(args, dcc::kBufSend, r, bytes);
+    set_extent(args, dcc::kBufRecv, r, bytes);
+  }
   if (algo == DCC_ALGO_TWO_SHOT_SCRATCH) {
     for (int r = 0; r < c->n; ++r) {
       size_t b, e;
@@ -294,6 +298,7 @@ int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t coun
         if (overlaps(w.ptr, need, send[p], bytes) || overlaps(w.ptr, need, recv[p], bytes))
           return DCC_ERR_INVALID_ARG;
       args.scratch[r] = w.ptr;
+      set_extent(args, dcc::kBufScratch, r, need);
     }
   }
   Shape sh;
@@ -336,7 +341,8 @@ bool visit_kernels(F&& visit) {
         !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_bulk_kernel<__half>(n)))
       return false;
-  return v(dcc::ring_barrier_kernel()) && v(dcc::channel_put_kernel()) && v(dcc::channel_get_kernel());
+  return v(dcc::ring_barrier_kernel()) && v(dcc::ring_barrier_cluster_kernel()) && v(dcc::channel_put_kernel()) &&
+         v(dcc::channel_get_kernel());
 }
 
 }  // namespace
@@ -415,6 +421,12 @@ int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   }
   a.rows = rows;
   a.kp = kp;
+  for (int r = 0; r < c->n; ++r) {
+    set_extent(a, dcc::kBufSend, r, wb);
+    set_extent(a, dcc::kBufX, r, xb);
+    set_extent(a, dcc::kBufRecv, r, yb);
+    set_extent(a, dcc::kBufResidual, r, residual ? yb : 0);
+  }
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &a};
   if (c->fused_bulk > 0 || (c->fused_bulk < 0 && kp >= kFusedBulkMinKp)) {
@@ -450,6 +462,7 @@ const char* dcc_error_string(int code) {
     case DCC_ERR_LAUNCH: return "DCC_ERR_LAUNCH";
     case DCC_ERR_TIMEOUT: return "DCC_ERR_TIMEOUT";
     case DCC_ERR_UNSUPPORTED: return "DCC_ERR_UNSUPPORTED";
+    case DCC_ERR_BOUNDS: return "DCC_ERR_BOUNDS";
     default: return "DCC_ERR_UNKNOWN";
   }
 }
@@ -554,6 +567,7 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   }
   c->entry_barrier = env_flag("DCC_ENTRY_BARRIER");
   if (const char* v = std::getenv("DCC_PDL")) c->pdl = std::strcmp(v, "0") != 0;
+  if (const char* v = std::getenv("DCC_RING_CLUSTER")) c->ring_cluster = std::strcmp(v, "0") != 0;
   c->dev.sem = c->d_block;
   c->dev.expect = c->d_block + sem_words;
   c->dev.status = c->d_block + sem_words + dcc::kSemSlots + 8;  // own 64-byte line
@@ -747,6 +761,10 @@ int dcc_reduce_scatter_op(dcc_comm_t c, void* const* send, void* const* recv, si
     args.recv[r] = recv[r];
   }
   args.count = recv_count;
+  for (int r = 0; r < c->n; ++r) {
+    set_extent(args, dcc::kBufSend, r, sb);
+    set_extent(args, dcc::kBufRecv, r, rb);
+  }
   // with the entry barrier the CTAs wait on one another: one cooperative wave
   const bool coop = c->entry_barrier && c->n > 1;
   const void* fn = op_kernel_for(t, (int)op, coop ? dcc::kReduceScatterEB : dcc::kReduceScatter, c->n);
@@ -783,6 +801,10 @@ int dcc_allgather(dcc_comm_t c, void* const* send, void* const* recv, size_t sen
     args.recv[r] = recv[r];
   }
   args.count = send_count;
+  for (int r = 0; r < c->n; ++r) {
+    set_extent(args, dcc::kBufSend, r, sb);
+    set_extent(args, dcc::kBufRecv, r, rb);
+  }
   int eb = (int)elem_bytes(t);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &args, &eb};
@@ -829,6 +851,13 @@ int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {
   if (!ds.ok()) return DCC_ERR_CUDA;
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &iters};
+  // up to 8 ranks (the portable cluster size) the token goes through
+  // distributed shared memory, one CTA per rank in one cluster
+  if (c->ring_cluster && c->n <= 8) {
+    const int rc = launch(dcc::ring_barrier_cluster_kernel(), c->n, 32, false, kargs, static_cast<cudaStream_t>(s), 0,
+                          false, c->n);
+    if (rc != DCC_ERR_CUDA) return rc;  // a cluster shape the device refuses: the global-memory ring instead
+  }
   return launch(dcc::ring_barrier_kernel(), c->n, 32, true, kargs, static_cast<cudaStream_t>(s));
 }
 
@@ -846,10 +875,16 @@ int dcc_comm_check(dcc_comm_t c, dcc_stream_t s) {
     return DCC_ERR_CUDA;
   }
   if (st != 0 && c->sticky == DCC_OK) {
-    c->sticky = DCC_ERR_TIMEOUT;
     c->err_rank = (int)((st >> 8) & 0xFF);
     c->err_peer = (int)((st >> 16) & 0xFF);
-    c->err_block = (int)((st >> 24) & 0xFFFF);
+    if ((st & 0xFF) == dcc::kStatusBounds) {  // bounds-checked build: buffer kind, 16-byte offset
+      const unsigned long long off = st >> 24;
+      c->sticky = DCC_ERR_BOUNDS;
+      c->err_block = off > 0x7fffffffull ? 0x7fffffff : (int)off;
+    } else {
+      c->sticky = DCC_ERR_TIMEOUT;
+      c->err_block = (int)((st >> 24) & 0xFFFF);
+    }
   }
   return c->sticky;
 }

@@ -25,6 +25,22 @@ __host__ __device__ inline unsigned long long pack_status(unsigned long long cod
          ((unsigned long long)(peer & 0xFF) << 16) | ((unsigned long long)(blk & 0xFFFF) << 24);
 }
 
+// Bounds-checked build (compiled with -DDCC_CHECK_BOUNDS=1, libdcc_checked.so):
+// every data access of the collectives and the fused layer is checked against
+// the extent of the registered window its pointer lies in; the first access
+// outside is skipped and recorded as
+//   bits 0..7 code 2, 8..15 the buffer's rank, 16..23 the buffer kind,
+//   24..63 the offending byte offset / 16 from the buffer pointer.
+#ifndef DCC_CHECK_BOUNDS
+#define DCC_CHECK_BOUNDS 0
+#endif
+constexpr unsigned long long kStatusBounds = 2ull;
+enum BufKind { kBufSend = 0, kBufRecv = 1, kBufScratch = 2, kBufX = 3, kBufResidual = 4, kNumBufKinds = 5 };
+__host__ __device__ inline unsigned long long pack_bounds(int rank, int kind, size_t byte_off) {
+  return kStatusBounds | ((unsigned long long)(rank & 0xFF) << 8) | ((unsigned long long)(kind & 0xFF) << 16) |
+         (((unsigned long long)(byte_off / 16) & ((1ull << 40) - 1)) << 24);
+}
+
 // Device view of a communicator, passed by value to every kernel.
 struct DevComm {
   int n;                        // virtual ranks
@@ -58,6 +74,9 @@ struct CollArgs {
   int blocks;     // CTAs per rank
   int inplace;    // some rank has send == recv
   int unroll;     // in-place one-shot: vectors per thread per chunk (1..4; 0 = 4)
+#if DCC_CHECK_BOUNDS
+  size_t ext[kNumBufKinds][DCC_MAX_RANKS];  // bytes from each pointer to its window's end
+#endif
 };
 
 // Arguments of the primitive (put/get) kernels.

@@ -49,6 +49,9 @@ struct LinearArgs {
   void* y[DCC_MAX_RANKS];               // rows
   size_t rows, kp;
   int blocks;
+#if DCC_CHECK_BOUNDS
+  size_t ext[kNumBufKinds][DCC_MAX_RANKS];  // weight: kBufSend, y: kBufRecv, x: kBufX, residual: kBufResidual
+#endif
 };
 
 template <typename T>
@@ -68,8 +71,11 @@ static_assert(DCC_MAX_RANKS <= 32, "lane q of warp 0 serves output rank q");
 // Lane q < N of warp 0: residual q's two rows of item v (0 without
 // residuals).  Loaded when the item starts, so that the load overlaps the
 // weight stream instead of adding a memory round trip to the epilogue.
-__device__ __forceinline__ uint32_t load_residual(const LinearArgs& a, int n, int lane, size_t v) {
-  return a.residual[0] != nullptr && lane < n ? static_cast<const uint32_t*>(a.residual[lane])[v] : 0u;
+__device__ __forceinline__ uint32_t load_residual(const DevComm& dc, const LinearArgs& a, int n, int lane,
+                                                  size_t v) {
+  return a.residual[0] != nullptr && lane < n && in_bounds(dc, a, kBufResidual, lane, v * 4, 4)
+             ? static_cast<const uint32_t*>(a.residual[lane])[v]
+             : 0u;
 }
 
 // Puts item v's two rows (fp32 sums y0, y1) into the N outputs: one packed
@@ -79,13 +85,13 @@ __device__ __forceinline__ uint32_t load_residual(const LinearArgs& a, int n, in
 // writes output q, so they may be the same buffer (the in-place
 // residual-stream update).
 template <typename T>
-__device__ __forceinline__ void put_rows(const LinearArgs& a, int n, int lane, size_t v, float y0, float y1,
-                                         uint32_t res) {
+__device__ __forceinline__ void put_rows(const DevComm& dc, const LinearArgs& a, int n, int lane, size_t v,
+                                         float y0, float y1, uint32_t res) {
   using L = Lanes<T>;
   if (a.residual[0] == nullptr) {
     const uint32_t packed = L::narrow2(y0, y1);
-    if (lane < n) static_cast<uint32_t*>(a.y[lane])[v] = packed;
-  } else if (lane < n) {
+    if (lane < n && in_bounds(dc, a, kBufRecv, lane, v * 4, 4)) static_cast<uint32_t*>(a.y[lane])[v] = packed;
+  } else if (lane < n && in_bounds(dc, a, kBufRecv, lane, v * 4, 4)) {
     const float2 r = L::widen2(res);
     static_cast<uint32_t*>(a.y[lane])[v] = L::narrow2(__fadd_rn(y0, r.x), __fadd_rn(y1, r.y));
   }
@@ -97,16 +103,9 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Asks L2 to fetch [p, p + bytes) from memory (bytes a multiple of 16, p
-// 16-byte aligned).  A prefetch returns no data to the thread, so it may be
-// issued before the programmatic-dependent-launch wait: whatever the previous
-// kernel writes later still lands in L2, which the loads after the wait read.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 template <typename T, int NT>
 __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, LinearArgs a) {
+  pdl_prologue();
   constexpr int R = kFusedRows, V = kFusedVecs;
   static_assert(R == 2, "the epilogue packs two rows per item");
   const int n = NT > 0 ? NT : dc.n;
@@ -118,16 +117,8 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
   __shared__ float part_s[DCC_MAX_RANKS][R];
   size_t s0, s1;
   shard_vecs(items, n, rank, s0, s1);
-  // The weight rows of the CTA's first item start their way into L2 while the
-  // previous kernel on the stream may still be finishing (launched with
-  // programmatic dependent launch, this CTA can start before it ends); the
-  // rows are contiguous per rank, one prefetch per rank.
-  if (lane == 0 && s0 + blk < s1 && R * kv * 16 <= 0xffffffffu)
-    for (int p = warp; p < n; p += nwarps)
-      prefetch_l2(static_cast<const uint4*>(a.weight[p]) + (s0 + blk) * R * kv, (uint32_t)(R * kv * 16));
-  pdl_prologue();
   for (size_t v = s0 + blk; v < s1; v += B) {
-    const uint32_t res = warp == 0 ? load_residual(a, n, lane, v) : 0u;
+    const uint32_t res = warp == 0 ? load_residual(dc, a, n, lane, v) : 0u;
     // warp w computes the partial products of ranks w, w + nwarps, ... for
     // the item's rows; the ranks' partials meet in shared memory
     for (int p = warp; p < n; p += nwarps) {
@@ -142,9 +133,11 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
         for (int j = 0; j < V; ++j) {
           const size_t k = k0 + j * 32 + lane;
           const bool in = k < kv;
-          xv[j] = in ? ld_vec(x + k) : make_uint4(0, 0, 0, 0);
+          xv[j] = in && in_bounds(dc, a, kBufX, p, k * 16, 16) ? ld_vec(x + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int r = 0; r < R; ++r) wv[r][j] = in ? ld_vec(w + r * kv + k) : make_uint4(0, 0, 0, 0);
+          for (int r = 0; r < R; ++r)
+            wv[r][j] = in && in_bounds(dc, a, kBufSend, p, ((v * R + r) * kv + k) * 16, 16) ? ld_vec(w + r * kv + k)
+                                                                                            : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int j = 0; j < V; ++j)
@@ -167,7 +160,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce(DevComm dc, 
         for (int p = 1; p < n; ++p) acc = __fadd_rn(acc, part_s[p][lane]);
       }
       const float y0 = __shfl_sync(0xffffffffu, acc, 0), y1 = __shfl_sync(0xffffffffu, acc, 1);
-      put_rows<T>(a, n, lane, v, y0, y1, res);
+      put_rows<T>(dc, a, n, lane, v, y0, y1, res);
     }
     // kept even after the CTA's last item: skipping it there measured slower
     // on GB300 (32.4 vs 26.2 us at 8 ranks x 8192 rows x kp 1024)

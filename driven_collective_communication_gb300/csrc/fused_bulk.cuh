@@ -78,11 +78,14 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
     const int u = (int)(g % ST), p = t / nch, c = t % nch;
     const uint32_t bytes = (uint32_t)(chunk_elems(c) * 2);
     unsigned char* st = stage0 + (size_t)u * kFusedBulkStageBytes;
-    mbar_arrive_expect_tx(&full[u], bytes * (RI + 1));
-    const char* w = static_cast<const char*>(a.weight[p]) + (v * RI * kp + (size_t)c * kFusedBulkChunk) * 2;
+    const size_t woff = (v * RI * kp + (size_t)c * kFusedBulkChunk) * 2, xoff = (size_t)c * kFusedBulkChunk * 2;
+    bool ok = in_bounds(dc, a, kBufX, p, xoff, bytes);  // bounds-checked build: a bad tile loads nothing
+    for (int r = 0; r < RI; ++r) ok = in_bounds(dc, a, kBufSend, p, woff + (size_t)r * kp * 2, bytes) && ok;
+    mbar_arrive_expect_tx(&full[u], ok ? bytes * (RI + 1) : 0u);
+    if (!ok) return;
+    const char* w = static_cast<const char*>(a.weight[p]) + woff;
     for (int r = 0; r < RI; ++r) bulk_load(st + r * ROWB, w + (size_t)r * kp * 2, bytes, &full[u]);
-    bulk_load(st + RI * ROWB, static_cast<const char*>(a.x[p]) + (size_t)c * kFusedBulkChunk * 2, bytes,
-              &full[u]);
+    bulk_load(st + RI * ROWB, static_cast<const char*>(a.x[p]) + xoff, bytes, &full[u]);
   };
 
   if (threadIdx.x == 0) {
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
     for (int u = 0; u < ST; ++u) issue_next(iv, it);
 
   for (size_t v = s0 + (size_t)blk; v < s1 && !failed; v += (size_t)B) {
-    const uint32_t res = warp == 0 ? load_residual(a, n, lane, v) : 0u;
+    const uint32_t res = warp == 0 ? load_residual(dc, a, n, lane, v) : 0u;
     float acc = 0.0f;
     for (int t = 0; t < ntiles; ++t, ++g) {
       const int u = (int)(g % ST), p = t / nch, c = t % nch;
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_linear_allreduce_bulk(DevComm
         }
       }
       const float y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 1);
-      put_rows<T>(a, n, lane, v, y0, y1, res);
+      put_rows<T>(dc, a, n, lane, v, y0, y1, res);
     }
     __syncthreads();  // part_s is rewritten by the next item
   }

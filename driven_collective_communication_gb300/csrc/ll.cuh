@@ -153,10 +153,10 @@ __device__ __forceinline__ bool ll_reduce(const DevComm& dc, int n, int rank, in
 
 // The element tail (< one vector) travels as one zero-padded vector at index nvec.
 template <typename T>
-__device__ __forceinline__ uint4 load_padded(const void* buf, size_t nvec, size_t count) {
+__device__ __forceinline__ uint4 load_padded(const DevComm& dc, const CollArgs& a, int rank, size_t nvec) {
   using S = typename Lanes<T>::S;
   S e[16 / sizeof(S)] = {};
-  for (size_t i = nvec * Lanes<T>::VW, k = 0; i < count; ++i, ++k) e[k] = static_cast<const S*>(buf)[i];
+  for (size_t i = nvec * Lanes<T>::VW, k = 0; i < a.count; ++i, ++k) e[k] = get_elem<S>(dc, a, rank, i);
   uint4 x;
   memcpy(&x, e, 16);
   return x;
@@ -175,18 +175,17 @@ __global__ void __launch_bounds__(kLLThreads) k_allreduce_oneshot_ll(DevComm dc,
   const size_t nvec = a.count / L::VW;
   const size_t nv = nvec + (a.count % L::VW ? 1 : 0);
   const size_t first = (size_t)blk * kLLThreads + threadIdx.x, stride = (size_t)kLLBlocks * kLLThreads;
-  const uint4* src = static_cast<const uint4*>(a.send[rank]);
   uint4* mine = reinterpret_cast<uint4*>(dc.ll_buf + (size_t)rank * kLLBufBytes);
 
   // publish: my input as packets (the owner of index nvec also publishes the padded tail)
   for (size_t v = first; v < nvec; v += stride) {
-    const uint4 x = ld_vec(src + v);
+    const uint4 x = get_vec(dc, a, rank, v);
     st_ll(mine + 2 * v, x.x, x.y, flag);
     st_ll(mine + 2 * v + 1, x.z, x.w, flag);
   }
   const bool tail_owner = nv > nvec && (nvec % stride) == first;
   if (tail_owner) {
-    const uint4 x = load_padded<T>(a.send[rank], nvec, a.count);
+    const uint4 x = load_padded<T>(dc, a, rank, nvec);
     st_ll(mine + 2 * nvec, x.x, x.y, flag);
     st_ll(mine + 2 * nvec + 1, x.z, x.w, flag);
   }
@@ -194,16 +193,16 @@ __global__ void __launch_bounds__(kLLThreads) k_allreduce_oneshot_ll(DevComm dc,
   bool ok = true;
   for (size_t v = first; v < nvec && ok; v += stride) {
     uint4 r;
-    ok = ll_reduce<T, NT>(dc, n, rank, blk, v, flag, ld_vec(src + v), r);
-    if (ok) st_vec(static_cast<uint4*>(a.recv[rank]) + v, r);
+    ok = ll_reduce<T, NT>(dc, n, rank, blk, v, flag, get_vec(dc, a, rank, v), r);
+    if (ok) put_vec<kBufRecv>(dc, a, rank, v, r);
   }
   if (ok && tail_owner) {
     uint4 r;
-    ok = ll_reduce<T, NT>(dc, n, rank, blk, nvec, flag, load_padded<T>(a.send[rank], nvec, a.count), r);
+    ok = ll_reduce<T, NT>(dc, n, rank, blk, nvec, flag, load_padded<T>(dc, a, rank, nvec), r);
     if (ok) {
       S e[16 / sizeof(S)];
       memcpy(e, &r, 16);
-      for (size_t i = nvec * L::VW, k = 0; i < a.count; ++i, ++k) static_cast<S*>(a.recv[rank])[i] = e[k];
+      for (size_t i = nvec * L::VW, k = 0; i < a.count; ++i, ++k) put_elem<S>(dc, a, rank, i, e[k]);
     }
   }
   __syncthreads();

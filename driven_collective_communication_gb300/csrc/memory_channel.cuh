@@ -76,6 +76,26 @@ __device__ __forceinline__ uint4 ld_vec(const uint4* p) { return *p; }
 __device__ __forceinline__ uint4 ld_vec_l2(const uint4* p) { return __ldcg(p); }
 __device__ __forceinline__ void st_vec(uint4* p, uint4 v) { *p = v; }
 
+// Bounds check of one data access (bounds-checked build only; otherwise a
+// constant true that the compiler removes): [off, off + bytes) from the
+// pointer of buffer `kind` of `rank` must lie inside the extent the host put
+// in a.ext.  On a violation the first one is recorded in the status word and
+// the caller skips the access, so the kernel's control flow (and every
+// barrier in it) stays the same and the kernel ends normally.
+template <typename A>
+__device__ __forceinline__ bool in_bounds(const DevComm& dc, const A& a, int kind, int rank, size_t off,
+                                          size_t bytes) {
+#if DCC_CHECK_BOUNDS
+  const size_t e = a.ext[kind][rank];
+  if (off <= e && bytes <= e - off) return true;
+  atomicCAS(dc.status, 0ull, pack_bounds(rank, kind, off));
+  return false;
+#else
+  (void)dc; (void)a; (void)kind; (void)rank; (void)off; (void)bytes;
+  return true;
+#endif
+}
+
 // ---------------------------------------------------------------- channel
 struct MemoryChannel {
   const char* remote_src;                 // peer memory this rank gets from

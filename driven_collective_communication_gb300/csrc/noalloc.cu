@@ -101,6 +101,15 @@ const void* scratch_kernel(dcc_dtype_t t, int n) {
   }
 }
 
+// the bounds-checked build's extent of pointer `rank` of buffer `kind`
+void dcc_set_extent_(dcc::CollArgs& a, int kind, int rank, size_t bytes) {
+#if DCC_CHECK_BOUNDS
+  a.ext[kind][rank] = bytes;
+#else
+  (void)a; (void)kind; (void)rank; (void)bytes;
+#endif
+}
+
 size_t elem_size(dcc_dtype_t t) {
   return (t == DCC_INT32 || t == DCC_FP32) ? 4 : (t == DCC_FP16 || t == DCC_BF16) ? 2 : 0;
 }
@@ -188,6 +197,12 @@ extern "C" int dcc_allreduce_noalloc(int n_ranks, void* const* send, void* const
   a.count = count;
   a.blocks = blocks;
   a.inplace = inplace ? 1 : 0;
+  for (int r = 0; r < n_ranks; ++r) {
+    dcc_set_extent_(a, dcc::kBufSend, r, bytes);
+    dcc_set_extent_(a, dcc::kBufRecv, r, bytes);
+    // rank r's shard: `per` vectors, the last rank also the remaining vectors and the element tail
+    dcc_set_extent_(a, dcc::kBufScratch, r, r == n_ranks - 1 ? bytes - per * (size_t)r * 16 : per * 16);
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(s);
   cudaLaunchConfig_t cfg = {};

@@ -151,28 +151,32 @@ struct PickVec {
 // compile-time N all N gets are issued before the first combine.  A NaN is
 // canonical for every N, one rank included.
 template <typename T, int NT, int OP>
-__device__ __forceinline__ uint4 pick_ranks_vec(void* const* src, int n, size_t v) {
+__device__ __forceinline__ uint4 pick_ranks_vec(const DevComm& dc, const CollArgs& a, int n, size_t v) {
   PickVec<T, OP> acc;
+  auto get = [&](int p) {
+    return in_bounds(dc, a, kBufSend, p, v * 16, 16) ? ld_vec(static_cast<const uint4*>(a.send[p]) + v)
+                                                     : make_uint4(0, 0, 0, 0);
+  };
   if constexpr (NT > 0) {
     uint4 x[NT];
 #pragma unroll
-    for (int p = 0; p < NT; ++p) x[p] = ld_vec(static_cast<const uint4*>(src[p]) + v);
+    for (int p = 0; p < NT; ++p) x[p] = get(p);
     acc.init(x[0]);
 #pragma unroll
     for (int p = 1; p < NT; ++p) acc.add(x[p]);
   } else {
-    acc.init(ld_vec(static_cast<const uint4*>(src[0]) + v));
-    for (int p = 1; p < n; ++p) acc.add(ld_vec(static_cast<const uint4*>(src[p]) + v));
+    acc.init(get(0));
+    for (int p = 1; p < n; ++p) acc.add(get(p));
   }
   return acc.result();
 }
 
 // one element i; S is the element's storage type (int32_t, float, uint16_t)
 template <typename T, int OP, typename S>
-__device__ __forceinline__ S pick_ranks_scalar(void* const* src, int n, size_t i) {
+__device__ __forceinline__ S pick_ranks_scalar(const DevComm& dc, const CollArgs& a, int n, size_t i) {
   static_assert(sizeof(S) == sizeof(T), "storage type");
   auto bits = [&](int p) {
-    S x = static_cast<const S*>(src[p])[i];
+    S x = in_bounds(dc, a, kBufSend, p, i * sizeof(S), sizeof(S)) ? static_cast<const S*>(a.send[p])[i] : S{};
     uint32_t b = 0;
     memcpy(&b, &x, sizeof(S));
     return b;

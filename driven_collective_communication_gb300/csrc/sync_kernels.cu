@@ -32,6 +32,95 @@ __global__ void k_ring_barrier(DevComm dc, int iters) {
   *from_prev.local_expect = expected;
 }
 
+// The same ring with the N ranks as the N CTAs of one thread-block cluster
+// (N <= 8), which the hardware schedules together on one GPC.  The token then
+// travels through distributed shared memory: signal is a release-ordered
+// arrive (cluster scope) on the next rank's mbarrier, wait an acquire-ordered
+// poll of the rank's own mbarrier phase.  Measured on GB300, 8 ranks: 0.26 us
+// per hop against 0.76 us for the same release/acquire pair through L2, where
+// every other signal and poll form measured the same 0.76 us (relaxed polls
+// with a fence after: 0.89 us).  Cluster scope orders every memory access of
+// the cluster's threads, global memory included, so the barrier orders the
+// ranks' data as the global-memory one does.  At the end each rank adds its
+// signals sent to the channel's inbound counter of the next rank and its
+// completed waits to its own waiter count, so the communicator's counters read
+// as after the global-memory ring (and either kernel may follow the other).
+// Waits are bounded as MemoryChannel::wait; every CTA reaches the closing
+// cluster barrier (a peer may still arrive on its mbarrier until then).
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void k_ring_barrier_cluster(DevComm dc, int iters) {
+  __shared__ __align__(8) unsigned long long bar;
+  const int n = dc.n, rank = (int)cluster_ctarank();
+  const int next = (rank + 1) % n, prev = (rank + n - 1) % n;
+  const uint32_t my_bar = (uint32_t)__cvta_generic_to_shared(&bar);
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(my_bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  cluster_barrier();  // every rank's mbarrier exists before the first arrive
+  if (threadIdx.x == 0) {
+    uint32_t next_bar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(next_bar) : "r"(my_bar), "r"((uint32_t)next));
+    unsigned long long sent = 0, waited = 0;
+    auto signal = [&]() {
+      if (dc.skip_signal_rank == rank) return;  // test knob: a lost signal
+      asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(next_bar) : "memory");
+      ++sent;
+    };
+    auto poll = [&](uint32_t parity) {
+      uint32_t done;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(my_bar), "r"(parity)
+          : "memory");
+      return done != 0;
+    };
+    // one arrive completes a phase; at most one token is in flight per rank
+    auto wait = [&]() {
+      const uint32_t parity = (uint32_t)(waited & 1ull);
+      if (!poll(parity)) {
+        const unsigned long long t0 = global_timer_ns();
+        for (unsigned it = 1;; ++it) {
+          if (poll(parity)) break;
+          if ((it & 31u) == 0) {
+            if (ld_relaxed_gpu(dc.status) != 0ull) return false;
+            if (global_timer_ns() - t0 > dc.timeout_ns) {
+              atomicCAS(dc.status, 0ull, pack_status(kStatusTimeout, rank, prev, 0));
+              return false;
+            }
+          }
+        }
+      }
+      ++waited;
+      return true;
+    };
+    for (int it = 0; it < iters; ++it) {
+      if (rank == 0) {
+        signal();
+        if (!wait()) break;
+      } else {
+        if (!wait()) break;
+        signal();
+      }
+    }
+    if (sent) red_release_gpu_add(dc.sem + sem_slot(next, rank, 0) * kSemWords, sent);
+    dc.expect[sem_slot(rank, prev, 0)] += waited;
+  }
+  __syncthreads();
+  cluster_barrier();
+}
+
 // CTA 0 plays src: put, then (optionally) flush + signal.  CTA 1 plays dst:
 // waits for that signal on its own channel to src.
 __global__ void k_channel_put(DevComm dc, PrimArgs pa) {
@@ -61,6 +150,7 @@ __global__ void k_channel_get(DevComm dc, PrimArgs pa) {
 }
 
 const void* ring_barrier_kernel() { return reinterpret_cast<const void*>(&k_ring_barrier); }
+const void* ring_barrier_cluster_kernel() { return reinterpret_cast<const void*>(&k_ring_barrier_cluster); }
 const void* channel_put_kernel() { return reinterpret_cast<const void*>(&k_channel_put); }
 const void* channel_get_kernel() { return reinterpret_cast<const void*>(&k_channel_get); }
 

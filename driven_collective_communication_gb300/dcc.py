@@ -15,11 +15,15 @@ import os
 import torch  # loads the CUDA runtime that libdcc shares
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdcc.so")
+# DCC_CHECK_BOUNDS=1 in the environment selects the bounds-checked build of the
+# same library (every kernel data access checked; build with build(checked=True))
+CHECKED = os.environ.get("DCC_CHECK_BOUNDS", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libdcc_checked.so" if CHECKED else "libdcc.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libdcc.so is not built (expected at %s); run "
-                      "`python -c 'import __graft_entry__ as g; g.build()'` first" % LIB_PATH)
+    raise ImportError("%s is not built (expected at %s); run "
+                      "`python -c 'import __graft_entry__ as g; g.build()'` first"
+                      % (os.path.basename(LIB_PATH), LIB_PATH))
 _lib = ctypes.CDLL(LIB_PATH)
 
 # ------------------------------------------------------------------ constants (dcc.h)
@@ -32,6 +36,7 @@ DCC_ERR_CUDA = -5
 DCC_ERR_LAUNCH = -6
 DCC_ERR_TIMEOUT = -7
 DCC_ERR_UNSUPPORTED = -8
+DCC_ERR_BOUNDS = -9
 
 DCC_INT32, DCC_FP32, DCC_FP16, DCC_BF16 = 0, 1, 2, 3
 DCC_ALGO_AUTO, DCC_ALGO_ONE_SHOT, DCC_ALGO_TWO_SHOT, DCC_ALGO_TWO_SHOT_SCRATCH = 0, 1, 2, 3

@@ -73,7 +73,9 @@ typedef enum {
   DCC_ERR_CUDA = -5,           /* a CUDA runtime call failed */
   DCC_ERR_LAUNCH = -6,         /* the grid cannot be co-resident on this GPU */
   DCC_ERR_TIMEOUT = -7,        /* a device wait gave up (sticky for the communicator) */
-  DCC_ERR_UNSUPPORTED = -8     /* valid request the library does not implement */
+  DCC_ERR_UNSUPPORTED = -8,    /* valid request the library does not implement */
+  DCC_ERR_BOUNDS = -9          /* bounds-checked build only: a kernel access fell outside the
+                                  call's range (sticky for the communicator) */
 } dcc_result_t;
 
 typedef enum { DCC_INT32 = 0, DCC_FP32 = 1, DCC_FP16 = 2, DCC_BF16 = 3 } dcc_dtype_t;
@@ -237,7 +239,11 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
 /* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
  * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
  * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One
- * kernel runs all `iters` (>= 0) iterations. */
+ * kernel runs all `iters` (>= 0) iterations.  With at most 8 ranks the ranks
+ * are the CTAs of one thread-block cluster and each signal is a cluster-scope
+ * release arrive on the next rank's shared-memory barrier (DCC_RING_CLUSTER=0
+ * at communicator creation keeps the global-memory semaphores); either way
+ * the channels' signal counters advance by one per iteration and hop. */
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s);
 
 /* Synchronise s, read the device status word and return DCC_OK or the first
@@ -246,7 +252,14 @@ int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s);
 int dcc_comm_check(dcc_comm_t c, dcc_stream_t s);
 
 /* After dcc_comm_check returned a failure: the rank, peer and block of the
- * wait that gave up (any pointer may be NULL).  INVALID_ARG if none. */
+ * wait that gave up (any pointer may be NULL).  INVALID_ARG if none.
+ * For DCC_ERR_BOUNDS (the bounds-checked build, libdcc_checked.so, compiled
+ * with DCC_CHECK_BOUNDS=1: every data access of the collectives and the fused
+ * layer is checked against the byte range the call gave each pointer; the
+ * first access outside is skipped and recorded, and the kernel runs to its
+ * normal end): *rank = the buffer's rank, *peer = the buffer (0 send / weight,
+ * 1 recv / y, 2 scratch, 3 x, 4 residual), *block = the offending byte offset
+ * from that pointer / 16 (saturating at INT_MAX). */
 int dcc_comm_error_detail(dcc_comm_t c, int* rank, int* peer, int* block);
 
 /* Name of a dcc_result_t (static storage). */

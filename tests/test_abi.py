@@ -56,6 +56,19 @@ def test_every_exported_symbol_is_declared(dcc):
     assert exported <= set(declared_functions()), sorted(exported - set(declared_functions()))
 
 
+def test_bounds_checked_build_compiles_and_exports_the_same_boundary(dcc):
+    """The DCC_CHECK_BOUNDS=1 build of the same sources (libdcc_checked.so)
+    compiles and exports exactly the entry points of the default library."""
+    from driven_collective_communication_gb300 import build
+    path = build.build(checked=True)
+
+    def exported(lib):
+        out = subprocess.run(["nm", "-D", "--defined-only", lib], capture_output=True, text=True,
+                             check=True).stdout
+        return set(re.findall(r"\bT (dcc_\w+)$", out, flags=re.M))
+    assert exported(path) == exported(dcc.LIB_PATH)
+
+
 def test_build_targets_sm103a_only():
     """The build generates device code for sm_103a alone (one -gencode, no PTX
     for other architectures); the GPU test below checks what the runtime sees."""
@@ -75,7 +88,8 @@ def test_every_kernel_runs_as_sm103a_binary(dcc):
 def test_error_strings(dcc):
     for code, name in [(0, "DCC_OK"), (-1, "DCC_ERR_INVALID_ARG"), (-2, "DCC_ERR_NOT_REGISTERED"),
                        (-3, "DCC_ERR_MISALIGNED"), (-4, "DCC_ERR_NO_CHANNEL"), (-5, "DCC_ERR_CUDA"),
-                       (-6, "DCC_ERR_LAUNCH"), (-7, "DCC_ERR_TIMEOUT"), (-8, "DCC_ERR_UNSUPPORTED")]:
+                       (-6, "DCC_ERR_LAUNCH"), (-7, "DCC_ERR_TIMEOUT"), (-8, "DCC_ERR_UNSUPPORTED"),
+                       (-9, "DCC_ERR_BOUNDS")]:
         assert dcc.dcc_error_string(code) == name
     assert dcc.dcc_error_string(-99) == "DCC_ERR_UNKNOWN"
     assert "sm_103a" in dcc.dcc_version()

@@ -55,3 +55,15 @@ def test_timing_helpers_on_the_host():
     import bench
     assert bench.spread([3.0, 1.0, 2.0]) == {"min_ms": 1.0, "mean_ms": 2.0}
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_crossover_rule_minimises_summed_time():
+    """The AUTO threshold the bench derives from a sweep: the cut that minimises
+    the summed time, robust to one noisy point."""
+    sys.path.insert(0, ROOT)
+    import bench
+    sizes = [4, 8, 16, 32, 64]
+    assert bench.crossover_rule(sizes, [1, 1, 1, 1, 1], [2, 2, 2, 2, 2]) == 64   # one-shot always faster
+    assert bench.crossover_rule(sizes, [2, 2, 2, 2, 2], [1, 1, 1, 1, 1]) == 0    # never
+    assert bench.crossover_rule(sizes, [1, 1.1, 1, 2, 3], [1.5, 1.0, 1.5, 1.5, 1.5]) == 16  # one noisy loss at 8
+    assert bench.crossover_rule(sizes, [1, 1, 1, 1, 1], [1, 1, 1, 1, 1]) == 0    # ties: the smaller threshold

@@ -480,8 +480,14 @@ def test_random_rs_ag_configurations_match_oracle(dcc, monkeypatch):
 
 
 # ---------------------------------------------------------------- synchronisation
-@pytest.mark.parametrize("n", [1, 2, 8, 16])
-def test_ring_barrier_counts(dcc, n):
+@pytest.mark.parametrize("transport", ["default", "l2"])
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+def test_ring_barrier_counts(dcc, n, transport, monkeypatch):
+    """10^4 iterations: every channel's signal counter and waiter count equal the
+    oracle's; up to 8 ranks the default runs the ranks as one cluster (the
+    counters are added at the end), "l2" forces the global-memory semaphores."""
+    if transport == "l2":
+        monkeypatch.setenv("DCC_RING_CLUSTER", "0")
     iters = W.BARRIER_ITERS
     comm = dcc.Comm(n, connect="ring")
     try:
@@ -700,9 +706,13 @@ def test_concurrent_streams(dcc):
         assert same(W.to_storage(yd[r]), expect, "fp32")
 
 
-def test_lost_signal_times_out_cleanly(dcc):
+@pytest.mark.parametrize("transport", ["default", "l2"])
+def test_lost_signal_times_out_cleanly(dcc, transport, monkeypatch):
     """A rank that never signals makes its peers' waits run out: the kernel
-    records DCC_ERR_TIMEOUT and returns; the GPU stays usable."""
+    records DCC_ERR_TIMEOUT and returns; the GPU stays usable (the ring barrier
+    through a cluster's shared memory and through the global semaphores)."""
+    if transport == "l2":
+        monkeypatch.setenv("DCC_RING_CLUSTER", "0")
     n = 4
     comm = dcc.Comm(n, connect="all")
     try:
