@@ -913,6 +913,40 @@ def other_workloads(dcc, dev, stream):
             assert lc.check(stream) == dcc.DCC_OK
         out["linear_allreduce_bf16_n8_rows8192_kp%d" % kp] = res
         del wts, xin, yf, part, ysep, hres
+    # the row-parallel layer over a batch of tokens on the tensor cores vs
+    # per-rank cuBLAS GEMM then the AllReduce (8 ranks x 8192 rows x kp 1024)
+    for tokens in (1, 16, 64, 128, 256):
+        rows, kp = 8192, 1024
+        g = torch.Generator(device=dev)
+        g.manual_seed(6)
+        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+        xin = [torch.randn(tokens, kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
+        yt = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        part = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        ysep = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        with dcc.Comm(8) as tc:
+            for bufs, kind in ((wts, "input"), (xin, "input"), (part, "input"), (yt, "output"), (ysep, "output")):
+                tc.register_all(kind, bufs)
+            fused = lambda: dcc.dcc_linear_allreduce_tokens(tc.handle, wts, xin, yt, tokens, rows, kp, "bf16",  # noqa
+                                                            stream)
+            ar = dcc.prepare_allreduce(tc.handle, part, ysep, tokens * rows, "bf16", "auto", stream)
+
+            def unfused():
+                with torch.cuda.stream(stream):
+                    for r in range(8):
+                        torch.matmul(xin[r], wts[r].t(), out=part[r])
+                ar()
+            res = {}
+            for name, fn in (("fused_tensor", fused), ("gemm_then_allreduce", unfused)):
+                for _ in range(3):
+                    fn()
+                us = graph_us(fn, stream, reps=20, replays=5)
+                res[name + "_us"] = round(us, 2)
+                res[name + "_tflops"] = round(2 * 8 * rows * kp * tokens / (us * 1e-6) / 1e12, 1)
+                res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
+            assert tc.check(stream) == dcc.DCC_OK
+        out["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % tokens] = res
+        del wts, xin, yt, part, ysep
     # the ring barrier: default transport (8 ranks: one cluster, distributed
     # shared memory) and the global-memory semaphores (DCC_RING_CLUSTER=0)
     for key, env in (("c5_ring_barrier", None), ("c5_ring_barrier_l2_semaphores", "0")):
@@ -975,7 +1009,7 @@ def run_reference(args, dist):
 PROFILE_CASES = ("allreduce_two_shot", "allreduce_two_shot_bulk", "allreduce_one_shot",
                  "allreduce_one_shot_inplace", "allreduce_two_shot_scratch", "allreduce_one_shot_ll",
                  "allreduce_two_shot_max", "reduce_scatter",
-                 "allgather", "ring_barrier", "linear_allreduce")
+                 "allgather", "ring_barrier", "linear_allreduce", "linear_tokens")
 
 
 def run_profile_case(args):
@@ -1008,6 +1042,26 @@ def run_profile_case(args):
         if rc != dcc.DCC_OK:
             raise RuntimeError(dcc.dcc_error_string(rc))
         print(json.dumps({"profile_case": case, "rows": rows, "kp": kp, "launches": args.warmup + args.steps}))
+        return
+    if case == "linear_tokens":  # --count is the number of tokens; 8192 rows x kp 1024 per rank, bf16
+        tokens, rows, kp = args.count, 8192, 1024
+        g = torch.Generator(device=dev)
+        g.manual_seed(6)
+        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(n)]
+        xin = [torch.randn(tokens, kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(n)]
+        yt = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        with dcc.Comm(n) as tc:
+            tc.register_all("input", wts)
+            tc.register_all("input", xin)
+            tc.register_all("output", yt)
+            for _ in range(args.warmup + args.steps):
+                dcc.dcc_linear_allreduce_tokens(tc.handle, wts, xin, yt, tokens, rows, kp, "bf16")
+            torch.cuda.synchronize()
+            rc = tc.check()
+        if rc != dcc.DCC_OK:
+            raise RuntimeError(dcc.dcc_error_string(rc))
+        print(json.dumps({"profile_case": case, "tokens": tokens, "rows": rows, "kp": kp,
+                          "launches": args.warmup + args.steps}))
         return
     xs = W.rank_inputs(w, device=dev)
     comm = dcc.Comm(n, connect="ring" if case == "ring_barrier" else "all")

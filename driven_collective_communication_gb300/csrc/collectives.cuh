@@ -35,6 +35,11 @@ namespace dcc {
 
 constexpr int kThreads = 512;       // threads per CTA of the data kernels
 constexpr int kInplaceUnroll = 4;   // most vectors per thread per chunk, in-place one-shot
+constexpr int kInplaceLargeThreads = 256;  // threads per CTA, large in-place messages
+#ifndef DCC_INPLACE_PREFETCH
+#define DCC_INPLACE_PREFETCH 1
+#endif
+constexpr int kInplacePrefetch = DCC_INPLACE_PREFETCH;  // chunks of its slot the in-place one-shot asks L2 for ahead
 
 // ------------------------------------------------------------- element lanes
 template <typename T>
@@ -224,14 +229,29 @@ __device__ __forceinline__ bool entry_barrier(const DevComm& dc, int rank, int n
   return ok;
 }
 
+// L2 prefetch of chunk c of rank `rank`'s input (chunk = vectors per chunk):
+// a hint that returns nothing to the thread, issued for whole 16-byte vectors
+// inside the buffer.
+__device__ __forceinline__ void prefetch_chunk_l2(const DevComm& dc, const CollArgs& a, int rank, size_t c,
+                                                  size_t chunk, size_t nvec) {
+  const size_t v0 = c * chunk, nv = nvec - v0 < chunk ? nvec - v0 : chunk;
+  if (!in_bounds(dc, a, kBufSend, rank, v0 * 16, nv * 16)) return;
+  const char* p = static_cast<const char*>(a.send[rank]) + v0 * 16;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(nv * 16)) : "memory");
+}
+
 // ------------------------------------------------------------- one-shot
 // Every rank gets all N inputs and reduces its whole output.  Out of place no
 // rank writes what another reads, so there is no synchronisation.  In place,
 // rank r's output is an input of every peer: the N CTAs of a block slot
 // process the same chunk together -- get and reduce into registers, then a
-// signal/wait barrier ("everyone has read this chunk"), then store.  (Getting
-// the next chunk while the signals travel measured slower on GB300: 0.53 vs
-// 0.43 ms for 8 x 64 MiB int32.)
+// signal/wait barrier ("everyone has read this chunk"), then store.  The
+// barrier keeps the N CTAs of a slot in step, so all N read a chunk at the
+// same moment and the first reader's L2 miss holds up the other N-1; each CTA
+// therefore asks L2 for its own rank's part of its next chunk before it
+// starts the current one.  (Getting the next chunk into registers while the
+// signals travel, holding two chunks' results, measured slower on GB300:
+// 0.49 vs 0.42 ms for 8 x 64 MiB int32.)
 template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
   pdl_prologue();
@@ -260,12 +280,21 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   if (waiter) expected = dc.expect[sem_slot(rank, threadIdx.x, blk)];
   // U vectors per thread per chunk: 1 for small messages (one chunk per CTA,
   // all loads of a thread in flight at once), kInplaceUnroll for large ones
-  // (fewer chunks, so fewer barrier rounds)
+  // (fewer chunks, so fewer barrier rounds).  The loop over the U vectors is
+  // unrolled so all of a thread's loads of a chunk are in flight together
+  // (holding the results in shared memory with a runtime U instead measured
+  // slower on GB300: 0.350 vs 0.310 ms at U = 4, slower still at 8 and 16).
   const int U = a.unroll > 0 && a.unroll < kInplaceUnroll ? a.unroll : kInplaceUnroll;
   const size_t chunk = (size_t)U * blockDim.x;
   const size_t nchunks = (nvec + chunk - 1) / chunk;
   bool ok = true;
+  // prefetch distance: kInplacePrefetch chunks of this slot ahead
+  if (threadIdx.x == 0)
+    for (int d = 0; d < kInplacePrefetch; ++d)
+      if ((size_t)blk + (size_t)d * B < nchunks) prefetch_chunk_l2(dc, a, rank, blk + (size_t)d * B, chunk, nvec);
   for (size_t c = blk; c < nchunks; c += B) {
+    const size_t cp = c + (size_t)kInplacePrefetch * B;
+    if (threadIdx.x == 0 && cp < nchunks) prefetch_chunk_l2(dc, a, rank, cp, chunk, nvec);
     uint4 res[kInplaceUnroll];
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {

@@ -1,6 +1,7 @@
 // comm.h -- the communicator object and host helpers shared by the host
 // translation units of libdcc (dcc_host.cu, proxy.cu).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -109,6 +110,23 @@ struct dcc_comm {
   cudaStream_t pipe_in = nullptr, pipe_out = nullptr;
   cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_kernel = nullptr, ev_done = nullptr;
   ProxyState* proxy = nullptr;  // PortChannel proxy (created by dcc_proxy_start)
+  // tensor maps of the tensor-core linear layer, by (pointer, inner extent,
+  // outer extent, box rows, element type); encoded on the host once
+  struct MapKey {
+    const void* ptr;
+    unsigned long long inner, outer;
+    unsigned box_rows, dtype;
+    bool operator==(const MapKey& o) const {
+      return ptr == o.ptr && inner == o.inner && outer == o.outer && box_rows == o.box_rows && dtype == o.dtype;
+    }
+  };
+  struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+      return std::hash<const void*>()(k.ptr) ^ (std::hash<unsigned long long>()(k.inner * 1315423911ull + k.outer) << 1) ^
+             ((size_t)k.box_rows << 20) ^ k.dtype;
+    }
+  };
+  std::unordered_map<MapKey, CUtensorMap, MapKeyHash> tmaps;
 };
 
 namespace dcc_host {
@@ -219,7 +237,7 @@ inline void set_extent(A& a, int kind, int rank, size_t bytes) {
 // with pdl_prologue() and whose CTAs never wait on one another; never together
 // with a cooperative launch).
 // cluster > 0: thread-block clusters of that many CTAs along x (grid a
-// multiple of it; never together with the other two).
+// multiple of it; never with cooperative, may go with pdl).
 inline int launch(const void* fn, int grid, int threads, bool cooperative, void** args, cudaStream_t s,
            size_t smem = 0, bool pdl = false, int cluster = 0) {
   cudaLaunchConfig_t cfg = {};
@@ -227,25 +245,26 @@ inline int launch(const void* fn, int grid, int threads, bool cooperative, void*
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (cluster > 0) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  } else if (cooperative) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  } else if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  } else if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();

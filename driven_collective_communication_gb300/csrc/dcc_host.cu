@@ -22,6 +22,7 @@
 #include "comm.h"
 #include "fused.cuh"
 #include "fused_bulk.cuh"
+#include "fused_mma.cuh"
 #include "sync_kernels.cuh"
 
 namespace {
@@ -223,7 +224,10 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   if (algo == DCC_ALGO_ONE_SHOT && inplace) {
     // one vector per thread while one chunk per CTA of the co-resident grid
     // covers the message (a single barrier round, every load in flight at
-    // once), else kInplaceUnroll vectors per thread and fewer barrier rounds
+    // once), else kInplaceUnroll vectors per thread in 256-thread CTAs (fewer
+    // barrier rounds, four CTAs per SM: measured on GB300 at 8 x 64 MiB int32,
+    // 0.310 ms against 0.340 with 512-thread CTAs)
+    if (c->threads_override <= 0 && work > 65536) sh->threads = dcc::kInplaceLargeThreads;
     sh->unroll = c->inplace_unroll;
     if (sh->unroll <= 0) {
       int b1 = 0;
@@ -236,7 +240,7 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
   // one-shot keeps one wave even out of place: every rank reads every input,
   // and the ranks' CTAs reading a region together is what lets L2 serve it
   const bool one_wave = sh->cooperative || algo == DCC_ALGO_ONE_SHOT;
-  return pick_blocks(c, sh->fn, sh->threads, work, &sh->blocks, 0, 0, one_wave);
+  return pick_blocks(c, sh->fn, sh->threads, work, &sh->blocks, sh->smem, 0, one_wave);
 }
 
 int run_allreduce(dcc_comm* c, void* const* send, void* const* recv, size_t count, dcc_dtype_t t,
@@ -339,7 +343,7 @@ bool visit_kernels(F&& visit) {
     if (!v(dcc::allgather_kernel(n, false)) || !v(dcc::allgather_kernel(n, true)) ||
         !v(dcc::allgather_bulk_kernel(n)) || !v(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
-        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)))
+        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) || !v(dcc::linear_allreduce_mma_kernel(n)))
       return false;
   return v(dcc::ring_barrier_kernel()) && v(dcc::ring_barrier_cluster_kernel()) && v(dcc::channel_put_kernel()) &&
          v(dcc::channel_get_kernel());
@@ -444,6 +448,53 @@ int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   rc = pick_blocks(c, fn, dcc::kFusedThreads, items, &a.blocks, 0, 1, false);  // one item per CTA
   if (rc != DCC_OK) return rc;
   return launch(fn, a.blocks * c->n, dcc::kFusedThreads, false, kargs, static_cast<cudaStream_t>(s), 0, c->pdl);
+}
+
+// cuTensorMapEncodeTiled from the driver (through the runtime, so the library
+// needs no link against the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// A 2-D tensor map over a row-major outer x inner matrix of 16-bit elements,
+// box 64 (inner, one 128-byte swizzle row) x box_rows, 128-byte swizzle,
+// elements outside the matrix read as zero.  Cached on the communicator.
+int tensor_map(dcc_comm* c, const void* ptr, size_t inner, size_t outer, unsigned box_rows, dcc_dtype_t t,
+               CUtensorMap* out) {
+  const dcc_comm::MapKey key{ptr, inner, outer, box_rows, (unsigned)t};
+  auto it = c->tmaps.find(key);
+  if (it != c->tmaps.end()) {
+    *out = it->second;
+    return DCC_OK;
+  }
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return DCC_ERR_UNSUPPORTED;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)dcc::kMmaBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  if (enc(&m, t == DCC_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return DCC_ERR_INVALID_ARG;
+  if (c->tmaps.size() >= 4096) c->tmaps.clear();
+  c->tmaps.emplace(key, m);
+  *out = m;
+  return DCC_OK;
 }
 
 }  // namespace
@@ -839,6 +890,94 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
                                   void* const* y, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
   if (!residual) return DCC_ERR_INVALID_ARG;
   return linear_launch(c, weight, x, residual, y, rows, kp, t, s);
+}
+
+int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
+                                size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+  if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
+  if (c->sticky != DCC_OK) return c->sticky;
+  if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
+  if (tokens > (size_t)dcc::kMmaMaxTokens || rows % 8 || kp % dcc::kMmaBK) return DCC_ERR_UNSUPPORTED;
+  if (tokens == 0 || rows == 0 || kp == 0) return DCC_OK;
+  if (rows > ((size_t)1 << 31) || kp > ((size_t)1 << 31) / (size_t)c->n) return DCC_ERR_UNSUPPORTED;
+  const size_t wb = rows * kp * 2, xb = tokens * kp * 2, yb = tokens * rows * 2;
+  for (int r = 0; r < c->n; ++r) {
+    if (!weight[r] || !x[r] || !y[r]) return DCC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(weight[r]) | reinterpret_cast<uintptr_t>(x[r]) |
+         reinterpret_cast<uintptr_t>(y[r])) & 15u)
+      return DCC_ERR_MISALIGNED;
+    const void* ptrs[3] = {weight[r], x[r], y[r]};
+    const size_t lens[3] = {wb, xb, yb};
+    for (int j = 0; j < 3; ++j)
+      if (!in_window(c, r, DCC_BUF_INPUT, ptrs[j], lens[j]) && !in_window(c, r, DCC_BUF_OUTPUT, ptrs[j], lens[j]))
+        return DCC_ERR_NOT_REGISTERED;
+  }
+  for (int r = 0; r < c->n; ++r)
+    for (int p = 0; p < c->n; ++p) {
+      if (overlaps(y[r], yb, weight[p], wb) || overlaps(y[r], yb, x[p], xb)) return DCC_ERR_INVALID_ARG;
+      if (p != r && overlaps(y[r], yb, y[p], yb)) return DCC_ERR_INVALID_ARG;
+    }
+  int rc = check_channels_all_pairs(c);
+  if (rc != DCC_OK) return rc;
+  DeviceScope ds(c->device);
+  if (!ds.ok()) return DCC_ERR_CUDA;
+  const int ntile = tokens <= 16 ? 16 : (int)((tokens + 15) / 16 * 16);
+  dcc::MmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  // Launch shape: tiles of bm weight rows (a multiple of 8, at most 128) and
+  // ks K splits (a cluster of ks CTAs per tile, ks <= kMmaMaxSplit and at
+  // most one 64-element block each), chosen so the grid fills the most SMs in
+  // one wave (ties: fewer splits, then taller tiles).  The weight stream is
+  // bound by the bytes each SM keeps in flight, so every SM counts.
+  const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
+  int best_bm = dcc::kMmaBM, best_ks = 1;
+  long long best = -1;
+  auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
+  for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2)
+    for (int bm = 64; bm <= dcc::kMmaBM; bm += 8) {  // shorter tiles: more CTAs
+      if (tiles(bm) * ks > c->num_sms) continue;
+      int tall = bm;  // the tallest tile with the same tile count
+      while (tall + 8 <= dcc::kMmaBM && tiles(tall + 8) == tiles(bm)) tall += 8;
+      if (tiles(bm) * ks > best) {
+        best = tiles(bm) * ks;
+        best_bm = tall;
+        best_ks = ks;
+      }
+      break;
+    }
+  if (best < 0) {  // more tiles than SMs even at 128 rows: several waves, no split
+    best_bm = dcc::kMmaBM;
+    best_ks = 1;
+  }
+  for (int r = 0; r < c->n; ++r) {
+    rc = tensor_map(c, weight[r], kp, rows, (unsigned)best_bm, t, &maps.w[r]);
+    if (rc == DCC_OK) rc = tensor_map(c, x[r], kp, tokens, (unsigned)ntile, t, &maps.x[r]);
+    if (rc != DCC_OK) return rc;
+  }
+  dcc::MmaArgs a{};
+  for (int r = 0; r < c->n; ++r) {
+    a.y[r] = y[r];
+    set_extent(a, dcc::kBufRecv, r, yb);
+  }
+  a.tokens = (int)tokens;
+  a.rows = (int)rows;
+  a.kp = (int)kp;
+  a.ntile = ntile;
+  a.fp16 = t == DCC_FP16 ? 1 : 0;
+  a.stages = dcc::mma_stages(ntile);
+  a.bm = best_bm;
+  a.ks = best_ks;
+  const int mtiles = (int)((rows + best_bm - 1) / best_bm);
+  const void* fn = dcc::linear_allreduce_mma_kernel(c->n);
+  const size_t smem = dcc::mma_smem_bytes(ntile, a.stages);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  dcc::DevComm dc = dev_view(c);
+  void* kargs[] = {&maps, &dc, &a};
+  return launch(fn, mtiles * best_ks, dcc::kMmaThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl,
+                best_ks);
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {

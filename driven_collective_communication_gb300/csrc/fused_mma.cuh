@@ -1,0 +1,328 @@
+// fused_mma.cuh -- the row-parallel linear layer over a batch of tokens fused
+// with the sum AllReduce, on the fifth-generation tensor cores.
+//
+// The project summary ("How It Works") counts overlapping communication with
+// computation among the channel interfaces' uses and its "Highlighted
+// Details" single out AllReduce for tensor-parallel serving.  With several
+// tokens per step (batched decode, speculative decoding, prefill chunks) the
+// row-parallel layer is a contraction:
+//
+//   Y[t][i] = R( sum_p sum_k W_p[i][k] * X_p[t][k] ),  every rank receives Y
+//
+// W_p rows x kp (row-major), X_p tokens x kp (row-major), Y tokens x rows
+// (token t's hidden vector contiguous).  Seen as one GEMM, D = A B^T with
+// A = [W_0 | ... | W_{N-1}] (rows x N*kp) and B = [X_0 | ... | X_{N-1}]
+// (tokens x N*kp): the ranks' shards are slices of the contraction
+// dimension, and the AllReduce is the sum over them.
+//
+// Kernel.  A CTA owns a 128-row tile of Y for every token (the MMA's M = 128
+// rows, N = tokens rounded up to a multiple of 16, at most 256) and a slice
+// of the contraction dimension; the KS CTAs of a thread-block cluster split
+// the contraction (rank slices in rank order) and meet in distributed shared
+// memory.  Per CTA (128 threads):
+//   warp 0, one thread   TMA producer: per 64-element K block, the 128 x 64
+//                         tile of W_p and the tokens x 64 tile of X_p (both
+//                         128-byte swizzled, K-major) onto a stage mbarrier;
+//   warp 1, one thread   MMA issuer: four tcgen05.mma (K = 16 each) per
+//                         stage into the fp32 accumulator in tensor memory,
+//                         then tcgen05.commit frees the stage;
+//   warp 2               allocates / frees the tensor-memory columns;
+//   all four warps       epilogue: tcgen05.ld of the accumulator (warp w
+//                         reads lanes 32w..32w+31 = its 32 rows), partials to
+//                         shared memory, cluster barrier, each CTA of the
+//                         cluster adds the KS partials of its share of the
+//                         tokens in split order, rounds once and stores 16
+//                         bytes (8 rows) at a time into all N outputs.
+// Tokens beyond the batch and rows beyond the matrix are zero-filled by the
+// tensor map and masked at the store.  The fp32 accumulation order inside
+// the tensor core is the hardware's, so results are exact when every partial
+// sum is exact (small-integer data) and otherwise within the error bound of
+// an fp32 sum of N*kp exact products plus the one rounding.
+//
+// Every wait is bounded: a wait that runs out records a timeout in the
+// status word; the thread stops issuing work but every thread still reaches
+// both cluster barriers and the tensor memory is always freed.
+#pragma once
+#include <cuda.h>
+
+#include "collectives.cuh"
+
+namespace dcc {
+
+constexpr int kMmaThreads = 128;
+constexpr int kMmaBM = 128;      // accumulator rows per CTA (TMEM lanes)
+constexpr int kMmaBK = 64;       // K elements per stage (one 128-byte swizzle atom row)
+constexpr int kMmaMaxTokens = 256;
+constexpr int kMmaMaxSplit = 8;  // CTAs per cluster along K
+
+struct MmaMaps {
+  CUtensorMap w[DCC_MAX_RANKS];  // rows x kp, box 64 x 128
+  CUtensorMap x[DCC_MAX_RANKS];  // tokens x kp, box 64 x ntile
+};
+
+struct MmaArgs {
+  void* y[DCC_MAX_RANKS];  // tokens x rows
+  int tokens, rows, kp, ntile, ks, stages;
+  int bm;                  // weight rows per CTA (multiple of 8, at most kMmaBM)
+  int fp16;                // element type: 0 bf16, 1 fp16
+#if DCC_CHECK_BOUNDS
+  size_t ext[kNumBufKinds][DCC_MAX_RANKS];
+#endif
+};
+
+__host__ __device__ constexpr size_t mma_stage_bytes(int ntile) {
+  return (size_t)kMmaBM * kMmaBK * 2 + (size_t)ntile * kMmaBK * 2;
+}
+constexpr int kMmaMaxStages = 16;
+// dynamic shared memory: 1 KiB for alignment, the stages, and the mbarriers
+__host__ __device__ constexpr size_t mma_smem_bytes(int ntile, int stages) {
+  return 1024 + (size_t)stages * mma_stage_bytes(ntile) + 16 * (size_t)stages + 64;
+}
+// Stages: as many as fit in 216 KiB (at most kMmaMaxStages) -- the weight
+// stream is bound by the bytes in flight (on GB300 a loaded HBM read takes
+// about 4 us, so saturating it takes some 28 MB in flight across the GPU) --
+// and at least as many bytes as the fp32 partial tile the epilogue puts in
+// their place.
+inline int mma_stages(int ntile) {
+  const size_t st = mma_stage_bytes(ntile);
+  int s = (int)((216u * 1024u) / st);
+  if (s > kMmaMaxStages) s = kMmaMaxStages;
+  while ((size_t)s * st < (size_t)ntile * kMmaBM * 4) ++s;
+  return s;
+}
+
+__device__ __forceinline__ uint32_t smem_addr_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mma_mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mma_mbar_expect(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mma_mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// bounded wait on a phase; gives up at once when another wait already failed
+__device__ __forceinline__ bool mma_mbar_wait(uint32_t bar, uint32_t parity, const DevComm& dc, int rank,
+                                              int blk) {
+  if (mma_mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (unsigned it = 1;; ++it) {
+    if (mma_mbar_try(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (ld_relaxed_gpu(dc.status) != 0ull) return false;
+      if (global_timer_ns() - t0 > dc.timeout_ns) {
+        atomicCAS(dc.status, 0ull, pack_status(kStatusTimeout, rank, rank, blk));
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// asks L2 for a tile of a tensor map (no data comes back to the CTA)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void mma_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
+// swizzled layout the tensor map writes: rows of 128 bytes, 8-row groups
+// 1024 bytes apart (stride offset), descriptor version 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t mma_smem_desc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B of the same
+// 16-bit type (bf16 or fp16), both K-major, M = 128, N = ntile.
+__device__ __forceinline__ uint32_t mma_instr_desc(int ntile, bool fp16) {
+  const uint32_t ab = fp16 ? 0u : 1u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(ntile >> 3) << 17) | ((uint32_t)(kMmaBM >> 4) << 24);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const __grid_constant__ MmaMaps maps,
+                                                                          DevComm dc, MmaArgs a) {
+  extern __shared__ unsigned char mma_raw[];
+  __shared__ uint32_t tmem_slot;
+  const int n = NT > 0 ? NT : dc.n;
+  const uint32_t raw_u32 = smem_addr_u32(mma_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte alignment
+  unsigned char* gbase = mma_raw + (base - raw_u32);
+  const int S = a.stages, NTILE = a.ntile, KS = a.ks;
+  const uint32_t a_bytes = kMmaBM * kMmaBK * 2, st_bytes = (uint32_t)mma_stage_bytes(NTILE);
+  const uint32_t bars = base + (uint32_t)S * st_bytes;  // full[S], empty[S], accumulator ready
+  auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
+  auto empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
+  const uint32_t accf = bars + 16u * (uint32_t)S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned split = 0;
+  if (KS > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(split));
+  const int mtile = (int)blockIdx.x / KS, m0 = mtile * a.bm;
+  const int kpb = a.kp / kMmaBK, nb = n * kpb;
+  const int b0 = (int)((long long)split * nb / KS), b1 = (int)((long long)(split + 1) * nb / KS);
+  const int nk = b1 - b0;
+  const uint32_t ncols = NTILE <= 32 ? 32u : NTILE <= 64 ? 64u : NTILE <= 128 ? 128u : 256u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mma_mbar_init(full(s), 1);
+      mma_mbar_init(empty(s), 1);
+    }
+    mma_mbar_init(accf, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr_u32(&tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // Launched with programmatic dependent launch, everything above overlaps
+  // the end of the previous kernel on the stream, and so do L2 prefetches of
+  // the first weight tiles (a prefetch returns nothing, so whatever that
+  // kernel still writes lands in L2 before the loads below read it).  No data
+  // is read before griddepcontrol.wait.
+  if (warp == 0 && lane == 0)
+    for (int i = 0; i < nk && i < S; ++i) {
+      const int g = b0 + i;
+      tma_prefetch_2d(&maps.w[g / kpb], (g % kpb) * kMmaBK, m0);
+    }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0 && lane == 0) {  // TMA producer
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      if (i >= S && !mma_mbar_wait(empty(s), (uint32_t)(((i / S) - 1) & 1), dc, mtile, (int)split)) break;
+      const int g = b0 + i, p = g / kpb, k0 = (g % kpb) * kMmaBK;
+      const uint32_t sa = base + (uint32_t)s * st_bytes;
+      // the weight box is bm rows (the tile's rows bm..127 are never written and
+      // only reach accumulator rows the epilogue discards)
+      mma_mbar_expect(full(s), st_bytes - (uint32_t)(kMmaBM - a.bm) * (kMmaBK * 2));
+      tma_load_2d(sa, &maps.w[p], k0, m0, full(s));
+      tma_load_2d(sa + a_bytes, &maps.x[p], k0, 0, full(s));
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer
+    const uint32_t idesc = mma_instr_desc(NTILE, a.fp16 != 0);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      if (!mma_mbar_wait(full(s), (uint32_t)((i / S) & 1), dc, mtile, (int)split)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t sa = base + (uint32_t)s * st_bytes, sb = sa + a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < kMmaBK / 16; ++kk) {
+        const uint64_t ad = mma_smem_desc(sa + (uint32_t)kk * 32u), bd = mma_smem_desc(sb + (uint32_t)kk * 32u);
+        const uint32_t accumulate = (i > 0 || kk > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
+            : "memory");
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty(s))
+                   : "memory");
+    }
+    // arrives once every MMA issued above has completed (at once if none)
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(accf)
+                 : "memory");
+  }
+  __syncwarp();
+
+  // epilogue 1: the accumulator (row = TMEM lane) into partial[token][row] fp32
+  const int row = warp * 32 + lane;
+  const bool acc_ok = nk > 0 && mma_mbar_wait(accf, 0, dc, mtile, (int)split);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
+  for (int c0 = 0; c0 < NTILE; c0 += 16) {
+    uint32_t v[16];
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (KS > 1) mma_cluster_sync();  // every split's partials are in its shared memory
+
+  // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); a thread
+  // takes 8 consecutive rows of one token, adds the KS partials in split
+  // order (distributed shared memory), rounds once, and stores 16 bytes into
+  // each of the N outputs
+  const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;
+  for (int w = threadIdx.x; w < (t_hi - t_lo) * (kMmaBM / 8); w += kMmaThreads) {
+    const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int s2 = 0; s2 < KS; ++s2) {
+      const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
+      float4 lo, hi;
+      if (KS == 1) {
+        lo = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
+        hi = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
+      } else {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
+                     : "r"(remote)
+                     : "memory");
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
+                     : "r"(remote + 16u)
+                     : "memory");
+      }
+      const float pv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = s2 == 0 ? pv[j] : __fadd_rn(acc[j], pv[j]);
+    }
+    const int i0 = m0 + r8;
+    // rows come in multiples of 8 (and bm too): all 8 rows or none
+    if (t >= a.tokens || r8 >= a.bm || i0 >= a.rows) continue;
+    uint4 out;
+    if (a.fp16) {
+      out = make_uint4(HalfLanes<__half2, F16Ops>::narrow2(acc[0], acc[1]),
+                       HalfLanes<__half2, F16Ops>::narrow2(acc[2], acc[3]),
+                       HalfLanes<__half2, F16Ops>::narrow2(acc[4], acc[5]),
+                       HalfLanes<__half2, F16Ops>::narrow2(acc[6], acc[7]));
+    } else {
+      out = make_uint4(HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[0], acc[1]),
+                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[2], acc[3]),
+                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[4], acc[5]),
+                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[6], acc[7]));
+    }
+    const size_t off = ((size_t)t * a.rows + (size_t)i0) * 2;  // bytes
+    for (int q = 0; q < n; ++q)
+      if (in_bounds(dc, a, kBufRecv, q, off, 16)) st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off), out);
+  }
+  if (KS > 1) mma_cluster_sync();  // no CTA leaves while a peer may still read its partials
+  __syncthreads();
+  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+}
+
+const void* linear_allreduce_mma_kernel(int n);
+
+}  // namespace dcc

@@ -236,6 +236,25 @@ int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void
 int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual,
                                   void* const* y, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s);
 
+/* The same row-parallel layer for a batch of tokens, on the tensor cores
+ * (batched decode, speculative decoding, prefill chunks): rank p holds
+ * weight[p] (rows x kp, row-major) and x[p] (tokens x kp, row-major: token
+ * t's slice of the contraction dimension at x[p] + t*kp), and every rank
+ * receives
+ *   y[r][t*rows + i] = R( sum_p sum_k weight[p][i*kp + k] * x[p][t*kp + k] ),
+ * y[r] holding tokens x rows elements, row-major.  One kernel: 128-row tiles
+ * of y, tcgen05 MMAs on bf16 / fp16 operands loaded by TMA with fp32
+ * accumulation in tensor memory, the contraction split across the CTAs of a
+ * thread-block cluster whose partials meet in distributed shared memory, one
+ * rounding, and the result put into all N outputs.  fp16 or bf16; tokens
+ * 1..256, kp a multiple of 64, rows a multiple of 8 (UNSUPPORTED
+ * otherwise); 16-byte aligned, registered, outputs disjoint from every input.
+ * Exact when every fp32 partial sum is exact (small-integer data), otherwise
+ * within the fp32 dot-product error bound plus the one rounding (the tensor
+ * core's accumulation order).  Errors as dcc_linear_allreduce. */
+int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
+                                size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s);
+
 /* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
  * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
  * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One

@@ -25,7 +25,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # LL kernels, entry barrier, host buffers) at sizes the checked build runs quickly
 SELECT = ("parity_sweep or random or ragged or special_values or launch_shape or c3_bf16 or "
           "c1_fp32 or entry_barrier_same or empty_inputs or from_host or allgather_bulk or "
-          "integer_data or within_bound or reduce_scatter_op_parity or op_with_entry_barrier or "
+          "integer_data or within_bound or random_shapes or reduce_scatter_op_parity or op_with_entry_barrier or "
           "graph_replay or dependent_chain or fused_layer_chain")
 
 
@@ -35,7 +35,7 @@ def test_parity_sweep_clean_under_bounds_checked_build():
     build.build(checked=True)
     env = dict(os.environ, DCC_CHECK_BOUNDS="1")
     files = ["tests/test_gpu_collectives.py", "tests/test_gpu_reduce_ops.py", "tests/test_gpu_fused.py",
-             "tests/test_gpu_pdl.py"]
+             "tests/test_gpu_fused_mma.py", "tests/test_gpu_pdl.py"]
     probe = subprocess.run([sys.executable, "-c",
                             "from driven_collective_communication_gb300 import dcc; print(dcc.LIB_PATH)"],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)

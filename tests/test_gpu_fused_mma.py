@@ -1,0 +1,159 @@
+"""Row-parallel linear layer over a batch of tokens, fused with the AllReduce
+on the tensor cores, against the oracle.
+
+Small-integer data make every fp32 partial sum exact, so the kernel must match
+the oracle bit for bit whatever order the tensor cores accumulate in.  Random
+data are held to the bound of an fp32 sum of K = N*kp products (exact in
+fp32) plus the KS split partials, with a unit roundoff of 2^-23 per add (so a
+truncating adder is covered too), before the one rounding to the output type:
+  |y - y_oracle| <= gamma_{K + KS} * sum|w x| + ulp_out,  gamma_m = m u / (1 - m u).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from driven_collective_communication_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TD = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def dcc():
+    from driven_collective_communication_gb300 import build
+    build.build()
+    from driven_collective_communication_gb300 import dcc as mod
+    torch.cuda.set_device(0)
+    return mod
+
+
+def run(dcc, ws, xs, tokens, rows, kp, dtype, fill=float("nan")):
+    n = len(ws)
+    dw = [w.cuda() for w in ws]
+    dx = [x.cuda() for x in xs]
+    dy = [torch.full((tokens * rows,), fill, dtype=TD[dtype], device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", dw)
+        for r in range(n):
+            comm.register(r, "input", dx[r])
+        comm.register_all("output", dy)
+        dcc.dcc_linear_allreduce_tokens(comm.handle, dw, dx, dy, tokens, rows, kp, dtype)
+        assert comm.check() == dcc.DCC_OK
+    for r in range(1, n):
+        assert torch.equal(dy[r].view(torch.int16), dy[0].view(torch.int16)), r
+    return W.to_storage(dy[0])
+
+
+def small_ints(g, size, dtype, lo=-3, hi=3):
+    return torch.randint(lo, hi + 1, (size,), generator=g).to(TD[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,tokens,rows,kp", [
+    (1, 1, 128, 64), (2, 16, 256, 64), (8, 1, 1024, 128), (8, 17, 1024, 192), (3, 100, 136, 256),
+    (8, 256, 512, 64), (16, 64, 512, 64), (5, 255, 264, 320), (8, 33, 8192, 64), (4, 128, 128, 1024)])
+def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
+    """Ragged token counts (padded to a multiple of 16 inside), a partial last
+    row tile (136, 264 rows), 1..16 ranks, K splits from 1 to 8."""
+    g = torch.Generator().manual_seed(n * 7919 + tokens * 31 + kp)
+    ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
+    xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
+    got = run(dcc, ws, xs, tokens, rows, kp, dtype)
+    expect = oracle.linear_allreduce_tokens([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                            dtype, tokens, rows, kp)
+    assert np.array_equal(got, expect)
+
+
+def test_tokens_random_shapes_bit_exact(dcc):
+    """Forty seeded random mixes of rank count, tokens, rows, kp and dtype on
+    small-integer data: exact against the oracle."""
+    rng = np.random.default_rng(2026)
+    for case in range(40):
+        n = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16]))
+        tokens = int(rng.integers(1, 257))
+        rows = 8 * int(rng.integers(1, 80))
+        kp = 64 * int(rng.integers(1, 9))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        g = torch.Generator().manual_seed(5000 + case)
+        ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
+        xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
+        got = run(dcc, ws, xs, tokens, rows, kp, dtype)
+        expect = oracle.linear_allreduce_tokens([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                                dtype, tokens, rows, kp)
+        assert np.array_equal(got, expect), (case, n, tokens, rows, kp, dtype)
+
+
+def ulp_out(v, dtype):
+    big = np.maximum(np.abs(v), 2.0 ** (-126 if dtype == "bf16" else -14))
+    return np.exp2(np.floor(np.log2(big)) - (7 if dtype == "bf16" else 10))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,tokens,rows,kp", [(8, 64, 1024, 1024), (8, 256, 256, 512), (3, 5, 264, 2048)])
+def test_tokens_random_data_within_bound(dcc, dtype, n, tokens, rows, kp):
+    g = torch.Generator().manual_seed(17 + n + kp + tokens)
+    ws = [(torch.randn(rows * kp, generator=g) * 0.05).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randn(tokens * kp, generator=g).to(TD[dtype]) for _ in range(n)]
+    got = run(dcc, ws, xs, tokens, rows, kp, dtype)
+    expect = oracle.linear_allreduce_tokens([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                            dtype, tokens, rows, kp)
+    gf = W.from_storage(got, dtype).double().numpy()
+    ef = W.from_storage(expect, dtype).double().numpy()
+    s = sum(np.abs(x.double().numpy().reshape(tokens, kp)) @ np.abs(w.double().numpy().reshape(rows, kp)).T
+            for w, x in zip(ws, xs)).ravel()
+    m = n * kp + 8  # products plus at most 8 split partials
+    u = 2.0 ** -23
+    gamma = m * u / (1 - m * u)
+    bound = gamma * s + ulp_out(np.maximum(np.abs(gf), np.abs(ef)), dtype)
+    assert np.all(np.abs(gf - ef) <= bound), float(np.max(np.abs(gf - ef) / bound))
+    assert np.mean(got == expect) > 0.9
+
+
+def test_tokens_full_size_sampled_rows(dcc):
+    """8 ranks x 8192 rows x kp 1024, 256 tokens (the bench's largest batch),
+    integer data: 1024 rows spread over the matrix (every row tile touched,
+    the first and last rows included) against the oracle, every token."""
+    n, tokens, rows, kp, dtype = 8, 256, 8192, 1024, "bf16"
+    g = torch.Generator().manual_seed(99)
+    ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
+    xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
+    got = run(dcc, ws, xs, tokens, rows, kp, dtype).reshape(tokens, rows)
+    pick = np.unique(np.concatenate([np.arange(0, rows, 8), [rows - 1]]))[:1025]
+    wsel = [W.to_storage(w).reshape(rows, kp)[pick].ravel() for w in ws]
+    expect = oracle.linear_allreduce_tokens(wsel, [W.to_storage(x) for x in xs], dtype, tokens, len(pick),
+                                            kp).reshape(tokens, len(pick))
+    assert np.array_equal(got[:, pick], expect)
+
+
+def test_tokens_argument_errors(dcc):
+    n, tokens, rows, kp = 2, 4, 64, 64
+    w = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    x = [torch.zeros(tokens * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    y = [torch.zeros(tokens * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", w)
+        comm.register_all("input", x)
+        comm.register_all("output", y)
+        h = comm.handle
+
+        def code(*args):
+            try:
+                dcc.dcc_linear_allreduce_tokens(h, *args)
+                return dcc.DCC_OK
+            except dcc.DccError as e:
+                return e.code
+        assert code(w, x, y, tokens, rows, kp, "bf16") == dcc.DCC_OK
+        assert code(w, x, y, 0, rows, kp, "bf16") == dcc.DCC_OK          # nothing to do
+        assert code(w, x, y, 257, rows, kp, "bf16") == dcc.DCC_ERR_UNSUPPORTED
+        assert code(w, x, y, tokens, rows, 32, "bf16") == dcc.DCC_ERR_UNSUPPORTED  # kp % 64
+        assert code(w, x, y, tokens, 60, kp, "bf16") == dcc.DCC_ERR_UNSUPPORTED   # rows % 8
+        assert code(w, x, y, tokens, rows, kp, "fp32") == dcc.DCC_ERR_UNSUPPORTED
+        assert code(w, x, y, tokens, rows * 2, kp, "bf16") == dcc.DCC_ERR_NOT_REGISTERED
+        bad = [t[1:] for t in y]
+        assert code(w, x, bad, tokens, rows - 8, kp, "bf16") == dcc.DCC_ERR_MISALIGNED
+        assert code(w, x, [y[0], y[0]], tokens, rows, kp, "bf16") == dcc.DCC_ERR_NOT_REGISTERED  # not rank 1's
+        comm.register(1, "output", y[0])
+        assert code(w, x, [y[0], y[0]], tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # outputs overlap
+        assert code(w, x, [x[0], y[1]], tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # output is an input
+        assert comm.check() == dcc.DCC_OK
