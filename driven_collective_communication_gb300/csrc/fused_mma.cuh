@@ -251,72 +251,106 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   const bool acc_ok = nk > 0 && mma_mbar_wait(accf, 0, dc, mtile, (int)split);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
-  for (int c0 = 0; c0 < NTILE; c0 += 16) {
-    uint32_t v[16];
+  for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
+    uint32_t v[32];
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
+    if (c0 + 32 <= NTILE) {
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+          "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          : "r"(taddr));
+    } else {
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+          : "r"(taddr));
+    }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    const int cols = c0 + 32 <= NTILE ? 32 : 16;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
+    for (int j = 0; j < 32; ++j)
+      if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (KS > 1) mma_cluster_sync();  // every split's partials are in its shared memory
 
-  // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); a thread
-  // takes 8 consecutive rows of one token, adds the KS partials in split
-  // order (distributed shared memory), rounds once, and stores 16 bytes into
-  // each of the N outputs
+  // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); an item
+  // is 8 consecutive rows of one token: its KS partials are added in split
+  // order (distributed shared memory), rounded once and stored 16 bytes into
+  // each of the N outputs.  A thread gathers the partials of kBatch items
+  // before it adds and stores any, so their loads are in flight together.
+  constexpr int kBatch = 4;
   const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;
-  for (int w = threadIdx.x; w < (t_hi - t_lo) * (kMmaBM / 8); w += kMmaThreads) {
-    const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
-    float acc[8];
+  const int items = (t_hi - t_lo) * (kMmaBM / 8);
+  for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
+    float acc[kBatch][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[b][j] = 0.0f;
     for (int s2 = 0; s2 < KS; ++s2) {
-      const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
-      float4 lo, hi;
-      if (KS == 1) {
-        lo = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
-        hi = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
-      } else {
-        uint32_t remote;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
-        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
-                     : "r"(remote)
-                     : "memory");
-        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
-                     : "r"(remote + 16u)
-                     : "memory");
-      }
-      const float pv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      float4 lo[kBatch], hi[kBatch];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = s2 == 0 ? pv[j] : __fadd_rn(acc[j], pv[j]);
+      for (int b = 0; b < kBatch; ++b) {
+        const int w = w0 + b * kMmaThreads;
+        if (w >= items) continue;
+        const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
+        const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
+        if (KS == 1) {
+          lo[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
+          hi[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
+        } else {
+          uint32_t remote;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
+          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(lo[b].x), "=f"(lo[b].y), "=f"(lo[b].z), "=f"(lo[b].w)
+                       : "r"(remote)
+                       : "memory");
+          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(hi[b].x), "=f"(hi[b].y), "=f"(hi[b].z), "=f"(hi[b].w)
+                       : "r"(remote + 16u)
+                       : "memory");
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (w0 + b * kMmaThreads >= items) continue;
+        const float pv[8] = {lo[b].x, lo[b].y, lo[b].z, lo[b].w, hi[b].x, hi[b].y, hi[b].z, hi[b].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[b][j] = s2 == 0 ? pv[j] : __fadd_rn(acc[b][j], pv[j]);
+      }
     }
-    const int i0 = m0 + r8;
-    // rows come in multiples of 8 (and bm too): all 8 rows or none
-    if (t >= a.tokens || r8 >= a.bm || i0 >= a.rows) continue;
-    uint4 out;
-    if (a.fp16) {
-      out = make_uint4(HalfLanes<__half2, F16Ops>::narrow2(acc[0], acc[1]),
-                       HalfLanes<__half2, F16Ops>::narrow2(acc[2], acc[3]),
-                       HalfLanes<__half2, F16Ops>::narrow2(acc[4], acc[5]),
-                       HalfLanes<__half2, F16Ops>::narrow2(acc[6], acc[7]));
-    } else {
-      out = make_uint4(HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[0], acc[1]),
-                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[2], acc[3]),
-                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[4], acc[5]),
-                       HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[6], acc[7]));
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int w = w0 + b * kMmaThreads;
+      if (w >= items) continue;
+      const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
+      const int i0 = m0 + r8;
+      // rows come in multiples of 8 (and bm too): all 8 rows or none
+      if (t >= a.tokens || r8 >= a.bm || i0 >= a.rows) continue;
+      uint4 out;
+      if (a.fp16) {
+        out = make_uint4(HalfLanes<__half2, F16Ops>::narrow2(acc[b][0], acc[b][1]),
+                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][2], acc[b][3]),
+                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][4], acc[b][5]),
+                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][6], acc[b][7]));
+      } else {
+        out = make_uint4(HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][0], acc[b][1]),
+                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][2], acc[b][3]),
+                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][4], acc[b][5]),
+                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][6], acc[b][7]));
+      }
+      const size_t off = ((size_t)t * a.rows + (size_t)i0) * 2;  // bytes
+      for (int q = 0; q < n; ++q)
+        if (in_bounds(dc, a, kBufRecv, q, off, 16))
+          st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off), out);
     }
-    const size_t off = ((size_t)t * a.rows + (size_t)i0) * 2;  // bytes
-    for (int q = 0; q < n; ++q)
-      if (in_bounds(dc, a, kBufRecv, q, off, 16)) st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off), out);
   }
   if (KS > 1) mma_cluster_sync();  // no CTA leaves while a peer may still read its partials
   __syncthreads();
