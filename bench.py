@@ -770,6 +770,16 @@ def other_workloads(dcc, dev, stream):
             res["with_barrier_us" if on else "without_us"] = round(e0.elapsed_time(e1) * 1e3 / 1000, 2)
         assert c16.check(stream) == dcc.DCC_OK
         out["c3_16KiB_two_shot_entry_barrier_graph"] = res
+    # the allocation-free entry point on the same 16 KiB decode size (two-shot
+    # via its static array, cooperative launch): per launch and back to back
+    ys16n = [torch.empty_like(x) for x in xs16]
+    na = lambda: dcc.dcc_allreduce_noalloc(8, xs16, ys16n, w16.count, "bf16", stream)  # noqa: E731
+    for _ in range(20):
+        na()
+    per, _ = time_launches(na, 200, stream)
+    out["c3_16KiB_noalloc"] = {"p50_event_us": round(statistics.median(per) * 1e3, 2),
+                               "back_to_back_us": round(time_queued_span(na, 100, stream), 2)}
+    assert dcc.dcc_noalloc_check(stream)[0] == dcc.DCC_OK
     del xs, ys, scr
     # more ranks and another dtype at the large size (two-shot push, 256 MiB per rank)
     for n_ranks, dtype in ((2, "bf16"), (4, "bf16"), (16, "bf16"), (8, "fp32")):
