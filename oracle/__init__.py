@@ -46,10 +46,13 @@ def _load():
                                                       ctypes.POINTER(vp), sz, sz, i32, vp]
         lib.orc_linear_allreduce_tokens.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, sz, sz,
                                                     i32, vp]
+        lib.orc_linear_allreduce_tokens_residual.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                             ctypes.POINTER(vp), sz, sz, sz, i32, vp]
         for name in ("orc_allreduce", "orc_allreduce_at", "orc_allreduce_mt",
                      "orc_reduce_scatter", "orc_allgather", "orc_ring_barrier_counts",
                      "orc_convert_to_f32", "orc_convert_from_f32", "orc_linear_allreduce",
-                     "orc_allreduce_op", "orc_linear_allreduce_residual", "orc_linear_allreduce_tokens"):
+                     "orc_allreduce_op", "orc_linear_allreduce_residual", "orc_linear_allreduce_tokens",
+                     "orc_linear_allreduce_tokens_residual"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -219,6 +222,29 @@ def linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp):
     _ok(lib.orc_linear_allreduce_tokens(len(warrs), wp, xp, tokens, rows, kp, DTYPES[dtype], out.ctypes.data),
         "linear_allreduce_tokens")
     return out
+
+
+def linear_allreduce_tokens_residual(ws, xs, res, dtype, tokens, rows, kp):
+    """Y_q[t, i] = R(sum_p sum_k W_p[i, k] X_p[t, k] + res_q[t, i]) for every
+    rank q (res_q tokens*rows, row-major like the output), the residual added
+    before the one rounding.  Returns the N outputs as a list."""
+    lib = _load()
+    if dtype not in ("fp16", "bf16"):
+        raise ValueError("fp16 or bf16 only")
+    warrs = [np.ascontiguousarray(a, dtype=np.uint16).ravel() for a in ws]
+    xarrs = [np.ascontiguousarray(a, dtype=np.uint16).ravel() for a in xs]
+    rarrs = [np.ascontiguousarray(a, dtype=np.uint16).ravel() for a in res]
+    n = len(warrs)
+    if (len(xarrs) != n or len(rarrs) != n or any(len(a) != rows * kp for a in warrs)
+            or any(len(a) != tokens * kp for a in xarrs) or any(len(a) != tokens * rows for a in rarrs)):
+        raise ValueError("shapes")
+    wp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in warrs])
+    xp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in xarrs])
+    rp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in rarrs])
+    out = np.empty(n * tokens * rows, dtype=np.uint16)
+    _ok(lib.orc_linear_allreduce_tokens_residual(n, wp, xp, rp, tokens, rows, kp, DTYPES[dtype], out.ctypes.data),
+        "linear_allreduce_tokens_residual")
+    return [out[q * tokens * rows:(q + 1) * tokens * rows].copy() for q in range(n)]
 
 
 def library_path():

@@ -417,6 +417,35 @@ int orc_linear_allreduce_tokens(int n, const void* const* w, const void* const* 
 }
 
 /* ---------------------------------------------------------------------- */
+/* The batched layer with a residual per output rank (the residual stream  */
+/* of a multi-token step, h_q <- h_q + layer): res_q holds tokens x rows     */
+/* elements like the output, and the residual joins the binary64 sum       */
+/* before the single rounding,                                              */
+/*   y_q[t][i] = R( sum_p sum_k W_p[i][k] * x_p[t][k] + res_q[t][i] ).     */
+/* out holds the N outputs one after another (rank q's at out + q*tokens*rows). */
+/* ---------------------------------------------------------------------- */
+int orc_linear_allreduce_tokens_residual(int n, const void* const* w, const void* const* x,
+                                         const void* const* res, size_t tokens, size_t rows, size_t kp,
+                                         int dtype, void* out)
+{
+    if (n < 1 || !w || !x || !res || (tokens && rows && !out) || (dtype != ORC_FP16 && dtype != ORC_BF16))
+        return -1;
+    for (int p = 0; p < n; ++p) if (!w[p] || !x[p] || !res[p]) return -1;
+    for (size_t t = 0; t < tokens; ++t)
+        for (size_t i = 0; i < rows; ++i) {
+            double dot = 0.0;
+            for (int p = 0; p < n; ++p)
+                for (size_t k = 0; k < kp; ++k)
+                    dot += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);
+            for (int q = 0; q < n; ++q) {
+                const double y = dot + (double)widen(res[q], t * rows + i, dtype);
+                ((uint16_t*)out)[((size_t)q * tokens + t) * rows + i] = f64_to_half_once(y, dtype);
+            }
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* The same layer with a residual added for each output rank (the          */
 /* tensor-parallel residual stream: h_q <- h_q + the layer's AllReduced    */
 /* output).  Reading taken: the residual joins the binary64 sum before the */

@@ -485,6 +485,31 @@ def test_linear_tokens_matches_float64_matmul(dtype):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_linear_tokens_residual_reduces_to_its_parts(dtype):
+    """The batched layer with residuals: zero weights give each rank its own
+    residual; a zero residual gives the batched layer; every token of rank q
+    equals the pinned one-token residual layer on that token's slices."""
+    n, tokens, rows, kp = 3, 4, 16, 8
+    rng = np.random.default_rng(23)
+    ws = [_small_ints(rng, dtype, -3, 3, rows * kp) for _ in range(n)]
+    xs = [_small_ints(rng, dtype, -2, 2, tokens * kp) for _ in range(n)]
+    res = [_small_ints(rng, dtype, -50, 50, tokens * rows) for _ in range(n)]
+    zw = [np.full(rows * kp, value_to_storage(0, dtype), np.uint16) for _ in range(n)]
+    for q, y in enumerate(oracle.linear_allreduce_tokens_residual(zw, xs, res, dtype, tokens, rows, kp)):
+        assert np.array_equal(storage_to_float(y, dtype), storage_to_float(res[q], dtype)), q
+    zres = [np.full(tokens * rows, value_to_storage(0, dtype), np.uint16) for _ in range(n)]
+    plain = oracle.linear_allreduce_tokens(ws, xs, dtype, tokens, rows, kp)
+    for y in oracle.linear_allreduce_tokens_residual(ws, xs, zres, dtype, tokens, rows, kp):
+        assert np.array_equal(y, plain)
+    ys = oracle.linear_allreduce_tokens_residual(ws, xs, res, dtype, tokens, rows, kp)
+    for t in range(tokens):
+        one = oracle.linear_allreduce_residual(ws, [x[t * kp:(t + 1) * kp] for x in xs],
+                                               [r[t * rows:(t + 1) * rows] for r in res], dtype, rows, kp)
+        for q in range(n):
+            assert np.array_equal(ys[q][t * rows:(t + 1) * rows], one[q]), (t, q)
+
+
 # --------------------------------------------------------------------- linear layer + residual
 def _small_ints(rng, dtype, lo, hi, size):
     return np.array([value_to_storage(int(v), dtype) for v in rng.integers(lo, hi + 1, size=size)], np.uint16)

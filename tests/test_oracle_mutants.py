@@ -56,20 +56,26 @@ MUTANTS = {
     "op_skips_rank_0": ("float acc = widen(in[0], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op",
                         "float acc = widen(in[n - 1], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op"),
     "op_nan_not_canonical_at_one_rank": ("if (isnan(acc)) acc = NAN;   /* canonical", "if (0) acc = NAN;   /* canonical"),
-    "residual_of_rank_0": ("const double y = acc + (double)widen(res[q], i, dtype);",
-                           "const double y = acc + (double)widen(res[0], i, dtype);"),
-    "residual_dropped": ("const double y = acc + (double)widen(res[q], i, dtype);",
+    "residual_of_rank_0": ("const double y = dot + (double)widen(res[q], i, dtype);",
+                           "const double y = dot + (double)widen(res[0], i, dtype);"),
+    "residual_dropped": ("const double y = dot + (double)widen(res[q], i, dtype);",
                          "const double y = acc + 0.0 * (double)widen(res[q], i, dtype);"),
     "residual_after_rounding_the_layer": (
-        "const double y = acc + (double)widen(res[q], i, dtype);",
+        "const double y = dot + (double)widen(res[q], i, dtype);",
         "const double y = (double)(dtype == ORC_FP16 ? orc_f16_to_f32(f64_to_half_once(acc, dtype))"
         " : orc_bf16_to_f32(f64_to_half_once(acc, dtype))) + (double)widen(res[q], i, dtype);"),
-    "tokens_ignore_token_offset": ("(double)widen(x[p], t * kp + k, dtype);",
-                                   "(double)widen(x[p], k, dtype);"),
+    "tokens_ignore_token_offset": ("acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);",
+                                   "acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], k, dtype);"),
     "tokens_output_transposed": ("((uint16_t*)out)[t * rows + i] = f64_to_half_once(acc, dtype);",
                                  "((uint16_t*)out)[i * tokens + t] = f64_to_half_once(acc, dtype);"),
     "tokens_drop_last_rank": ("            for (int p = 0; p < n; ++p)\n                for (size_t k = 0; k < kp; ++k)\n                    acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);",
                               "            for (int p = 0; p < n - 1; ++p)\n                for (size_t k = 0; k < kp; ++k)\n                    acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);"),
+    "tokens_residual_of_rank_0": ("const double y = dot + (double)widen(res[q], t * rows + i, dtype);",
+                                  "const double y = dot + (double)widen(res[0], t * rows + i, dtype);"),
+    "tokens_residual_wrong_token": ("const double y = dot + (double)widen(res[q], t * rows + i, dtype);",
+                                    "const double y = dot + (double)widen(res[q], i, dtype);"),
+    "tokens_residual_product_of_rank_0": ("dot += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p],",
+                                          "dot += (double)widen(w[0], i * kp + k, dtype) * (double)widen(x[p],"),
     "allreduce_at_wrong_slot": ("reduce_one(n, in, (size_t)idx[k], out, k, dtype);",
                                 "reduce_one(n, in, (size_t)idx[k], out, (size_t)idx[k] % (nidx ? nidx : 1), dtype);"),
 }
