@@ -56,12 +56,12 @@ MUTANTS = {
     "op_skips_rank_0": ("float acc = widen(in[0], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op",
                         "float acc = widen(in[n - 1], i, dtype);\n        for (int p = 1; p < n; ++p)\n            acc = op"),
     "op_nan_not_canonical_at_one_rank": ("if (isnan(acc)) acc = NAN;   /* canonical", "if (0) acc = NAN;   /* canonical"),
-    "residual_of_rank_0": ("const double y = dot + (double)widen(res[q], i, dtype);",
-                           "const double y = dot + (double)widen(res[0], i, dtype);"),
-    "residual_dropped": ("const double y = dot + (double)widen(res[q], i, dtype);",
+    "residual_of_rank_0": ("const double y = acc + (double)widen(res[q], i, dtype);",
+                           "const double y = acc + (double)widen(res[0], i, dtype);"),
+    "residual_dropped": ("const double y = acc + (double)widen(res[q], i, dtype);",
                          "const double y = acc + 0.0 * (double)widen(res[q], i, dtype);"),
     "residual_after_rounding_the_layer": (
-        "const double y = dot + (double)widen(res[q], i, dtype);",
+        "const double y = acc + (double)widen(res[q], i, dtype);",
         "const double y = (double)(dtype == ORC_FP16 ? orc_f16_to_f32(f64_to_half_once(acc, dtype))"
         " : orc_bf16_to_f32(f64_to_half_once(acc, dtype))) + (double)widen(res[q], i, dtype);"),
     "tokens_ignore_token_offset": ("acc += (double)widen(w[p], i * kp + k, dtype) * (double)widen(x[p], t * kp + k, dtype);",
