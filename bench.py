@@ -934,11 +934,15 @@ def other_workloads(dcc, dev, stream):
         yt = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         part = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         ysep = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        hres = [torch.randn(tokens, rows, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
         with dcc.Comm(8) as tc:
-            for bufs, kind in ((wts, "input"), (xin, "input"), (part, "input"), (yt, "output"), (ysep, "output")):
+            for bufs, kind in ((wts, "input"), (xin, "input"), (part, "input"), (yt, "output"), (ysep, "output"),
+                               (hres, "output")):
                 tc.register_all(kind, bufs)
             fused = lambda: dcc.dcc_linear_allreduce_tokens(tc.handle, wts, xin, yt, tokens, rows, kp, "bf16",  # noqa
                                                             stream)
+            fused_res = lambda: dcc.dcc_linear_allreduce_tokens_residual(  # noqa: E731 (h <- h + layer, in place)
+                tc.handle, wts, xin, hres, hres, tokens, rows, kp, "bf16", stream)
             ar = dcc.prepare_allreduce(tc.handle, part, ysep, tokens * rows, "bf16", "auto", stream)
 
             def unfused():
@@ -947,7 +951,8 @@ def other_workloads(dcc, dev, stream):
                         torch.matmul(xin[r], wts[r].t(), out=part[r])
                 ar()
             res = {}
-            for name, fn in (("fused_tensor", fused), ("gemm_then_allreduce", unfused)):
+            for name, fn in (("fused_tensor", fused), ("fused_tensor_residual_inplace", fused_res),
+                             ("gemm_then_allreduce", unfused)):
                 for _ in range(3):
                     fn()
                 us = graph_us(fn, stream, reps=20, replays=5)
@@ -956,7 +961,7 @@ def other_workloads(dcc, dev, stream):
                 res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
             assert tc.check(stream) == dcc.DCC_OK
         out["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % tokens] = res
-        del wts, xin, yt, part, ysep
+        del wts, xin, yt, part, ysep, hres
     # the ring barrier: default transport (8 ranks: one cluster, distributed
     # shared memory) and the global-memory semaphores (DCC_RING_CLUSTER=0)
     for key, env in (("c5_ring_barrier", None), ("c5_ring_barrier_l2_semaphores", "0")):

@@ -8,6 +8,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <map>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -68,6 +70,14 @@ constexpr size_t kPipeChunkBytes = 8u << 20;
 // 3584 79.1 / 75.1, 4096 87.3 / 80.5, 8192 169 / 152.
 constexpr size_t kFusedBulkMinKp = 3584;
 
+// Tensor-core layer over a batch of tokens: up to this many tokens (the token
+// tile rounded up to 16) a CTA holds two accumulators, a tile of up to 256
+// weight rows sharing each token tile, with a deeper K split (8 ranks x 8192
+// rows x kp 1024 on GB300: 24.0 / 24.9 us at 1 / 16 tokens against 27.6 with
+// one accumulator); from 64 tokens one accumulator is faster (29.1 vs 29.7 us
+// at 64, 39.1 vs 53.6 at 256: the token tile takes more of each stage).
+constexpr int kMmaTwoAccMaxTokens = 32;
+
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;
 
@@ -95,6 +105,8 @@ struct dcc_comm {
   // fused linear + AllReduce through the bulk-copy kernel: -1 by kp (measured
   // crossover), 0 never, 1 always (DCC_FUSED_BULK)
   int fused_bulk = -1;
+  // tensor-core layer: accumulators per CTA, -1 by token count, 1 or 2 forced (DCC_MMA_ACC)
+  int mma_acc = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier
   bool pdl = true;             // DCC_PDL / dcc_set_pdl: programmatic dependent launch of the wait-free kernels
   bool ring_cluster = true;    // DCC_RING_CLUSTER=0: the ring barrier through L2 even when the ranks fit one cluster
@@ -127,6 +139,9 @@ struct dcc_comm {
     }
   };
   std::unordered_map<MapKey, CUtensorMap, MapKeyHash> tmaps;
+  // clusters of the tensor-core layer that fit on the device at once, by
+  // (kernel, cluster size, dynamic shared memory); 0 = not measured yet
+  std::map<std::tuple<const void*, int, size_t>, int> mma_clusters;
 };
 
 namespace dcc_host {

@@ -343,7 +343,8 @@ bool visit_kernels(F&& visit) {
     if (!v(dcc::allgather_kernel(n, false)) || !v(dcc::allgather_kernel(n, true)) ||
         !v(dcc::allgather_bulk_kernel(n)) || !v(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
-        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) || !v(dcc::linear_allreduce_mma_kernel(n)))
+        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) || !v(dcc::linear_allreduce_mma_kernel(n, 1)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 2)))
       return false;
   return v(dcc::ring_barrier_kernel()) && v(dcc::ring_barrier_cluster_kernel()) && v(dcc::channel_put_kernel()) &&
          v(dcc::channel_get_kernel());
@@ -612,6 +613,10 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_bulk = std::strcmp(v, "0") != 0 ? 1 : 0;
+  if (const char* v = std::getenv("DCC_MMA_ACC")) {
+    const int m = std::atoi(v);
+    if (m == 1 || m == 2) c->mma_acc = m;
+  }
   if (const char* v = std::getenv("DCC_INPLACE_UNROLL")) {
     const int u = std::atoi(v);
     if (u >= 1 && u <= dcc::kInplaceUnroll) c->inplace_unroll = u;
@@ -892,8 +897,9 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
   return linear_launch(c, weight, x, residual, y, rows, kp, t, s);
 }
 
-int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
-                                size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+namespace {
+int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
+                  size_t tokens, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
   if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
   if (c->sticky != DCC_OK) return c->sticky;
   if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
@@ -917,6 +923,16 @@ int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* 
       if (overlaps(y[r], yb, weight[p], wb) || overlaps(y[r], yb, x[p], xb)) return DCC_ERR_INVALID_ARG;
       if (p != r && overlaps(y[r], yb, y[p], yb)) return DCC_ERR_INVALID_ARG;
     }
+  if (residual) {
+    for (int r = 0; r < c->n; ++r) {
+      if (!residual[r]) return DCC_ERR_INVALID_ARG;
+      if (reinterpret_cast<uintptr_t>(residual[r]) & 15u) return DCC_ERR_MISALIGNED;
+      if (!in_window(c, r, DCC_BUF_INPUT, residual[r], yb) && !in_window(c, r, DCC_BUF_OUTPUT, residual[r], yb))
+        return DCC_ERR_NOT_REGISTERED;
+      for (int p = 0; p < c->n; ++p)
+        if (overlaps(residual[r], yb, y[p], yb) && !(p == r && residual[r] == y[r])) return DCC_ERR_INVALID_ARG;
+    }
+  }
   int rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
   DeviceScope ds(c->device);
@@ -924,20 +940,58 @@ int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* 
   const int ntile = tokens <= 16 ? 16 : (int)((tokens + 15) / 16 * 16);
   dcc::MmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  // Launch shape: tiles of bm weight rows (a multiple of 8, at most 128) and
-  // ks K splits (a cluster of ks CTAs per tile, ks <= kMmaMaxSplit and at
-  // most one 64-element block each), chosen so the grid fills the most SMs in
-  // one wave (ties: fewer splits, then taller tiles).  The weight stream is
-  // bound by the bytes each SM keeps in flight, so every SM counts.
+  // Launch shape: macc accumulators per CTA (two up to kMmaTwoAccMaxTokens
+  // tokens: a tile of up to 256 weight rows shares each token tile), tiles of bm
+  // weight rows (a multiple of 8; 64..128 with one accumulator, 136..256 with
+  // two) and ks K splits (a cluster of ks CTAs per tile, ks <= kMmaMaxSplit
+  // and at most one 64-element block each), chosen so the grid fills the most
+  // SMs in one wave (ties: fewer splits, then taller tiles).  The weight
+  // stream is bound by the bytes each SM keeps in flight, so every SM counts;
+  // one wave means at most as many clusters as fit on the device at once,
+  // which the GPCs' SM counts make fewer than SMs / ks.
+  int macc = c->mma_acc > 0 ? c->mma_acc : ntile <= kMmaTwoAccMaxTokens ? 2 : 1;
+  if (rows <= (size_t)dcc::kMmaBM) macc = 1;
+  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc);
+  const int stages = dcc::mma_stages(ntile, macc);
+  const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  auto fit = [&](int ks) -> long long {  // clusters of ks CTAs resident at once
+    const auto key = std::make_tuple(fn, ks, smem);
+    const auto it = c->mma_clusters.find(key);
+    if (it != c->mma_clusters.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks);
+    cfg.blockDim = dim3((unsigned)dcc::kMmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)ks;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int num = 0;
+    if (cudaOccupancyMaxActiveClusters(&num, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      num = c->num_sms / ks;
+    }
+    c->mma_clusters[key] = num;
+    return num;
+  };
+  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
   const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
-  int best_bm = dcc::kMmaBM, best_ks = 1;
+  int best_bm = bm_hi, best_ks = 1;
   long long best = -1;
   auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
-  for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2)
-    for (int bm = 64; bm <= dcc::kMmaBM; bm += 8) {  // shorter tiles: more CTAs
-      if (tiles(bm) * ks > c->num_sms) continue;
+  for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2) {
+    const long long cap = fit(ks);
+    for (int bm = bm_lo; bm <= bm_hi; bm += 8) {  // shorter tiles: more CTAs
+      if (tiles(bm) > cap) continue;
       int tall = bm;  // the tallest tile with the same tile count
-      while (tall + 8 <= dcc::kMmaBM && tiles(tall + 8) == tiles(bm)) tall += 8;
+      while (tall + 8 <= bm_hi && tiles(tall + 8) == tiles(bm)) tall += 8;
       if (tiles(bm) * ks > best) {
         best = tiles(bm) * ks;
         best_bm = tall;
@@ -945,39 +999,56 @@ int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* 
       }
       break;
     }
-  if (best < 0) {  // more tiles than SMs even at 128 rows: several waves, no split
-    best_bm = dcc::kMmaBM;
+  }
+  if (best < 0) {  // more tiles than fit even at the tallest tile: several waves, no split
+    best_bm = bm_hi;
     best_ks = 1;
   }
+  const int bm0 = best_bm < dcc::kMmaBM ? best_bm : dcc::kMmaBM;
   for (int r = 0; r < c->n; ++r) {
-    rc = tensor_map(c, weight[r], kp, rows, (unsigned)best_bm, t, &maps.w[r]);
+    rc = tensor_map(c, weight[r], kp, rows, (unsigned)bm0, t, &maps.w[r]);
+    if (rc == DCC_OK && macc == 2)
+      rc = tensor_map(c, weight[r], kp, rows, (unsigned)(best_bm - dcc::kMmaBM), t, &maps.w2[r]);
     if (rc == DCC_OK) rc = tensor_map(c, x[r], kp, tokens, (unsigned)ntile, t, &maps.x[r]);
     if (rc != DCC_OK) return rc;
   }
   dcc::MmaArgs a{};
   for (int r = 0; r < c->n; ++r) {
     a.y[r] = y[r];
+    a.res[r] = residual ? residual[r] : nullptr;
     set_extent(a, dcc::kBufRecv, r, yb);
+    set_extent(a, dcc::kBufResidual, r, residual ? yb : 0);
   }
   a.tokens = (int)tokens;
   a.rows = (int)rows;
   a.kp = (int)kp;
   a.ntile = ntile;
   a.fp16 = t == DCC_FP16 ? 1 : 0;
-  a.stages = dcc::mma_stages(ntile);
+  a.macc = macc;
+  a.stages = stages;
   a.bm = best_bm;
   a.ks = best_ks;
   const int mtiles = (int)((rows + best_bm - 1) / best_bm);
-  const void* fn = dcc::linear_allreduce_mma_kernel(c->n);
-  const size_t smem = dcc::mma_smem_bytes(ntile, a.stages);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-    cudaGetLastError();
-    return DCC_ERR_LAUNCH;
-  }
+  if (c->log)
+    std::fprintf(stderr, "dcc_linear_allreduce_tokens: tokens=%zu rows=%zu kp=%zu macc=%d bm=%d ks=%d ctas=%d stages=%d\n",
+                 tokens, rows, kp, macc, best_bm, best_ks, mtiles * best_ks, stages);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&maps, &dc, &a};
   return launch(fn, mtiles * best_ks, dcc::kMmaThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl,
                 best_ks);
+}
+}  // namespace
+
+int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
+                                size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
+  return tokens_launch(c, weight, x, nullptr, y, tokens, rows, kp, t, s);
+}
+
+int dcc_linear_allreduce_tokens_residual(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual,
+                                         void* const* y, size_t tokens, size_t rows, size_t kp, dcc_dtype_t t,
+                                         dcc_stream_t s) {
+  if (!residual) return DCC_ERR_INVALID_ARG;
+  return tokens_launch(c, weight, x, residual, y, tokens, rows, kp, t, s);
 }
 
 int dcc_ring_barrier(dcc_comm_t c, int iters, dcc_stream_t s) {

@@ -33,6 +33,10 @@
 //                         cluster adds the KS partials of its share of the
 //                         tokens in split order, rounds once and stores 16
 //                         bytes (8 rows) at a time into all N outputs.
+// With a residual per output rank (the residual stream of the layer,
+// h_q <- h_q + layer) output q gets R(sum + residual_q): the residual joins
+// the fp32 sum before the one rounding, and the thread that reads residual q
+// writes output q, so the two may be one buffer.
 // Tokens beyond the batch and rows beyond the matrix are zero-filled by the
 // tensor map and masked at the store.  The fp32 accumulation order inside
 // the tensor core is the hardware's, so results are exact when every partial
@@ -56,35 +60,39 @@ constexpr int kMmaMaxTokens = 256;
 constexpr int kMmaMaxSplit = 8;  // CTAs per cluster along K
 
 struct MmaMaps {
-  CUtensorMap w[DCC_MAX_RANKS];  // rows x kp, box 64 x 128
-  CUtensorMap x[DCC_MAX_RANKS];  // tokens x kp, box 64 x ntile
+  CUtensorMap w[DCC_MAX_RANKS];   // rows x kp, box 64 x min(bm, 128)
+  CUtensorMap x[DCC_MAX_RANKS];   // tokens x kp, box 64 x ntile
+  CUtensorMap w2[DCC_MAX_RANKS];  // with two accumulators: rows x kp, box 64 x (bm - 128)
 };
 
 struct MmaArgs {
-  void* y[DCC_MAX_RANKS];  // tokens x rows
+  void* y[DCC_MAX_RANKS];          // tokens x rows
+  const void* res[DCC_MAX_RANKS];  // tokens x rows residuals (res[0] null: none)
   int tokens, rows, kp, ntile, ks, stages;
-  int bm;                  // weight rows per CTA (multiple of 8, at most kMmaBM)
+  int bm;                  // weight rows per CTA (multiple of 8, at most macc * kMmaBM)
+  int macc;                // accumulators per CTA (the kernel's MACC): 1, or 2 (rows 128..bm-1 in the second)
   int fp16;                // element type: 0 bf16, 1 fp16
 #if DCC_CHECK_BOUNDS
   size_t ext[kNumBufKinds][DCC_MAX_RANKS];
 #endif
 };
 
-__host__ __device__ constexpr size_t mma_stage_bytes(int ntile) {
-  return (size_t)kMmaBM * kMmaBK * 2 + (size_t)ntile * kMmaBK * 2;
+// a stage: macc weight tiles of 128 x 64 and the token tile ntile x 64
+__host__ __device__ constexpr size_t mma_stage_bytes(int ntile, int macc) {
+  return (size_t)macc * kMmaBM * kMmaBK * 2 + (size_t)ntile * kMmaBK * 2;
 }
 constexpr int kMmaMaxStages = 16;
 // dynamic shared memory: 1 KiB for alignment, the stages, and the mbarriers
-__host__ __device__ constexpr size_t mma_smem_bytes(int ntile, int stages) {
-  return 1024 + (size_t)stages * mma_stage_bytes(ntile) + 16 * (size_t)stages + 64;
+__host__ __device__ constexpr size_t mma_smem_bytes(int ntile, int stages, int macc) {
+  return 1024 + (size_t)stages * mma_stage_bytes(ntile, macc) + 16 * (size_t)stages + 64;
 }
 // Stages: as many as fit in 216 KiB (at most kMmaMaxStages) -- the weight
 // stream is bound by the bytes in flight (on GB300 a loaded HBM read takes
 // about 4 us, so saturating it takes some 28 MB in flight across the GPU) --
 // and at least as many bytes as the fp32 partial tile the epilogue puts in
 // their place.
-inline int mma_stages(int ntile) {
-  const size_t st = mma_stage_bytes(ntile);
+inline int mma_stages(int ntile, int macc) {
+  const size_t st = mma_stage_bytes(ntile, macc);
   int s = (int)((216u * 1024u) / st);
   if (s > kMmaMaxStages) s = kMmaMaxStages;
   while ((size_t)s * st < (size_t)ntile * kMmaBM * 4) ++s;
@@ -131,6 +139,32 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// L2 eviction policies: the weights stream through once (evict first); the
+// token tiles, read by every CTA, and the residuals, prefetched for the
+// epilogue, stay (evict last)
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+// asks L2 for `bytes` (a multiple of 16) at a 16-byte aligned global address
+__device__ __forceinline__ void l2_prefetch_bytes(const void* p, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
+               : "memory");
+}
 // asks L2 for a tile of a tensor map (no data comes back to the CTA)
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
@@ -153,7 +187,30 @@ __device__ __forceinline__ uint32_t mma_instr_desc(int ntile, bool fp16) {
   return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(ntile >> 3) << 17) | ((uint32_t)(kMmaBM >> 4) << 24);
 }
 
-template <int NT>
+// 8 fp32 values rounded once to 8 packed 16-bit values (fp16 or bf16), and back
+__device__ __forceinline__ uint4 mma_narrow8(const float* v, bool fp16) {
+  if (fp16)
+    return make_uint4(HalfLanes<__half2, F16Ops>::narrow2(v[0], v[1]), HalfLanes<__half2, F16Ops>::narrow2(v[2], v[3]),
+                      HalfLanes<__half2, F16Ops>::narrow2(v[4], v[5]), HalfLanes<__half2, F16Ops>::narrow2(v[6], v[7]));
+  return make_uint4(HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(v[0], v[1]),
+                    HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(v[2], v[3]),
+                    HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(v[4], v[5]),
+                    HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(v[6], v[7]));
+}
+__device__ __forceinline__ void mma_widen8(uint4 w, bool fp16, float* v) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = fp16 ? F16Ops::widen2(u[k]) : Bf16Ops::widen2(u[k]);
+    v[2 * k] = f.x;
+    v[2 * k + 1] = f.y;
+  }
+}
+
+// MACC (accumulators per CTA) is a template parameter: with a run-time
+// count the loops over the accumulators cost about 12 us per launch at 8 x
+// 8192 x 1024 (measured on GB300: 40 vs 28 us).
+template <int NT, int MACC>
 __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const __grid_constant__ MmaMaps maps,
                                                                           DevComm dc, MmaArgs a) {
   extern __shared__ unsigned char mma_raw[];
@@ -163,7 +220,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte alignment
   unsigned char* gbase = mma_raw + (base - raw_u32);
   const int S = a.stages, NTILE = a.ntile, KS = a.ks;
-  const uint32_t a_bytes = kMmaBM * kMmaBK * 2, st_bytes = (uint32_t)mma_stage_bytes(NTILE);
+  const uint32_t a_bytes = kMmaBM * kMmaBK * 2, st_bytes = (uint32_t)mma_stage_bytes(NTILE, MACC);
+  const uint32_t b_off = (uint32_t)MACC * a_bytes;      // the token tile follows the weight tiles
   const uint32_t bars = base + (uint32_t)S * st_bytes;  // full[S], empty[S], accumulator ready
   auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
@@ -172,10 +230,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   unsigned split = 0;
   if (KS > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(split));
   const int mtile = (int)blockIdx.x / KS, m0 = mtile * a.bm;
+  const int bm0 = a.bm < kMmaBM ? a.bm : kMmaBM;  // rows of the first accumulator; the second has bm - 128
   const int kpb = a.kp / kMmaBK, nb = n * kpb;
   const int b0 = (int)((long long)split * nb / KS), b1 = (int)((long long)(split + 1) * nb / KS);
   const int nk = b1 - b0;
-  const uint32_t ncols = NTILE <= 32 ? 32u : NTILE <= 64 ? 64u : NTILE <= 128 ? 128u : 256u;
+  // columns of one accumulator (a power of two, at least 32); the second follows the first
+  const uint32_t acc_cols = NTILE <= 32 ? 32u : NTILE <= 64 ? 64u : NTILE <= 128 ? 128u : 256u;
+  const uint32_t ncols = acc_cols * (uint32_t)MACC;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -200,6 +261,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
     for (int i = 0; i < nk && i < S; ++i) {
       const int g = b0 + i;
       tma_prefetch_2d(&maps.w[g / kpb], (g % kpb) * kMmaBK, m0);
+      if (MACC == 2) tma_prefetch_2d(&maps.w2[g / kpb], (g % kpb) * kMmaBK, m0 + kMmaBM);
     }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -208,17 +270,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
 
+  const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;  // this CTA's epilogue tokens
   if (warp == 0 && lane == 0) {  // TMA producer
+    // the weight boxes are bm0 and bm - 128 rows (tile rows beyond them are
+    // never written and only reach accumulator rows the epilogue discards)
+    const uint32_t tx = st_bytes - (uint32_t)(MACC * kMmaBM - a.bm) * (kMmaBK * 2);
+    const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
       if (i >= S && !mma_mbar_wait(empty(s), (uint32_t)(((i / S) - 1) & 1), dc, mtile, (int)split)) break;
       const int g = b0 + i, p = g / kpb, k0 = (g % kpb) * kMmaBK;
       const uint32_t sa = base + (uint32_t)s * st_bytes;
-      // the weight box is bm rows (the tile's rows bm..127 are never written and
-      // only reach accumulator rows the epilogue discards)
-      mma_mbar_expect(full(s), st_bytes - (uint32_t)(kMmaBM - a.bm) * (kMmaBK * 2));
-      tma_load_2d(sa, &maps.w[p], k0, m0, full(s));
-      tma_load_2d(sa + a_bytes, &maps.x[p], k0, 0, full(s));
+      mma_mbar_expect(full(s), tx);
+      tma_load_2d_hint(sa, &maps.w[p], k0, m0, full(s), pol_w);
+      if (MACC == 2) tma_load_2d_hint(sa + a_bytes, &maps.w2[p], k0, m0 + kMmaBM, full(s), pol_w);
+      tma_load_2d_hint(sa + b_off, &maps.x[p], k0, 0, full(s), pol_x);
+    }
+  } else if (warp >= 2 && a.res[0] != nullptr) {
+    // idle during the main loop: ask L2 for the residual rows of this CTA's
+    // epilogue (per rank and token, the tile's rows are contiguous), to be
+    // kept there while the weights stream past
+    const uint64_t pol = l2_evict_last();
+    const int per_tok = n * MACC;
+    for (int j = threadIdx.x - 64; j < (t_hi - t_lo) * per_tok; j += kMmaThreads - 64) {
+      const int t = t_lo + j / per_tok, q = (j % per_tok) / MACC, h = j % MACC;
+      const int mh = m0 + h * kMmaBM, bmh = h == 0 ? bm0 : a.bm - kMmaBM;
+      const int nr = mh + bmh <= a.rows ? bmh : a.rows - mh;
+      if (t >= a.tokens || nr <= 0) continue;
+      const size_t off = ((size_t)t * a.rows + (size_t)mh) * 2;
+      if (in_bounds(dc, a, kBufResidual, q, off, (size_t)nr * 2))
+        l2_prefetch_bytes(static_cast<const char*>(a.res[q]) + off, (uint32_t)nr * 2u, pol);
     }
   } else if (warp == 1 && lane == 0) {  // MMA issuer
     const uint32_t idesc = mma_instr_desc(NTILE, a.fp16 != 0);
@@ -226,16 +307,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
       const int s = i % S;
       if (!mma_mbar_wait(full(s), (uint32_t)((i / S) & 1), dc, mtile, (int)split)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t sa = base + (uint32_t)s * st_bytes, sb = sa + a_bytes;
+      const uint32_t sa = base + (uint32_t)s * st_bytes, sb = sa + b_off;
 #pragma unroll
       for (int kk = 0; kk < kMmaBK / 16; ++kk) {
-        const uint64_t ad = mma_smem_desc(sa + (uint32_t)kk * 32u), bd = mma_smem_desc(sb + (uint32_t)kk * 32u);
+        const uint64_t bd = mma_smem_desc(sb + (uint32_t)kk * 32u);
         const uint32_t accumulate = (i > 0 || kk > 0) ? 1u : 0u;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-            "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
-            : "memory");
+        for (int h = 0; h < MACC; ++h) {  // both accumulators share the token tile
+          const uint64_t ad = mma_smem_desc(sa + (uint32_t)h * a_bytes + (uint32_t)kk * 32u);
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + (uint32_t)h * acc_cols),
+              "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
+              : "memory");
+        }
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty(s))
                    : "memory");
@@ -246,117 +330,146 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   }
   __syncwarp();
 
-  // epilogue 1: the accumulator (row = TMEM lane) into partial[token][row] fp32
   const int row = warp * 32 + lane;
   const bool acc_ok = nk > 0 && mma_mbar_wait(accf, 0, dc, mtile, (int)split);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
-  for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
-    uint32_t v[32];
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
-    if (c0 + 32 <= NTILE) {
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-          "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-          : "r"(taddr));
-    } else {
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-          : "r"(taddr));
+  for (int h = 0; h < MACC; ++h) {
+    // epilogue 1: accumulator h (row = TMEM lane) into partial[token][row] fp32
+    for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
+      uint32_t v[32];
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
+      if (c0 + 32 <= NTILE) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(taddr));
+      } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+            : "r"(taddr));
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const int cols = c0 + 32 <= NTILE ? 32 : 16;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
     }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    const int cols = c0 + 32 <= NTILE ? 32 : 16;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (KS > 1) mma_cluster_sync();  // every split's partials are in its shared memory
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (KS > 1) mma_cluster_sync();  // every split's partials are in its shared memory
 
-  // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); an item
-  // is 8 consecutive rows of one token: its KS partials are added in split
-  // order (distributed shared memory), rounded once and stored 16 bytes into
-  // each of the N outputs.  A thread gathers the partials of kBatch items
-  // before it adds and stores any, so their loads are in flight together.
-  constexpr int kBatch = 4;
-  const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;
-  const int items = (t_hi - t_lo) * (kMmaBM / 8);
-  for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
-    float acc[kBatch][8];
+    // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); an
+    // item is 8 consecutive rows of one token: its KS partials are added in
+    // split order (distributed shared memory), rounded once and stored 16
+    // bytes into each of the N outputs.  A thread gathers the partials of
+    // kBatch items before it adds and stores any, so their loads are in
+    // flight together.
+    constexpr int kBatch = 4;
+    const int mh = m0 + h * kMmaBM;                         // first row of accumulator h
+    const int bmh = h == 0 ? bm0 : a.bm - kMmaBM;           // its rows in this tile
+    const int items = (t_hi - t_lo) * (kMmaBM / 8);
+    for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
+      float acc[kBatch][8];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b)
+      for (int b = 0; b < kBatch; ++b)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[b][j] = 0.0f;
-    for (int s2 = 0; s2 < KS; ++s2) {
-      float4 lo[kBatch], hi[kBatch];
+        for (int j = 0; j < 8; ++j) acc[b][j] = 0.0f;
+      for (int s2 = 0; s2 < KS; ++s2) {
+        float4 lo[kBatch], hi[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int w = w0 + b * kMmaThreads;
+          if (w >= items) continue;
+          const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
+          const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
+          if (KS == 1) {
+            lo[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
+            hi[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
+          } else {
+            uint32_t remote;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
+            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(lo[b].x), "=f"(lo[b].y), "=f"(lo[b].z), "=f"(lo[b].w)
+                         : "r"(remote)
+                         : "memory");
+            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(hi[b].x), "=f"(hi[b].y), "=f"(hi[b].z), "=f"(hi[b].w)
+                         : "r"(remote + 16u)
+                         : "memory");
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (w0 + b * kMmaThreads >= items) continue;
+          const float pv[8] = {lo[b].x, lo[b].y, lo[b].z, lo[b].w, hi[b].x, hi[b].y, hi[b].z, hi[b].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[b][j] = s2 == 0 ? pv[j] : __fadd_rn(acc[b][j], pv[j]);
+        }
+      }
+      // item b's place in the outputs (bytes), or -1 when it lies beyond the
+      // batch or the matrix (rows come in multiples of 8, and bm too: all 8
+      // rows or none)
+      long long off[kBatch];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int w = w0 + b * kMmaThreads;
-        if (w >= items) continue;
         const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
-        const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
-        if (KS == 1) {
-          lo[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
-          hi[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
-        } else {
-          uint32_t remote;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
-          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(lo[b].x), "=f"(lo[b].y), "=f"(lo[b].z), "=f"(lo[b].w)
-                       : "r"(remote)
-                       : "memory");
-          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(hi[b].x), "=f"(hi[b].y), "=f"(hi[b].z), "=f"(hi[b].w)
-                       : "r"(remote + 16u)
-                       : "memory");
+        off[b] = (w < items && t < a.tokens && r8 < bmh && mh + r8 < a.rows)
+                     ? (long long)(((size_t)t * a.rows + (size_t)(mh + r8)) * 2)
+                     : -1;
+      }
+      if (a.res[0] == nullptr) {  // one rounding shared by every output
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (off[b] < 0) continue;
+          const uint4 out = mma_narrow8(acc[b], a.fp16 != 0);
+          for (int q = 0; q < n; ++q)
+            if (in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16))
+              st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), out);
+        }
+      } else {  // output q: R(sum + residual_q); the thread that reads residual q writes output q
+        // rank q+1's residuals are loaded before rank q's outputs are stored,
+        // so two ranks' loads are in flight at a time
+        auto load_res = [&](int q, uint4* rv) {
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b)
+            rv[b] = off[b] >= 0 && in_bounds(dc, a, kBufResidual, q, (size_t)off[b], 16)
+                        ? *reinterpret_cast<const uint4*>(static_cast<const char*>(a.res[q]) + off[b])
+                        : make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 cur[kBatch], nxt[kBatch];
+        load_res(0, cur);
+        for (int q = 0; q < n; ++q) {
+          if (q + 1 < n) load_res(q + 1, nxt);
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            if (off[b] < 0 || !in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16)) continue;
+            float r[8], v[8];
+            mma_widen8(cur[b], a.fp16 != 0, r);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(acc[b][j], r[j]);
+            st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), mma_narrow8(v, a.fp16 != 0));
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) cur[b] = nxt[b];
         }
       }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        if (w0 + b * kMmaThreads >= items) continue;
-        const float pv[8] = {lo[b].x, lo[b].y, lo[b].z, lo[b].w, hi[b].x, hi[b].y, hi[b].z, hi[b].w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[b][j] = s2 == 0 ? pv[j] : __fadd_rn(acc[b][j], pv[j]);
-      }
     }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int w = w0 + b * kMmaThreads;
-      if (w >= items) continue;
-      const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
-      const int i0 = m0 + r8;
-      // rows come in multiples of 8 (and bm too): all 8 rows or none
-      if (t >= a.tokens || r8 >= a.bm || i0 >= a.rows) continue;
-      uint4 out;
-      if (a.fp16) {
-        out = make_uint4(HalfLanes<__half2, F16Ops>::narrow2(acc[b][0], acc[b][1]),
-                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][2], acc[b][3]),
-                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][4], acc[b][5]),
-                         HalfLanes<__half2, F16Ops>::narrow2(acc[b][6], acc[b][7]));
-      } else {
-        out = make_uint4(HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][0], acc[b][1]),
-                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][2], acc[b][3]),
-                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][4], acc[b][5]),
-                         HalfLanes<__nv_bfloat162, Bf16Ops>::narrow2(acc[b][6], acc[b][7]));
-      }
-      const size_t off = ((size_t)t * a.rows + (size_t)i0) * 2;  // bytes
-      for (int q = 0; q < n; ++q)
-        if (in_bounds(dc, a, kBufRecv, q, off, 16))
-          st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off), out);
-    }
+    // no CTA overwrites or frees its partials while a peer may still read them
+    if (KS > 1) mma_cluster_sync();
+    __syncthreads();
   }
-  if (KS > 1) mma_cluster_sync();  // no CTA leaves while a peer may still read its partials
-  __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
-const void* linear_allreduce_mma_kernel(int n);
+const void* linear_allreduce_mma_kernel(int n, int macc);
 
 }  // namespace dcc

@@ -105,6 +105,7 @@ _SIGS = {
     "dcc_linear_allreduce": [_vp, _PP, _PP, _PP, _sz, _sz, _i, _vp],
     "dcc_linear_allreduce_residual": [_vp, _PP, _PP, _PP, _PP, _sz, _sz, _i, _vp],
     "dcc_linear_allreduce_tokens": [_vp, _PP, _PP, _PP, _sz, _sz, _sz, _i, _vp],
+    "dcc_linear_allreduce_tokens_residual": [_vp, _PP, _PP, _PP, _PP, _sz, _sz, _sz, _i, _vp],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -243,6 +244,12 @@ def dcc_linear_allreduce_tokens(comm, weight, x, y, tokens, rows, kp, dtype, str
     return _check(_lib.dcc_linear_allreduce_tokens(comm, _ptrs(weight), _ptrs(x), _ptrs(y), tokens, rows, kp,
                                                    _dtype(dtype), _stream(stream)),
                   "dcc_linear_allreduce_tokens")
+
+
+def dcc_linear_allreduce_tokens_residual(comm, weight, x, residual, y, tokens, rows, kp, dtype, stream=None):
+    return _check(_lib.dcc_linear_allreduce_tokens_residual(comm, _ptrs(weight), _ptrs(x), _ptrs(residual), _ptrs(y),
+                                                            tokens, rows, kp, _dtype(dtype), _stream(stream)),
+                  "dcc_linear_allreduce_tokens_residual")
 
 
 def dcc_ring_barrier(comm, iters, stream=None):

@@ -255,6 +255,20 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
 int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
                                 size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s);
 
+/* The batched layer with a residual per output rank (the residual stream of
+ * a multi-token step, h <- h + layer(h)):
+ *   y[r][t*rows + i] = R( sum_p sum_k weight[p][i*kp + k] * x[p][t*kp + k]
+ *                         + residual[r][t*rows + i] ).
+ * The residual joins the fp32 sum before the one rounding (the reading taken
+ * for the fused epilogue; the pages give none).  residual[r] holds tokens x
+ * rows elements of t laid out like y[r], registered and 16-byte aligned;
+ * residual[r] == y[r] updates the residual in place, any other overlap with
+ * an output is rejected.  Shapes, kernel, results on small-integer data and
+ * errors as dcc_linear_allreduce_tokens; residual NULL is INVALID_ARG. */
+int dcc_linear_allreduce_tokens_residual(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual,
+                                         void* const* y, size_t tokens, size_t rows, size_t kp, dcc_dtype_t t,
+                                         dcc_stream_t s);
+
 /* Ring barrier (the README's two-rank barrier, "signal, flush, wait", chained
  * around all N ranks): per iteration rank 0 signals rank 1 and waits for rank
  * N-1; rank r > 0 waits for rank r-1 and then signals rank (r+1) mod N.  One

@@ -124,6 +124,7 @@ def test_null_communicator_is_rejected(dcc):
         ("dcc_linear_allreduce", None, arr, arr, arr, 8, 8, 3, None),
         ("dcc_linear_allreduce_residual", None, arr, arr, arr, arr, 8, 8, 3, None),
         ("dcc_linear_allreduce_tokens", None, arr, arr, arr, 1, 8, 64, 3, None),
+        ("dcc_linear_allreduce_tokens_residual", None, arr, arr, arr, arr, 1, 8, 64, 3, None),
         ("dcc_allreduce_from_host", None, arr, arr, arr, arr, 4, 1, 0, None),
         ("dcc_ring_barrier", None, 1, None),
         ("dcc_comm_check", None, None),

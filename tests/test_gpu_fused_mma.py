@@ -65,6 +65,30 @@ def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
     assert np.array_equal(got, expect)
 
 
+@pytest.mark.parametrize("acc", ["1", "2"])
+@pytest.mark.parametrize("n,tokens,rows,kp", [
+    (1, 1, 136, 64), (2, 17, 264, 128), (8, 256, 1032, 64), (3, 200, 200, 192), (8, 64, 8192, 64),
+    (16, 130, 520, 64)])
+def test_tokens_one_or_two_accumulators_bit_exact(dcc, monkeypatch, acc, n, tokens, rows, kp):
+    """Both tile forms (one accumulator of up to 128 rows, or two sharing the
+    token tile, up to 256 rows) on the same shapes, whatever the token count
+    would pick: partial second accumulators (136, 200, 264 rows), residuals."""
+    monkeypatch.setenv("DCC_MMA_ACC", acc)
+    g = torch.Generator().manual_seed(n * 17 + tokens + rows)
+    ws = [small_ints(g, rows * kp, "bf16") for _ in range(n)]
+    xs = [small_ints(g, tokens * kp, "bf16", -2, 2) for _ in range(n)]
+    got = run(dcc, ws, xs, tokens, rows, kp, "bf16")
+    expect = oracle.linear_allreduce_tokens([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                            "bf16", tokens, rows, kp)
+    assert np.array_equal(got, expect)
+    res = [small_ints(g, tokens * rows, "bf16", -50, 50) for _ in range(n)]
+    got = run_residual(dcc, ws, xs, res, tokens, rows, kp, "bf16", inplace=True)
+    expect = oracle.linear_allreduce_tokens_residual([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                                     [W.to_storage(r) for r in res], "bf16", tokens, rows, kp)
+    for q in range(n):
+        assert np.array_equal(got[q], expect[q]), q
+
+
 def test_tokens_random_shapes_bit_exact(dcc):
     """Forty seeded random mixes of rank count, tokens, rows, kp and dtype on
     small-integer data: exact against the oracle."""
@@ -156,4 +180,98 @@ def test_tokens_argument_errors(dcc):
         comm.register(1, "output", y[0])
         assert code(w, x, [y[0], y[0]], tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # outputs overlap
         assert code(w, x, [x[0], y[1]], tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # output is an input
+        assert comm.check() == dcc.DCC_OK
+
+
+def run_residual(dcc, ws, xs, res, tokens, rows, kp, dtype, inplace=False):
+    n = len(ws)
+    dw = [w.cuda() for w in ws]
+    dx = [x.cuda() for x in xs]
+    dr = [r.cuda() for r in res]
+    dy = dr if inplace else [torch.full((tokens * rows,), float("nan"), dtype=TD[dtype], device="cuda")
+                             for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", dw)
+        for r in range(n):
+            comm.register(r, "input", dx[r])
+        comm.register_all("output", dy)
+        if not inplace:
+            comm.register_all("input", dr)
+        dcc.dcc_linear_allreduce_tokens_residual(comm.handle, dw, dx, dr, dy, tokens, rows, kp, dtype)
+        assert comm.check() == dcc.DCC_OK
+    return [W.to_storage(y) for y in dy]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n,tokens,rows,kp,inplace", [
+    (1, 1, 128, 64, False), (2, 16, 256, 64, True), (8, 17, 1024, 192, False), (3, 100, 136, 256, True),
+    (8, 256, 512, 64, False), (16, 64, 512, 64, True), (5, 255, 264, 320, False), (8, 33, 8192, 64, True)])
+def test_tokens_residual_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp, inplace):
+    """Each rank's output is the batched layer plus its own residual, exact on
+    small-integer data; in place the residual buffer is the output."""
+    g = torch.Generator().manual_seed(n * 131 + tokens * 7 + kp + int(inplace))
+    ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
+    xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
+    res = [small_ints(g, tokens * rows, dtype, -100, 100) for _ in range(n)]
+    got = run_residual(dcc, ws, xs, res, tokens, rows, kp, dtype, inplace)
+    expect = oracle.linear_allreduce_tokens_residual([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                                     [W.to_storage(r) for r in res], dtype, tokens, rows, kp)
+    for q in range(n):
+        assert np.array_equal(got[q], expect[q]), q
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tokens_residual_random_data_within_bound(dcc, dtype):
+    n, tokens, rows, kp = 8, 64, 1024, 1024
+    g = torch.Generator().manual_seed(404)
+    ws = [(torch.randn(rows * kp, generator=g) * 0.05).to(TD[dtype]) for _ in range(n)]
+    xs = [torch.randn(tokens * kp, generator=g).to(TD[dtype]) for _ in range(n)]
+    res = [torch.randn(tokens * rows, generator=g).to(TD[dtype]) for _ in range(n)]
+    got = run_residual(dcc, ws, xs, res, tokens, rows, kp, dtype)
+    expect = oracle.linear_allreduce_tokens_residual([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                                     [W.to_storage(r) for r in res], dtype, tokens, rows, kp)
+    s = sum(np.abs(x.double().numpy().reshape(tokens, kp)) @ np.abs(w.double().numpy().reshape(rows, kp)).T
+            for w, x in zip(ws, xs)).ravel()
+    m = n * kp + 8 + 1  # products, at most 8 split partials, the residual
+    u = 2.0 ** -23
+    gamma = m * u / (1 - m * u)
+    for q in range(n):
+        gf = W.from_storage(got[q], dtype).double().numpy()
+        ef = W.from_storage(expect[q], dtype).double().numpy()
+        rq = np.abs(res[q].double().numpy())
+        bound = gamma * (s + rq) + ulp_out(np.maximum(np.abs(gf), np.abs(ef)), dtype)
+        assert np.all(np.abs(gf - ef) <= bound), (q, float(np.max(np.abs(gf - ef) / bound)))
+        assert np.mean(got[q] == expect[q]) > 0.9
+
+
+def test_tokens_residual_argument_errors(dcc):
+    n, tokens, rows, kp = 2, 4, 64, 64
+    z = lambda size: torch.zeros(size, dtype=torch.bfloat16, device="cuda")
+    w = [z(rows * kp) for _ in range(n)]
+    x = [z(tokens * kp) for _ in range(n)]
+    y = [z(tokens * rows) for _ in range(n)]
+    res = [z(tokens * rows + 8) for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", w)
+        comm.register_all("input", x)
+        comm.register_all("output", y)
+        h = comm.handle
+
+        def code(*args):
+            try:
+                dcc.dcc_linear_allreduce_tokens_residual(h, *args)
+                return dcc.DCC_OK
+            except dcc.DccError as e:
+                return e.code
+        assert dcc.raw_call("dcc_linear_allreduce_tokens_residual", h, dcc._ptrs(w), dcc._ptrs(x), None,
+                            dcc._ptrs(y), tokens, rows, kp, dcc._dtype("bf16"), None) == dcc.DCC_ERR_INVALID_ARG
+        assert code(w, x, res, y, tokens, rows, kp, "bf16") == dcc.DCC_ERR_NOT_REGISTERED
+        comm.register_all("input", res)
+        assert code(w, x, res, y, tokens, rows, kp, "bf16") == dcc.DCC_OK
+        assert code(w, x, y, y, tokens, rows, kp, "bf16") == dcc.DCC_OK                      # in place
+        assert code(w, x, [r[1:] for r in res], y, tokens, rows, kp, "bf16") == dcc.DCC_ERR_MISALIGNED
+        assert code(w, x, [y[1], y[0]], y, tokens, rows, kp, "bf16") == dcc.DCC_ERR_NOT_REGISTERED
+        comm.register(0, "output", y[1])
+        comm.register(1, "output", y[0])
+        assert code(w, x, [y[1], y[0]], y, tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # another's output
         assert comm.check() == dcc.DCC_OK
