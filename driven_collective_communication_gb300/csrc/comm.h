@@ -73,10 +73,11 @@ constexpr size_t kFusedBulkMinKp = 3584;
 // Tensor-core layer over a batch of tokens: up to this many tokens (the token
 // tile rounded up to 16) a CTA holds two accumulators, a tile of up to 256
 // weight rows sharing each token tile, with a deeper K split (8 ranks x 8192
-// rows x kp 1024 on GB300: 24.0 / 24.9 us at 1 / 16 tokens against 27.6 with
-// one accumulator); from 64 tokens one accumulator is faster (29.1 vs 29.7 us
-// at 64, 39.1 vs 53.6 at 256: the token tile takes more of each stage).
-constexpr int kMmaTwoAccMaxTokens = 32;
+// rows x kp 1024 on GB300: 23.2 / 23.7 / 26.6 us at 1 / 16 / 64 tokens
+// against 27.2 / 27.3 / 28.2 with one accumulator); above, the token tile
+// takes too much of each stage (128 tokens: 31.5 vs 29.8 us, 256: 55.3 vs
+// 36.5).
+constexpr int kMmaTwoAccMaxTokens = 64;
 
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;

@@ -987,6 +987,7 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   long long best = -1;
   auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
   for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2) {
+    if (!dcc::mma_epilogue_fits(ntile, stages, macc, ks)) break;  // no room for the epilogue's inbox
     const long long cap = fit(ks);
     for (int bm = bm_lo; bm <= bm_hi; bm += 8) {  // shorter tiles: more CTAs
       if (tiles(bm) > cap) continue;

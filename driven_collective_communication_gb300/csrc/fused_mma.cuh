@@ -90,13 +90,22 @@ __host__ __device__ constexpr size_t mma_smem_bytes(int ntile, int stages, int m
 // stream is bound by the bytes in flight (on GB300 a loaded HBM read takes
 // about 4 us, so saturating it takes some 28 MB in flight across the GPU) --
 // and at least as many bytes as the fp32 partial tile the epilogue puts in
-// their place.
+// their place.  The epilogue's inbox (the other splits' slices, see
+// mma_epilogue) also needs room: mma_epilogue_fits says whether a K split
+// leaves it.
 inline int mma_stages(int ntile, int macc) {
   const size_t st = mma_stage_bytes(ntile, macc);
   int s = (int)((216u * 1024u) / st);
   if (s > kMmaMaxStages) s = kMmaMaxStages;
   while ((size_t)s * st < (size_t)ntile * kMmaBM * 4) ++s;
   return s;
+}
+
+// the partial tile (ntile x 128 fp32) plus the inbox for the other ks - 1
+// splits' token slices fit in the stage buffers
+inline bool mma_epilogue_fits(int ntile, int stages, int macc, int ks) {
+  const size_t need = ((size_t)2 * ntile - (size_t)ntile / ks) * kMmaBM * 4;
+  return need <= (size_t)stages * mma_stage_bytes(ntile, macc);
 }
 
 __device__ __forceinline__ uint32_t smem_addr_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -207,6 +216,167 @@ __device__ __forceinline__ void mma_widen8(uint4 w, bool fp16, float* v) {
   }
 }
 
+// Epilogue of the tensor-core layer, for each accumulator h of the CTA:
+//  1. each thread (row = TMEM lane) reads its row of the accumulator
+//     (tcgen05.ld, 32 tokens at a time) into part[token][row] (fp32, local);
+//  2. tokens are dealt out to the CTAs of the cluster in KSC equal slices of
+//     T = NTILE / KSC; after a cluster barrier one thread sends slice o of
+//     part (T x 128 fp32, contiguous) to CTA o with one bulk copy into its
+//     inbox, completing on that CTA's inbox mbarrier;
+//  3. once its inbox is full each CTA adds, for 8 consecutive rows of one of
+//     its tokens at a time, the KSC partials in split order (its own from
+//     part, the others from the inbox: local shared memory only), rounds once
+//     and stores 16 bytes into each of the N outputs (with residuals:
+//     R(sum + residual_q) into output q; the thread that reads residual q
+//     writes output q).
+// part and the inbox reuse the stage buffers (part: NTILE x 128 floats, the
+// inbox after it: (KSC - 1) x T x 128), so the copies start only once every
+// CTA of the cluster is past its main loop (the barrier of step 2).
+template <int KSC, int MACC>
+__device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a, uint32_t tmem, uint32_t acc_cols,
+                                             float* part, uint32_t inbar, int n, unsigned split, int m0, int bm0,
+                                             bool acc_ok, int mtile) {
+  constexpr int kBatch = 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, row = warp * 32 + lane;
+  const int NTILE = a.ntile, T = NTILE / KSC;
+  float* inbox = part + (size_t)NTILE * kMmaBM;
+  const uint32_t slice_bytes = (uint32_t)T * kMmaBM * 4u;
+  const int t_lo = (int)split * T;
+  bool ok = acc_ok;
+  for (int h = 0; h < MACC; ++h) {
+    for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
+      uint32_t v[32];
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
+      if (c0 + 32 <= NTILE) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(taddr));
+      } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+            : "r"(taddr));
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const int cols = c0 + 32 <= NTILE ? 32 : 16;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    if (KSC > 1) {
+      // the bulk copies read part through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (threadIdx.x == 0) mma_mbar_expect(inbar, (uint32_t)(KSC - 1) * slice_bytes);
+      mma_cluster_sync();  // parts written, inboxes armed, every CTA past its main loop
+      if (threadIdx.x == 0) {
+        for (int o = 0; o < KSC; ++o) {
+          if (o == (int)split) continue;
+          const int slot = (int)split < o ? (int)split : (int)split - 1;  // my place in o's inbox
+          uint32_t dst, bar;
+          const uint32_t ldst = smem_addr_u32(inbox + (size_t)slot * T * kMmaBM);
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(ldst), "r"((uint32_t)o));
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(inbar), "r"((uint32_t)o));
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  dst),
+              "r"(smem_addr_u32(part + (size_t)o * T * kMmaBM)), "r"(slice_bytes), "r"(bar)
+              : "memory");
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+      ok = mma_mbar_wait(inbar, (uint32_t)(h & 1), dc, mtile, (int)split) && ok;  // my inbox is full
+    } else {
+      __syncthreads();
+    }
+
+    const int mh = m0 + h * kMmaBM, bmh = h == 0 ? bm0 : a.bm - kMmaBM;  // rows of accumulator h
+    const int items = T * (kMmaBM / 8);
+    for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
+      float acc[kBatch][8];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int w = w0 + b * kMmaThreads;
+        const int tl = w < items ? w / (kMmaBM / 8) : 0, r8 = (w % (kMmaBM / 8)) * 8;
+#pragma unroll
+        for (int s2 = 0; s2 < KSC; ++s2) {  // split order
+          const float* src = s2 == (int)split ? &part[(t_lo + tl) * kMmaBM + r8]
+                                              : &inbox[((s2 < (int)split ? s2 : s2 - 1) * T + tl) * kMmaBM + r8];
+          const float4 lo = *reinterpret_cast<const float4*>(src), hi = *reinterpret_cast<const float4*>(src + 4);
+          const float v8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[b][j] = s2 == 0 ? v8[j] : __fadd_rn(acc[b][j], v8[j]);
+        }
+      }
+      // item b's place in the outputs (bytes), or -1 when it lies beyond the
+      // batch or the matrix (rows come in multiples of 8, and bm too: all 8
+      // rows or none)
+      long long off[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int w = w0 + b * kMmaThreads;
+        const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
+        off[b] = (w < items && t < a.tokens && r8 < bmh && mh + r8 < a.rows)
+                     ? (long long)(((size_t)t * a.rows + (size_t)(mh + r8)) * 2)
+                     : -1;
+      }
+      if (a.res[0] == nullptr) {  // one rounding shared by every output
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (off[b] < 0) continue;
+          const uint4 out = mma_narrow8(acc[b], a.fp16 != 0);
+          for (int q = 0; q < n; ++q)
+            if (in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16))
+              st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), out);
+        }
+      } else {
+        // rank q+1's residuals are loaded before rank q's outputs are stored,
+        // so two ranks' loads are in flight at a time
+        auto load_res = [&](int q, uint4* rv) {
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b)
+            rv[b] = off[b] >= 0 && in_bounds(dc, a, kBufResidual, q, (size_t)off[b], 16)
+                        ? *reinterpret_cast<const uint4*>(static_cast<const char*>(a.res[q]) + off[b])
+                        : make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 cur[kBatch], nxt[kBatch];
+        load_res(0, cur);
+        for (int q = 0; q < n; ++q) {
+          if (q + 1 < n) load_res(q + 1, nxt);
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            if (off[b] < 0 || !in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16)) continue;
+            float r[8], v[8];
+            mma_widen8(cur[b], a.fp16 != 0, r);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(acc[b][j], r[j]);
+            st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), mma_narrow8(v, a.fp16 != 0));
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) cur[b] = nxt[b];
+        }
+      }
+    }
+    if (KSC > 1) {
+      // my copies have read part before it is overwritten or the CTA exits
+      if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      // the next accumulator's copies refill the inboxes: every CTA is done reading its own
+      if (h + 1 < MACC) mma_cluster_sync();
+      else __syncthreads();
+    } else if (h + 1 < MACC) {
+      __syncthreads();
+    }
+  }
+  (void)ok;
+}
+
 // MACC (accumulators per CTA) is a template parameter: with a run-time
 // count the loops over the accumulators cost about 12 us per launch at 8 x
 // 8192 x 1024 (measured on GB300: 40 vs 28 us).
@@ -225,7 +395,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   const uint32_t bars = base + (uint32_t)S * st_bytes;  // full[S], empty[S], accumulator ready
   auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
-  const uint32_t accf = bars + 16u * (uint32_t)S;
+  const uint32_t accf = bars + 16u * (uint32_t)S, inbar = accf + 8u;  // accumulator ready, epilogue inbox full
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned split = 0;
   if (KS > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(split));
@@ -244,6 +414,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
       mma_mbar_init(empty(s), 1);
     }
     mma_mbar_init(accf, 1);
+    mma_mbar_init(inbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 2) {
@@ -330,142 +501,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   }
   __syncwarp();
 
-  const int row = warp * 32 + lane;
   const bool acc_ok = nk > 0 && mma_mbar_wait(accf, 0, dc, mtile, (int)split);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
-  for (int h = 0; h < MACC; ++h) {
-    // epilogue 1: accumulator h (row = TMEM lane) into partial[token][row] fp32
-    for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
-      uint32_t v[32];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
-      if (c0 + 32 <= NTILE) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
-              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-              "=r"(v[30]), "=r"(v[31])
-            : "r"(taddr));
-      } else {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-            : "r"(taddr));
-      }
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int cols = c0 + 32 <= NTILE ? 32 : 16;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    if (KS > 1) mma_cluster_sync();  // every split's partials are in its shared memory
-
-    // epilogue 2: CTA `split` of the cluster takes tokens [t_lo, t_hi); an
-    // item is 8 consecutive rows of one token: its KS partials are added in
-    // split order (distributed shared memory), rounded once and stored 16
-    // bytes into each of the N outputs.  A thread gathers the partials of
-    // kBatch items before it adds and stores any, so their loads are in
-    // flight together.
-    constexpr int kBatch = 4;
-    const int mh = m0 + h * kMmaBM;                         // first row of accumulator h
-    const int bmh = h == 0 ? bm0 : a.bm - kMmaBM;           // its rows in this tile
-    const int items = (t_hi - t_lo) * (kMmaBM / 8);
-    for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
-      float acc[kBatch][8];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[b][j] = 0.0f;
-      for (int s2 = 0; s2 < KS; ++s2) {
-        float4 lo[kBatch], hi[kBatch];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int w = w0 + b * kMmaThreads;
-          if (w >= items) continue;
-          const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
-          const uint32_t local = smem_addr_u32(&part[t * kMmaBM + r8]);
-          if (KS == 1) {
-            lo[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8]);
-            hi[b] = *reinterpret_cast<const float4*>(&part[t * kMmaBM + r8 + 4]);
-          } else {
-            uint32_t remote;
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)s2));
-            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(lo[b].x), "=f"(lo[b].y), "=f"(lo[b].z), "=f"(lo[b].w)
-                         : "r"(remote)
-                         : "memory");
-            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(hi[b].x), "=f"(hi[b].y), "=f"(hi[b].z), "=f"(hi[b].w)
-                         : "r"(remote + 16u)
-                         : "memory");
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          if (w0 + b * kMmaThreads >= items) continue;
-          const float pv[8] = {lo[b].x, lo[b].y, lo[b].z, lo[b].w, hi[b].x, hi[b].y, hi[b].z, hi[b].w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[b][j] = s2 == 0 ? pv[j] : __fadd_rn(acc[b][j], pv[j]);
-        }
-      }
-      // item b's place in the outputs (bytes), or -1 when it lies beyond the
-      // batch or the matrix (rows come in multiples of 8, and bm too: all 8
-      // rows or none)
-      long long off[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int w = w0 + b * kMmaThreads;
-        const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
-        off[b] = (w < items && t < a.tokens && r8 < bmh && mh + r8 < a.rows)
-                     ? (long long)(((size_t)t * a.rows + (size_t)(mh + r8)) * 2)
-                     : -1;
-      }
-      if (a.res[0] == nullptr) {  // one rounding shared by every output
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          if (off[b] < 0) continue;
-          const uint4 out = mma_narrow8(acc[b], a.fp16 != 0);
-          for (int q = 0; q < n; ++q)
-            if (in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16))
-              st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), out);
-        }
-      } else {  // output q: R(sum + residual_q); the thread that reads residual q writes output q
-        // rank q+1's residuals are loaded before rank q's outputs are stored,
-        // so two ranks' loads are in flight at a time
-        auto load_res = [&](int q, uint4* rv) {
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b)
-            rv[b] = off[b] >= 0 && in_bounds(dc, a, kBufResidual, q, (size_t)off[b], 16)
-                        ? *reinterpret_cast<const uint4*>(static_cast<const char*>(a.res[q]) + off[b])
-                        : make_uint4(0u, 0u, 0u, 0u);
-        };
-        uint4 cur[kBatch], nxt[kBatch];
-        load_res(0, cur);
-        for (int q = 0; q < n; ++q) {
-          if (q + 1 < n) load_res(q + 1, nxt);
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            if (off[b] < 0 || !in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16)) continue;
-            float r[8], v[8];
-            mma_widen8(cur[b], a.fp16 != 0, r);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(acc[b][j], r[j]);
-            st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), mma_narrow8(v, a.fp16 != 0));
-          }
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) cur[b] = nxt[b];
-        }
-      }
-    }
-    // no CTA overwrites or frees its partials while a peer may still read them
-    if (KS > 1) mma_cluster_sync();
-    __syncthreads();
+  switch (KS) {  // a power of two up to kMmaMaxSplit
+    case 1: mma_epilogue<1, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
+    case 2: mma_epilogue<2, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
+    case 4: mma_epilogue<4, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
+    default: mma_epilogue<8, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
   }
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
