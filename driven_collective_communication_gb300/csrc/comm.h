@@ -70,6 +70,12 @@ constexpr size_t kPipeChunkBytes = 8u << 20;
 // 3584 79.1 / 75.1, 4096 87.3 / 80.5, 8192 169 / 152.
 constexpr size_t kFusedBulkMinKp = 3584;
 
+// One-token fused linear + AllReduce: kp a multiple of 64 up to this runs on
+// the tensor-core kernel (the batched layer with one token).  Measured on
+// GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load or bulk (us):
+// kp 1024 23.5 / 25.1, 2048 41.9 / 44.2, 3584 71.8 / 71.6, 8192 160 / 149.
+constexpr size_t kFusedTensorMaxKp = 2048;
+
 // Tensor-core layer over a batch of tokens: up to this many tokens (the token
 // tile rounded up to 16) a CTA holds two accumulators, a tile of up to 256
 // weight rows sharing each token tile, with a deeper K split (8 ranks x 8192
@@ -103,9 +109,10 @@ struct dcc_comm {
   // AUTO: messages of at least bulk_min_bytes per rank run large_algo
   size_t bulk_min_bytes = (size_t)1 << 62;
   dcc_algo_t large_algo = DCC_ALGO_TWO_SHOT;
-  // fused linear + AllReduce through the bulk-copy kernel: -1 by kp (measured
-  // crossover), 0 never, 1 always (DCC_FUSED_BULK)
-  int fused_bulk = -1;
+  // kernel of the one-token fused linear + AllReduce: -1 by kp (measured
+  // crossovers), 0 thread loads, 1 bulk copies (DCC_FUSED_BULK=0 / 1), 2 the
+  // tensor-core kernel where kp allows (DCC_FUSED_KERNEL=thread|bulk|tensor)
+  int fused_kernel = -1;
   // tensor-core layer: accumulators per CTA, -1 by token count, 1 or 2 forced (DCC_MMA_ACC)
   int mma_acc = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier

@@ -377,6 +377,9 @@ namespace {
 // The fused layer with (residual != nullptr) or without a residual per output
 // rank.  Residual q is rows elements like y; it may be y[q] itself (in place)
 // but must not partially overlap y[q] nor overlap any other output.
+int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
+                  size_t tokens, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s);
+
 int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
                   size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
   if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
@@ -413,6 +416,11 @@ int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
         if (overlaps(residual[r], yb, y[p], yb) && !(p == r && residual[r] == y[r])) return DCC_ERR_INVALID_ARG;
     }
   }
+  // kp a multiple of 64 up to kFusedTensorMaxKp: the tensor-core kernel, as
+  // the batched layer with one token (same layouts: x is 1 x kp, y 1 x rows)
+  if (kp % dcc::kMmaBK == 0 && kp <= ((size_t)1 << 31) / (size_t)c->n &&
+      (c->fused_kernel == 2 || (c->fused_kernel < 0 && kp <= kFusedTensorMaxKp)))
+    return tokens_launch(c, weight, x, residual, y, 1, rows, kp, t, s);
   int rc = check_channels_all_pairs(c);
   if (rc != DCC_OK) return rc;
   DeviceScope ds(c->device);
@@ -434,7 +442,7 @@ int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   }
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&dc, &a};
-  if (c->fused_bulk > 0 || (c->fused_bulk < 0 && kp >= kFusedBulkMinKp)) {
+  if (c->fused_kernel == 1 || (c->fused_kernel < 0 && kp >= kFusedBulkMinKp)) {
     const void* fn = t == DCC_BF16 ? dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(c->n)
                                    : dcc::linear_allreduce_bulk_kernel<__half>(c->n);
     const size_t smem = dcc::fused_bulk_smem_bytes();
@@ -612,7 +620,12 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   c->log = env_flag("DCC_LOG");
   if (const char* v = std::getenv("DCC_AG_BULK")) c->ag_bulk = std::strcmp(v, "0") != 0;
   if (const char* v = std::getenv("DCC_ZERO_COPY")) c->zero_copy = std::strcmp(v, "0") != 0;
-  if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_bulk = std::strcmp(v, "0") != 0 ? 1 : 0;
+  if (const char* v = std::getenv("DCC_FUSED_BULK")) c->fused_kernel = std::strcmp(v, "0") != 0 ? 1 : 0;
+  if (const char* v = std::getenv("DCC_FUSED_KERNEL")) {
+    if (!std::strcmp(v, "thread")) c->fused_kernel = 0;
+    else if (!std::strcmp(v, "bulk")) c->fused_kernel = 1;
+    else if (!std::strcmp(v, "tensor")) c->fused_kernel = 2;
+  }
   if (const char* v = std::getenv("DCC_MMA_ACC")) {
     const int m = std::atoi(v);
     if (m == 1 || m == 2) c->mma_acc = m;
@@ -897,6 +910,8 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
   return linear_launch(c, weight, x, residual, y, rows, kp, t, s);
 }
 
+}  // extern "C"
+
 namespace {
 int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
                   size_t tokens, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
@@ -1039,6 +1054,8 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
                 best_ks);
 }
 }  // namespace
+
+extern "C" {
 
 int dcc_linear_allreduce_tokens(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t tokens,
                                 size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {

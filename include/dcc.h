@@ -212,16 +212,22 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
  * the project summary's overlap of communication with computation): rank p holds
  * weight[p] (rows x kp, row-major) and x[p] (kp elements), and every rank
  * receives y[r][i] = R(sum_p sum_k weight[p][i*kp + k] * x[p][k]), i < rows.
- * One kernel: rank r's CTAs compute shard r of the rows, getting every rank's
- * weight rows and input slice, accumulate fp32 dot products, add the ranks'
- * partials in rank order, and put the result into all N outputs.  fp16/bf16;
- * rows and kp multiples of 8 (UNSUPPORTED otherwise); 16-byte aligned,
- * registered, outputs disjoint from every input.  The dot products use a
- * fixed lane/shuffle order: exact when every fp32 partial sum is exact, else
- * within the fp32 dot-product error bound before the final rounding.  Rows of
- * at least 3584 elements stream their weights through shared memory with
- * bulk copies (TMA), shorter ones through thread loads; DCC_FUSED_BULK=1 / 0
- * in the environment at communicator creation forces one or the other. */
+ * One kernel, which puts the result into all N outputs; fp16/bf16; rows and
+ * kp multiples of 8 (UNSUPPORTED otherwise); 16-byte aligned, registered,
+ * outputs disjoint from every input.  Exact when every fp32 partial sum is
+ * exact (small-integer data), else within the fp32 dot-product error bound of
+ * the kernel that ran, before the final rounding.  The kernel, by kp:
+ *  - a multiple of 64 up to 2048: the tensor-core kernel of
+ *    dcc_linear_allreduce_tokens with one token (the tensor core's
+ *    accumulation order, then the K-split partials in split order);
+ *  - otherwise below 3584: thread loads, rank r's CTAs computing shard r of
+ *    the rows with fp32 dot products in a fixed lane/shuffle order and the
+ *    ranks' partials added in rank order;
+ *  - otherwise: the same with the weights streamed through shared memory by
+ *    bulk copies (TMA).
+ * DCC_FUSED_KERNEL=thread|bulk|tensor (DCC_FUSED_BULK=0 / 1 for the first
+ * two) in the environment at communicator creation forces one (tensor only
+ * where kp is a multiple of 64). */
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
                          size_t kp, dcc_dtype_t t, dcc_stream_t s);
 
