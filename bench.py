@@ -351,6 +351,12 @@ def run_ours(args, dist):
         out["e2e"] = e2e_host(dcc, comm, xs, ys, w, args, stream, dist)
     if dist.ws == 1 and not args.quick:  # single-GPU extras and the CPU leg (N = 1 only)
         out["sweep_c3"] = sweep_c3(dcc, dev, stream)
+        # the AUTO crossover check runs here, in the state the tuning sweep
+        # (--write-auto-table, a fresh process) measures in: later in this
+        # process, after the other workloads, the same sweep read 0.1-0.2 us
+        # less at 4-16 KiB and 0.3 us more for one-shot at 64 KiB, a shift no
+        # single workload reproduced on its own
+        crossover = crossover_sweep(dcc, dev, stream)[8]
         out["graph_node_floor_us"] = graph_node_floor(stream)
         out["eager_launch_floor"] = eager_floor(stream)
         out["sweep_large"] = sweep_large(dcc, dev, stream)
@@ -361,7 +367,7 @@ def run_ours(args, dist):
                                "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
                                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s",
                                                  "cores": 1, "sample": sample1}}
-        out["crossover_n8"] = crossover_sweep(dcc, dev, stream)[8]
+        out["crossover_n8"] = crossover
         # compact figures last, so that a reader keeping only the end of the line has them
         out["summary"] = summary(dcc, out)
         out["latency_16KiB_us"] = latency_16k(dcc, out)
@@ -583,6 +589,25 @@ def combine_sweeps(paths):
     return sweep, "mean of %d sweeps: %s" % (len(docs), "; ".join(d["source"] for d in docs))
 
 
+def warm_up_gpu(dcc, dev, stream, seconds):
+    """Back-to-back 8 x 64 MiB bf16 AllReduces for about `seconds`."""
+    with torch.cuda.stream(stream):
+        xs = [torch.ones(32 << 20, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        ys = [torch.empty_like(x) for x in xs]
+    torch.cuda.synchronize()
+    with dcc.Comm(8) as c:
+        c.register_all("input", xs)
+        c.register_all("output", ys)
+        step = dcc.prepare_allreduce(c.handle, xs, ys, xs[0].numel(), "bf16", "two_shot", stream)
+        t0 = time.time()
+        while time.time() - t0 < seconds:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
+        assert c.check(stream) == dcc.DCC_OK
+    del xs, ys
+
+
 def write_auto_table(args):
     """Measure the crossover for every rank count 2..16 and dtype (or combine
     earlier sweeps, --combine) and write the tuning JSON that the library
@@ -596,10 +621,17 @@ def write_auto_table(args):
         torch.cuda.set_device(0)
         dev = torch.device("cuda", 0)
         stream = torch.cuda.Stream(device=dev)
+        # the same state the bench's own crossover sweep meets: a GPU that has
+        # been busy for a while (a cold start measured small messages 0.1-0.2 us
+        # slower)
+        warm_up_gpu(dcc, dev, stream, seconds=3.0)
+        clocks = ClockSampler(0)
+        clocks.start()
         sweep = crossover_sweep(dcc, dev, stream, ranks=tuple(range(2, 17)))
+        ck = clocks.stop()
         props = torch.cuda.get_device_properties(dev)
-        source = "python bench.py --write-auto-table on %s (%d SMs), %s" % (
-            props.name, props.multi_processor_count, time.strftime("%Y-%m-%d"))
+        source = "python bench.py --write-auto-table on %s (%d SMs), %s, SM clock median %s MHz" % (
+            props.name, props.multi_processor_count, time.strftime("%Y-%m-%d"), ck.get("sm_mhz"))
     table = {"1": {t: 0 for t in build.DTYPE_ORDER}}
     for n, per in sweep.items():
         table[str(n)] = {t: per[t]["one_shot_max_bytes"] for t in build.DTYPE_ORDER}

@@ -15,21 +15,24 @@
 // (tokens x N*kp): the ranks' shards are slices of the contraction
 // dimension, and the AllReduce is the sum over them.
 //
-// Kernel.  A CTA owns a 128-row tile of Y for every token (the MMA's M = 128
-// rows, N = tokens rounded up to a multiple of 16, at most 256) and a slice
-// of the contraction dimension; the KS CTAs of a thread-block cluster split
-// the contraction (rank slices in rank order) and meet in distributed shared
-// memory.  Per CTA (128 threads):
+// Kernel.  A CTA owns a tile of up to 128 rows of Y (one accumulator: the
+// MMA's M = 128, N = tokens rounded up to a multiple of 16, at most 256) or
+// up to 256 rows (two accumulators sharing each token tile) for every token,
+// and a slice of the contraction dimension; the KS CTAs of a thread-block
+// cluster split the contraction (rank slices in rank order).  Per CTA (256
+// threads):
 //   warp 0, one thread   TMA producer: per 64-element K block, the 128 x 64
-//                         tile of W_p and the tokens x 64 tile of X_p (both
+//                         tile(s) of W_p and the tokens x 64 tile of X_p (all
 //                         128-byte swizzled, K-major) onto a stage mbarrier;
 //   warp 1, one thread   MMA issuer: four tcgen05.mma (K = 16 each) per
-//                         stage into the fp32 accumulator in tensor memory,
-//                         then tcgen05.commit frees the stage;
+//                         stage and accumulator into fp32 accumulators in
+//                         tensor memory, then tcgen05.commit frees the stage;
 //   warp 2               allocates / frees the tensor-memory columns;
-//   all four warps       epilogue: tcgen05.ld of the accumulator (warp w
-//                         reads lanes 32w..32w+31 = its 32 rows), partials to
-//                         shared memory, cluster barrier, each CTA of the
+//   warps 2-7            (with residuals) ask L2 for the epilogue's residual
+//                         rows while the main loop runs;
+//   all eight warps      epilogue (mma_epilogue): tcgen05.ld of the
+//                         accumulators into shared memory, the split partials
+//                         exchanged through each CTA's inbox, each CTA of the
 //                         cluster adds the KS partials of its share of the
 //                         tokens in split order, rounds once and stores 16
 //                         bytes (8 rows) at a time into all N outputs.
@@ -53,7 +56,10 @@
 
 namespace dcc {
 
-constexpr int kMmaThreads = 128;
+// 8 warps: the epilogue's loads and stores are latency-bound, so all eight
+// take part (warps w and w + 4 read the same tensor-memory lanes, alternate
+// 32-column chunks)
+constexpr int kMmaThreads = 256;
 constexpr int kMmaBM = 128;      // accumulator rows per CTA (TMEM lanes)
 constexpr int kMmaBK = 64;       // K elements per stage (one 128-byte swizzle atom row)
 constexpr int kMmaMaxTokens = 256;
@@ -237,16 +243,19 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
                                              float* part, uint32_t inbar, int n, unsigned split, int m0, int bm0,
                                              bool acc_ok, int mtile) {
   constexpr int kBatch = 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, row = warp * 32 + lane;
+  // a warp reaches the tensor-memory lanes 32 (warp mod 4) .. + 31 only
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quad = warp & 3, row = quad * 32 + lane;
   const int NTILE = a.ntile, T = NTILE / KSC;
   float* inbox = part + (size_t)NTILE * kMmaBM;
   const uint32_t slice_bytes = (uint32_t)T * kMmaBM * 4u;
   const int t_lo = (int)split * T;
   bool ok = acc_ok;
   for (int h = 0; h < MACC; ++h) {
-    for (int c0 = 0; c0 < NTILE; c0 += 32) {  // NTILE is a multiple of 16: the last step may take 16
+    // warps w and w + 4 take alternate 32-column chunks; NTILE is a multiple
+    // of 16, so the last chunk may have 16 columns
+    for (int c0 = (warp >> 2) * 32; c0 < NTILE; c0 += 64) {
       uint32_t v[32];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
       if (c0 + 32 <= NTILE) {
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
