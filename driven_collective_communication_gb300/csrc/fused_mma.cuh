@@ -308,11 +308,23 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
 
     const int mh = m0 + h * kMmaBM, bmh = h == 0 ? bm0 : a.bm - kMmaBM;  // rows of accumulator h
     const int items = T * (kMmaBM / 8);
-    for (int w0 = threadIdx.x; w0 < items; w0 += kMmaThreads * kBatch) {
+    // With residuals and items for less than kBatch passes of the threads, G
+    // threads share an item, thread g of the group taking ranks g, g + G, ...:
+    // their residual loads are in flight together instead of one rank after
+    // another (each of the G adds the item's partials itself).  Otherwise
+    // G = 1.
+    int G = 1;
+    if (a.res[0] != nullptr) {
+      G = kMmaThreads * kBatch / items;
+      if (G > n) G = n;
+      if (G < 1) G = 1;
+    }
+    const int g = (int)threadIdx.x % G, lanes = kMmaThreads / G;  // threads per item slot
+    for (int w0 = (int)threadIdx.x / G; w0 < items && (int)threadIdx.x < lanes * G; w0 += lanes * kBatch) {
       float acc[kBatch][8];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
-        const int w = w0 + b * kMmaThreads;
+        const int w = w0 + b * lanes;
         const int tl = w < items ? w / (kMmaBM / 8) : 0, r8 = (w % (kMmaBM / 8)) * 8;
 #pragma unroll
         for (int s2 = 0; s2 < KSC; ++s2) {  // split order
@@ -330,7 +342,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
       long long off[kBatch];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
-        const int w = w0 + b * kMmaThreads;
+        const int w = w0 + b * lanes;
         const int t = t_lo + w / (kMmaBM / 8), r8 = (w % (kMmaBM / 8)) * 8;
         off[b] = (w < items && t < a.tokens && r8 < bmh && mh + r8 < a.rows)
                      ? (long long)(((size_t)t * a.rows + (size_t)(mh + r8)) * 2)
@@ -346,8 +358,8 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
               st_vec(reinterpret_cast<uint4*>(static_cast<char*>(a.y[q]) + off[b]), out);
         }
       } else {
-        // rank q+1's residuals are loaded before rank q's outputs are stored,
-        // so two ranks' loads are in flight at a time
+        // rank q+G's residuals are loaded before rank q's outputs are stored,
+        // so two of this thread's ranks' loads are in flight at a time
         auto load_res = [&](int q, uint4* rv) {
 #pragma unroll
           for (int b = 0; b < kBatch; ++b)
@@ -356,9 +368,9 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
                         : make_uint4(0u, 0u, 0u, 0u);
         };
         uint4 cur[kBatch], nxt[kBatch];
-        load_res(0, cur);
-        for (int q = 0; q < n; ++q) {
-          if (q + 1 < n) load_res(q + 1, nxt);
+        load_res(g, cur);
+        for (int q = g; q < n; q += G) {
+          if (q + G < n) load_res(q + G, nxt);
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
             if (off[b] < 0 || !in_bounds(dc, a, kBufRecv, q, (size_t)off[b], 16)) continue;
