@@ -965,7 +965,12 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   // one wave means at most as many clusters as fit on the device at once,
   // which the GPCs' SM counts make fewer than SMs / ks.
   int macc = c->mma_acc > 0 ? c->mma_acc : ntile <= kMmaTwoAccMaxTokens ? 2 : 1;
-  if (rows <= (size_t)dcc::kMmaBM) macc = 1;
+  // fewer accumulators where the rows, the tensor memory (512 columns) or the
+  // epilogue's room in the stage buffers do not allow them
+  const int acc_cols = ntile <= 32 ? 32 : ntile <= 64 ? 64 : ntile <= 128 ? 128 : 256;
+  while (macc > 1 && (rows <= (size_t)dcc::kMmaBM * (macc - 1) || acc_cols * macc > 512 ||
+                      !dcc::mma_epilogue_fits(ntile, dcc::mma_stages(ntile, macc), macc, 1)))
+    macc /= 2;
   const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc);
   const int stages = dcc::mma_stages(ntile, macc);
   const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
@@ -996,7 +1001,7 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
     c->mma_clusters[key] = num;
     return num;
   };
-  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
+  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM * (macc - 1) + 8, bm_hi = macc * dcc::kMmaBM;
   const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
   int best_bm = bm_hi, best_ks = 1;
   long long best = -1;
@@ -1020,11 +1025,10 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
     best_bm = bm_hi;
     best_ks = 1;
   }
-  const int bm0 = best_bm < dcc::kMmaBM ? best_bm : dcc::kMmaBM;
+  const int bm0 = macc == 1 ? best_bm : dcc::kMmaBM, bm_last = best_bm - dcc::kMmaBM * (macc - 1);
   for (int r = 0; r < c->n; ++r) {
     rc = tensor_map(c, weight[r], kp, rows, (unsigned)bm0, t, &maps.w[r]);
-    if (rc == DCC_OK && macc == 2)
-      rc = tensor_map(c, weight[r], kp, rows, (unsigned)(best_bm - dcc::kMmaBM), t, &maps.w2[r]);
+    if (rc == DCC_OK && macc > 1) rc = tensor_map(c, weight[r], kp, rows, (unsigned)bm_last, t, &maps.w2[r]);
     if (rc == DCC_OK) rc = tensor_map(c, x[r], kp, tokens, (unsigned)ntile, t, &maps.x[r]);
     if (rc != DCC_OK) return rc;
   }

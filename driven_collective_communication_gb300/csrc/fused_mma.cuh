@@ -17,7 +17,8 @@
 //
 // Kernel.  A CTA owns a tile of up to 128 rows of Y (one accumulator: the
 // MMA's M = 128, N = tokens rounded up to a multiple of 16, at most 256) or
-// up to 256 rows (two accumulators sharing each token tile) for every token,
+// up to 256 rows (MACC = 2 accumulators sharing each token tile) for every
+// token,
 // and a slice of the contraction dimension; the KS CTAs of a thread-block
 // cluster split the contraction (rank slices in rank order).  Per CTA (256
 // threads):
@@ -66,9 +67,9 @@ constexpr int kMmaMaxTokens = 256;
 constexpr int kMmaMaxSplit = 8;  // CTAs per cluster along K
 
 struct MmaMaps {
-  CUtensorMap w[DCC_MAX_RANKS];   // rows x kp, box 64 x min(bm, 128)
+  CUtensorMap w[DCC_MAX_RANKS];   // rows x kp, box 64 x bm (one accumulator) or 64 x 128
   CUtensorMap x[DCC_MAX_RANKS];   // tokens x kp, box 64 x ntile
-  CUtensorMap w2[DCC_MAX_RANKS];  // with two accumulators: rows x kp, box 64 x (bm - 128)
+  CUtensorMap w2[DCC_MAX_RANKS];  // several accumulators: the last one's box, 64 x (bm - 128 (macc - 1))
 };
 
 struct MmaArgs {
@@ -76,7 +77,7 @@ struct MmaArgs {
   const void* res[DCC_MAX_RANKS];  // tokens x rows residuals (res[0] null: none)
   int tokens, rows, kp, ntile, ks, stages;
   int bm;                  // weight rows per CTA (multiple of 8, at most macc * kMmaBM)
-  int macc;                // accumulators per CTA (the kernel's MACC): 1, or 2 (rows 128..bm-1 in the second)
+  int macc;                // accumulators per CTA (the kernel's MACC): 1 or 2, 128 rows each but the last
   int fp16;                // element type: 0 bf16, 1 fp16
 #if DCC_CHECK_BOUNDS
   size_t ext[kNumBufKinds][DCC_MAX_RANKS];
@@ -240,8 +241,8 @@ __device__ __forceinline__ void mma_widen8(uint4 w, bool fp16, float* v) {
 // CTA of the cluster is past its main loop (the barrier of step 2).
 template <int KSC, int MACC>
 __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a, uint32_t tmem, uint32_t acc_cols,
-                                             float* part, uint32_t inbar, int n, unsigned split, int m0, int bm0,
-                                             bool acc_ok, int mtile) {
+                                             float* part, uint32_t inbar, int n, unsigned split, int m0,
+                                             int bm_last, bool acc_ok, int mtile) {
   constexpr int kBatch = 4;
   // a warp reaches the tensor-memory lanes 32 (warp mod 4) .. + 31 only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quad = warp & 3, row = quad * 32 + lane;
@@ -306,7 +307,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
       __syncthreads();
     }
 
-    const int mh = m0 + h * kMmaBM, bmh = h == 0 ? bm0 : a.bm - kMmaBM;  // rows of accumulator h
+    const int mh = m0 + h * kMmaBM, bmh = h == MACC - 1 ? bm_last : kMmaBM;  // rows of accumulator h
     const int items = T * (kMmaBM / 8);
     // With residuals and items for less than kBatch passes of the threads, G
     // threads share an item, thread g of the group taking ranks g, g + G, ...:
@@ -421,7 +422,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   unsigned split = 0;
   if (KS > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(split));
   const int mtile = (int)blockIdx.x / KS, m0 = mtile * a.bm;
-  const int bm0 = a.bm < kMmaBM ? a.bm : kMmaBM;  // rows of the first accumulator; the second has bm - 128
+  // rows of the last accumulator (the others have 128 each)
+  const int bm_last = a.bm - kMmaBM * (MACC - 1);
   const int kpb = a.kp / kMmaBK, nb = n * kpb;
   const int b0 = (int)((long long)split * nb / KS), b1 = (int)((long long)(split + 1) * nb / KS);
   const int nk = b1 - b0;
@@ -453,7 +455,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
     for (int i = 0; i < nk && i < S; ++i) {
       const int g = b0 + i;
       tma_prefetch_2d(&maps.w[g / kpb], (g % kpb) * kMmaBK, m0);
-      if (MACC == 2) tma_prefetch_2d(&maps.w2[g / kpb], (g % kpb) * kMmaBK, m0 + kMmaBM);
+      for (int h = 1; h < MACC; ++h)
+        tma_prefetch_2d(h == MACC - 1 ? &maps.w2[g / kpb] : &maps.w[g / kpb], (g % kpb) * kMmaBK, m0 + h * kMmaBM);
     }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -464,8 +467,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
 
   const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;  // this CTA's epilogue tokens
   if (warp == 0 && lane == 0) {  // TMA producer
-    // the weight boxes are bm0 and bm - 128 rows (tile rows beyond them are
-    // never written and only reach accumulator rows the epilogue discards)
+    // the weight boxes are 128 rows for all accumulators but the last, which
+    // has bm_last (tile rows beyond them are never written and only reach
+    // accumulator rows the epilogue discards)
     const uint32_t tx = st_bytes - (uint32_t)(MACC * kMmaBM - a.bm) * (kMmaBK * 2);
     const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
     for (int i = 0; i < nk; ++i) {
@@ -475,7 +479,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
       const uint32_t sa = base + (uint32_t)s * st_bytes;
       mma_mbar_expect(full(s), tx);
       tma_load_2d_hint(sa, &maps.w[p], k0, m0, full(s), pol_w);
-      if (MACC == 2) tma_load_2d_hint(sa + a_bytes, &maps.w2[p], k0, m0 + kMmaBM, full(s), pol_w);
+#pragma unroll
+      for (int h = 1; h < MACC; ++h)
+        tma_load_2d_hint(sa + (uint32_t)h * a_bytes, h == MACC - 1 ? &maps.w2[p] : &maps.w[p], k0, m0 + h * kMmaBM,
+                         full(s), pol_w);
       tma_load_2d_hint(sa + b_off, &maps.x[p], k0, 0, full(s), pol_x);
     }
   } else if (warp >= 2 && a.res[0] != nullptr) {
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
     const int per_tok = n * MACC;
     for (int j = threadIdx.x - 64; j < (t_hi - t_lo) * per_tok; j += kMmaThreads - 64) {
       const int t = t_lo + j / per_tok, q = (j % per_tok) / MACC, h = j % MACC;
-      const int mh = m0 + h * kMmaBM, bmh = h == 0 ? bm0 : a.bm - kMmaBM;
+      const int mh = m0 + h * kMmaBM, bmh = h == MACC - 1 ? bm_last : kMmaBM;
       const int nr = mh + bmh <= a.rows ? bmh : a.rows - mh;
       if (t >= a.tokens || nr <= 0) continue;
       const size_t off = ((size_t)t * a.rows + (size_t)mh) * 2;
@@ -526,10 +533,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
   switch (KS) {  // a power of two up to kMmaMaxSplit
-    case 1: mma_epilogue<1, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
-    case 2: mma_epilogue<2, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
-    case 4: mma_epilogue<4, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
-    default: mma_epilogue<8, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm0, acc_ok, mtile); break;
+    case 1: mma_epilogue<1, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+    case 2: mma_epilogue<2, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+    case 4: mma_epilogue<4, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+    default: mma_epilogue<8, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
   }
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
