@@ -244,14 +244,16 @@ __device__ __forceinline__ void prefetch_chunk_l2(const DevComm& dc, const CollA
 // Every rank gets all N inputs and reduces its whole output.  Out of place no
 // rank writes what another reads, so there is no synchronisation.  In place,
 // rank r's output is an input of every peer: the N CTAs of a block slot
-// process the same chunk together -- get and reduce into registers, then a
-// signal/wait barrier ("everyone has read this chunk"), then store.  The
-// barrier keeps the N CTAs of a slot in step, so all N read a chunk at the
-// same moment and the first reader's L2 miss holds up the other N-1; each CTA
-// therefore asks L2 for its own rank's part of its next chunk before it
-// starts the current one.  (Getting the next chunk into registers while the
-// signals travel, holding two chunks' results, measured slower on GB300:
-// 0.49 vs 0.42 ms for 8 x 64 MiB int32.)
+// process the same chunk together -- get and reduce into registers, signal
+// "this CTA has read the chunk", and store once every peer has signalled the
+// same.  The wait is split from the signal: the reduced chunk waits in shared
+// memory (thread-private slots) while the next chunk's gets are in flight
+// (measured on GB300 for 8 x 64 MiB int32: 0.289 ms against 0.308 with signal
+// and wait back to back; holding the two chunks in registers instead took
+// 0.49 ms, the extra registers costing occupancy).  The barrier keeps the N
+// CTAs of a slot in step, so all N read a chunk at the same moment and the
+// first reader's L2 miss holds up the other N-1; each CTA therefore asks L2
+// for its own rank's part of a chunk one chunk before it gets it.
 template <typename T, int NT, bool EB = false, int OP = kOpSum>
 __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, CollArgs a) {
   pdl_prologue();
@@ -282,31 +284,53 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_oneshot(DevComm dc, Coll
   // all loads of a thread in flight at once), kInplaceUnroll for large ones
   // (fewer chunks, so fewer barrier rounds).  The loop over the U vectors is
   // unrolled so all of a thread's loads of a chunk are in flight together
-  // (holding the results in shared memory with a runtime U instead measured
-  // slower on GB300: 0.350 vs 0.310 ms at U = 4, slower still at 8 and 16).
+  // (a loop over a run-time U measured slower on GB300: 0.350 vs 0.310 ms at
+  // U = 4, slower still at 8 and 16; so did a compile-time 8 in the pipelined
+  // form below, 0.42-0.49 ms: its registers cost occupancy).
   const int U = a.unroll > 0 && a.unroll < kInplaceUnroll ? a.unroll : kInplaceUnroll;
   const size_t chunk = (size_t)U * blockDim.x;
   const size_t nchunks = (nvec + chunk - 1) / chunk;
   bool ok = true;
   // prefetch distance: kInplacePrefetch chunks of this slot ahead
   if (threadIdx.x == 0)
-    for (int d = 0; d < kInplacePrefetch; ++d)
+    for (int d = 0; d <= kInplacePrefetch; ++d)
       if ((size_t)blk + (size_t)d * B < nchunks) prefetch_chunk_l2(dc, a, rank, blk + (size_t)d * B, chunk, nvec);
-  for (size_t c = blk; c < nchunks; c += B) {
-    const size_t cp = c + (size_t)kInplacePrefetch * B;
-    if (threadIdx.x == 0 && cp < nchunks) prefetch_chunk_l2(dc, a, rank, cp, chunk, nvec);
-    uint4 res[kInplaceUnroll];
+  // Pipelined: the reduced chunk c waits in shared memory (thread-private
+  // slots) for the peers' signals while the next chunk's loads are in flight.
+  extern __shared__ uint4 held[];
+  auto reduce_chunk = [&](size_t c, uint4* res) {
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
       if (u < U && v < nvec) res[u] = reduce_vec<T, NT, OP>(dc, a, n, v);
     }
-    ok = group_barrier(dc, rank, n, blk, expected);
+  };
+  if ((size_t)blk < nchunks) {
+    uint4 res[kInplaceUnroll];
+    reduce_chunk(blk, res);
+#pragma unroll
+    for (int u = 0; u < kInplaceUnroll; ++u)
+      if (u < U) held[u * blockDim.x + threadIdx.x] = res[u];
+    group_signal(dc, rank, n, blk);
+  }
+  for (size_t c = blk; c < nchunks; c += B) {
+    const size_t cn = c + B;
+    const size_t cp = cn + (size_t)kInplacePrefetch * B;
+    if (threadIdx.x == 0 && kInplacePrefetch > 0 && cp < nchunks) prefetch_chunk_l2(dc, a, rank, cp, chunk, nvec);
+    uint4 res[kInplaceUnroll];
+    if (cn < nchunks) reduce_chunk(cn, res);
+    ok = group_wait(dc, rank, n, blk, expected);  // every peer has read chunk c
     if (!ok) break;
 #pragma unroll
     for (int u = 0; u < kInplaceUnroll; ++u) {
       const size_t v = c * chunk + (size_t)u * blockDim.x + threadIdx.x;
-      if (u < U && v < nvec) put_vec<kBufRecv>(dc, a, rank, v, res[u]);
+      if (u < U && v < nvec) put_vec<kBufRecv>(dc, a, rank, v, held[u * blockDim.x + threadIdx.x]);
+    }
+    if (cn < nchunks) {
+#pragma unroll
+      for (int u = 0; u < kInplaceUnroll; ++u)
+        if (u < U) held[u * blockDim.x + threadIdx.x] = res[u];
+      group_signal(dc, rank, n, blk);  // this CTA has read chunk cn
     }
   }
   if (ok && blk == 0 && tail0 < a.count) {  // same on every rank: all slot-0 CTAs take part

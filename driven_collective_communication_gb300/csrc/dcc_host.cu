@@ -225,8 +225,8 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
     // one vector per thread while one chunk per CTA of the co-resident grid
     // covers the message (a single barrier round, every load in flight at
     // once), else kInplaceUnroll vectors per thread in 256-thread CTAs (fewer
-    // barrier rounds, four CTAs per SM: measured on GB300 at 8 x 64 MiB int32,
-    // 0.310 ms against 0.340 with 512-thread CTAs)
+    // barrier rounds: measured on GB300 at 8 x 64 MiB int32, 0.289 ms against
+    // 0.306 with 512-thread CTAs, 0.320 with 128 and 0.342 with two vectors)
     if (c->threads_override <= 0 && work > 65536) sh->threads = dcc::kInplaceLargeThreads;
     sh->unroll = c->inplace_unroll;
     if (sh->unroll <= 0) {
@@ -236,6 +236,7 @@ int allreduce_shape(const dcc_comm* c, size_t count, dcc_dtype_t t, dcc_algo_t a
       sh->unroll = (size_t)b1 * sh->threads >= nvec ? 1 : dcc::kInplaceUnroll;
     }
     work = (nvec + sh->unroll - 1) / sh->unroll;
+    sh->smem = (size_t)dcc::kInplaceUnroll * sh->threads * 16;  // the chunk held while the signals travel
   }
   // one-shot keeps one wave even out of place: every rank reads every input,
   // and the ranks' CTAs reading a region together is what lets L2 serve it

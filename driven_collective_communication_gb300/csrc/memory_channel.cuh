@@ -198,4 +198,27 @@ __device__ __forceinline__ bool group_barrier(const DevComm& dc, int self, int n
   return __syncthreads_and(ok) != 0;
 }
 
+// The two halves of group_barrier, for a pipelined caller: group_signal
+// tells every peer that this CTA has finished reading (its threads' loads are
+// consumed before the block barrier), group_wait waits for every peer's
+// matching signal.
+__device__ __forceinline__ void group_signal(const DevComm& dc, int self, int n, int blk) {
+  __syncthreads();
+  const int p = threadIdx.x;
+  if (p < n && p != self) {
+    MemoryChannel ch = MemoryChannel::make(dc, self, p, blk, nullptr, nullptr);
+    ch.signal(dc, self);
+  }
+}
+__device__ __forceinline__ bool group_wait(const DevComm& dc, int self, int n, int blk,
+                                           unsigned long long& expected) {
+  bool ok = true;
+  const int p = threadIdx.x;
+  if (p < n && p != self) {
+    MemoryChannel ch = MemoryChannel::make(dc, self, p, blk, nullptr, nullptr);
+    ok = ch.wait(dc, expected, self, p, blk);
+  }
+  return __syncthreads_and(ok) != 0;
+}
+
 }  // namespace dcc
