@@ -72,9 +72,11 @@ constexpr size_t kFusedBulkMinKp = 3584;
 
 // One-token fused linear + AllReduce: kp a multiple of 64 up to this runs on
 // the tensor-core kernel (the batched layer with one token).  Measured on
-// GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load or bulk (us):
-// kp 1024 23.5 / 25.1, 2048 41.9 / 44.2, 3584 71.8 / 71.6, 8192 160 / 149.
-constexpr size_t kFusedTensorMaxKp = 2048;
+// GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load / bulk-copy
+// kernel (us): kp 1024 23.5 / 25.1 / -, 2048 42.1 / 44.0 / 60.2, 2560 52.3 /
+// 55.3 / 63.9, 3072 62.2 / 63.9 / 67.2, 3584 71.7 / 74.5 / 71.7, 4096 81.5 /
+// 82.8 / 78.2, 8192 160 / 169 / 149.
+constexpr size_t kFusedTensorMaxKp = 3584;
 
 // Tensor-core layer over a batch of tokens: up to this many tokens (the token
 // tile rounded up to 16) a CTA holds two accumulators, a tile of up to 256

@@ -217,7 +217,7 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
  * outputs disjoint from every input.  Exact when every fp32 partial sum is
  * exact (small-integer data), else within the fp32 dot-product error bound of
  * the kernel that ran, before the final rounding.  The kernel, by kp:
- *  - a multiple of 64 up to 2048: the tensor-core kernel of
+ *  - a multiple of 64 up to 3584: the tensor-core kernel of
  *    dcc_linear_allreduce_tokens with one token (the tensor core's
  *    accumulation order, then the K-split partials in split order);
  *  - otherwise below 3584: thread loads, rank r's CTAs computing shard r of
