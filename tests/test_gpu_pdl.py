@@ -123,12 +123,15 @@ def test_graph_dependent_chain(dcc):
         comm.close()
 
 
-@pytest.mark.parametrize("kp", [1024, 4096])
-def test_fused_layer_chain(dcc, kp):
+@pytest.mark.parametrize("kp,kernel", [(1024, "thread"), (1024, "tensor"), (4096, "bulk"), (4096, "tensor")])
+def test_fused_layer_chain(dcc, monkeypatch, kp, kernel):
     """Fused linear layers feeding one another (rows == kp, y of one layer is x
-    of the next) with PDL, for the thread kernel (kp 1024) and the bulk-copy
-    kernel (kp 4096).  Weights are permutations on rank 0 and zero elsewhere,
-    so values neither grow nor round; the oracle follows the chain."""
+    of the next) with PDL, on each kernel (thread loads, bulk copies, tensor
+    cores: the last prefetches weights into L2 before its dependent-launch
+    wait, and must read its input only after it).  Weights are permutations
+    on rank 0 and zero elsewhere, so values neither grow nor round; the oracle
+    follows the chain."""
+    monkeypatch.setenv("DCC_FUSED_KERNEL", kernel)
     n, steps = 4, 8
     gen = np.random.default_rng(5)
     perms = [gen.permutation(kp) for _ in range(2)]
