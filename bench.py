@@ -406,6 +406,12 @@ def summary(dcc, out):
         "fused_kp1024_us": o["linear_allreduce_bf16_n8_rows8192_kp1024"]["fused_us"],
         "fused_kp1024_weight_frac": round(o["linear_allreduce_bf16_n8_rows8192_kp1024"]["fused_weight_gbs"]
                                           / measured_peaks()[0], 3),
+        # the tensor-core layer over 1 / 16 / 64 / 128 / 256 tokens (8 x 8192 x 1024 bf16) and
+        # per-rank cuBLAS GEMM then the AllReduce on the same shapes, us
+        "linear_tokens_us": {t: o["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % t]["fused_tensor_us"]
+                             for t in (1, 16, 64, 128, 256)},
+        "gemm_then_allreduce_us": {t: o["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % t]["gemm_then_allreduce_us"]
+                                   for t in (1, 16, 64, 128, 256)},
     }
 
 
