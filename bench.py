@@ -394,9 +394,18 @@ def summary(dcc, out):
     o = out["other"]
     table = build.load_auto_table()
     cross = {t: v["one_shot_max_bytes"] for t, v in out["crossover_n8"].items()}
+
+    def summed(v, limit):  # the sweep's summed time with one-shot up to `limit` bytes
+        return sum(a if size <= limit else b for size, a, b in zip(v["sizes"], v["one_shot_us"], v["two_shot_us"]))
+    # what the compiled table costs over this sweep against the sweep's own best threshold, %:
+    # near the crossover the schedules differ by hundredths of a microsecond, so the best
+    # threshold itself moves between boxes while the cost of either stays small
+    excess = {t: round(100.0 * (summed(v, table[8][t]) / summed(v, cross[t]) - 1.0), 2)
+              for t, v in out["crossover_n8"].items()}
     return {
         "crossover_n8_bytes": cross,
         "crossover_n8_matches_compiled_table": all(table[8][t] == b for t, b in cross.items()),
+        "crossover_n8_compiled_table_excess_pct": excess,
         "c2_int32_inplace_ms": {"one_shot": o["c2_int32_inplace_one_shot"]["ms"],
                                 "two_shot": o["c2_int32_inplace_two_shot"]["ms"]},
         "c2_one_shot_roofline_frac": round(o["c2_int32_inplace_one_shot"]["hbm_gbs_2NS"]
