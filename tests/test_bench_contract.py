@@ -67,3 +67,35 @@ def test_crossover_rule_minimises_summed_time():
     assert bench.crossover_rule(sizes, [2, 2, 2, 2, 2], [1, 1, 1, 1, 1]) == 0    # never
     assert bench.crossover_rule(sizes, [1, 1.1, 1, 2, 3], [1.5, 1.0, 1.5, 1.5, 1.5]) == 16  # one noisy loss at 8
     assert bench.crossover_rule(sizes, [1, 1, 1, 1, 1], [1, 1, 1, 1, 1]) == 0    # ties: the smaller threshold
+
+
+def test_summary_keys_from_the_extras():
+    """The compact summary the bench line ends with, built from extras of the
+    shapes the GPU run produces: every key present, the AUTO table's cost 0
+    when the sweep's best threshold is the compiled one, positive otherwise."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from driven_collective_communication_gb300 import build
+    table = build.load_auto_table()
+    sizes = [4096 << k for k in range(7)]
+
+    def sweep(limit):  # one-shot faster up to `limit`, two-shot above
+        return {"sizes": sizes, "one_shot_us": [1.0 if s <= limit else 2.0 for s in sizes],
+                "two_shot_us": [1.5] * len(sizes), "one_shot_max_bytes": limit}
+    other = {"c2_int32_inplace_one_shot": {"ms": 0.29, "hbm_gbs_2NS": 3700.0},
+             "c2_int32_inplace_two_shot": {"ms": 0.16}, "c5_reduce_scatter": {"ms": 0.088},
+             "c5_allgather": {"ms": 0.094}, "c5_ring_barrier": {"per_hop_us": 0.26},
+             "linear_allreduce_bf16_n8_rows8192_kp1024": {"fused_us": 23.5, "fused_weight_gbs": 5700.0}}
+    for t in (1, 16, 64, 128, 256):
+        other["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % t] = {"fused_tensor_us": 24.0 + t / 20,
+                                                                   "gemm_then_allreduce_us": 37.0 + t / 10}
+    matching = {"other": other, "crossover_n8": {t: sweep(table[8][t]) for t in table[8]}}
+    s = bench.summary(None, matching)
+    assert s["crossover_n8_matches_compiled_table"] is True
+    assert all(v == 0 for v in s["crossover_n8_compiled_table_excess_pct"].values())
+    assert set(s["linear_tokens_us"]) == {1, 16, 64, 128, 256} and s["fused_kp1024_us"] == 23.5
+    other_limit = {t: (4096 if table[8][t] != 4096 else 262144) for t in table[8]}
+    moved = {"other": other, "crossover_n8": {t: sweep(other_limit[t]) for t in table[8]}}
+    s = bench.summary(None, moved)
+    assert s["crossover_n8_matches_compiled_table"] is False
+    assert all(v > 0 for v in s["crossover_n8_compiled_table_excess_pct"].values())
