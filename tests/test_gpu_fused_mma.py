@@ -52,10 +52,12 @@ def small_ints(g, size, dtype, lo=-3, hi=3):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("n,tokens,rows,kp", [
     (1, 1, 128, 64), (2, 16, 256, 64), (8, 1, 1024, 128), (8, 17, 1024, 192), (3, 100, 136, 256),
-    (8, 256, 512, 64), (16, 64, 512, 64), (5, 255, 264, 320), (8, 33, 8192, 64), (4, 128, 128, 1024)])
+    (8, 256, 512, 64), (16, 64, 512, 64), (5, 255, 264, 320), (8, 33, 8192, 64), (4, 128, 128, 1024),
+    (16, 256, 8, 64), (2, 1, 8, 64), (1, 255, 16, 64)])
 def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
     """Ragged token counts (padded to a multiple of 16 inside), a partial last
-    row tile (136, 264 rows), 1..16 ranks, K splits from 1 to 8."""
+    row tile (136, 264 rows), tiles of 8 and 16 rows, 1..16 ranks, K splits
+    from 1 to 8 (fewer where the epilogue's inbox would not fit)."""
     g = torch.Generator().manual_seed(n * 7919 + tokens * 31 + kp)
     ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
     xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
