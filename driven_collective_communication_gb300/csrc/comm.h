@@ -71,21 +71,25 @@ constexpr size_t kPipeChunkBytes = 8u << 20;
 constexpr size_t kFusedBulkMinKp = 3584;
 
 // One-token fused linear + AllReduce: kp a multiple of 64 up to this runs on
-// the tensor-core kernel (the batched layer with one token).  Measured on
-// GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load / bulk-copy
-// kernel (us): kp 1024 23.5 / 25.1 / -, 2048 42.1 / 44.0 / 60.2, 2560 52.3 /
-// 55.3 / 63.9, 3072 62.2 / 63.9 / 67.2, 3584 71.7 / 74.5 / 71.7, 4096 81.5 /
-// 82.8 / 78.2, 8192 160 / 169 / 149.
+// the tensor-core kernel (the batched layer with one token, pair form).
+// Measured on GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load /
+// bulk-copy kernel (us): kp 1024 20.9 / 25.1 / 53.4, 2048 40.5 / 44.1 / 60.3,
+// 3584 69.4 / 74.4 / 71.6, 4096 80.2 / 82.5 / 78.1, 6144 118.3 / 121.3 /
+// 119.5, 8192 155.9 / 159.9 / 149.1.
 constexpr size_t kFusedTensorMaxKp = 3584;
 
-// Tensor-core layer over a batch of tokens: up to this many tokens (the token
-// tile rounded up to 16) a CTA holds two accumulators, a tile of up to 256
-// weight rows sharing each token tile, with a deeper K split (8 ranks x 8192
-// rows x kp 1024 on GB300: 23.2 / 23.7 / 26.6 us at 1 / 16 / 64 tokens
-// against 27.2 / 27.3 / 28.2 with one accumulator); above, the token tile
-// takes too much of each stage (128 tokens: 31.5 vs 29.8 us, 256: 55.3 vs
-// 36.5).
-constexpr int kMmaTwoAccMaxTokens = 64;
+// Tensor-core layer over a batch of tokens, its forms: "pair" (128-thread
+// CTAs, two per SM, one accumulator), "one" (256-thread CTAs, one per SM,
+// one accumulator), "two" (the same with two accumulators sharing each token
+// tile).  Up to kMmaPairMaxTokens tokens (the token tile rounded up to 16)
+// the pair form runs, above it the one-accumulator form.  Measured on GB300,
+// 8 ranks x 8192 rows x kp 1024 bf16, pair / one / two (us): 1 token 20.5 /
+// 27.4 / 23.2, 16 tokens 21.0 / 27.5 / 23.7, 64 tokens 24.5 / 28.7 / 26.9,
+// 128 tokens 35.2 (2-way split: a 4-way one leaves no room for the epilogue)
+// / 30.4 / 32.6; the pair form with the in-place residual 20.6 / 21.8 / 25.0
+// at 1 / 16 / 64 tokens.
+enum { kMmaFormPair = 0, kMmaFormOne = 1, kMmaFormTwo = 2 };
+constexpr int kMmaPairMaxTokens = 64;
 
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;
@@ -115,8 +119,8 @@ struct dcc_comm {
   // crossovers), 0 thread loads, 1 bulk copies (DCC_FUSED_BULK=0 / 1), 2 the
   // tensor-core kernel where kp allows (DCC_FUSED_KERNEL=thread|bulk|tensor)
   int fused_kernel = -1;
-  // tensor-core layer: accumulators per CTA, -1 by token count, 1 or 2 forced (DCC_MMA_ACC)
-  int mma_acc = -1;
+  // tensor-core layer: its form (kMmaForm*), -1 by token count (DCC_MMA_FORM)
+  int mma_form = -1;
   bool entry_barrier = false;  // DCC_ENTRY_BARRIER / dcc_set_entry_barrier
   bool pdl = true;             // DCC_PDL / dcc_set_pdl: programmatic dependent launch of the wait-free kernels
   bool ring_cluster = true;    // DCC_RING_CLUSTER=0: the ring barrier through L2 even when the ranks fit one cluster

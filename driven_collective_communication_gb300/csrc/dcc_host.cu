@@ -344,8 +344,10 @@ bool visit_kernels(F&& visit) {
     if (!v(dcc::allgather_kernel(n, false)) || !v(dcc::allgather_kernel(n, true)) ||
         !v(dcc::allgather_bulk_kernel(n)) || !v(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
-        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) || !v(dcc::linear_allreduce_mma_kernel(n, 1)) ||
-        !v(dcc::linear_allreduce_mma_kernel(n, 2)))
+        !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaPairThreads)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaThreads)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 2, dcc::kMmaThreads)))
       return false;
   return v(dcc::ring_barrier_kernel()) && v(dcc::ring_barrier_cluster_kernel()) && v(dcc::channel_put_kernel()) &&
          v(dcc::channel_get_kernel());
@@ -627,9 +629,10 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
     else if (!std::strcmp(v, "bulk")) c->fused_kernel = 1;
     else if (!std::strcmp(v, "tensor")) c->fused_kernel = 2;
   }
-  if (const char* v = std::getenv("DCC_MMA_ACC")) {
-    const int m = std::atoi(v);
-    if (m == 1 || m == 2) c->mma_acc = m;
+  if (const char* v = std::getenv("DCC_MMA_FORM")) {
+    if (!std::strcmp(v, "pair")) c->mma_form = kMmaFormPair;
+    else if (!std::strcmp(v, "one")) c->mma_form = kMmaFormOne;
+    else if (!std::strcmp(v, "two")) c->mma_form = kMmaFormTwo;
   }
   if (const char* v = std::getenv("DCC_INPLACE_UNROLL")) {
     const int u = std::atoi(v);
@@ -956,26 +959,35 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   const int ntile = tokens <= 16 ? 16 : (int)((tokens + 15) / 16 * 16);
   dcc::MmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  // Launch shape: macc accumulators per CTA (two up to kMmaTwoAccMaxTokens
-  // tokens: a tile of up to 256 weight rows shares each token tile), tiles of bm
+  // Launch shape.  The form: up to kMmaPairMaxTokens tokens, 128-thread CTAs
+  // two to an SM, each with half the shared memory and one accumulator (the
+  // K split can then be twice as deep at the same bytes in flight per SM);
+  // above, 256-thread CTAs one to an SM with one accumulator -- or two
+  // sharing each token tile, on request (DCC_MMA_FORM).  Then tiles of bm
   // weight rows (a multiple of 8; 64..128 with one accumulator, 136..256 with
   // two) and ks K splits (a cluster of ks CTAs per tile, ks <= kMmaMaxSplit
-  // and at most one 64-element block each), chosen so the grid fills the most
-  // SMs in one wave (ties: fewer splits, then taller tiles).  The weight
-  // stream is bound by the bytes each SM keeps in flight, so every SM counts;
-  // one wave means at most as many clusters as fit on the device at once,
-  // which the GPCs' SM counts make fewer than SMs / ks.
-  int macc = c->mma_acc > 0 ? c->mma_acc : ntile <= kMmaTwoAccMaxTokens ? 2 : 1;
-  // fewer accumulators where the rows, the tensor memory (512 columns) or the
-  // epilogue's room in the stage buffers do not allow them
+  // and at most one 64-element block each): for each ks the tile count that
+  // fills the most of one wave (at most as many clusters as fit on the device
+  // at once, which the GPCs' SM counts make fewer than SMs / ks), and of
+  // those the deepest split that keeps at least 3/4 of the best CTA count
+  // (measured on GB300: the weight stream runs faster the deeper the split,
+  // 23.5 us for 134 MB with a 4-way split against 27.3 with a 2-way one).
+  int form = c->mma_form >= 0 ? c->mma_form : ntile <= kMmaPairMaxTokens ? kMmaFormPair : kMmaFormOne;
+  int macc = form == kMmaFormTwo ? 2 : 1;
+  // one accumulator where the rows, the tensor memory (512 columns) or the
+  // epilogue's room in the stage buffers do not allow two
   const int acc_cols = ntile <= 32 ? 32 : ntile <= 64 ? 64 : ntile <= 128 ? 128 : 256;
-  while (macc > 1 && (rows <= (size_t)dcc::kMmaBM * (macc - 1) || acc_cols * macc > 512 ||
-                      !dcc::mma_epilogue_fits(ntile, dcc::mma_stages(ntile, macc), macc, 1)))
-    macc /= 2;
-  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc);
-  const int stages = dcc::mma_stages(ntile, macc);
+  if (macc == 2 && (rows <= (size_t)dcc::kMmaBM || acc_cols * 2 > 512 ||
+                    !dcc::mma_epilogue_fits(ntile, dcc::mma_stages(ntile, 2), 2, 1)))
+    macc = 1;
+  const int threads = form == kMmaFormPair ? dcc::kMmaPairThreads : dcc::kMmaThreads;
+  const unsigned budget = form == kMmaFormPair ? dcc::kMmaPairStageBudget : dcc::kMmaStageBudget;
+  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads);
+  const int stages = dcc::mma_stages(ntile, macc, budget);
   const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+  // all of the SM's unified memory as shared memory (two pair-form CTAs)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
     cudaGetLastError();
     return DCC_ERR_LAUNCH;
   }
@@ -985,7 +997,7 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
     if (it != c->mma_clusters.end()) return it->second;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ks);
-    cfg.blockDim = dim3((unsigned)dcc::kMmaThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -999,14 +1011,20 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
       cudaGetLastError();
       num = c->num_sms / ks;
     }
+    // The query counts one CTA per SM for a kernel that allocates tensor
+    // memory; two pair-form CTAs (half the shared memory, 32-256 columns
+    // each) run side by side (measured on GB300: a grid of twice the SMs
+    // takes the time of one).  Were they not to, the extra clusters would
+    // only form a second wave: no cluster waits on another.
+    if (threads == dcc::kMmaPairThreads) num *= 2;
     c->mma_clusters[key] = num;
     return num;
   };
-  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM * (macc - 1) + 8, bm_hi = macc * dcc::kMmaBM;
+  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
   const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
-  int best_bm = bm_hi, best_ks = 1;
-  long long best = -1;
   auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
+  int ks_bm[dcc::kMmaMaxSplit + 1] = {};  // per split: the tile height, 0 = none fits one wave
+  long long ks_ctas[dcc::kMmaMaxSplit + 1] = {}, most = 0;
   for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2) {
     if (!dcc::mma_epilogue_fits(ntile, stages, macc, ks)) break;  // no room for the epilogue's inbox
     const long long cap = fit(ks);
@@ -1014,18 +1032,19 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
       if (tiles(bm) > cap) continue;
       int tall = bm;  // the tallest tile with the same tile count
       while (tall + 8 <= bm_hi && tiles(tall + 8) == tiles(bm)) tall += 8;
-      if (tiles(bm) * ks > best) {
-        best = tiles(bm) * ks;
-        best_bm = tall;
-        best_ks = ks;
-      }
+      ks_bm[ks] = tall;
+      ks_ctas[ks] = tiles(bm) * ks;
+      if (ks_ctas[ks] > most) most = ks_ctas[ks];
       break;
     }
   }
-  if (best < 0) {  // more tiles than fit even at the tallest tile: several waves, no split
-    best_bm = bm_hi;
-    best_ks = 1;
-  }
+  int best_bm = bm_hi, best_ks = 1;  // more tiles than fit even at the tallest tile: several waves, no split
+  for (int ks = dcc::kMmaMaxSplit; ks >= 1; ks /= 2)
+    if (ks_bm[ks] && 4 * ks_ctas[ks] >= 3 * most) {
+      best_bm = ks_bm[ks];
+      best_ks = ks;
+      break;
+    }
   const int bm0 = macc == 1 ? best_bm : dcc::kMmaBM, bm_last = best_bm - dcc::kMmaBM * (macc - 1);
   for (int r = 0; r < c->n; ++r) {
     rc = tensor_map(c, weight[r], kp, rows, (unsigned)bm0, t, &maps.w[r]);
@@ -1051,12 +1070,15 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   a.ks = best_ks;
   const int mtiles = (int)((rows + best_bm - 1) / best_bm);
   if (c->log)
-    std::fprintf(stderr, "dcc_linear_allreduce_tokens: tokens=%zu rows=%zu kp=%zu macc=%d bm=%d ks=%d ctas=%d stages=%d\n",
-                 tokens, rows, kp, macc, best_bm, best_ks, mtiles * best_ks, stages);
+    std::fprintf(stderr,
+                 "dcc_linear_allreduce_tokens: tokens=%zu rows=%zu kp=%zu threads=%d macc=%d bm=%d ks=%d ctas=%d "
+                 "stages=%d smem=%zu resident clusters of 1/2/4/8: %lld/%lld/%lld/%lld\n",
+                 tokens, rows, kp, threads, macc, best_bm, best_ks, mtiles * best_ks, stages, smem,
+                 kblocks >= 1 ? fit(1) : 0, kblocks >= 2 ? fit(2) : 0, kblocks >= 4 ? fit(4) : 0,
+                 kblocks >= 8 ? fit(8) : 0);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&maps, &dc, &a};
-  return launch(fn, mtiles * best_ks, dcc::kMmaThreads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl,
-                best_ks);
+  return launch(fn, mtiles * best_ks, threads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl, best_ks);
 }
 }  // namespace
 

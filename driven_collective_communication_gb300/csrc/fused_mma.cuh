@@ -20,8 +20,8 @@
 // up to 256 rows (MACC = 2 accumulators sharing each token tile) for every
 // token,
 // and a slice of the contraction dimension; the KS CTAs of a thread-block
-// cluster split the contraction (rank slices in rank order).  Per CTA (256
-// threads):
+// cluster split the contraction (rank slices in rank order).  Per CTA (128
+// threads in the pair form, two CTAs to an SM; 256 otherwise):
 //   warp 0, one thread   TMA producer: per 64-element K block, the 128 x 64
 //                         tile(s) of W_p and the tokens x 64 tile of X_p (all
 //                         128-byte swizzled, K-major) onto a stage mbarrier;
@@ -29,9 +29,9 @@
 //                         stage and accumulator into fp32 accumulators in
 //                         tensor memory, then tcgen05.commit frees the stage;
 //   warp 2               allocates / frees the tensor-memory columns;
-//   warps 2-7            (with residuals) ask L2 for the epilogue's residual
+//   warps 2 and up       (with residuals) ask L2 for the epilogue's residual
 //                         rows while the main loop runs;
-//   all eight warps      epilogue (mma_epilogue): tcgen05.ld of the
+//   all warps            epilogue (mma_epilogue): tcgen05.ld of the
 //                         accumulators into shared memory, the split partials
 //                         exchanged through each CTA's inbox, each CTA of the
 //                         cluster adds the KS partials of its share of the
@@ -57,10 +57,17 @@
 
 namespace dcc {
 
-// 8 warps: the epilogue's loads and stores are latency-bound, so all eight
-// take part (warps w and w + 4 read the same tensor-memory lanes, alternate
-// 32-column chunks)
+// Threads per CTA, the kernel's THREADS: 256 (8 warps; the epilogue's loads
+// and stores are latency-bound, so all eight take part, warps w and w + 4
+// reading the same tensor-memory lanes in alternate 32-column chunks) with
+// one CTA per SM, or 128 (the "pair" form: two CTAs per SM, each with half
+// the shared memory, so the K split can be twice as deep at the same bytes
+// in flight per SM).
 constexpr int kMmaThreads = 256;
+constexpr int kMmaPairThreads = 128;
+// Shared memory for the stages: one CTA per SM, or two
+constexpr unsigned kMmaStageBudget = 216u * 1024u;
+constexpr unsigned kMmaPairStageBudget = 108u * 1024u;
 constexpr int kMmaBM = 128;      // accumulator rows per CTA (TMEM lanes)
 constexpr int kMmaBK = 64;       // K elements per stage (one 128-byte swizzle atom row)
 constexpr int kMmaMaxTokens = 256;
@@ -93,16 +100,16 @@ constexpr int kMmaMaxStages = 16;
 __host__ __device__ constexpr size_t mma_smem_bytes(int ntile, int stages, int macc) {
   return 1024 + (size_t)stages * mma_stage_bytes(ntile, macc) + 16 * (size_t)stages + 64;
 }
-// Stages: as many as fit in 216 KiB (at most kMmaMaxStages) -- the weight
+// Stages: as many as fit in the budget (at most kMmaMaxStages) -- the weight
 // stream is bound by the bytes in flight (on GB300 a loaded HBM read takes
 // about 4 us, so saturating it takes some 28 MB in flight across the GPU) --
 // and at least as many bytes as the fp32 partial tile the epilogue puts in
 // their place.  The epilogue's inbox (the other splits' slices, see
 // mma_epilogue) also needs room: mma_epilogue_fits says whether a K split
-// leaves it.
-inline int mma_stages(int ntile, int macc) {
+// leaves it, and the kernel checks it again before it writes.
+inline int mma_stages(int ntile, int macc, unsigned budget = kMmaStageBudget) {
   const size_t st = mma_stage_bytes(ntile, macc);
-  int s = (int)((216u * 1024u) / st);
+  int s = (int)(budget / st);
   if (s > kMmaMaxStages) s = kMmaMaxStages;
   while ((size_t)s * st < (size_t)ntile * kMmaBM * 4) ++s;
   return s;
@@ -110,7 +117,7 @@ inline int mma_stages(int ntile, int macc) {
 
 // the partial tile (ntile x 128 fp32) plus the inbox for the other ks - 1
 // splits' token slices fit in the stage buffers
-inline bool mma_epilogue_fits(int ntile, int stages, int macc, int ks) {
+__host__ __device__ inline bool mma_epilogue_fits(int ntile, int stages, int macc, int ks) {
   const size_t need = ((size_t)2 * ntile - (size_t)ntile / ks) * kMmaBM * 4;
   return need <= (size_t)stages * mma_stage_bytes(ntile, macc);
 }
@@ -239,7 +246,7 @@ __device__ __forceinline__ void mma_widen8(uint4 w, bool fp16, float* v) {
 // part and the inbox reuse the stage buffers (part: NTILE x 128 floats, the
 // inbox after it: (KSC - 1) x T x 128), so the copies start only once every
 // CTA of the cluster is past its main loop (the barrier of step 2).
-template <int KSC, int MACC>
+template <int KSC, int MACC, int THREADS>
 __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a, uint32_t tmem, uint32_t acc_cols,
                                              float* part, uint32_t inbar, int n, unsigned split, int m0,
                                              int bm_last, bool acc_ok, int mtile) {
@@ -252,9 +259,9 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
   const int t_lo = (int)split * T;
   bool ok = acc_ok;
   for (int h = 0; h < MACC; ++h) {
-    // warps w and w + 4 take alternate 32-column chunks; NTILE is a multiple
-    // of 16, so the last chunk may have 16 columns
-    for (int c0 = (warp >> 2) * 32; c0 < NTILE; c0 += 64) {
+    // with 8 warps, warps w and w + 4 take alternate 32-column chunks; NTILE
+    // is a multiple of 16, so the last chunk may have 16 columns
+    for (int c0 = (warp >> 2) * 32; c0 < NTILE; c0 += 32 * (THREADS / 128)) {
       uint32_t v[32];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
       if (c0 + 32 <= NTILE) {
@@ -316,11 +323,11 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
     // G = 1.
     int G = 1;
     if (a.res[0] != nullptr) {
-      G = kMmaThreads * kBatch / items;
+      G = THREADS * kBatch / items;
       if (G > n) G = n;
       if (G < 1) G = 1;
     }
-    const int g = (int)threadIdx.x % G, lanes = kMmaThreads / G;  // threads per item slot
+    const int g = (int)threadIdx.x % G, lanes = THREADS / G;  // threads per item slot
     for (int w0 = (int)threadIdx.x / G; w0 < items && (int)threadIdx.x < lanes * G; w0 += lanes * kBatch) {
       float acc[kBatch][8];
 #pragma unroll
@@ -402,9 +409,9 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
 // MACC (accumulators per CTA) is a template parameter: with a run-time
 // count the loops over the accumulators cost about 12 us per launch at 8 x
 // 8192 x 1024 (measured on GB300: 40 vs 28 us).
-template <int NT, int MACC>
-__global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const __grid_constant__ MmaMaps maps,
-                                                                          DevComm dc, MmaArgs a) {
+template <int NT, int MACC, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
+    k_linear_allreduce_mma(const __grid_constant__ MmaMaps maps, DevComm dc, MmaArgs a) {
   extern __shared__ unsigned char mma_raw[];
   __shared__ uint32_t tmem_slot;
   const int n = NT > 0 ? NT : dc.n;
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
     // kept there while the weights stream past
     const uint64_t pol = l2_evict_last();
     const int per_tok = n * MACC;
-    for (int j = threadIdx.x - 64; j < (t_hi - t_lo) * per_tok; j += kMmaThreads - 64) {
+    for (int j = threadIdx.x - 64; j < (t_hi - t_lo) * per_tok; j += THREADS - 64) {
       const int t = t_lo + j / per_tok, q = (j % per_tok) / MACC, h = j % MACC;
       const int mh = m0 + h * kMmaBM, bmh = h == MACC - 1 ? bm_last : kMmaBM;
       const int nr = mh + bmh <= a.rows ? bmh : a.rows - mh;
@@ -532,15 +539,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_linear_allreduce_mma(const _
   const bool acc_ok = nk > 0 && mma_mbar_wait(accf, 0, dc, mtile, (int)split);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   float* part = reinterpret_cast<float*>(gbase);  // reuses the stage buffers (all loads consumed)
-  switch (KS) {  // a power of two up to kMmaMaxSplit
-    case 1: mma_epilogue<1, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-    case 2: mma_epilogue<2, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-    case 4: mma_epilogue<4, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-    default: mma_epilogue<8, MACC>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+  // The epilogue's partial tile and inbox must fit the stage buffers and the
+  // split must be one the epilogue knows: a launch that breaks this (the
+  // host's shape search never makes one) is reported as an out-of-bounds
+  // plan for the scratch space, and every CTA of the cluster skips the
+  // epilogue alike, touching nothing outside its own shared memory.
+  const bool plan_ok = (KS == 1 || KS == 2 || KS == 4 || KS == 8) && NTILE % KS == 0 &&
+                       mma_epilogue_fits(NTILE, S, MACC, KS);
+  if (!plan_ok) {
+    if (threadIdx.x == 0)
+      atomicCAS(dc.status, 0ull, pack_bounds(mtile, kBufScratch, ((size_t)2 * NTILE) * kMmaBM * 4));
+  } else {
+    switch (KS) {
+      case 1: mma_epilogue<1, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      case 2: mma_epilogue<2, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      case 4: mma_epilogue<4, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      default: mma_epilogue<8, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+    }
   }
+  __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
-const void* linear_allreduce_mma_kernel(int n, int macc);
+const void* linear_allreduce_mma_kernel(int n, int macc, int threads);
 
 }  // namespace dcc

@@ -26,7 +26,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SELECT = ("parity_sweep or random or ragged or special_values or launch_shape or c3_bf16 or "
           "c1_fp32 or entry_barrier_same or empty_inputs or from_host or allgather_bulk or "
           "integer_data or within_bound or random_shapes or reduce_scatter_op_parity or op_with_entry_barrier or "
-          "graph_replay or dependent_chain or fused_layer_chain or accumulators")
+          "graph_replay or dependent_chain or fused_layer_chain or every_form")
 
 
 def test_parity_sweep_clean_under_bounds_checked_build():

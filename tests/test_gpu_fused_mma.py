@@ -67,16 +67,18 @@ def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
     assert np.array_equal(got, expect)
 
 
-@pytest.mark.parametrize("acc", ["1", "2"])
+@pytest.mark.parametrize("form", ["pair", "one", "two"])
 @pytest.mark.parametrize("n,tokens,rows,kp", [
     (1, 1, 136, 64), (2, 17, 264, 128), (8, 256, 1032, 64), (3, 200, 200, 192), (8, 64, 8192, 64),
     (16, 130, 520, 64), (8, 1, 8192, 128), (4, 33, 1000, 64), (2, 16, 520, 64)])
-def test_tokens_one_or_two_accumulators_bit_exact(dcc, monkeypatch, acc, n, tokens, rows, kp):
-    """Both tile forms (one accumulator of up to 128 rows, or two sharing the
-    token tile, up to 256 rows; one where the rows, tensor memory or the
-    epilogue's room do not allow two) on the same shapes, whatever the token
-    count would pick: partial last accumulators (136, 200, 264 rows), residuals."""
-    monkeypatch.setenv("DCC_MMA_ACC", acc)
+def test_tokens_every_form_bit_exact(dcc, monkeypatch, form, n, tokens, rows, kp):
+    """Every form of the kernel (128-thread CTAs two per SM with one
+    accumulator; 256-thread CTAs one per SM with one accumulator of up to 128
+    rows, or two sharing the token tile, up to 256 rows -- one where the rows,
+    tensor memory or the epilogue's room do not allow two) on the same shapes,
+    whatever the token count would pick: partial last accumulators (136, 200,
+    264 rows), residuals."""
+    monkeypatch.setenv("DCC_MMA_FORM", form)
     g = torch.Generator().manual_seed(n * 17 + tokens + rows)
     ws = [small_ints(g, rows * kp, "bf16") for _ in range(n)]
     xs = [small_ints(g, tokens * kp, "bf16", -2, 2) for _ in range(n)]
