@@ -280,3 +280,30 @@ def test_tokens_residual_argument_errors(dcc):
         comm.register(1, "output", y[0])
         assert code(w, x, [y[1], y[0]], y, tokens, rows, kp, "bf16") == dcc.DCC_ERR_INVALID_ARG  # another's output
         assert comm.check() == dcc.DCC_OK
+
+
+def test_tokens_form_by_batch_size(dcc, monkeypatch, capfd):
+    """The launch the library picks for 8 ranks x 8192 rows x kp 1024 (the
+    decode shape): up to 64 tokens the pair form (128-thread CTAs, two per
+    SM) with a K split of at least 4; above, 256-thread CTAs.  Read from the
+    library's launch log."""
+    monkeypatch.setenv("DCC_LOG", "1")
+    n, rows, kp = 8, 8192, 1024
+    w = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    for tokens, threads, min_ks in ((1, 128, 4), (64, 128, 4), (65, 256, 1), (256, 256, 1)):
+        x = [torch.zeros(tokens * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        y = [torch.empty(tokens * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        with dcc.Comm(n) as comm:
+            comm.register_all("input", w)
+            comm.register_all("input", x)
+            comm.register_all("output", y)
+            capfd.readouterr()
+            dcc.dcc_linear_allreduce_tokens(comm.handle, w, x, y, tokens, rows, kp, "bf16")
+            torch.cuda.synchronize()
+            err = capfd.readouterr().err
+            assert comm.check() == dcc.DCC_OK
+        line = [l for l in err.splitlines() if "dcc_linear_allreduce_tokens:" in l][-1]
+        fields = dict(f.split("=") for f in line.split() if "=" in f)
+        assert int(fields["threads"]) == threads, line
+        assert int(fields["ks"]) >= min_ks, line
+        assert all(float(v) == 0 for v in y[0].float()[:64]), "zero weights give zero"
