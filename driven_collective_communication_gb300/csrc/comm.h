@@ -84,12 +84,13 @@ constexpr size_t kFusedTensorMaxKp = 3584;
 // tile).  Up to kMmaPairMaxTokens tokens (the token tile rounded up to 16)
 // the pair form runs, above it the one-accumulator form.  Measured on GB300,
 // 8 ranks x 8192 rows x kp 1024 bf16, pair / one / two (us): 1 token 20.5 /
-// 27.4 / 23.2, 16 tokens 21.0 / 27.5 / 23.7, 64 tokens 24.5 / 28.7 / 26.9,
-// 128 tokens 35.2 (2-way split: a 4-way one leaves no room for the epilogue)
-// / 30.4 / 32.6; the pair form with the in-place residual 20.6 / 21.8 / 25.0
-// at 1 / 16 / 64 tokens.
+// 27.9 / 23.2, 16 tokens 21.0 / 27.5 / 23.7, 64 tokens 24.6 / 29.1 / 26.9,
+// 96 tokens 27.5 / 29.8 / -, 128 tokens 31.1 (4-way split, epilogue in two
+// rounds) / 30.7 / 32.6, 160 tokens 33.4 / 31.9 / -, 256 tokens 56.9 (one
+// CTA per SM: the token tile leaves no room for two) / 37.5 / 55.3; with the
+// in-place residual, pair 20.9 / 21.8 / 25.4 / 29.8 at 1 / 16 / 64 / 96.
 enum { kMmaFormPair = 0, kMmaFormOne = 1, kMmaFormTwo = 2 };
-constexpr int kMmaPairMaxTokens = 64;
+constexpr int kMmaPairMaxTokens = 96;
 
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;

@@ -1065,6 +1065,7 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   a.ntile = ntile;
   a.fp16 = t == DCC_FP16 ? 1 : 0;
   a.macc = macc;
+  a.rounds = dcc::mma_epilogue_rounds(ntile, stages, macc, best_ks);
   a.stages = stages;
   a.bm = best_bm;
   a.ks = best_ks;
@@ -1072,8 +1073,8 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   if (c->log)
     std::fprintf(stderr,
                  "dcc_linear_allreduce_tokens: tokens=%zu rows=%zu kp=%zu threads=%d macc=%d bm=%d ks=%d ctas=%d "
-                 "stages=%d smem=%zu resident clusters of 1/2/4/8: %lld/%lld/%lld/%lld\n",
-                 tokens, rows, kp, threads, macc, best_bm, best_ks, mtiles * best_ks, stages, smem,
+                 "stages=%d rounds=%d smem=%zu resident clusters of 1/2/4/8: %lld/%lld/%lld/%lld\n",
+                 tokens, rows, kp, threads, macc, best_bm, best_ks, mtiles * best_ks, stages, a.rounds, smem,
                  kblocks >= 1 ? fit(1) : 0, kblocks >= 2 ? fit(2) : 0, kblocks >= 4 ? fit(4) : 0,
                  kblocks >= 8 ? fit(8) : 0);
   dcc::DevComm dc = dev_view(c);

@@ -85,6 +85,7 @@ struct MmaArgs {
   int tokens, rows, kp, ntile, ks, stages;
   int bm;                  // weight rows per CTA (multiple of 8, at most macc * kMmaBM)
   int macc;                // accumulators per CTA (the kernel's MACC): 1 or 2, 128 rows each but the last
+  int rounds;              // epilogue rounds (token ranges exchanged one after another): 1, 2 or 4
   int fp16;                // element type: 0 bf16, 1 fp16
 #if DCC_CHECK_BOUNDS
   size_t ext[kNumBufKinds][DCC_MAX_RANKS];
@@ -115,11 +116,26 @@ inline int mma_stages(int ntile, int macc, unsigned budget = kMmaStageBudget) {
   return s;
 }
 
-// the partial tile (ntile x 128 fp32) plus the inbox for the other ks - 1
-// splits' token slices fit in the stage buffers
-__host__ __device__ inline bool mma_epilogue_fits(int ntile, int stages, int macc, int ks) {
-  const size_t need = ((size_t)2 * ntile - (size_t)ntile / ks) * kMmaBM * 4;
+// The epilogue takes the tokens in `rounds` ranges of w = ntile / rounds
+// (a multiple of 16 and of ks); a round's partial tile (w x 128 fp32) plus
+// the inbox for the other ks - 1 splits' token slices must fit the stage
+// buffers.
+constexpr int kMmaMaxRounds = 4;
+__host__ __device__ inline bool mma_round_fits(int ntile, int stages, int macc, int ks, int rounds) {
+  if (rounds < 1 || rounds > kMmaMaxRounds || ntile % (16 * rounds) != 0) return false;
+  const int w = ntile / rounds;
+  if (w % ks != 0) return false;
+  const size_t need = ((size_t)2 * w - (size_t)w / ks) * kMmaBM * 4;
   return need <= (size_t)stages * mma_stage_bytes(ntile, macc);
+}
+// the fewest rounds that fit, 0 if none does
+__host__ __device__ inline int mma_epilogue_rounds(int ntile, int stages, int macc, int ks) {
+  for (int r = 1; r <= kMmaMaxRounds; r *= 2)
+    if (mma_round_fits(ntile, stages, macc, ks, r)) return r;
+  return 0;
+}
+__host__ __device__ inline bool mma_epilogue_fits(int ntile, int stages, int macc, int ks) {
+  return mma_epilogue_rounds(ntile, stages, macc, ks) > 0;
 }
 
 __device__ __forceinline__ uint32_t smem_addr_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -253,18 +269,28 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
   constexpr int kBatch = 4;
   // a warp reaches the tensor-memory lanes 32 (warp mod 4) .. + 31 only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quad = warp & 3, row = quad * 32 + lane;
-  const int NTILE = a.ntile, T = NTILE / KSC;
-  float* inbox = part + (size_t)NTILE * kMmaBM;
+  // tokens in R ranges of W, each dealt out in KSC slices of T
+  const int NTILE = a.ntile, R = a.rounds, W = NTILE / R, T = W / KSC;
+  float* inbox = part + (size_t)W * kMmaBM;
   const uint32_t slice_bytes = (uint32_t)T * kMmaBM * 4u;
-  const int t_lo = (int)split * T;
   bool ok = acc_ok;
-  for (int h = 0; h < MACC; ++h) {
-    // with 8 warps, warps w and w + 4 take alternate 32-column chunks; NTILE
-    // is a multiple of 16, so the last chunk may have 16 columns
-    for (int c0 = (warp >> 2) * 32; c0 < NTILE; c0 += 32 * (THREADS / 128)) {
+  int phase = 0;
+  for (int h = 0; h < MACC; ++h)
+  for (int r = 0; r < R; ++r, ++phase) {
+    const int w_lo = r * W, w_hi = w_lo + W;  // this round's tokens
+    const int t_lo = w_lo + (int)split * T;   // this CTA's share of them
+    // the previous round's copies refill the inboxes and part: every CTA is
+    // done reading its own
+    if (phase > 0) {
+      if (KSC > 1) mma_cluster_sync();
+      else __syncthreads();
+    }
+    // with 8 warps, warps w and w + 4 take alternate 32-column chunks; W is a
+    // multiple of 16, so the last chunk may have 16 columns
+    for (int c0 = w_lo + (warp >> 2) * 32; c0 < w_hi; c0 += 32 * (THREADS / 128)) {
       uint32_t v[32];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)h * acc_cols + (uint32_t)c0;
-      if (c0 + 32 <= NTILE) {
+      if (c0 + 32 <= w_hi) {
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
             "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -282,10 +308,10 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
             : "r"(taddr));
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int cols = c0 + 32 <= NTILE ? 32 : 16;
+      const int cols = c0 + 32 <= w_hi ? 32 : 16;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j < cols) part[(c0 + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
+        if (j < cols) part[(c0 - w_lo + j) * kMmaBM + row] = acc_ok ? __uint_as_float(v[j]) : 0.0f;
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     if (KSC > 1) {
@@ -309,7 +335,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
         }
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
-      ok = mma_mbar_wait(inbar, (uint32_t)(h & 1), dc, mtile, (int)split) && ok;  // my inbox is full
+      ok = mma_mbar_wait(inbar, (uint32_t)(phase & 1), dc, mtile, (int)split) && ok;  // my inbox is full
     } else {
       __syncthreads();
     }
@@ -336,7 +362,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
         const int tl = w < items ? w / (kMmaBM / 8) : 0, r8 = (w % (kMmaBM / 8)) * 8;
 #pragma unroll
         for (int s2 = 0; s2 < KSC; ++s2) {  // split order
-          const float* src = s2 == (int)split ? &part[(t_lo + tl) * kMmaBM + r8]
+          const float* src = s2 == (int)split ? &part[((int)split * T + tl) * kMmaBM + r8]
                                               : &inbox[((s2 < (int)split ? s2 : s2 - 1) * T + tl) * kMmaBM + r8];
           const float4 lo = *reinterpret_cast<const float4*>(src), hi = *reinterpret_cast<const float4*>(src + 4);
           const float v8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -393,15 +419,8 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
         }
       }
     }
-    if (KSC > 1) {
-      // my copies have read part before it is overwritten or the CTA exits
-      if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      // the next accumulator's copies refill the inboxes: every CTA is done reading its own
-      if (h + 1 < MACC) mma_cluster_sync();
-      else __syncthreads();
-    } else if (h + 1 < MACC) {
-      __syncthreads();
-    }
+    // my copies have read part before it is overwritten or the CTA exits
+    if (KSC > 1 && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
   (void)ok;
 }
@@ -472,7 +491,6 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
 
-  const int t_lo = (int)split * NTILE / KS, t_hi = ((int)split + 1) * NTILE / KS;  // this CTA's epilogue tokens
   if (warp == 0 && lane == 0) {  // TMA producer
     // the weight boxes are 128 rows for all accumulators but the last, which
     // has bm_last (tile rows beyond them are never written and only reach
@@ -498,8 +516,14 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
     // kept there while the weights stream past
     const uint64_t pol = l2_evict_last();
     const int per_tok = n * MACC;
-    for (int j = threadIdx.x - 64; j < (t_hi - t_lo) * per_tok; j += THREADS - 64) {
-      const int t = t_lo + j / per_tok, q = (j % per_tok) / MACC, h = j % MACC;
+    // this CTA's epilogue tokens: in each of the rounds' ranges of W, its
+    // slice of T (see mma_epilogue); a launch plan the epilogue rejects
+    // prefetches nothing
+    const int R = a.rounds >= 1 && a.rounds <= kMmaMaxRounds ? a.rounds : 1, W = NTILE / R,
+              T = KS >= 1 && W % KS == 0 ? W / KS : 0;
+    for (int j = threadIdx.x - 64; j < R * T * per_tok; j += THREADS - 64) {
+      const int jt = j / per_tok, t = (jt / T) * W + (int)split * T + jt % T;
+      const int q = (j % per_tok) / MACC, h = j % MACC;
       const int mh = m0 + h * kMmaBM, bmh = h == MACC - 1 ? bm_last : kMmaBM;
       const int nr = mh + bmh <= a.rows ? bmh : a.rows - mh;
       if (t >= a.tokens || nr <= 0) continue;
@@ -544,8 +568,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
   // host's shape search never makes one) is reported as an out-of-bounds
   // plan for the scratch space, and every CTA of the cluster skips the
   // epilogue alike, touching nothing outside its own shared memory.
-  const bool plan_ok = (KS == 1 || KS == 2 || KS == 4 || KS == 8) && NTILE % KS == 0 &&
-                       mma_epilogue_fits(NTILE, S, MACC, KS);
+  const bool plan_ok = (KS == 1 || KS == 2 || KS == 4 || KS == 8) && mma_round_fits(NTILE, S, MACC, KS, a.rounds);
   if (!plan_ok) {
     if (threadIdx.x == 0)
       atomicCAS(dc.status, 0ull, pack_bounds(mtile, kBufScratch, ((size_t)2 * NTILE) * kMmaBM * 4));

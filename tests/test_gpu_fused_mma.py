@@ -284,13 +284,13 @@ def test_tokens_residual_argument_errors(dcc):
 
 def test_tokens_form_by_batch_size(dcc, monkeypatch, capfd):
     """The launch the library picks for 8 ranks x 8192 rows x kp 1024 (the
-    decode shape): up to 64 tokens the pair form (128-thread CTAs, two per
+    decode shape): up to 96 tokens the pair form (128-thread CTAs, two per
     SM) with a K split of at least 4; above, 256-thread CTAs.  Read from the
     library's launch log."""
     monkeypatch.setenv("DCC_LOG", "1")
     n, rows, kp = 8, 8192, 1024
     w = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
-    for tokens, threads, min_ks in ((1, 128, 4), (64, 128, 4), (65, 256, 1), (256, 256, 1)):
+    for tokens, threads, min_ks in ((1, 128, 4), (96, 128, 4), (97, 256, 1), (256, 256, 1)):
         x = [torch.zeros(tokens * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
         y = [torch.empty(tokens * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
         with dcc.Comm(n) as comm:
