@@ -248,11 +248,15 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
  * t's slice of the contraction dimension at x[p] + t*kp), and every rank
  * receives
  *   y[r][t*rows + i] = R( sum_p sum_k weight[p][i*kp + k] * x[p][t*kp + k] ),
- * y[r] holding tokens x rows elements, row-major.  One kernel: 128-row tiles
- * of y, tcgen05 MMAs on bf16 / fp16 operands loaded by TMA with fp32
- * accumulation in tensor memory, the contraction split across the CTAs of a
- * thread-block cluster whose partials meet in distributed shared memory, one
- * rounding, and the result put into all N outputs.  fp16 or bf16; tokens
+ * y[r] holding tokens x rows elements, row-major.  One kernel: tiles of up
+ * to 128 rows of y (up to 256 with two accumulators), tcgen05 MMAs on bf16 /
+ * fp16 operands loaded by TMA with fp32 accumulation in tensor memory, the
+ * contraction split across the CTAs of a thread-block cluster whose partials
+ * meet through bulk copies between their shared memories, one rounding, and
+ * the result put into all N outputs.  Up to 96 tokens the CTAs run two to an
+ * SM with a deeper split, above one to an SM; DCC_MMA_FORM=pair|one|two at
+ * communicator creation forces a form (results as above in every form).
+ * fp16 or bf16; tokens
  * 1..256, kp a multiple of 64, rows a multiple of 8 (UNSUPPORTED
  * otherwise); 16-byte aligned, registered, outputs disjoint from every input.
  * Exact when every fp32 partial sum is exact (small-integer data), otherwise
