@@ -74,8 +74,10 @@ typedef enum {
   DCC_ERR_LAUNCH = -6,         /* the grid cannot be co-resident on this GPU */
   DCC_ERR_TIMEOUT = -7,        /* a device wait gave up (sticky for the communicator) */
   DCC_ERR_UNSUPPORTED = -8,    /* valid request the library does not implement */
-  DCC_ERR_BOUNDS = -9          /* bounds-checked build only: a kernel access fell outside the
-                                  call's range (sticky for the communicator) */
+  DCC_ERR_BOUNDS = -9          /* bounds-checked build: a kernel access fell outside the call's
+                                  range; any build: a tensor-core layer launch whose epilogue would
+                                  not fit its shared memory (the library's own shape search never
+                                  makes one; nothing is written) -- sticky for the communicator */
 } dcc_result_t;
 
 typedef enum { DCC_INT32 = 0, DCC_FP32 = 1, DCC_FP16 = 2, DCC_BF16 = 3 } dcc_dtype_t;
