@@ -81,16 +81,14 @@ constexpr size_t kFusedTensorMaxKp = 3584;
 // Tensor-core layer over a batch of tokens, its forms: "pair" (128-thread
 // CTAs, two per SM, one accumulator), "one" (256-thread CTAs, one per SM,
 // one accumulator), "two" (the same with two accumulators sharing each token
-// tile).  Up to kMmaPairMaxTokens tokens (the token tile rounded up to 16)
-// the pair form runs, above it the one-accumulator form.  Measured on GB300,
-// 8 ranks x 8192 rows x kp 1024 bf16, pair / one / two (us): 1 token 20.5 /
-// 27.9 / 23.2, 16 tokens 21.0 / 27.5 / 23.7, 64 tokens 24.6 / 29.1 / 26.9,
-// 96 tokens 27.5 / 29.8 / -, 128 tokens 31.1 (4-way split, epilogue in two
-// rounds) / 30.7 / 32.6, 160 tokens 33.4 / 31.9 / -, 256 tokens 56.9 (one
-// CTA per SM: the token tile leaves no room for two) / 37.5 / 55.3; with the
-// in-place residual, pair 20.9 / 21.8 / 25.4 / 29.8 at 1 / 16 / 64 / 96.
+// tile).  With no form requested the library plans the forms and runs the
+// better plan (plan_mma, better_plan).  Measured on GB300, 8 ranks x 8192
+// rows x kp 1024 bf16, pair / one / two (us): 1 token 21.0 / 28.0 / 24.4,
+// 32 tokens 22.8 / 28.4 / 25.8, 96 tokens 27.9 / 29.8 / 31.0, 128 tokens
+// 31.3 (4-way split, epilogue in two rounds) / 30.6 / 33.3, 160 tokens 33.6
+// / 31.8 / 35.6, 256 tokens 42.0 (one CTA per SM: the token tile leaves no
+// room for two) / 36.5 / 48.8.
 enum { kMmaFormPair = 0, kMmaFormOne = 1, kMmaFormTwo = 2 };
-constexpr int kMmaPairMaxTokens = 96;
 
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;
@@ -101,6 +99,8 @@ struct dcc_comm {
   int n = 0;
   int device = 0;
   int num_sms = 0;
+  int smem_per_sm = 0;       // shared memory per SM and reserved per CTA, bytes
+  int smem_reserved_cta = 0;
   std::vector<dcc_host::Window> win[DCC_MAX_RANKS][3];
   bool chan[DCC_MAX_RANKS][DCC_MAX_RANKS] = {};
   bool table_dirty = true;

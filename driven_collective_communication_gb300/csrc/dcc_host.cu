@@ -572,7 +572,9 @@ int dcc_comm_create(int n_ranks, dcc_comm_t* out) {
   c->n = n_ranks;
   c->device = dev;
   for (int t = 0; t < 4; ++t) c->one_shot_max[t] = dcc_host::default_one_shot_max(n_ranks, (dcc_dtype_t)t);
-  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->smem_reserved_cta, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
     cudaGetLastError();
     delete c;
     return DCC_ERR_CUDA;
@@ -917,6 +919,130 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
 }  // extern "C"
 
 namespace {
+// A launch plan of the tensor-core layer for one form (kMmaForm*): the kernel,
+// its threads, accumulators, stages and shared memory, the tile height bm and
+// K split ks, the epilogue's rounds, and whether the grid fits one wave.
+struct MmaPlan {
+  int rc = DCC_OK;
+  const void* fn = nullptr;
+  int threads = 0, macc = 1, stages = 0, bm = 0, ks = 1, rounds = 1;
+  size_t smem = 0;
+  bool one_wave = false;
+};
+
+// The form: "pair", 128-thread CTAs two to an SM with half the shared memory
+// each and one accumulator (the K split can then be twice as deep at the same
+// bytes in flight per SM); "one", 256-thread CTAs one to an SM with one
+// accumulator; "two", the same with two accumulators sharing each token tile.
+// Then tiles of bm weight rows (a multiple of 8; 64..128 with one
+// accumulator, 136..256 with two) and ks K splits (a cluster of ks CTAs per
+// tile, ks <= kMmaMaxSplit and at most one 64-element block each): for each
+// ks the tile count that fills the most of one wave (at most as many
+// clusters as fit on the device at once, which the GPCs' SM counts make
+// fewer than SMs / ks), and of those the deepest split that keeps at least
+// 3/4 of the best CTA count (measured on GB300: the weight stream runs faster
+// the deeper the split, 23.5 us for 134 MB with a 4-way split against 27.3
+// with a 2-way one).
+MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
+  MmaPlan p;
+  int macc = form == kMmaFormTwo ? 2 : 1;
+  // one accumulator where the rows, the tensor memory (512 columns) or the
+  // epilogue's room in the stage buffers do not allow two
+  const int acc_cols = ntile <= 32 ? 32 : ntile <= 64 ? 64 : ntile <= 128 ? 128 : 256;
+  if (macc == 2 && (rows <= (size_t)dcc::kMmaBM || acc_cols * 2 > 512 ||
+                    !dcc::mma_epilogue_fits(ntile, dcc::mma_stages(ntile, 2), 2, 1)))
+    macc = 1;
+  const int threads = form == kMmaFormPair ? dcc::kMmaPairThreads : dcc::kMmaThreads;
+  const unsigned budget = form == kMmaFormPair ? dcc::kMmaPairStageBudget : dcc::kMmaStageBudget;
+  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads);
+  const int stages = dcc::mma_stages(ntile, macc, budget);
+  const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
+  // all of the SM's unified memory as shared memory (two pair-form CTAs)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
+    cudaGetLastError();
+    p.rc = DCC_ERR_LAUNCH;
+    return p;
+  }
+  // two CTAs' shared memory fit one SM (the pair form with a small token tile)
+  const bool two_per_sm = threads == dcc::kMmaPairThreads &&
+                          2 * (smem + (size_t)c->smem_reserved_cta) <= (size_t)c->smem_per_sm;
+  auto fit = [&](int ks) -> long long {  // clusters of ks CTAs resident at once
+    const auto key = std::make_tuple(fn, ks, smem);
+    const auto it = c->mma_clusters.find(key);
+    if (it != c->mma_clusters.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)ks;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int num = 0;
+    if (cudaOccupancyMaxActiveClusters(&num, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      num = c->num_sms / ks;
+    }
+    // The query counts one CTA per SM for a kernel that allocates tensor
+    // memory; two pair-form CTAs whose shared memory fits run side by side
+    // (measured on GB300: a grid of twice the SMs takes the time of one).
+    // Were they not to, the extra clusters would only form a second wave: no
+    // cluster waits on another.
+    if (two_per_sm) num *= 2;
+    c->mma_clusters[key] = num;
+    return num;
+  };
+  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
+  const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
+  auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
+  int ks_bm[dcc::kMmaMaxSplit + 1] = {};  // per split: the tile height, 0 = none fits one wave
+  long long ks_ctas[dcc::kMmaMaxSplit + 1] = {}, most = 0;
+  for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2) {
+    if (!dcc::mma_epilogue_fits(ntile, stages, macc, ks)) break;  // no room for the epilogue's inbox
+    const long long cap = fit(ks);
+    for (int bm = bm_lo; bm <= bm_hi; bm += 8) {  // shorter tiles: more CTAs
+      if (tiles(bm) > cap) continue;
+      int tall = bm;  // the tallest tile with the same tile count
+      while (tall + 8 <= bm_hi && tiles(tall + 8) == tiles(bm)) tall += 8;
+      ks_bm[ks] = tall;
+      ks_ctas[ks] = tiles(bm) * ks;
+      if (ks_ctas[ks] > most) most = ks_ctas[ks];
+      break;
+    }
+  }
+  p.bm = bm_hi;  // more tiles than fit even at the tallest tile: several waves, no split
+  p.ks = 1;
+  for (int ks = dcc::kMmaMaxSplit; ks >= 1; ks /= 2)
+    if (ks_bm[ks] && 4 * ks_ctas[ks] >= 3 * most) {
+      p.bm = ks_bm[ks];
+      p.ks = ks;
+      p.one_wave = true;
+      break;
+    }
+  p.fn = fn;
+  p.threads = threads;
+  p.macc = macc;
+  p.stages = stages;
+  p.smem = smem;
+  p.rounds = dcc::mma_epilogue_rounds(ntile, stages, macc, p.ks);
+  return p;
+}
+
+// Whether plan a should run rather than plan b: a grid in one wave first,
+// then an epilogue in one round, then the deeper K split; on a tie b stays.
+// Measured on GB300 (8 ranks, bf16): with the two-accumulator form's rule
+// beside it, this picks the faster form, or one within 2 %, over rows 4096 /
+// 8192 / 16384 / 28672, kp 512 / 1024 / 2048 and 1 to 256 tokens.
+bool better_plan(const MmaPlan& a, const MmaPlan& b) {
+  if (a.one_wave != b.one_wave) return a.one_wave;
+  if ((a.rounds == 1) != (b.rounds == 1)) return a.rounds == 1;
+  return a.ks > b.ks;
+}
+
 int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const* residual, void* const* y,
                   size_t tokens, size_t rows, size_t kp, dcc_dtype_t t, dcc_stream_t s) {
   if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
@@ -959,92 +1085,32 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   const int ntile = tokens <= 16 ? 16 : (int)((tokens + 15) / 16 * 16);
   dcc::MmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  // Launch shape.  The form: up to kMmaPairMaxTokens tokens, 128-thread CTAs
-  // two to an SM, each with half the shared memory and one accumulator (the
-  // K split can then be twice as deep at the same bytes in flight per SM);
-  // above, 256-thread CTAs one to an SM with one accumulator -- or two
-  // sharing each token tile, on request (DCC_MMA_FORM).  Then tiles of bm
-  // weight rows (a multiple of 8; 64..128 with one accumulator, 136..256 with
-  // two) and ks K splits (a cluster of ks CTAs per tile, ks <= kMmaMaxSplit
-  // and at most one 64-element block each): for each ks the tile count that
-  // fills the most of one wave (at most as many clusters as fit on the device
-  // at once, which the GPCs' SM counts make fewer than SMs / ks), and of
-  // those the deepest split that keeps at least 3/4 of the best CTA count
-  // (measured on GB300: the weight stream runs faster the deeper the split,
-  // 23.5 us for 134 MB with a 4-way split against 27.3 with a 2-way one).
-  int form = c->mma_form >= 0 ? c->mma_form : ntile <= kMmaPairMaxTokens ? kMmaFormPair : kMmaFormOne;
-  int macc = form == kMmaFormTwo ? 2 : 1;
-  // one accumulator where the rows, the tensor memory (512 columns) or the
-  // epilogue's room in the stage buffers do not allow two
-  const int acc_cols = ntile <= 32 ? 32 : ntile <= 64 ? 64 : ntile <= 128 ? 128 : 256;
-  if (macc == 2 && (rows <= (size_t)dcc::kMmaBM || acc_cols * 2 > 512 ||
-                    !dcc::mma_epilogue_fits(ntile, dcc::mma_stages(ntile, 2), 2, 1)))
-    macc = 1;
-  const int threads = form == kMmaFormPair ? dcc::kMmaPairThreads : dcc::kMmaThreads;
-  const unsigned budget = form == kMmaFormPair ? dcc::kMmaPairStageBudget : dcc::kMmaStageBudget;
-  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads);
-  const int stages = dcc::mma_stages(ntile, macc, budget);
-  const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
-  // all of the SM's unified memory as shared memory (two pair-form CTAs)
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
-    cudaGetLastError();
-    return DCC_ERR_LAUNCH;
-  }
-  auto fit = [&](int ks) -> long long {  // clusters of ks CTAs resident at once
-    const auto key = std::make_tuple(fn, ks, smem);
-    const auto it = c->mma_clusters.find(key);
-    if (it != c->mma_clusters.end()) return it->second;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ks);
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)ks;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int num = 0;
-    if (cudaOccupancyMaxActiveClusters(&num, fn, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      num = c->num_sms / ks;
-    }
-    // The query counts one CTA per SM for a kernel that allocates tensor
-    // memory; two pair-form CTAs (half the shared memory, 32-256 columns
-    // each) run side by side (measured on GB300: a grid of twice the SMs
-    // takes the time of one).  Were they not to, the extra clusters would
-    // only form a second wave: no cluster waits on another.
-    if (threads == dcc::kMmaPairThreads) num *= 2;
-    c->mma_clusters[key] = num;
-    return num;
-  };
-  const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
-  const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
-  auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
-  int ks_bm[dcc::kMmaMaxSplit + 1] = {};  // per split: the tile height, 0 = none fits one wave
-  long long ks_ctas[dcc::kMmaMaxSplit + 1] = {}, most = 0;
-  for (int ks = 1; ks <= dcc::kMmaMaxSplit && ks <= kblocks; ks *= 2) {
-    if (!dcc::mma_epilogue_fits(ntile, stages, macc, ks)) break;  // no room for the epilogue's inbox
-    const long long cap = fit(ks);
-    for (int bm = bm_lo; bm <= bm_hi; bm += 8) {  // shorter tiles: more CTAs
-      if (tiles(bm) > cap) continue;
-      int tall = bm;  // the tallest tile with the same tile count
-      while (tall + 8 <= bm_hi && tiles(tall + 8) == tiles(bm)) tall += 8;
-      ks_bm[ks] = tall;
-      ks_ctas[ks] = tiles(bm) * ks;
-      if (ks_ctas[ks] > most) most = ks_ctas[ks];
-      break;
+  // Launch shape (plan_mma): with no form requested, the pair form and the
+  // one-accumulator form are both planned and the better plan runs
+  // (better_plan); the two-accumulator form only where neither fits one wave
+  // and it does (its taller tiles halve the tile count; measured on GB300,
+  // 28672 rows x 256 tokens: 106 us against 126, while with both in one wave
+  // its deeper split loses to the one-accumulator form's, 33.3 against 30.6
+  // us at 8192 rows x 128 tokens).  DCC_MMA_FORM forces one.
+  MmaPlan plan;
+  if (c->mma_form >= 0) {
+    plan = plan_mma(c, c->mma_form, ntile, rows, kp);
+  } else {
+    plan = plan_mma(c, kMmaFormOne, ntile, rows, kp);
+    if (plan.rc != DCC_OK) return plan.rc;
+    const MmaPlan pair = plan_mma(c, kMmaFormPair, ntile, rows, kp);
+    if (pair.rc != DCC_OK) return pair.rc;
+    if (better_plan(pair, plan)) plan = pair;
+    if (!plan.one_wave) {
+      const MmaPlan two = plan_mma(c, kMmaFormTwo, ntile, rows, kp);
+      if (two.rc != DCC_OK) return two.rc;
+      if (two.macc == 2 && two.one_wave) plan = two;
     }
   }
-  int best_bm = bm_hi, best_ks = 1;  // more tiles than fit even at the tallest tile: several waves, no split
-  for (int ks = dcc::kMmaMaxSplit; ks >= 1; ks /= 2)
-    if (ks_bm[ks] && 4 * ks_ctas[ks] >= 3 * most) {
-      best_bm = ks_bm[ks];
-      best_ks = ks;
-      break;
-    }
+  if (plan.rc != DCC_OK) return plan.rc;
+  const void* fn = plan.fn;
+  const int threads = plan.threads, macc = plan.macc, stages = plan.stages, best_bm = plan.bm, best_ks = plan.ks;
+  const size_t smem = plan.smem;
   const int bm0 = macc == 1 ? best_bm : dcc::kMmaBM, bm_last = best_bm - dcc::kMmaBM * (macc - 1);
   for (int r = 0; r < c->n; ++r) {
     rc = tensor_map(c, weight[r], kp, rows, (unsigned)bm0, t, &maps.w[r]);
@@ -1065,7 +1131,7 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   a.ntile = ntile;
   a.fp16 = t == DCC_FP16 ? 1 : 0;
   a.macc = macc;
-  a.rounds = dcc::mma_epilogue_rounds(ntile, stages, macc, best_ks);
+  a.rounds = plan.rounds;
   a.stages = stages;
   a.bm = best_bm;
   a.ks = best_ks;
@@ -1073,10 +1139,9 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   if (c->log)
     std::fprintf(stderr,
                  "dcc_linear_allreduce_tokens: tokens=%zu rows=%zu kp=%zu threads=%d macc=%d bm=%d ks=%d ctas=%d "
-                 "stages=%d rounds=%d smem=%zu resident clusters of 1/2/4/8: %lld/%lld/%lld/%lld\n",
+                 "stages=%d rounds=%d smem=%zu one_wave=%d\n",
                  tokens, rows, kp, threads, macc, best_bm, best_ks, mtiles * best_ks, stages, a.rounds, smem,
-                 kblocks >= 1 ? fit(1) : 0, kblocks >= 2 ? fit(2) : 0, kblocks >= 4 ? fit(4) : 0,
-                 kblocks >= 8 ? fit(8) : 0);
+                 plan.one_wave ? 1 : 0);
   dcc::DevComm dc = dev_view(c);
   void* kargs[] = {&maps, &dc, &a};
   return launch(fn, mtiles * best_ks, threads, false, kargs, static_cast<cudaStream_t>(s), smem, c->pdl, best_ks);

@@ -255,9 +255,13 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
  * fp16 operands loaded by TMA with fp32 accumulation in tensor memory, the
  * contraction split across the CTAs of a thread-block cluster whose partials
  * meet through bulk copies between their shared memories, one rounding, and
- * the result put into all N outputs.  Up to 96 tokens the CTAs run two to an
- * SM with a deeper split, above one to an SM; DCC_MMA_FORM=pair|one|two at
- * communicator creation forces a form (results as above in every form).
+ * the result put into all N outputs.  The launch is planned for three forms
+ * (128-thread CTAs two to an SM with a deeper split; 256-thread CTAs one to
+ * an SM with one accumulator, or with two) and the one whose grid fits one
+ * wave, whose epilogue takes one round and whose split is deepest runs (with
+ * 8192 rows: the first up to 96 tokens, the second above);
+ * DCC_MMA_FORM=pair|one|two at communicator creation forces a form (results
+ * as above in every form).
  * fp16 or bf16; tokens
  * 1..256, kp a multiple of 64, rows a multiple of 8 (UNSUPPORTED
  * otherwise); 16-byte aligned, registered, outputs disjoint from every input.

@@ -282,28 +282,35 @@ def test_tokens_residual_argument_errors(dcc):
         assert comm.check() == dcc.DCC_OK
 
 
-def test_tokens_form_by_batch_size(dcc, monkeypatch, capfd):
-    """The launch the library picks for 8 ranks x 8192 rows x kp 1024 (the
-    decode shape): up to 96 tokens the pair form (128-thread CTAs, two per
-    SM) with a K split of at least 4; above, 256-thread CTAs.  Read from the
+@pytest.mark.parametrize("rows,tokens,threads,macc,min_ks", [
+    (8192, 1, 128, 1, 4), (8192, 96, 128, 1, 4), (8192, 97, 256, 1, 1), (8192, 256, 256, 1, 1),
+    (4096, 96, 256, 1, 4), (28672, 1, 128, 1, 1), (28672, 256, 256, 2, 1)])
+def test_tokens_form_by_shape(dcc, monkeypatch, capfd, rows, tokens, threads, macc, min_ks):
+    """The launch the library picks for 8 ranks x kp 1024: at 8192 rows (the
+    decode shape) up to 96 tokens the pair form (128-thread CTAs, two per SM)
+    with a K split of at least 4, above it 256-thread CTAs with one
+    accumulator; at 4096 rows, where both forms fit a 4-way split in one
+    wave, the 256-thread form; at 28672 rows x 256 tokens, where only two
+    accumulators per CTA fit the tiles in one wave, that form.  Read from the
     library's launch log."""
     monkeypatch.setenv("DCC_LOG", "1")
-    n, rows, kp = 8, 8192, 1024
+    n, kp = 8, 1024
     w = [torch.zeros(rows * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
-    for tokens, threads, min_ks in ((1, 128, 4), (96, 128, 4), (97, 256, 1), (256, 256, 1)):
-        x = [torch.zeros(tokens * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
-        y = [torch.empty(tokens * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
-        with dcc.Comm(n) as comm:
-            comm.register_all("input", w)
-            comm.register_all("input", x)
-            comm.register_all("output", y)
-            capfd.readouterr()
-            dcc.dcc_linear_allreduce_tokens(comm.handle, w, x, y, tokens, rows, kp, "bf16")
-            torch.cuda.synchronize()
-            err = capfd.readouterr().err
-            assert comm.check() == dcc.DCC_OK
-        line = [l for l in err.splitlines() if "dcc_linear_allreduce_tokens:" in l][-1]
-        fields = dict(f.split("=") for f in line.split() if "=" in f)
-        assert int(fields["threads"]) == threads, line
-        assert int(fields["ks"]) >= min_ks, line
-        assert all(float(v) == 0 for v in y[0].float()[:64]), "zero weights give zero"
+    x = [torch.zeros(tokens * kp, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    y = [torch.empty(tokens * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    with dcc.Comm(n) as comm:
+        comm.register_all("input", w)
+        comm.register_all("input", x)
+        comm.register_all("output", y)
+        capfd.readouterr()
+        dcc.dcc_linear_allreduce_tokens(comm.handle, w, x, y, tokens, rows, kp, "bf16")
+        torch.cuda.synchronize()
+        err = capfd.readouterr().err
+        assert comm.check() == dcc.DCC_OK
+    line = [l for l in err.splitlines() if "dcc_linear_allreduce_tokens:" in l][-1]
+    fields = dict(f.split("=") for f in line.split() if "=" in f)
+    assert int(fields["threads"]) == threads, line
+    assert int(fields["macc"]) == macc, line
+    assert int(fields["ks"]) >= min_ks, line
+    assert int(fields["one_wave"]) == 1, line
+    assert all(float(v) == 0 for v in y[0].float()[:64]), "zero weights give zero"
