@@ -998,6 +998,17 @@ def other_workloads(dcc, dev, stream):
                         torch.matmul(xin[r], wts[r].t(), out=part[r])
                 ar()
             res = {}
+            # host cost of one eager call (argument checks, the cached launch
+            # plan, the launch), arguments marshalled once, no device wait
+            step = dcc.prepare_linear_allreduce_tokens(tc.handle, wts, xin, yt, tokens, rows, kp, "bf16", stream)
+            for _ in range(3):
+                step()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(200):
+                step()
+            res["fused_tensor_host_us_per_call"] = round((time.perf_counter() - t0) * 1e6 / 200, 2)
+            stream.synchronize()
             for name, fn in (("fused_tensor", fused), ("fused_tensor_residual_inplace", fused_res),
                              ("gemm_then_allreduce", unfused)):
                 for _ in range(3):

@@ -90,6 +90,17 @@ constexpr size_t kFusedTensorMaxKp = 3584;
 // room for two) / 36.5 / 48.8.
 enum { kMmaFormPair = 0, kMmaFormOne = 1, kMmaFormTwo = 2 };
 
+// A launch plan of the tensor-core layer for one form (kMmaForm*): the kernel,
+// its threads, accumulators, stages and shared memory, the tile height bm and
+// K split ks, the epilogue's rounds, and whether the grid fits one wave.
+struct MmaPlan {
+  int rc = DCC_OK;
+  const void* fn = nullptr;
+  int threads = 0, macc = 1, stages = 0, bm = 0, ks = 1, rounds = 1;
+  size_t smem = 0;
+  bool one_wave = false;
+};
+
 // AllGather inputs of at least this many bytes per rank use the bulk-copy kernel.
 constexpr size_t kAgBulkMinBytes = 64 * 1024;
 
@@ -157,6 +168,8 @@ struct dcc_comm {
   // clusters of the tensor-core layer that fit on the device at once, by
   // (kernel, cluster size, dynamic shared memory); 0 = not measured yet
   std::map<std::tuple<const void*, int, size_t>, int> mma_clusters;
+  // launch plans of the tensor-core layer by (form, token tile, rows, kp)
+  std::map<std::tuple<int, int, size_t, size_t>, dcc_host::MmaPlan> mma_plans;
 };
 
 namespace dcc_host {

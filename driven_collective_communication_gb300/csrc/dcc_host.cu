@@ -919,16 +919,24 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
 }  // extern "C"
 
 namespace {
-// A launch plan of the tensor-core layer for one form (kMmaForm*): the kernel,
-// its threads, accumulators, stages and shared memory, the tile height bm and
-// K split ks, the epilogue's rounds, and whether the grid fits one wave.
-struct MmaPlan {
-  int rc = DCC_OK;
-  const void* fn = nullptr;
-  int threads = 0, macc = 1, stages = 0, bm = 0, ks = 1, rounds = 1;
-  size_t smem = 0;
-  bool one_wave = false;
-};
+// Raises fn's dynamic shared-memory limit on the current device to at least
+// smem, with all of the SM's unified memory as shared memory.  It never
+// lowers the limit (a function attribute holds for every communicator, and a
+// plan one of them cached must stay launchable).  Called when a plan is made.
+int raise_smem_limit(const void* fn, size_t smem) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return DCC_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
+    cudaGetLastError();
+    return DCC_ERR_LAUNCH;
+  }
+  return DCC_OK;
+}
 
 // The form: "pair", 128-thread CTAs two to an SM with half the shared memory
 // each and one accumulator (the K split can then be twice as deep at the same
@@ -944,6 +952,9 @@ struct MmaPlan {
 // the deeper the split, 23.5 us for 134 MB with a 4-way split against 27.3
 // with a 2-way one).
 MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
+  const auto pkey = std::make_tuple(form, ntile, rows, kp);
+  const auto hit = c->mma_plans.find(pkey);
+  if (hit != c->mma_plans.end()) return hit->second;
   MmaPlan p;
   int macc = form == kMmaFormTwo ? 2 : 1;
   // one accumulator where the rows, the tensor memory (512 columns) or the
@@ -957,13 +968,8 @@ MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
   const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads);
   const int stages = dcc::mma_stages(ntile, macc, budget);
   const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
-  // all of the SM's unified memory as shared memory (two pair-form CTAs)
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
-    cudaGetLastError();
-    p.rc = DCC_ERR_LAUNCH;
-    return p;
-  }
+  p.rc = raise_smem_limit(fn, smem);
+  if (p.rc != DCC_OK) return p;
   // two CTAs' shared memory fit one SM (the pair form with a small token tile)
   const bool two_per_sm = threads == dcc::kMmaPairThreads &&
                           2 * (smem + (size_t)c->smem_reserved_cta) <= (size_t)c->smem_per_sm;
@@ -1029,6 +1035,8 @@ MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
   p.stages = stages;
   p.smem = smem;
   p.rounds = dcc::mma_epilogue_rounds(ntile, stages, macc, p.ks);
+  if (c->mma_plans.size() >= 4096) c->mma_plans.clear();
+  c->mma_plans.emplace(pkey, p);
   return p;
 }
 

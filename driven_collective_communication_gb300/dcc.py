@@ -438,6 +438,19 @@ def prepare_allreduce(comm, send, recv, count, dtype, algo="auto", stream=None):
     return call
 
 
+def prepare_linear_allreduce_tokens(comm, weight, x, y, tokens, rows, kp, dtype, stream=None):
+    """Marshal the arguments of one dcc_linear_allreduce_tokens once and return
+    a callable that repeats exactly that call."""
+    args = (comm, _ptrs(weight), _ptrs(x), _ptrs(y), tokens, rows, kp, _dtype(dtype), _stream(stream))
+    f = _lib.dcc_linear_allreduce_tokens
+
+    def call():
+        rc = f(*args)
+        if rc != DCC_OK:
+            raise DccError(rc, "dcc_linear_allreduce_tokens")
+    return call
+
+
 def raw_call(name, *args):
     """Call an entry point with raw ctypes arguments and return its code (tests of error paths)."""
     return getattr(_lib, name)(*args)

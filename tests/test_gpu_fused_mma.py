@@ -314,3 +314,37 @@ def test_tokens_form_by_shape(dcc, monkeypatch, capfd, rows, tokens, threads, ma
     assert int(fields["ks"]) >= min_ks, line
     assert int(fields["one_wave"]) == 1, line
     assert all(float(v) == 0 for v in y[0].float()[:64]), "zero weights give zero"
+
+
+def test_tokens_plans_cached_across_communicators(dcc, monkeypatch):
+    """Launch plans are cached per communicator and shape, and a kernel's
+    shared-memory limit only ever rises: two communicators alive at once
+    alternating a large token tile (more shared memory per CTA) with a small
+    one on the same kernel, each call bit-exact against the oracle."""
+    monkeypatch.setenv("DCC_MMA_FORM", "pair")
+    n, rows, kp = 8, 1024, 128
+    g = torch.Generator().manual_seed(4242)
+    ws = [small_ints(g, rows * kp, "bf16") for _ in range(n)]
+    dw = [w.cuda() for w in ws]
+    cases = {}
+    for tokens in (256, 16):
+        xs = [small_ints(g, tokens * kp, "bf16", -2, 2) for _ in range(n)]
+        expect = oracle.linear_allreduce_tokens([W.to_storage(w) for w in ws], [W.to_storage(x) for x in xs],
+                                                "bf16", tokens, rows, kp)
+        cases[tokens] = ([x.cuda() for x in xs], expect)
+    with dcc.Comm(n) as big, dcc.Comm(n) as small:
+        comms = {256: big, 16: small}
+        outs = {t: [torch.empty(t * rows, dtype=torch.bfloat16, device="cuda") for _ in range(n)] for t in cases}
+        for t, comm in comms.items():
+            comm.register_all("input", dw)
+            comm.register_all("input", cases[t][0])
+            comm.register_all("output", outs[t])
+        for tokens in (256, 16, 256, 16, 256):
+            for y in outs[tokens]:
+                y.fill_(float("nan"))
+            rc = dcc.dcc_linear_allreduce_tokens(comms[tokens].handle, dw, cases[tokens][0], outs[tokens], tokens,
+                                                 rows, kp, "bf16")
+            assert rc == dcc.DCC_OK
+            assert comms[tokens].check() == dcc.DCC_OK
+            for r in range(n):
+                assert np.array_equal(W.to_storage(outs[tokens][r]), cases[tokens][1]), (tokens, r)
