@@ -513,6 +513,17 @@ def graph_node_floor(stream, reps=100):
     return round(e0.elapsed_time(e1) * 1e3 / (10 * reps), 3)
 
 
+def alternate(sets):
+    """A callable returning sets[0], sets[1], ... in turn (the weights of
+    consecutive layers)."""
+    k = [0]
+
+    def nxt():
+        k[0] += 1
+        return sets[(k[0] - 1) % len(sets)]
+    return nxt
+
+
 def graph_us(step, stream, reps=100, replays=10):
     """Device time per call of `step` inside a CUDA graph of `reps` calls,
     replayed `replays` times after one untimed replay (steady state)."""
@@ -923,28 +934,36 @@ def other_workloads(dcc, dev, stream):
         rows = 8192
         g = torch.Generator(device=dev)
         g.manual_seed(5)
-        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+        # two weight sets, layer i of a graph taking set i % 2 (as consecutive
+        # layers of a model do): 2 x 134 MB at kp 1024 is more than L2, so no
+        # layer finds its weights left in L2 by the one before
+        wsets = [[(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+                 for _ in range(2)]
+        wts = wsets[0]
+        nxt = alternate(wsets)
         xin = [torch.randn(kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
         yf = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         part = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         ysep = [torch.empty(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         hres = [torch.zeros(rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]  # residual stream
         with dcc.Comm(8) as lc:
-            lc.register_all("input", wts)
+            for ws in wsets:
+                lc.register_all("input", ws)
             lc.register_all("input", xin)
             lc.register_all("output", yf)
             lc.register_all("input", part)
             lc.register_all("output", ysep)
             lc.register_all("output", hres)
-            fused = lambda: dcc.dcc_linear_allreduce(lc.handle, wts, xin, yf, rows, kp, "bf16", stream)  # noqa
+            fused = lambda: dcc.dcc_linear_allreduce(lc.handle, nxt(), xin, yf, rows, kp, "bf16", stream)  # noqa
             fused_res = lambda: dcc.dcc_linear_allreduce_residual(  # noqa: E731  h <- h + layer, in place
-                lc.handle, wts, xin, hres, hres, rows, kp, "bf16", stream)
+                lc.handle, nxt(), xin, hres, hres, rows, kp, "bf16", stream)
             ar = dcc.prepare_allreduce(lc.handle, part, ysep, rows, "bf16", "auto", stream)
 
             def unfused():
+                ws = nxt()
                 with torch.cuda.stream(stream):
                     for r in range(8):
-                        torch.matmul(wts[r], xin[r], out=part[r])
+                        torch.matmul(ws[r], xin[r], out=part[r])
                 ar()
             res = {}
             for name, fn in (("fused", fused), ("fused_residual_inplace", fused_res),
@@ -969,33 +988,37 @@ def other_workloads(dcc, dev, stream):
                 res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
             assert lc.check(stream) == dcc.DCC_OK
         out["linear_allreduce_bf16_n8_rows8192_kp%d" % kp] = res
-        del wts, xin, yf, part, ysep, hres
+        del wsets, wts, xin, yf, part, ysep, hres
     # the row-parallel layer over a batch of tokens on the tensor cores vs
     # per-rank cuBLAS GEMM then the AllReduce (8 ranks x 8192 rows x kp 1024)
     for tokens in (1, 16, 64, 128, 256):
         rows, kp = 8192, 1024
         g = torch.Generator(device=dev)
         g.manual_seed(6)
-        wts = [(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+        wsets = [[(torch.randn(rows, kp, generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+                 for _ in range(2)]  # alternating weight sets, as above
+        wts = wsets[0]
+        nxt = alternate(wsets)
         xin = [torch.randn(tokens, kp, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
         yt = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         part = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         ysep = [torch.empty(tokens, rows, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         hres = [torch.randn(tokens, rows, generator=g, device=dev).to(torch.bfloat16) for _ in range(8)]
         with dcc.Comm(8) as tc:
-            for bufs, kind in ((wts, "input"), (xin, "input"), (part, "input"), (yt, "output"), (ysep, "output"),
-                               (hres, "output")):
+            for bufs, kind in ((wsets[0], "input"), (wsets[1], "input"), (xin, "input"), (part, "input"),
+                               (yt, "output"), (ysep, "output"), (hres, "output")):
                 tc.register_all(kind, bufs)
-            fused = lambda: dcc.dcc_linear_allreduce_tokens(tc.handle, wts, xin, yt, tokens, rows, kp, "bf16",  # noqa
-                                                            stream)
+            fused = lambda: dcc.dcc_linear_allreduce_tokens(tc.handle, nxt(), xin, yt, tokens, rows, kp,  # noqa
+                                                            "bf16", stream)
             fused_res = lambda: dcc.dcc_linear_allreduce_tokens_residual(  # noqa: E731 (h <- h + layer, in place)
-                tc.handle, wts, xin, hres, hres, tokens, rows, kp, "bf16", stream)
+                tc.handle, nxt(), xin, hres, hres, tokens, rows, kp, "bf16", stream)
             ar = dcc.prepare_allreduce(tc.handle, part, ysep, tokens * rows, "bf16", "auto", stream)
 
             def unfused():
+                ws = nxt()
                 with torch.cuda.stream(stream):
                     for r in range(8):
-                        torch.matmul(xin[r], wts[r].t(), out=part[r])
+                        torch.matmul(xin[r], ws[r].t(), out=part[r])
                 ar()
             res = {}
             # host cost of one eager call (argument checks, the cached launch
@@ -1019,7 +1042,7 @@ def other_workloads(dcc, dev, stream):
                 res[name + "_weight_gbs"] = round(8 * rows * kp * 2 / (us * 1e-6) / GB, 1)
             assert tc.check(stream) == dcc.DCC_OK
         out["linear_tokens_bf16_n8_rows8192_kp1024_t%d" % tokens] = res
-        del wts, xin, yt, part, ysep, hres
+        del wsets, wts, xin, yt, part, ysep, hres
     # the ring barrier: default transport (8 ranks: one cluster, distributed
     # shared memory) and the global-memory semaphores (DCC_RING_CLUSTER=0)
     for key, env in (("c5_ring_barrier", None), ("c5_ring_barrier_l2_semaphores", "0")):
