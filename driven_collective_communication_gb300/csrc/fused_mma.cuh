@@ -457,13 +457,14 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
   const uint32_t acc_cols = NTILE <= 32 ? 32u : NTILE <= 64 ? 64u : NTILE <= 128 ? 128u : 256u;
   const uint32_t ncols = acc_cols * (uint32_t)MACC;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mma_mbar_init(full(s), 1);
-      mma_mbar_init(empty(s), 1);
-    }
-    mma_mbar_init(accf, 1);
-    mma_mbar_init(inbar, 1);
+  // The start is on the critical path of every launch (measured on GB300 at
+  // 1 token: 1.1 us from entry to the first load with one thread doing all
+  // of it): warp 0's lanes set up the mbarriers (full[S], empty[S], the
+  // accumulator and inbox barriers, all one arrival, laid out back to back),
+  // warp 2 allocates the tensor memory and warp 3 asks L2 for the first
+  // weight tiles, side by side.
+  if (warp == 0) {
+    for (int j = lane; j < 2 * S + 2; j += 32) mma_mbar_init(bars + 8u * (uint32_t)j, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 2) {
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
   // the first weight tiles (a prefetch returns nothing, so whatever that
   // kernel still writes lands in L2 before the loads below read it).  No data
   // is read before griddepcontrol.wait.
-  if (warp == 0 && lane == 0)
+  if (warp == 3 && lane == 0)
     for (int i = 0; i < nk && i < S; ++i) {
       const int g = b0 + i;
       tma_prefetch_2d(&maps.w[g / kpb], (g % kpb) * kMmaBK, m0);
