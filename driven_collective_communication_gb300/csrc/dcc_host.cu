@@ -1043,8 +1043,9 @@ MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
 // Whether plan a should run rather than plan b: a grid in one wave first,
 // then an epilogue in one round, then the deeper K split; on a tie b stays.
 // Measured on GB300 (8 ranks, bf16): with the two-accumulator form's rule
-// beside it, this picks the faster form, or one within 2 %, over rows 4096 /
-// 8192 / 16384 / 28672, kp 512 / 1024 / 2048 and 1 to 256 tokens.
+// beside it, this picks the faster form, or one within 4 % (about the
+// run-to-run spread), over rows 4096 / 8192 / 16384 / 28672, kp 512 / 1024 /
+// 2048 and 1 to 256 tokens.
 bool better_plan(const MmaPlan& a, const MmaPlan& b) {
   if (a.one_wave != b.one_wave) return a.one_wave;
   if ((a.rounds == 1) != (b.rounds == 1)) return a.rounds == 1;
