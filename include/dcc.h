@@ -257,9 +257,10 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
  * meet through bulk copies between their shared memories, one rounding, and
  * the result put into all N outputs.  The launch is planned for three forms
  * (128-thread CTAs two to an SM with a deeper split; 256-thread CTAs one to
- * an SM with one accumulator, or with two) and the one whose grid fits one
- * wave, whose epilogue takes one round and whose split is deepest runs (with
- * 8192 rows: the first up to 96 tokens, the second above);
+ * an SM with one accumulator, or with two): of the first two the one whose
+ * grid fits one wave, whose epilogue takes one round and whose split is
+ * deepest runs, the third only where it alone fits one wave (with 8192 rows:
+ * the first up to 96 tokens, the second above);
  * DCC_MMA_FORM=pair|one|two at communicator creation forces a form (results
  * as above in every form).
  * fp16 or bf16; tokens
