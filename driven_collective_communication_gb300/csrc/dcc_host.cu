@@ -1003,7 +1003,7 @@ MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
     return num;
   };
   const int bm_lo = macc == 1 ? 64 : dcc::kMmaBM + 8, bm_hi = macc * dcc::kMmaBM;
-  const int kblocks = c->n * (int)(kp / dcc::kMmaBK);
+  const int kblocks = c->n * (int)((kp + dcc::kMmaBK - 1) / dcc::kMmaBK);
   auto tiles = [&](int bm) { return (long long)((rows + bm - 1) / bm); };
   int ks_bm[dcc::kMmaMaxSplit + 1] = {};  // per split: the tile height, 0 = none fits one wave
   long long ks_ctas[dcc::kMmaMaxSplit + 1] = {}, most = 0;
@@ -1057,7 +1057,8 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   if (!c || !weight || !x || !y) return DCC_ERR_INVALID_ARG;
   if (c->sticky != DCC_OK) return c->sticky;
   if (t != DCC_BF16 && t != DCC_FP16) return DCC_ERR_UNSUPPORTED;
-  if (tokens > (size_t)dcc::kMmaMaxTokens || rows % 8 || kp % dcc::kMmaBK) return DCC_ERR_UNSUPPORTED;
+  // kp: rows of the tensor maps are 16-byte multiples
+  if (tokens > (size_t)dcc::kMmaMaxTokens || rows % 8 || kp % 8) return DCC_ERR_UNSUPPORTED;
   if (tokens == 0 || rows == 0 || kp == 0) return DCC_OK;
   if (rows > ((size_t)1 << 31) || kp > ((size_t)1 << 31) / (size_t)c->n) return DCC_ERR_UNSUPPORTED;
   const size_t wb = rows * kp * 2, xb = tokens * kp * 2, yb = tokens * rows * 2;

@@ -468,7 +468,11 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
   const int mtile = (int)blockIdx.x / KS, m0 = mtile * a.bm;
   // rows of the last accumulator (the others have 128 each)
   const int bm_last = a.bm - kMmaBM * (MACC - 1);
-  const int kpb = a.kp / kMmaBK, nb = n * kpb;
+  // 64-column blocks per rank, the last one partial when kp is not a multiple
+  // of 64: the TMA fills the columns past kp with zeros in the weight and the
+  // token tiles alike, so they add nothing (and the transaction counts the
+  // whole box)
+  const int kpb = (a.kp + kMmaBK - 1) / kMmaBK, nb = n * kpb;
   const int b0 = (int)((long long)split * nb / KS), b1 = (int)((long long)(split + 1) * nb / KS);
   const int nk = b1 - b0;
   // columns of one accumulator (a power of two, at least 32); the second follows the first

@@ -264,8 +264,9 @@ int dcc_linear_allreduce_residual(dcc_comm_t c, void* const* weight, void* const
  * DCC_MMA_FORM=pair|one|two at communicator creation forces a form (results
  * as above in every form).
  * fp16 or bf16; tokens
- * 1..256, kp a multiple of 64, rows a multiple of 8 (UNSUPPORTED
- * otherwise); 16-byte aligned, registered, outputs disjoint from every input.
+ * 1..256, kp and rows multiples of 8 (UNSUPPORTED otherwise; a kp that is
+ * not a multiple of 64 ends in a partial 64-column block, zero-filled by the
+ * TMA); 16-byte aligned, registered, outputs disjoint from every input.
  * Exact when every fp32 partial sum is exact (small-integer data), otherwise
  * within the fp32 dot-product error bound plus the one rounding (the tensor
  * core's accumulation order).  Errors as dcc_linear_allreduce. */

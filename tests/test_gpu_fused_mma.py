@@ -53,11 +53,14 @@ def small_ints(g, size, dtype, lo=-3, hi=3):
 @pytest.mark.parametrize("n,tokens,rows,kp", [
     (1, 1, 128, 64), (2, 16, 256, 64), (8, 1, 1024, 128), (8, 17, 1024, 192), (3, 100, 136, 256),
     (8, 256, 512, 64), (16, 64, 512, 64), (5, 255, 264, 320), (8, 33, 8192, 64), (4, 128, 128, 1024),
-    (16, 256, 8, 64), (2, 1, 8, 64), (1, 255, 16, 64)])
+    (16, 256, 8, 64), (2, 1, 8, 64), (1, 255, 16, 64),
+    (8, 5, 256, 72), (3, 17, 136, 200), (2, 1, 64, 8), (4, 130, 264, 1000), (8, 64, 1024, 1016)])
 def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
     """Ragged token counts (padded to a multiple of 16 inside), a partial last
     row tile (136, 264 rows), tiles of 8 and 16 rows, 1..16 ranks, K splits
-    from 1 to 8 (fewer where the epilogue's inbox would not fit)."""
+    from 1 to 8 (fewer where the epilogue's inbox would not fit), and kp not a
+    multiple of 64 (each rank's last 64-column block partial: 8, 72, 200,
+    1000, 1016)."""
     g = torch.Generator().manual_seed(n * 7919 + tokens * 31 + kp)
     ws = [small_ints(g, rows * kp, dtype) for _ in range(n)]
     xs = [small_ints(g, tokens * kp, dtype, -2, 2) for _ in range(n)]
@@ -70,7 +73,7 @@ def test_tokens_integer_data_bit_exact(dcc, dtype, n, tokens, rows, kp):
 @pytest.mark.parametrize("form", ["pair", "one", "two"])
 @pytest.mark.parametrize("n,tokens,rows,kp", [
     (1, 1, 136, 64), (2, 17, 264, 128), (8, 256, 1032, 64), (3, 200, 200, 192), (8, 64, 8192, 64),
-    (16, 130, 520, 64), (8, 1, 8192, 128), (4, 33, 1000, 64), (2, 16, 520, 64)])
+    (16, 130, 520, 64), (8, 1, 8192, 128), (4, 33, 1000, 64), (2, 16, 520, 64), (8, 96, 1032, 136)])
 def test_tokens_every_form_bit_exact(dcc, monkeypatch, form, n, tokens, rows, kp):
     """Every form of the kernel (128-thread CTAs two per SM with one
     accumulator; 256-thread CTAs one per SM with one accumulator of up to 128
@@ -175,7 +178,7 @@ def test_tokens_argument_errors(dcc):
         assert code(w, x, y, tokens, rows, kp, "bf16") == dcc.DCC_OK
         assert code(w, x, y, 0, rows, kp, "bf16") == dcc.DCC_OK          # nothing to do
         assert code(w, x, y, 257, rows, kp, "bf16") == dcc.DCC_ERR_UNSUPPORTED
-        assert code(w, x, y, tokens, rows, 32, "bf16") == dcc.DCC_ERR_UNSUPPORTED  # kp % 64
+        assert code(w, x, y, tokens, rows, 12, "bf16") == dcc.DCC_ERR_UNSUPPORTED  # kp % 8
         assert code(w, x, y, tokens, 60, kp, "bf16") == dcc.DCC_ERR_UNSUPPORTED   # rows % 8
         assert code(w, x, y, tokens, rows, kp, "fp32") == dcc.DCC_ERR_UNSUPPORTED
         assert code(w, x, y, tokens, rows * 2, kp, "bf16") == dcc.DCC_ERR_NOT_REGISTERED
