@@ -70,14 +70,16 @@ constexpr size_t kPipeChunkBytes = 8u << 20;
 // 3584 79.1 / 75.1, 4096 87.3 / 80.5, 8192 169 / 152.
 constexpr size_t kFusedBulkMinKp = 3584;
 
-// One-token fused linear + AllReduce: kp a multiple of 64 up to this runs on
-// the tensor-core kernel (the batched layer with one token, pair form).
+// One-token fused linear + AllReduce: kp up to this runs on the tensor-core
+// kernel (the batched layer with one token, pair form).
 // Measured on GB300, 8 ranks x 8192 rows bf16, tensor-core / thread-load /
 // bulk-copy kernel (us; one weight set reused by every call, which at kp 1024
 // stays partly in L2: 22.5 us for the tensor-core kernel with two sets
 // alternating): kp 1024 20.9 / 25.1 / 53.4, 2048 40.5 / 44.1 / 60.3,
 // 3584 69.4 / 74.4 / 71.6, 4096 80.2 / 82.5 / 78.1, 6144 118.3 / 121.3 /
-// 119.5, 8192 155.9 / 159.9 / 149.1.
+// 119.5, 8192 155.9 / 159.9 / 149.1; kp not a multiple of 64 (two weight
+// sets alternating), tensor-core / thread-load: 1000 22.8 / 25.1, 1016
+// 23.0 / 25.1, 1960 41.7 / 43.6, 3576 73.2 / 74.5.
 constexpr size_t kFusedTensorMaxKp = 3584;
 
 // Tensor-core layer over a batch of tokens, its forms: "pair" (128-thread

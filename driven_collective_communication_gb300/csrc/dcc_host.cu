@@ -419,9 +419,9 @@ int linear_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
         if (overlaps(residual[r], yb, y[p], yb) && !(p == r && residual[r] == y[r])) return DCC_ERR_INVALID_ARG;
     }
   }
-  // kp a multiple of 64 up to kFusedTensorMaxKp: the tensor-core kernel, as
-  // the batched layer with one token (same layouts: x is 1 x kp, y 1 x rows)
-  if (kp % dcc::kMmaBK == 0 && kp <= ((size_t)1 << 31) / (size_t)c->n &&
+  // kp up to kFusedTensorMaxKp: the tensor-core kernel, as the batched layer
+  // with one token (same layouts: x is 1 x kp, y 1 x rows)
+  if (kp <= ((size_t)1 << 31) / (size_t)c->n && rows <= ((size_t)1 << 31) &&
       (c->fused_kernel == 2 || (c->fused_kernel < 0 && kp <= kFusedTensorMaxKp)))
     return tokens_launch(c, weight, x, residual, y, 1, rows, kp, t, s);
   int rc = check_channels_all_pairs(c);

@@ -219,17 +219,15 @@ int dcc_allreduce_from_host(dcc_comm_t c, const void* const* host_send, void* co
  * outputs disjoint from every input.  Exact when every fp32 partial sum is
  * exact (small-integer data), else within the fp32 dot-product error bound of
  * the kernel that ran, before the final rounding.  The kernel, by kp:
- *  - a multiple of 64 up to 3584: the tensor-core kernel of
- *    dcc_linear_allreduce_tokens with one token (the tensor core's
- *    accumulation order, then the K-split partials in split order);
- *  - otherwise below 3584: thread loads, rank r's CTAs computing shard r of
- *    the rows with fp32 dot products in a fixed lane/shuffle order and the
- *    ranks' partials added in rank order;
- *  - otherwise: the same with the weights streamed through shared memory by
- *    bulk copies (TMA).
+ *  - up to 3584: the tensor-core kernel of dcc_linear_allreduce_tokens with
+ *    one token (the tensor core's accumulation order, then the K-split
+ *    partials in split order);
+ *  - above: rank r's CTAs compute shard r of the rows with fp32 dot products
+ *    in a fixed lane/shuffle order, the ranks' partials added in rank order,
+ *    the weights streamed through shared memory by bulk copies (TMA);
+ *  - on request the same with thread loads instead of bulk copies.
  * DCC_FUSED_KERNEL=thread|bulk|tensor (DCC_FUSED_BULK=0 / 1 for the first
- * two) in the environment at communicator creation forces one (tensor only
- * where kp is a multiple of 64). */
+ * two) in the environment at communicator creation forces one. */
 int dcc_linear_allreduce(dcc_comm_t c, void* const* weight, void* const* x, void* const* y, size_t rows,
                          size_t kp, dcc_dtype_t t, dcc_stream_t s);
 

@@ -6,8 +6,7 @@ the fp32 dot-product bound of the kernel that ran.  The thread-load and
 bulk-copy kernels sum each rank's kp products with fused multiply-adds (one
 rounding each) and a shuffle tree, then add the N partials, so
 |acc - exact| <= gamma_{kp+N} * sum|w x| with gamma_m = m u / (1 - m u),
-u = 2^-24 (round to nearest).  The tensor-core kernel (kp a multiple of 64)
-accumulates the N*kp products in the tensor core's own order and then adds
+u = 2^-24 (round to nearest).  The tensor-core kernel accumulates the N*kp products in the tensor core's own order and then adds
 its K-split partials: gamma_{N kp + KS} with u = 2^-23 (which also covers a
 truncating adder), KS <= 8.  The kernel and the oracle then round once each to
 the output type, which adds at most one output ulp:
@@ -38,8 +37,7 @@ def dcc():
 @pytest.fixture(params=["thread", "bulk", "tensor"])
 def path(request, monkeypatch):
     """Every kernel of the op: thread loads (fused.cuh), bulk copies
-    (fused_bulk.cuh) and, where kp is a multiple of 64, the tensor-core kernel
-    (fused_mma.cuh; other kp fall back to the other two)."""
+    (fused_bulk.cuh) and the tensor-core kernel (fused_mma.cuh)."""
     monkeypatch.setenv("DCC_FUSED_KERNEL", request.param)
     return request.param
 
@@ -50,7 +48,7 @@ def gamma(m, u=2.0 ** -24):
 
 def dot_gamma(path, n, kp, extra=0):
     """The bound's factor for the kernel `path` runs (see the module docstring)."""
-    if path == "tensor" and kp % 64 == 0:
+    if path == "tensor":
         return gamma(n * kp + 8 + extra, 2.0 ** -23)
     return gamma(kp + n + extra)
 
@@ -94,7 +92,7 @@ def test_random_shapes_bit_exact(dcc, monkeypatch):
         n = int(rng.choice([1, 2, 3, 5, 8, 9, 16]))
         rows = 8 * int(rng.integers(1, 40))
         kernel = str(rng.choice(["thread", "bulk", "tensor"]))
-        kp = 64 * int(rng.integers(1, 144)) if kernel == "tensor" else 8 * int(rng.integers(1, 1150))
+        kp = 8 * int(rng.integers(1, 1150))
         dtype = str(rng.choice(["bf16", "fp16"]))
         monkeypatch.setenv("DCC_FUSED_KERNEL", kernel)
         g = torch.Generator().manual_seed(1000 + case)
@@ -208,7 +206,7 @@ def test_residual_random_shapes_bit_exact(dcc, monkeypatch):
         n = int(rng.choice([1, 2, 3, 5, 8, 16]))
         rows = 8 * int(rng.integers(1, 40))
         kernel = str(rng.choice(["thread", "bulk", "tensor"]))
-        kp = 64 * int(rng.integers(1, 144)) if kernel == "tensor" else 8 * int(rng.integers(1, 1150))
+        kp = 8 * int(rng.integers(1, 1150))
         dtype = str(rng.choice(["bf16", "fp16"]))
         inplace = bool(rng.integers(0, 2))
         monkeypatch.setenv("DCC_FUSED_KERNEL", kernel)
