@@ -172,8 +172,8 @@ struct dcc_comm {
   // clusters of the tensor-core layer that fit on the device at once, by
   // (kernel, cluster size, dynamic shared memory); 0 = not measured yet
   std::map<std::tuple<const void*, int, size_t>, int> mma_clusters;
-  // launch plans of the tensor-core layer by (form, token tile, rows, kp)
-  std::map<std::tuple<int, int, size_t, size_t>, dcc_host::MmaPlan> mma_plans;
+  // launch plans of the tensor-core layer by (form, token tile, rows, kp, residual)
+  std::map<std::tuple<int, int, size_t, size_t, bool>, dcc_host::MmaPlan> mma_plans;
 };
 
 namespace dcc_host {

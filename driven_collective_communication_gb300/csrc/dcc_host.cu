@@ -345,9 +345,12 @@ bool visit_kernels(F&& visit) {
         !v(dcc::allgather_bulk_kernel(n)) || !v(dcc::linear_allreduce_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_kernel<__half>(n)) || !v(dcc::linear_allreduce_bulk_kernel<__nv_bfloat16>(n)) ||
         !v(dcc::linear_allreduce_bulk_kernel<__half>(n)) ||
-        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaPairThreads)) ||
-        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaThreads)) ||
-        !v(dcc::linear_allreduce_mma_kernel(n, 2, dcc::kMmaThreads)))
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaPairThreads, false)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaThreads, false)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 2, dcc::kMmaThreads, false)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaPairThreads, true)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 1, dcc::kMmaThreads, true)) ||
+        !v(dcc::linear_allreduce_mma_kernel(n, 2, dcc::kMmaThreads, true)))
       return false;
   return v(dcc::ring_barrier_kernel()) && v(dcc::ring_barrier_cluster_kernel()) && v(dcc::channel_put_kernel()) &&
          v(dcc::channel_get_kernel());
@@ -951,8 +954,8 @@ int raise_smem_limit(const void* fn, size_t smem) {
 // 3/4 of the best CTA count (measured on GB300: the weight stream runs faster
 // the deeper the split, 23.5 us for 134 MB with a 4-way split against 27.3
 // with a 2-way one).
-MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
-  const auto pkey = std::make_tuple(form, ntile, rows, kp);
+MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp, bool res) {
+  const auto pkey = std::make_tuple(form, ntile, rows, kp, res);
   const auto hit = c->mma_plans.find(pkey);
   if (hit != c->mma_plans.end()) return hit->second;
   MmaPlan p;
@@ -965,7 +968,7 @@ MmaPlan plan_mma(dcc_comm_t c, int form, int ntile, size_t rows, size_t kp) {
     macc = 1;
   const int threads = form == kMmaFormPair ? dcc::kMmaPairThreads : dcc::kMmaThreads;
   const unsigned budget = form == kMmaFormPair ? dcc::kMmaPairStageBudget : dcc::kMmaStageBudget;
-  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads);
+  const void* fn = dcc::linear_allreduce_mma_kernel(c->n, macc, threads, res);
   const int stages = dcc::mma_stages(ntile, macc, budget);
   const size_t smem = dcc::mma_smem_bytes(ntile, stages, macc);
   p.rc = raise_smem_limit(fn, smem);
@@ -1102,17 +1105,18 @@ int tokens_launch(dcc_comm_t c, void* const* weight, void* const* x, void* const
   // 28672 rows x 256 tokens: 106 us against 126, while with both in one wave
   // its deeper split loses to the one-accumulator form's, 33.3 against 30.6
   // us at 8192 rows x 128 tokens).  DCC_MMA_FORM forces one.
+  const bool res = residual != nullptr;  // the residual form is its own kernel
   MmaPlan plan;
   if (c->mma_form >= 0) {
-    plan = plan_mma(c, c->mma_form, ntile, rows, kp);
+    plan = plan_mma(c, c->mma_form, ntile, rows, kp, res);
   } else {
-    plan = plan_mma(c, kMmaFormOne, ntile, rows, kp);
+    plan = plan_mma(c, kMmaFormOne, ntile, rows, kp, res);
     if (plan.rc != DCC_OK) return plan.rc;
-    const MmaPlan pair = plan_mma(c, kMmaFormPair, ntile, rows, kp);
+    const MmaPlan pair = plan_mma(c, kMmaFormPair, ntile, rows, kp, res);
     if (pair.rc != DCC_OK) return pair.rc;
     if (better_plan(pair, plan)) plan = pair;
     if (!plan.one_wave) {
-      const MmaPlan two = plan_mma(c, kMmaFormTwo, ntile, rows, kp);
+      const MmaPlan two = plan_mma(c, kMmaFormTwo, ntile, rows, kp, res);
       if (two.rc != DCC_OK) return two.rc;
       if (two.macc == 2 && two.one_wave) plan = two;
     }

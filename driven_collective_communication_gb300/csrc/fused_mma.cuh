@@ -72,6 +72,9 @@ constexpr int kMmaBM = 128;      // accumulator rows per CTA (TMEM lanes)
 constexpr int kMmaBK = 64;       // K elements per stage (one 128-byte swizzle atom row)
 constexpr int kMmaMaxTokens = 256;
 constexpr int kMmaMaxSplit = 8;  // CTAs per cluster along K
+#ifndef DCC_MMA_PLAIN_BATCH
+#define DCC_MMA_PLAIN_BATCH 2  // epilogue items per thread per pass without residuals
+#endif
 
 struct MmaMaps {
   CUtensorMap w[DCC_MAX_RANKS];   // rows x kp, box 64 x bm (one accumulator) or 64 x 128
@@ -274,11 +277,14 @@ __device__ __forceinline__ void mma_widen8(uint4 w, bool fp16, float* v) {
 // part and the inbox reuse the stage buffers (part: NTILE x 128 floats, the
 // inbox after it: (KSC - 1) x T x 128), so the copies start only once every
 // CTA of the cluster is past its main loop (the barrier of step 2).
-template <int KSC, int MACC, int THREADS>
+template <int KSC, int MACC, int THREADS, bool RES>
 __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a, uint32_t tmem, uint32_t acc_cols,
                                              float* part, uint32_t inbar, int n, unsigned split, int m0,
                                              int bm_last, bool acc_ok, int mtile) {
-  constexpr int kBatch = 4;
+  // items per thread per pass: with residuals 4, whose loads then overlap;
+  // without, 2 (measured on GB300 at 8 x 8192 x 1024: 0.2-0.5 us faster than
+  // 4 from 1 to 256 tokens)
+  constexpr int kBatch = RES ? 4 : DCC_MMA_PLAIN_BATCH;
   // a warp reaches the tensor-memory lanes 32 (warp mod 4) .. + 31 only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quad = warp & 3, row = quad * 32 + lane;
   // tokens in R ranges of W, each dealt out in KSC slices of T
@@ -366,7 +372,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
     // another (each of the G adds the item's partials itself).  Otherwise
     // G = 1.
     int G = 1;
-    if (a.res[0] != nullptr) {
+    if (RES) {
       G = THREADS * kBatch / items;
       if (G > n) G = n;
       if (G < 1) G = 1;
@@ -400,7 +406,7 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
                      ? (long long)(((size_t)t * a.rows + (size_t)(mh + r8)) * 2)
                      : -1;
       }
-      if (a.res[0] == nullptr) {  // one rounding shared by every output
+      if constexpr (!RES) {  // one rounding shared by every output
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           if (off[b] < 0) continue;
@@ -446,7 +452,14 @@ __device__ __forceinline__ void mma_epilogue(const DevComm& dc, const MmaArgs& a
 // MACC (accumulators per CTA) is a template parameter: with a run-time
 // count the loops over the accumulators cost about 12 us per launch at 8 x
 // 8192 x 1024 (measured on GB300: 40 vs 28 us).
-template <int NT, int MACC, int THREADS>
+//
+// RES: the residual form (a.res set) is its own kernel, so the plain one
+// carries none of its code (the epilogue's code is fetched cold once per
+// launch: "no instruction" stalls at 2-5 per issue).  Measured on GB300 at
+// 8 x 8192 x 1024 against one kernel for both: the plain layer 0.6-0.85 us
+// faster from 1 to 256 tokens (21.2 against 21.8 us at 1 token), the
+// residual one 0.1-0.55 us.
+template <int NT, int MACC, int THREADS, bool RES>
 __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
     k_linear_allreduce_mma(const __grid_constant__ MmaMaps maps, DevComm dc, MmaArgs a) {
   extern __shared__ unsigned char mma_raw[];
@@ -533,7 +546,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
                          full(s), pol_w);
       tma_load_2d_hint(sa + b_off, &maps.x[p], k0, 0, full(s), pol_x);
     }
-  } else if (warp >= 2 && a.res[0] != nullptr) {
+  } else if (RES && warp >= 2) {
     // idle during the main loop: ask L2 for the residual rows of this CTA's
     // epilogue (per rank and token, the tile's rows are contiguous), to be
     // kept there while the weights stream past
@@ -597,16 +610,16 @@ __global__ void __launch_bounds__(THREADS, THREADS == kMmaPairThreads ? 2 : 1)
       atomicCAS(dc.status, 0ull, pack_bounds(mtile, kBufScratch, ((size_t)2 * NTILE) * kMmaBM * 4));
   } else {
     switch (KS) {
-      case 1: mma_epilogue<1, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-      case 2: mma_epilogue<2, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-      case 4: mma_epilogue<4, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
-      default: mma_epilogue<8, MACC, THREADS>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      case 1: mma_epilogue<1, MACC, THREADS, RES>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      case 2: mma_epilogue<2, MACC, THREADS, RES>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      case 4: mma_epilogue<4, MACC, THREADS, RES>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
+      default: mma_epilogue<8, MACC, THREADS, RES>(dc, a, tmem, acc_cols, part, inbar, n, split, m0, bm_last, acc_ok, mtile); break;
     }
   }
   __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
-const void* linear_allreduce_mma_kernel(int n, int macc, int threads);
+const void* linear_allreduce_mma_kernel(int n, int macc, int threads, bool res);
 
 }  // namespace dcc
